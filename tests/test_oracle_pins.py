@@ -1,0 +1,520 @@
+"""Pins for the CPU oracle: each test checks the oracle against something other
+than itself -- exact rational arithmetic, brute force on tiny inputs, closed
+forms, invariants, textbook routines (scipy softmax), or the numbers the pages
+print.  A plausible slip in the oracle (a dropped scale, a wrong sign or index,
+rounding instead of truncation, a transposed operand) fails at least one.
+
+Sources: article 9-2 (flash_attn_single_q_q8_neon) §1-§4, article 9-3 (q8 KV
+precision comparison) §1-§4, article 10-1 (why long context must be sparse)
+§1-§2.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+from query_decode_attention_gb300 import workloads as W
+
+F32_INV127 = np.float32(1.0) / np.float32(127.0)
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _round_half_away(fr: Fraction) -> int:
+    s = 1 if fr >= 0 else -1
+    a = abs(fr)
+    f = a.numerator // a.denominator
+    return s * (f + (1 if a - f >= Fraction(1, 2) else 0))
+
+
+def _trunc(fr: Fraction) -> int:
+    a = abs(fr)
+    return (1 if fr >= 0 else -1) * (a.numerator // a.denominator)
+
+
+# ---------------------------------------------------------------------------
+# Write path (article 9-3 §2)
+# ---------------------------------------------------------------------------
+
+def test_append_hand_example():
+    # Row [2, 1, -1, -0.5, 0 ...]: max_abs 2, step d = 2 * fl(1/127).  Because
+    # fl(1/127) lies just below 1/127, 1/d is just above 63.5 -> 64, and
+    # 0.5/d = 31.75... -> 32.  The max element maps to 127.
+    x = np.zeros(128, np.float32)
+    x[:4] = [2.0, 1.0, -1.0, -0.5]
+    x[77] = -2.0  # ties in |x| keep max_abs = 2
+    c, m = oracle.kv_quantize_rows(x[None])
+    assert m[0] == np.float32(2.0)
+    assert list(c[0, :4]) == [127, 64, -64, -32]
+    assert c[0, 77] == -127
+    assert not c[0, 4:77].any() and not c[0, 78:].any()
+
+
+def test_append_matches_exact_rational_rounding():
+    rng = np.random.default_rng(11)
+    rows = rng.standard_normal((64, 128)).astype(np.float32)
+    rows *= rng.choice([1e-30, 1e-3, 1.0, 37.0, 1e20], size=(64, 1)).astype(np.float32)
+    codes, maxima = oracle.kv_quantize_rows(rows)
+    near_ties = 0
+    for r in range(rows.shape[0]):
+        m = np.abs(rows[r]).max()
+        assert maxima[r] == m
+        d = Fraction(float(np.float32(m) * F32_INV127))
+        for i in range(128):
+            ratio = Fraction(float(rows[r, i])) / d
+            exp = max(-127, min(127, _round_half_away(ratio)))
+            if codes[r, i] != exp:
+                # only where fp32 division rounds across a half-integer
+                frac = abs(ratio) - math.floor(abs(ratio))
+                assert abs(frac - Fraction(1, 2)) < abs(ratio) * Fraction(1, 2**22), (r, i)
+                near_ties += 1
+    assert near_ties <= 2
+
+
+def test_append_error_bound_and_max_maps_to_127():
+    rng = np.random.default_rng(12)
+    rows = (rng.standard_t(3, (200, 128)) * rng.uniform(0.01, 100, (200, 1))).astype(np.float32)
+    codes, maxima = oracle.kv_quantize_rows(rows)
+    d = (maxima * F32_INV127).astype(np.float64)
+    err = np.abs(rows.astype(np.float64) - codes.astype(np.float64) * d[:, None])
+    assert np.all(err <= d[:, None] * 0.5 * (1 + 2**-20))
+    am = np.abs(rows).argmax(1)
+    top = codes[np.arange(200), am]
+    assert np.all(np.abs(top) == 127)
+    assert np.all(np.sign(top) == np.sign(rows[np.arange(200), am]))
+    assert codes.min() >= -127 and codes.max() <= 127
+
+
+def test_append_power_of_two_scaling_invariance():
+    # article 9-3 §4: per-row scaling makes the codes independent of the row's
+    # amplitude; for a power-of-two factor this holds bit for bit.
+    rng = np.random.default_rng(13)
+    rows = rng.standard_normal((32, 128)).astype(np.float32)
+    c0, m0 = oracle.kv_quantize_rows(rows)
+    for k in (-5, 3, 17):
+        c1, m1 = oracle.kv_quantize_rows(rows * np.float32(2.0**k))
+        assert np.array_equal(c0, c1)
+        assert np.array_equal(m1, m0 * np.float32(2.0**k))
+
+
+def test_append_zero_row_and_permutation():
+    c, m = oracle.kv_quantize_rows(np.zeros((1, 128), np.float32))
+    assert m[0] == 0 and not c.any()
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal(128).astype(np.float32)
+    p = rng.permutation(128)
+    c0, _ = oracle.kv_quantize_rows(x[None])
+    c1, _ = oracle.kv_quantize_rows(x[p][None])
+    assert np.array_equal(c0[0][p], c1[0])
+
+
+def test_dequant_is_code_times_step():
+    c = np.array([[127, -64, 3, 0] + [0] * 124], np.int8)
+    m = np.array([2.0], np.float32)
+    d = oracle.dequant(c, m)
+    step = np.float32(2.0) * F32_INV127
+    assert d[0, 0] == np.float32(127) * step and d[0, 1] == np.float32(-64) * step
+    assert d[0, 3] == 0
+
+
+# ---------------------------------------------------------------------------
+# Q quantisation (article 9-2 §2 segment 1)
+# ---------------------------------------------------------------------------
+
+def test_quantize_q_hand_example_truncates():
+    q = np.zeros(128, np.float32)
+    q[0:4] = [1.0, 0.5, -0.5, 0.25]       # block 0, max 1: 127/1 = 127 exactly
+    q[32] = 4.0                            # block 1, max 4: 127/4 = 31.75
+    q[33] = 1.0                            # 1 * 31.75 -> 31
+    q[34] = -3.0                           # -95.25 -> -95
+    qi, qsc = oracle.quantize_q(q)
+    # truncation, not rounding: 0.5 * 127 = 63.5 -> 63, 0.25*127 = 31.75 -> 31
+    assert list(qi[0:4]) == [127, 63, -63, 31]
+    assert list(qi[32:35]) == [127, 31, -95]
+    assert qsc[0] == np.float32(1.0) * F32_INV127
+    assert qsc[1] == np.float32(4.0) * F32_INV127
+    # blocks 2 and 3 are all zero: qm < 1e-6 -> 1, codes 0, qsc = 1/127
+    assert qsc[2] == F32_INV127 and qsc[3] == F32_INV127
+    assert not qi[64:].any()
+
+
+def test_quantize_q_exact_rational_truncation():
+    rng = np.random.default_rng(21)
+    for trial in range(20):
+        q = (rng.standard_normal(128) * rng.choice([1e-7, 1e-3, 1.0, 50.0])).astype(np.float32)
+        qi, qsc = oracle.quantize_q(q)
+        for b in range(4):
+            blk = q[b * 32:(b + 1) * 32]
+            qm = np.float32(np.abs(blk).max())
+            if qm < np.float32(1e-6):
+                qm = np.float32(1.0)
+            assert qsc[b] == qm * F32_INV127
+            iq = Fraction(float(np.float32(127.0) / qm))
+            for i in range(32):
+                v = Fraction(float(blk[i])) * iq
+                exp = max(-128, min(127, _trunc(v)))
+                got = int(qi[b * 32 + i])
+                if got != exp:
+                    # fp32 product rounding onto/off an integer
+                    assert abs(v - round(v)) < abs(v) * Fraction(1, 2**22) + Fraction(1, 2**40)
+                assert abs(got) <= 127
+                assert got == 0 or np.sign(got) == np.sign(blk[i])
+
+
+def test_quantize_q_blocks_are_independent():
+    rng = np.random.default_rng(22)
+    q = rng.standard_normal(128).astype(np.float32)
+    qi0, s0 = oracle.quantize_q(q)
+    q2 = q.copy()
+    q2[64:96] *= np.float32(100.0)
+    qi1, s1 = oracle.quantize_q(q2)
+    for b in (0, 1, 3):
+        assert np.array_equal(qi0[b * 32:(b + 1) * 32], qi1[b * 32:(b + 1) * 32])
+        assert s0[b] == s1[b]
+    assert s1[2] != s0[2]
+
+
+# ---------------------------------------------------------------------------
+# int32 block dots and the score (article 9-2 §2 segment 2, point 1)
+# ---------------------------------------------------------------------------
+
+def test_block_dots_brute_force_int64():
+    rng = np.random.default_rng(31)
+    for _ in range(50):
+        a = rng.integers(-127, 128, 128).astype(np.int8)
+        k = rng.integers(-127, 128, 128).astype(np.int8)
+        d = oracle.block_dots(a, k)
+        ref = (a.astype(np.int64).reshape(4, 32) * k.astype(np.int64).reshape(4, 32)).sum(1)
+        assert np.array_equal(d.astype(np.int64), ref)
+    full = np.full(128, 127, np.int8)
+    assert list(oracle.block_dots(full, full)) == [516128] * 4
+    assert list(oracle.block_dots(full, -full)) == [-516128] * 4
+
+
+def test_score_against_exact_product():
+    rng = np.random.default_rng(32)
+    for _ in range(200):
+        dots = rng.integers(-516128, 516129, 4).astype(np.int32)
+        qsc = rng.uniform(1e-4, 1.0, 4).astype(np.float32)
+        kst = np.float32(rng.uniform(0.01, 50.0))
+        scale = np.float32(1 / math.sqrt(128))
+        s = oracle.score(dots, qsc, kst, scale)
+        exact = (sum(Fraction(int(d)) * Fraction(float(c)) for d, c in zip(dots, qsc))
+                 * Fraction(float(kst * F32_INV127)) * Fraction(float(scale)))
+        bound = sum(abs(Fraction(int(d)) * Fraction(float(c))) for d, c in zip(dots, qsc)) \
+            * Fraction(float(kst * F32_INV127)) * Fraction(float(scale)) * Fraction(6, 2**24)
+        assert abs(Fraction(float(s)) - exact) <= bound
+    # doubling the stored K scale doubles the score exactly (K scale is used)
+    d = np.array([1000, -2000, 30, 7], np.int32)
+    c = np.array([0.01, 0.02, 0.03, 0.04], np.float32)
+    assert oracle.score(d, c, 4.0, 0.5) == 2 * oracle.score(d, c, 2.0, 0.5)
+    assert oracle.score(d, c, 2.0, 0.5) == 2 * oracle.score(d, c, 2.0, 0.25)
+
+
+# ---------------------------------------------------------------------------
+# One-pass online softmax (article 9-2 §1-§4)
+# ---------------------------------------------------------------------------
+
+def _cache(n, nkv=2, seed=0, kv_bs=32, scale_k=1.0, shuffle=None):
+    rng = np.random.default_rng(seed)
+    K = (rng.standard_normal((n, nkv, 128)) * scale_k).astype(np.float32)
+    V = rng.standard_normal((n, nkv, 128)).astype(np.float32)
+    k8, ks = oracle.kv_quantize_rows(K)
+    v8, vs = oracle.kv_quantize_rows(V)
+    return oracle.SeqCache(k8, ks, v8, vs, kv_bs=kv_bs, shuffle_seed=shuffle), (k8, ks, v8, vs)
+
+
+def _textbook(q, k8, ks, v8, vs, kh, scale, tokens=None):
+    """softmax(Q' K'^T * scale) V' in float64 via scipy, on dequantised data."""
+    qi, qsc = oracle.quantize_q(q)
+    qd = (qi.astype(np.float64).reshape(4, 32) * qsc.astype(np.float64)[:, None]).reshape(128)
+    idx = np.arange(k8.shape[0]) if tokens is None else np.asarray(tokens)
+    kst = (ks[idx, kh] * F32_INV127).astype(np.float64)
+    vst = (vs[idx, kh] * F32_INV127).astype(np.float64)
+    Kd = k8[idx, kh].astype(np.float64) * kst[:, None]
+    Vd = v8[idx, kh].astype(np.float64) * vst[:, None]
+    p = scipy.special.softmax(Kd @ qd * float(scale))
+    return p @ Vd
+
+
+@pytest.mark.parametrize("n", [1, 2, 31, 32, 33, 257, 1000])
+def test_one_pass_equals_textbook_softmax(n):
+    cache, (k8, ks, v8, vs) = _cache(n, seed=n)
+    q = np.random.default_rng(100 + n).standard_normal(128).astype(np.float32)
+    scale = np.float32(1 / math.sqrt(128))
+    for kh in (0, 1):
+        out = oracle.attn_single_q(q, cache, kh, scale)
+        ref = _textbook(q, k8, ks, v8, vs, kh, scale)
+        tol = 2e-6 * np.abs(ref).max() + 1e-7 * math.sqrt(n)
+        assert np.abs(out - ref).max() <= max(tol, 1e-6), (n, kh)
+        two = oracle.attn_two_pass_f64(q, cache, kh, scale)
+        assert np.abs(two - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_one_pass_heads_are_not_mixed():
+    cache, (k8, ks, v8, vs) = _cache(300, nkv=3, seed=5)
+    q = np.random.default_rng(6).standard_normal(128).astype(np.float32)
+    outs = [oracle.attn_single_q(q, cache, kh, 0.1) for kh in range(3)]
+    for kh in range(3):
+        ref = _textbook(q, k8, ks, v8, vs, kh, np.float32(0.1))
+        assert np.abs(outs[kh] - ref).max() < 1e-5
+    assert np.abs(outs[0] - outs[1]).max() > 1e-2
+
+
+def test_running_max_trace_and_visit_count():
+    # article 9-2 §4: the loop visits exactly seq_len tokens and M never decreases
+    cache, (k8, ks, v8, vs) = _cache(500, seed=7, scale_k=3.0)
+    q = np.random.default_rng(8).standard_normal(128).astype(np.float32)
+    out, tr, nv = oracle.attn_single_q(q, cache, 1, 0.088, trace=True)
+    assert nv == 500
+    assert np.all(np.diff(tr) >= 0)
+    qi, qsc = oracle.quantize_q(q)
+    s = np.array([oracle.score(oracle.block_dots(qi, k8[t, 1]), qsc, ks[t, 1], 0.088)
+                  for t in range(500)], np.float32)
+    assert np.array_equal(tr, np.maximum.accumulate(s))
+
+
+def test_single_token_is_dequantised_v():
+    cache, (k8, ks, v8, vs) = _cache(1, seed=9)
+    q = np.random.default_rng(10).standard_normal(128).astype(np.float32)
+    out = oracle.attn_single_q(q, cache, 0, 0.1)
+    assert np.array_equal(out, v8[0, 0].astype(np.float32) * (vs[0, 0] * F32_INV127))
+
+
+def test_identical_keys_give_mean_of_values():
+    n = 200
+    rng = np.random.default_rng(15)
+    krow = rng.standard_normal(128).astype(np.float32)
+    K = np.broadcast_to(krow, (n, 1, 128)).copy()
+    V = rng.standard_normal((n, 1, 128)).astype(np.float32)
+    k8, ks = oracle.kv_quantize_rows(K)
+    v8, vs = oracle.kv_quantize_rows(V)
+    cache = oracle.SeqCache(k8, ks, v8, vs)
+    out = oracle.attn_single_q(rng.standard_normal(128).astype(np.float32), cache, 0, 0.3)
+    mean = (v8[:, 0].astype(np.float64) * (vs[:, 0] * F32_INV127)[:, None]).mean(0)
+    assert np.abs(out - mean).max() < 1e-5
+
+
+def test_empty_sequence_gives_zero():
+    cache, _ = _cache(0, seed=1)
+    out = oracle.attn_single_q(np.ones(128, np.float32), cache, 0, 0.1)
+    assert not out.any()
+
+
+def test_wide_score_range_stays_finite_and_exact():
+    cache, (k8, ks, v8, vs) = _cache(400, seed=16, scale_k=40.0)
+    q = (np.random.default_rng(17).standard_normal(128) * 5).astype(np.float32)
+    out = oracle.attn_single_q(q, cache, 0, 0.088)
+    ref = _textbook(q, k8, ks, v8, vs, 0, np.float32(0.088))
+    assert np.all(np.isfinite(out))
+    assert np.abs(out - ref).max() < 1e-5 * max(1, np.abs(ref).max())
+
+
+def test_block_pointer_indirection_and_kv_bs():
+    # the same rows behind shuffled block pointers, or other block sizes,
+    # give bit-identical results (article 9-2 §2 point 2, block/row split)
+    _, (k8, ks, v8, vs) = _cache(333, seed=18)
+    q = np.random.default_rng(19).standard_normal(128).astype(np.float32)
+    base = oracle.attn_single_q(q, oracle.SeqCache(k8, ks, v8, vs, kv_bs=32), 1, 0.1)
+    for kv_bs, sh in ((32, 5), (16, None), (64, 3), (7, 1)):
+        o = oracle.attn_single_q(q, oracle.SeqCache(k8, ks, v8, vs, kv_bs=kv_bs, shuffle_seed=sh),
+                                 1, 0.1)
+        assert np.array_equal(o, base)
+
+
+def test_token_order_only_changes_rounding():
+    cache, (k8, ks, v8, vs) = _cache(300, seed=20)
+    q = np.random.default_rng(21).standard_normal(128).astype(np.float32)
+    perm = np.random.default_rng(22).permutation(300).astype(np.int32)
+    a = oracle.attn_single_q(q, cache, 0, 0.1)
+    b = oracle.attn_single_q(q, cache, 0, 0.1, tokens=perm)
+    assert np.abs(a - b).max() < 1e-5 * np.abs(a).max()
+
+
+def test_batch_driver_gqa_mapping_and_threads():
+    wl = W.custom(3, 8, 2, [40, 1, 129], seed=3)
+    q = W.host_q(wl)
+    k8s, kss, v8s, vss = [], [], [], []
+    for b in range(wl.B):
+        K, V = W.host_kv(wl, b)
+        k8, ks = oracle.kv_quantize_rows(K)
+        v8, vs = oracle.kv_quantize_rows(V)
+        k8s.append(k8); kss.append(ks); v8s.append(v8); vss.append(vs)
+    out1 = oracle.decode_batch(q, k8s, kss, v8s, vss, wl.scale, nthreads=1)
+    out4 = oracle.decode_batch(q, k8s, kss, v8s, vss, wl.scale, nthreads=4)
+    assert np.array_equal(out1, out4)
+    for b in range(wl.B):
+        c = oracle.SeqCache(k8s[b], kss[b], v8s[b], vss[b])
+        for h in range(wl.nq):
+            assert np.array_equal(out1[b, h], oracle.attn_single_q(q[b, h], c, h // 4, wl.scale))
+
+
+# ---------------------------------------------------------------------------
+# Precision experiment (article 9-3 §1-§4)
+# ---------------------------------------------------------------------------
+
+def _golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                k, *v = line.split()
+                vals[k] = [float(x) for x in v]
+    return vals
+
+
+def test_precision_experiment_magnitude():
+    g = _golden("precision_fp32_vs_q8_kv.txt")
+    n, hd = int(g["seq_len"][0]), int(g["head_dim"][0])
+    wl = W.tiny()
+    assert (wl.seq_lens[0], wl.hd) == (n, hd)
+    q = W.host_q(wl)[0]
+    K, V = W.host_kv(wl, 0)
+    k8, ks = oracle.kv_quantize_rows(K)
+    v8, vs = oracle.kv_quantize_rows(V)
+    Kd = oracle.dequant(k8, ks)
+    Vd = oracle.dequant(v8, vs)
+    cache = oracle.SeqCache(k8, ks, v8, vs)
+    scale = 1 / math.sqrt(hd)
+    d_kv, d_full = [], []
+    for h in range(wl.nq):
+        kh = h // wl.G
+        ref = oracle.attn_ref_f64(q[h], K[:, kh], V[:, kh], scale)
+        kvq = oracle.attn_ref_f64(q[h], Kd[:, kh], Vd[:, kh], scale)
+        full = oracle.attn_single_q(q[h], cache, kh, np.float32(scale))
+        d_kv.append(np.abs(kvq - ref))
+        d_full.append(np.abs(full - ref))
+    d_kv, d_full = np.array(d_kv), np.array(d_full)
+    page_max, page_mean = g["max_abs_dout"][0], g["mean_abs_dout"][0]
+    print(f"\n[article 9-3 §3] page: max|dout| {page_max} mean {page_mean}; "
+          f"KV-only here: max {d_kv.max():.5f} mean {d_kv.mean():.5f}; "
+          f"with Q truncated to int8: max {d_full.max():.5f} mean {d_full.mean():.5f}; "
+          f"avg K step {np.mean(ks * F32_INV127):.5f} (page {g['avg_k_scale'][0]})")
+    # acceptance band: the same order as the page's ~0.01, never above 0.02
+    assert d_kv.max() <= 0.02 and d_full.max() <= 0.02
+    assert d_full.max() >= 0.1 * page_max
+    assert 0.005 < float(np.mean(ks * F32_INV127)) < 0.05
+
+
+def test_value_error_is_a_convex_combination():
+    # K exact, V quantised: out_q - out_f = sum_t p_t (v'_t - v_t), so each
+    # component differs by at most max_t |v'_t - v_t| <= max_t step_t / 2.
+    rng = np.random.default_rng(40)
+    K = rng.standard_normal((256, 128)).astype(np.float32)
+    V = rng.standard_normal((256, 128)).astype(np.float32)
+    q = rng.standard_normal(128).astype(np.float32)
+    v8, vs = oracle.kv_quantize_rows(V)
+    Vd = oracle.dequant(v8, vs)
+    a = oracle.attn_ref_f64(q, K, V, 1 / math.sqrt(128))
+    b = oracle.attn_ref_f64(q, K, Vd, 1 / math.sqrt(128))
+    per_comp = np.abs(Vd.astype(np.float64) - V).max(0)
+    assert np.all(np.abs(a - b) <= per_comp + 1e-12)
+    assert per_comp.max() <= (vs * F32_INV127).max() / 2 * (1 + 1e-6)
+
+
+def test_amplitude_scaling_keeps_relative_error():
+    # article 9-3 §4: amplifying V leaves the relative error unchanged; for a
+    # factor 4 (power of two) exactly, for 3 approximately.
+    rng = np.random.default_rng(41)
+    K = rng.standard_normal((256, 128)).astype(np.float32)
+    V = rng.standard_normal((256, 128)).astype(np.float32)
+    q = rng.standard_normal(128).astype(np.float32)
+    s = 1 / math.sqrt(128)
+
+    def rel(Vx):
+        v8, vs = oracle.kv_quantize_rows(Vx)
+        a = oracle.attn_ref_f64(q, K, Vx, s)
+        b = oracle.attn_ref_f64(q, K, oracle.dequant(v8, vs), s)
+        return np.abs(a - b).max() / np.abs(a).max()
+
+    r1, r4, r3 = rel(V), rel(V * np.float32(4)), rel(V * np.float32(3))
+    assert abs(r4 - r1) <= 1e-12 * r1
+    assert 0.8 < r3 / r1 < 1.25
+
+
+# ---------------------------------------------------------------------------
+# Block-sparse (article 10-1 §1-§2, with the oracle's stated readings)
+# ---------------------------------------------------------------------------
+
+def test_sparse_gate_is_exact_path():
+    for n in (1, 33, 64):
+        cache, _ = _cache(n, seed=50 + n)
+        q = np.random.default_rng(n).standard_normal(128).astype(np.float32)
+        out, sel, used = oracle.sparse_attn_head(q, cache, 0, 0.1, 32, 32, 8)
+        assert not used and np.all(sel == -1)
+        assert np.array_equal(out, oracle.attn_single_q(q, cache, 0, 0.1))
+    cache, _ = _cache(65, seed=99)
+    _, sel, used = oracle.sparse_attn_head(np.ones(128, np.float32), cache, 0, 0.1, 32, 32, 8)
+    assert used and list(sel[:3]) == [0, 1, 2] and np.all(sel[3:] == -1)
+
+
+def test_sparse_keeps_everything_when_k_covers_all_blocks():
+    # n = 506, block 32 -> 16 blocks <= k = 32: nothing can be pruned
+    cache, _ = _cache(506, seed=60)
+    q = np.random.default_rng(61).standard_normal(128).astype(np.float32)
+    out, sel, used = oracle.sparse_attn_head(q, cache, 1, 0.1, 32, 32, 8)
+    assert used and list(sel[:16]) == list(range(16)) and np.all(sel[16:] == -1)
+    assert np.array_equal(out, oracle.attn_single_q(q, cache, 1, 0.1))
+
+
+def test_probe_positions_and_max_fusion():
+    n, block, probe = 640, 32, 8
+    cache, (k8, ks, v8, vs) = _cache(n, nkv=1, seed=70)
+    q = np.random.default_rng(71).standard_normal(128).astype(np.float32)
+    qi, qsc = oracle.quantize_q(q)
+    s = np.array([oracle.score(oracle.block_dots(qi, k8[t, 0]), qsc, ks[t, 0], 0.1)
+                  for t in range(n)], np.float32)
+    bs = oracle.probe_block_scores(q, cache, 0, 0.1, block, probe)
+    # probe p of block j at j*32 + 4p
+    ref = np.array([s[j * 32:(j + 1) * 32:4].max() for j in range(n // 32)], np.float32)
+    assert np.array_equal(bs, ref)
+    full = oracle.probe_block_scores(q, cache, 0, 0.1, block, block)
+    assert np.array_equal(full, s.reshape(-1, 32).max(1))
+    # a ragged last block only probes tokens < n
+    cache2 = oracle.SeqCache(k8[:613], ks[:613], v8[:613], vs[:613])
+    bs2 = oracle.probe_block_scores(q, cache2, 0, 0.1, block, probe)
+    assert bs2[-1] == s[608:613:4].max()
+
+
+def test_topk_brute_force_with_ties():
+    rng = np.random.default_rng(80)
+    for trial in range(200):
+        nblk = int(rng.integers(1, 90))
+        k = int(rng.integers(1, 40))
+        sc = rng.integers(-5, 6, nblk).astype(np.float32) * np.float32(0.5)
+        got = oracle.topk_blocks(sc, k)
+        order = sorted(range(nblk), key=lambda j: (-float(sc[j]), j))
+        assert list(got) == sorted(order[:k])
+
+
+def test_sparse_output_is_one_pass_over_kept_blocks():
+    n = 1000
+    cache, (k8, ks, v8, vs) = _cache(n, seed=90)
+    q = np.random.default_rng(91).standard_normal(128).astype(np.float32)
+    out, sel, used = oracle.sparse_attn_head(q, cache, 0, 0.1, 32, 4, 8)
+    assert used and np.all(sel >= 0) and np.all(np.diff(sel) > 0)
+    bs = oracle.probe_block_scores(q, cache, 0, 0.1, 32, 8)
+    assert list(sel) == sorted(sorted(range(len(bs)), key=lambda j: (-bs[j], j))[:4])
+    toks = np.concatenate([np.arange(j * 32, min((j + 1) * 32, n)) for j in sel]).astype(np.int32)
+    ref = _textbook(q, k8, ks, v8, vs, 0, np.float32(0.1), tokens=toks)
+    assert np.abs(out - ref).max() < 1e-5 * max(1, np.abs(ref).max())
+
+
+def test_planted_blocks_are_recalled():
+    wl = W.sparse_planted(4059, B=2)
+    q = W.host_q(wl)
+    for b in range(wl.B):
+        K, V = W.host_kv(wl, b, q=q)
+        k8, ks = oracle.kv_quantize_rows(K)
+        v8, vs = oracle.kv_quantize_rows(V)
+        cache = oracle.SeqCache(k8, ks, v8, vs)
+        for h in range(wl.nq):
+            kh = h // wl.G
+            _, sel, used = oracle.sparse_attn_head(q[b, h], cache, kh, wl.scale, wl.block,
+                                                   wl.topk, wl.probe)
+            assert used
+            assert set(sel.tolist()) == set(W.planted_blocks(wl, b, kh).tolist())
