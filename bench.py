@@ -1,0 +1,512 @@
+#!/usr/bin/env python3
+"""Benchmark: q8-KV decode attention throughput (effective KV GB/s) on GB300.
+
+One step = one decode token of the Qwen3-VL-8B-shaped serving batch: for each
+of its 36 layers, append the new token's K/V of every sequence into the paged
+q8 cache (kq8_append_kv) and run exact decode attention (kq8_decode_attn)
+over the ragged batch (B = 64, lengths uniform in [1K, 32K], 32 query / 8 KV
+heads).  value = algorithmic KV bytes the attention reads per step (264 B per
+token and KV head) / step time.  Each layer's pool (~2.3 GB) is far larger
+than L2, so consecutive layers never hit in L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kq8|reference]
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (the pages publish no GPU implementation to compare with).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "q8-KV decode attention: effective KV GB/s and % of GB300 HBM peak"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kq8", choices=["kq8", "reference"])
+    ap.add_argument("--layers", type=int, default=36)
+    ap.add_argument("--batch", type=int, default=64)
+    ap.add_argument("--no-extras", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "query_decode_attention_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None, None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None, None
+    return e.get("bytes_per_unit"), e.get("unit")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="kq8_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, val in zip(names[1:], parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_gbs(wl, seqs, nthreads):
+    """Time the oracle's exact decode over sequences `seqs` of layer 0 (all
+    query heads).  Returns (GB/s, seconds, bytes)."""
+    import oracle
+    from query_decode_attention_gb300 import workloads as W
+    q = W.host_q(wl)[seqs]
+    k8s, kss, v8s, vss = [], [], [], []
+    nbytes = 0
+    for b in seqs:
+        K, V = W.host_kv(wl, b)
+        k8, ks = oracle.kv_quantize_rows(K)
+        v8, vs = oracle.kv_quantize_rows(V)
+        k8s.append(k8)
+        kss.append(ks)
+        v8s.append(v8)
+        vss.append(vs)
+        nbytes += int(wl.seq_lens[b]) * wl.nkv * (2 * wl.hd + 8)
+    t0 = time.perf_counter()
+    oracle.decode_batch(q, k8s, kss, v8s, vss, wl.scale, kv_bs=wl.kv_bs, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, dt, nbytes
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample."""
+    if rank != 0:
+        return
+    from query_decode_attention_gb300 import workloads as W
+    import oracle
+    oracle.build()
+    wl = W.serving_8b(B=args.batch, layers=args.layers)
+    threads = max(1, os.cpu_count() or 1)
+    order = np.argsort(wl.seq_lens)[: max(1, min(4, wl.B))]  # shortest: bounded work
+    seqs = [int(order[i % len(order)]) for i in range(1)]
+    for _ in range(args.warmup):
+        oracle_sample_gbs(wl, seqs, threads)
+    vals, secs = [], 0.0
+    for _ in range(args.steps):
+        g, dt, nb = oracle_sample_gbs(wl, seqs, threads)
+        vals.append(g)
+        secs += dt
+    v = statistics.median(vals)
+    sample = (f"exact decode of {len(seqs)} sequence(s) x 32 query heads (n={int(wl.seq_lens[seqs[0]])}),"
+              f" layer 0 of the {wl.name} workload, per step")
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs / max(1, args.steps), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8xint8->int32, fp32 softmax",
+            "data": "synthetic", "config": {"workload": wl.name, "sample": sample},
+            "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    from query_decode_attention_gb300 import build as kbuild
+    kbuild.build()
+    from query_decode_attention_gb300 import kq8, paged
+    from query_decode_attention_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+
+    # ---- workload: each rank serves its own batch (weak scaling, no collective)
+    wl = W.serving_8b(B=args.batch, layers=args.layers, seed=3000 + rank)
+    free, total_mem = torch.cuda.mem_get_info(dev)
+    per_layer = None
+    caches = []
+    n_pools = wl.layers
+    t_setup = time.time()
+    for layer in range(wl.layers):
+        case = paged.fill_cache(wl, layer, dev)
+        if per_layer is None:
+            per_layer = case.cache.nbytes()
+            budget = int(free * 0.80) - 8 * per_layer
+            n_pools = max(2, min(wl.layers, budget // per_layer))
+        caches.append(case)
+        if len(caches) >= n_pools:
+            break
+    torch.cuda.synchronize()
+    setup_s = time.time() - t_setup
+    L = wl.layers
+    B, nq, nkv, hd = wl.B, wl.nq, wl.nkv, wl.hd
+
+    # per-step inputs (resident): q per layer, new K/V per layer, write slots
+    q_all = torch.stack([W.device_q(wl, l, dev) for l in range(L)])            # [L,B,nq,hd]
+    gk = W.device_generator(dev, 77 + rank)
+    k_new = torch.randn((L, B, nkv, hd), generator=gk, device=dev)
+    v_new = torch.randn((L, B, nkv, hd), generator=gk, device=dev)
+    last = np.array([W.slots_for(wl, caches[0].page_table_np, b, int(n) - 1, int(n))[0]
+                     for b, n in enumerate(wl.seq_lens)], np.int32)
+    slots = torch.tensor(last, dtype=torch.int32, device=dev)
+    out_all = torch.empty((L, B, nq, hd), dtype=torch.float32, device=dev)
+    ws_bytes = kq8.kq8_decode_workspace_bytes(B, nq, nkv, wl.max_seq_len)
+    ws = kq8.new_workspace(ws_bytes, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(timers=None):
+        for l in range(L):
+            case = caches[l % len(caches)]
+            kq8.kq8_append_kv(case.cache, k_new[l], v_new[l], slots, stream=stream)
+            if timers is not None:
+                timers[l][0].record(stream)
+            kq8.kq8_decode_attn(out_all[l], q_all[l], case.cache, case.page_table, case.seq_lens,
+                                wl.max_seq_len, wl.scale, ws, stream=stream)
+            if timers is not None:
+                timers[l][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = kq8.kq8_read_status(ws)
+
+    # ---- timed region
+    bytes_per_step = wl.kv_bytes_per_layer() * L
+    timers = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(L)] for _ in range(args.steps)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for s in range(args.steps):
+            step(timers[s])
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+    clocks = clk.summary()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    if pg:
+        t = torch.tensor([elapsed_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = bytes_per_step * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+    decode_ms = [timers[s][l][0].elapsed_time(timers[s][l][1])
+                 for s in range(args.steps) for l in range(L)]
+    dec_avg_ms = sum(decode_ms) / len(decode_ms)
+    peak, peak_kind = measured_peaks()
+    achieved = wl.kv_bytes_per_layer() / (dec_avg_ms * 1e-3) / 1e9
+    traffic_per_token_head, _ = committed_traffic("kq8_attn_kernel")
+    traffic = None
+    if traffic_per_token_head is not None:
+        traffic = int(traffic_per_token_head * wl.total_tokens * nkv)
+    chunk_tiles, num_chunks = kq8.kq8_decode_plan(B, nq, nkv, wl.max_seq_len)
+    launches_per_layer = 2 + (1 if num_chunks > 1 else 0)  # append, attention, merge
+    status |= kq8.kq8_read_status(ws)
+
+    # ---- end to end through the public API from pinned host buffers
+    e2e = e2e_measure(args, wl, caches, dev, stream, kq8, L, bytes_per_step, world, pg)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8xint8->int32 scores, fp32 softmax/accumulate", "data": "synthetic",
+        "config": {**W.describe(wl), "workload": wl.name,
+                   "step": f"{L} layers x (append {B} tokens + exact decode attention)",
+                   "distinct_layer_pools": len(caches),
+                   "l2": f"no flush: each layer pool is {per_layer / 1e9:.2f} GB (> 129 MB L2)",
+                   "bytes_per_step": bytes_per_step, "parallelism": f"replicas x{world}",
+                   "chunk_tiles": chunk_tiles, "num_chunks": num_chunks},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "kq8_attn_kernel + kq8_merge_kernel (one decode call)",
+                     "peak_kind": f"{peak_kind} hbm_gbs",
+                     "bytes_per_launch": wl.kv_bytes_per_layer(),
+                     "launch_ms": round(dec_avg_ms, 5)},
+        "e2e": e2e,
+        "gpu_launches": args.steps * L * launches_per_layer,
+        "clocks": clocks,
+        "status_word": status,
+        "setup_s": round(setup_s, 1),
+    }
+    if rank == 0 and not args.no_extras:
+        line["extras"] = extras(dev, kq8, paged, W, peak)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def e2e_measure(args, wl, caches, dev, stream, kq8, L, bytes_per_step, world, pg):
+    """Same step with its inputs copied from pinned host memory every step and
+    the outputs read back, all inside the timed region."""
+    import torch
+    B, nq, nkv, hd = wl.B, wl.nq, wl.nkv, wl.hd
+    h_q = torch.randn((L, B, nq, hd), dtype=torch.float32).pin_memory()
+    h_k = torch.randn((L, B, nkv, hd), dtype=torch.float32).pin_memory()
+    h_v = torch.randn((L, B, nkv, hd), dtype=torch.float32).pin_memory()
+    h_out = torch.empty((L, B, nq, hd), dtype=torch.float32).pin_memory()
+    d_q = torch.empty_like(h_q, device=dev)
+    d_k = torch.empty_like(h_k, device=dev)
+    d_v = torch.empty_like(h_v, device=dev)
+    d_out = torch.empty_like(h_out, device=dev)
+    last = np.array([W_slot(wl, caches[0].page_table_np, b) for b in range(B)], np.int32)
+    h_slots = torch.tensor(last, dtype=torch.int32).pin_memory()
+    d_slots = torch.empty_like(h_slots, device=dev)
+    ws = kq8.new_workspace(kq8.kq8_decode_workspace_bytes(B, nq, nkv, wl.max_seq_len), dev)
+
+    def step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_slots.copy_(h_slots, non_blocking=True)
+        for l in range(L):
+            case = caches[l % len(caches)]
+            kq8.kq8_append_kv(case.cache, d_k[l], d_v[l], d_slots, stream=stream)
+            kq8.kq8_decode_attn(d_out[l], d_q[l], case.cache, case.page_table, case.seq_lens,
+                                wl.max_seq_len, wl.scale, ws, stream=stream)
+        h_out.copy_(d_out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    steps = max(1, args.steps)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    h2d = (h_q.numel() + h_k.numel() + h_v.numel()) * 4 + h_slots.numel() * 4
+    d2h = h_out.numel() * 4
+    return {"value": round(bytes_per_step * steps * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / steps, 4)}
+
+
+def W_slot(wl, pt, b):
+    from query_decode_attention_gb300 import workloads as W
+    n = int(wl.seq_lens[b])
+    return int(W.slots_for(wl, pt, b, n - 1, n)[0])
+
+
+def _time_calls(fn, reps, stream):
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def extras(dev, kq8, paged, W, peak):
+    """Secondary measurements: long-context exact decode, the write path and
+    the block-sparse path (each timed alone with CUDA events, median of reps;
+    every working set exceeds L2)."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    # long context: B = 8, n = 131072, Student-t K with outlier channels
+    wl = W.long_context()
+    case = paged.fill_cache(wl, 0, dev)
+    out = torch.empty((wl.B, wl.nq, wl.hd), device=dev)
+    ws = kq8.new_workspace(kq8.kq8_decode_workspace_bytes(wl.B, wl.nq, wl.nkv, wl.max_seq_len), dev)
+    ms = _time_calls(lambda: kq8.kq8_decode_attn(out, case.q, case.cache, case.page_table,
+                                                 case.seq_lens, wl.max_seq_len, wl.scale, ws,
+                                                 stream=stream), 10, stream)
+    gbs = wl.kv_bytes_per_layer() / (ms * 1e-3) / 1e9
+    res["long_context_exact"] = {"workload": wl.name, "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                 "frac_of_peak": round(gbs / peak, 4)}
+    # write path: 8 x 4096 new tokens into that cache
+    T = 8 * 4096
+    g = W.device_generator(dev, 99)
+    kn = torch.randn((T, wl.nkv, wl.hd), generator=g, device=dev)
+    vn = torch.randn((T, wl.nkv, wl.hd), generator=g, device=dev)
+    sl = torch.tensor(np.concatenate([case.slots(b, 0, 4096) for b in range(8)]), dtype=torch.int32,
+                      device=dev)
+    ms = _time_calls(lambda: kq8.kq8_append_kv(case.cache, kn, vn, sl, stream=stream), 20, stream)
+    ab = T * wl.nkv * (2 * wl.hd * 4 + 2 * wl.hd + 8)
+    res["append_8x4096"] = {"ms": round(ms, 4), "GB/s": round(ab / (ms * 1e-3) / 1e9, 1),
+                            "bytes": ab, "frac_of_peak": round(ab / (ms * 1e-3) / 1e9 / peak, 4)}
+    del case, out, kn, vn
+    torch.cuda.empty_cache()
+    # block-sparse: B = 16, n = 65536, block 32, k 32, probe 8 (host-drawn planted inputs)
+    wl = W.sparse_planted(65536, B=16)
+    q = W.host_q(wl)
+    Ks, Vs = zip(*[W.host_kv(wl, b, q=q) for b in range(wl.B)])
+    case = paged.fill_from_host(wl, list(Ks), list(Vs), dev, q_host=q)
+    del Ks, Vs
+    out = torch.empty((wl.B, wl.nq, wl.hd), device=dev)
+    nb = kq8.kq8_sparse_decode_workspace_bytes(wl.B, wl.nq, wl.nkv, wl.max_seq_len, wl.block,
+                                               wl.topk)
+    ws = kq8.new_workspace(nb, dev)
+    ms = _time_calls(lambda: kq8.kq8_sparse_decode_attn(out, case.q, case.cache, case.page_table,
+                                                        case.seq_lens, wl.max_seq_len, wl.scale,
+                                                        wl.block, wl.topk, wl.probe, ws,
+                                                        stream=stream), 10, stream)
+    wsx = kq8.new_workspace(kq8.kq8_decode_workspace_bytes(wl.B, wl.nq, wl.nkv, wl.max_seq_len), dev)
+    ms_ex = _time_calls(lambda: kq8.kq8_decode_attn(out, case.q, case.cache, case.page_table,
+                                                    case.seq_lens, wl.max_seq_len, wl.scale, wsx,
+                                                    stream=stream), 10, stream)
+    nblk = -(-65536 // wl.block)
+    probe_bytes = wl.B * wl.nkv * nblk * wl.probe * (wl.hd + 4)
+    sel_bytes = wl.B * wl.nq * wl.topk * wl.block * (2 * wl.hd + 8)
+    res["sparse_n65536"] = {"workload": wl.name, "ms": round(ms, 4), "exact_ms": round(ms_ex, 4),
+                            "speedup_vs_exact": round(ms_ex / ms, 2),
+                            "probe_plus_selected_bytes": probe_bytes + sel_bytes,
+                            "exact_GB/s": round(wl.kv_bytes_per_layer() / (ms_ex * 1e-3) / 1e9, 1)}
+    return res
+
+
+def cpu_baseline(wl):
+    import oracle
+    oracle.build()
+    threads = max(1, os.cpu_count() or 1)
+    order = list(np.argsort(wl.seq_lens))
+    seqs, total_s = [], 0.0
+    g, dt, nb = 0.0, 0.0, 0
+    # grow the sample until ~10 s of CPU time (bounded to 8 sequences)
+    for b in order[:8]:
+        seqs.append(int(b))
+        g, dt, nb = oracle_sample_gbs(wl, seqs, threads)
+        if dt > 3.0:
+            break
+    return {"value": round(g, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"exact decode of {len(seqs)} of the {wl.B} sequences (all 32 query heads, "
+                      f"layer 0, {nb / 1e6:.1f} MB of KV), OpenMP over (sequence, head)",
+            "seconds": round(dt, 2)}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,216 @@
+/*
+ * kq8.h -- C ABI of libkq8: q8-KV single-query decode attention on NVIDIA GB300
+ * (sm_103a).
+ *
+ * Method sources (the three web pages the method is described on):
+ *   [9-2]  article 9-2, "flash_attn_single_q_q8_neon -- single q, one pass over
+ *          all KV": §1 one-pass online softmax; §2 the kernel's signature and
+ *          its segments 1 (Q quantisation), 2 (int8 scores + online softmax),
+ *          3 (final divide); §3 the two-pass alternative.
+ *   [9-3]  article 9-3, "q8 KV precision comparison": §2 the write-path
+ *          quantisation rule (kv_quantize_per_head).
+ *   [10-1] article 10-1, "why long context must be sparse": §1 block probe +
+ *          top-k + bounded exact attention; §2 the knobs and the gate.
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument is DEVICE memory owned by the caller, except the
+ *     kq8_cache_t itself (a host struct read during the call) and the
+ *     host-side outputs that are documented as such.  The library allocates
+ *     nothing and keeps no state between calls.
+ *   - Calls enqueue work on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and return without waiting for it.
+ *   - Return value: KQ8_OK (0) or a negative KQ8_ERR_* code.  On an error
+ *     nothing was enqueued.  kq8_strerror() names a code.
+ *   - Device-resident metadata (sequence lengths, page tables, write slots) is
+ *     not visible to the host: kernels check it and, on a bad value, skip the
+ *     affected work and OR a KQ8_STATUS_* bit into a status word (the first
+ *     word of the workspace, or the `status` argument of kq8_append_kv).
+ *     kq8_read_status() fetches and clears it.
+ */
+#ifndef KQ8_H
+#define KQ8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* An opaque CUDA stream (cudaStream_t). */
+typedef struct CUstream_st* kq8_stream_t;
+
+enum {
+    KQ8_OK = 0,
+    KQ8_ERR_INVALID_ARG = -1, /* null/misaligned pointer, negative size, ... */
+    KQ8_ERR_UNSUPPORTED = -2, /* shape outside what the kernels implement   */
+    KQ8_ERR_WORKSPACE = -3,   /* workspace missing, misaligned or too small  */
+    KQ8_ERR_CUDA = -4         /* a CUDA runtime call or launch failed        */
+};
+
+/* Status bits written by kernels into the status word. */
+#define KQ8_STATUS_BAD_PAGE 0x1u    /* a page id outside [0, num_pages)        */
+#define KQ8_STATUS_BAD_SEQLEN 0x2u  /* seq_len < 0 or > max_seq_len / pages   */
+#define KQ8_STATUS_BAD_SLOT 0x4u    /* a write slot outside the pool          */
+#define KQ8_STATUS_TIMEOUT 0x8u     /* a bounded wait on a copy ran out       */
+
+/*
+ * The paged q8 KV cache of one layer.  A pool of `num_pages` pages; page p holds
+ * kv_bs consecutive tokens of one sequence for all `num_kv_heads` KV heads.
+ *   k      : int8 [num_pages][nkv][kv_bs/32][hd/32][32][32]
+ *            page p, head h, token row r, element i lives at
+ *            ((p*nkv + h)*kv_bs*hd) + (r/32)*32*hd + (i/32)*1024 + (r%32)*32 + i%32
+ *            (each token's 32-element block is 32 contiguous bytes, the same
+ *            block of 32 tokens is 1 KB contiguous).
+ *   v      : int8 [num_pages][nkv][kv_bs][hd], token rows contiguous.
+ *   kscale : float [num_pages][nkv][kv_bs], the row's max |k| (the stored
+ *            scale of [9-3] §2; readers multiply by 1/127 as on [9-2] §2).
+ *   vscale : float [num_pages][nkv][kv_bs], likewise for V.
+ * The codes are the [9-3] §2 rule: round(x / (max|x| * (1/127))) clamped to
+ * [-127, 127].  All four arrays must be 16-byte aligned.  Supported: head_dim
+ * 128, kv_bs a multiple of 32 up to 256.
+ */
+typedef struct {
+    int8_t* k;
+    int8_t* v;
+    float* kscale;
+    float* vscale;
+    int32_t num_pages;
+    int32_t kv_bs;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+} kq8_cache_t;
+
+/*
+ * Write path ([9-3] §2, kv_quantize_per_head): quantise T new tokens of K and V
+ * into the cache.
+ *   k, v   : float [T][nkv][hd] (device).
+ *   slot   : int32 [T] (device); token t goes to page slot[t] / kv_bs, row
+ *            slot[t] % kv_bs.  slot < 0 skips the token; slot >= num_pages *
+ *            kv_bs skips it and sets KQ8_STATUS_BAD_SLOT.
+ *   status : optional uint32 word (device) receiving status bits; may be NULL.
+ * Per (token, head): m = max_i |x_i| is stored as the scale; codes are
+ * round(x / (m * (1/127))) clamped to [-127, 127] (round half away from zero,
+ * IEEE division); an all-zero row stores 0 and zero codes.
+ */
+int kq8_append_kv(const kq8_cache_t* cache, const float* k, const float* v, const int32_t* slot,
+                  int32_t T, uint32_t* status, kq8_stream_t stream);
+
+/*
+ * Bytes of workspace kq8_decode_attn needs for these sizes on the current
+ * device (>= 256).  The first 256 bytes hold the status word.
+ */
+size_t kq8_decode_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len);
+
+/*
+ * The split kq8_decode_attn uses for these sizes on the current device:
+ * *chunk_tiles 32-token tiles per CTA (a multiple of 4) and *num_chunks chunks
+ * for a sequence of max_seq_len tokens.  num_chunks > 1 means a merge kernel
+ * runs after the attention kernel.  Host pointers.
+ */
+int kq8_decode_plan(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len, int32_t* chunk_tiles,
+                    int32_t* num_chunks);
+
+/*
+ * Clears the status word of a workspace (one 256-byte memset on `stream`).
+ * Call once after allocating a workspace.
+ */
+int kq8_workspace_init(void* workspace, size_t workspace_bytes, kq8_stream_t stream);
+
+/*
+ * Exact decode attention ([9-2] §1-§2): for every sequence b and query head h,
+ *   out[b][h] = sum_t softmax_t(s_t) * V'_t   over t < seq_lens[b]
+ * with s_t the [9-2] §2 score: Q quantised once to int8 in 32-element
+ * max-abs blocks (truncating, [9-2] segment 1), int32 block dots with the
+ * int8 K row, s = ((sum_b dot_b * qsc_b) * (kscale_t/127)) * scale; V'_t the
+ * dequantised V row (code * vscale_t/127).  The softmax is evaluated online
+ * (running max and sum, rescaled when the max grows) over KV chunks that are
+ * merged by their log-sum-exp, with one divide per output at the end.
+ *   out        : float [B][nq][hd] (device), written.
+ *   q          : float [B][nq][hd] (device).
+ *   page_table : int32 [B][max_pages] (device); page of tokens
+ *                [j*kv_bs, (j+1)*kv_bs) of sequence b is page_table[b][j].
+ *   seq_lens   : int32 [B] (device), each in [0, max_seq_len]; seq_len counts
+ *                the token appended this step.  seq_len 0 gives out = 0.
+ *   max_seq_len: host bound on seq_lens, <= max_pages * kv_bs.
+ *   nq         : query heads; nq % nkv == 0 and G = nq / nkv in 1..8; query
+ *                head h reads KV head h / G.
+ *   scale      : the softmax scale (1/sqrt(hd) on the pages).
+ *   workspace  : device scratch of >= kq8_decode_workspace_bytes(...) bytes,
+ *                256-byte aligned, initialised once by kq8_workspace_init.
+ * Calls sharing a workspace must not overlap on the GPU.
+ */
+int kq8_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
+                    const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                    int32_t max_seq_len, int32_t B, int32_t nq, float scale, void* workspace,
+                    size_t workspace_bytes, kq8_stream_t stream);
+
+/*
+ * Bytes of workspace kq8_sparse_decode_attn needs (>= 256).
+ */
+size_t kq8_sparse_decode_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len,
+                                         int32_t block, int32_t topk);
+
+/*
+ * Block-sparse decode attention ([10-1] §1-§2).  Per sequence the gate of
+ * [10-1] §2 applies: seq_len <= 2*block runs the exact kernel above.  Otherwise,
+ * per query head: the sequence is cut into nblk = ceil(seq_len/block) blocks;
+ * block j is probed at tokens j*block + p*(block/probe), p < probe, that are
+ * < seq_len; its score is the max of the [9-2] scores there ("max-dot
+ * fusion"); the topk highest blocks are kept (equal scores: lower block index
+ * first; topk >= nblk keeps all) and exact one-pass attention runs over their
+ * tokens in ascending block order.  These probe/selection details are this
+ * library's reading: the page describing the probe is not available.
+ *   block      : positions per block, a multiple of 32 (32 on the page).
+ *   topk       : blocks kept per query head, >= 1 (32 on the page).
+ *   probe      : probes per block, 1 <= probe <= block (8 on the page).
+ *   sel_blocks : optional int32 [B][nq][topk] (device): kept block ids in
+ *                ascending order, -1 padded; all -1 for gated sequences.
+ * Other arguments as kq8_decode_attn; workspace from
+ * kq8_sparse_decode_workspace_bytes.
+ */
+int kq8_sparse_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
+                           const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                           int32_t max_seq_len, int32_t B, int32_t nq, float scale, int32_t block,
+                           int32_t topk, int32_t probe, int32_t* sel_blocks, void* workspace,
+                           size_t workspace_bytes, kq8_stream_t stream);
+
+/*
+ * Copies the status word of `workspace` (or of a kq8_append_kv status word) to
+ * *status (host), then clears it; synchronises `stream`.
+ */
+int kq8_read_status(void* status_word, uint32_t* status, kq8_stream_t stream);
+
+/* Text for a KQ8_* return code. */
+const char* kq8_strerror(int code);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int kq8_version(void);
+
+/* ---- test-only exports: the hot path's building blocks, for bit-exact checks ---- */
+
+/* Q quantisation of [9-2] segment 1 for `rows` rows of hd floats:
+ * qi int8 [rows][hd], qsc float [rows][hd/32] (device). */
+int kq8_debug_quantize_q(int8_t* qi, float* qsc, const float* q, int32_t rows, int32_t hd,
+                         kq8_stream_t stream);
+
+/* int32 block dots of every token with every query head ([9-2] segment 2):
+ * dots int32 [B][nq][max_seq_len][hd/32] (device); entries t >= seq_lens[b]
+ * are left untouched. */
+int kq8_debug_block_dots(int32_t* dots, const float* q, const kq8_cache_t* cache,
+                         const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                         int32_t max_seq_len, int32_t B, int32_t nq, kq8_stream_t stream);
+
+/* The sparse path's block scores float [B][nq][ceil(max_seq_len/block)] (device),
+ * as the probe kernel computes them (entries of gated sequences and of blocks
+ * >= nblk are left untouched). */
+int kq8_debug_probe_scores(float* scores, const float* q, const kq8_cache_t* cache,
+                           const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                           int32_t max_seq_len, int32_t B, int32_t nq, float scale, int32_t block,
+                           int32_t probe, kq8_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KQ8_H */

@@ -1,0 +1,340 @@
+// kq8_api.cu -- the C ABI of libkq8 (declared in include/kq8.h): argument
+// checks, workspace planning and kernel dispatch.  All compute runs in the
+// CUDA kernels; this file only validates, plans and launches.
+#include <cstdint>
+#include <cstring>
+
+#include "kq8_attn.cuh"
+#include "kq8_internal.h"
+#include "kq8_sparse.cuh"
+
+namespace kq8 {
+
+size_t attn_smem_bytes(int G);
+
+namespace {
+
+constexpr size_t WS_ALIGN = 256;
+constexpr size_t STATUS_BYTES = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return 148;
+    return sms;
+}
+
+// Split of each (sequence, KV head) list of `tiles_max` 32-token tiles into
+// chunks of `chunk_tiles` tiles (a multiple of the CTA's 4 warps).  The chunk
+// is sized so that B * nkv * (chunks) CTAs give about four waves of two CTAs
+// per SM, between 4 and 64 tiles (128 to 2048 tokens).
+void chunking(int64_t B, int64_t nkv, int64_t tiles_max, int sms, int& ct, int& nch) {
+    const int64_t total = B * nkv * tiles_max;
+    const int64_t target = (int64_t)sms * 2 * 4;
+    int64_t c = (total + target - 1) / (target > 0 ? target : 1);
+    c = (c + ATTN_WARPS - 1) / ATTN_WARPS * ATTN_WARPS;
+    if (c < ATTN_WARPS) c = ATTN_WARPS;
+    if (c > 64) c = 64;
+    ct = (int)c;
+    nch = (int)((tiles_max + c - 1) / c);
+    if (nch < 1) nch = 1;
+}
+
+struct Plan {
+    int chunk_tiles = ATTN_WARPS, num_chunks = 1;
+    size_t off_ms = 0, off_acc = 0;
+    int max_nblk = 0, list_cap = 0;
+    size_t off_scores = 0, off_masks = 0, off_list = 0, off_len = 0;
+    size_t total = STATUS_BYTES;
+};
+
+Plan plan_exact(int B, int nq, int nkv, int max_seq_len) {
+    Plan p;
+    const int64_t tiles = ((int64_t)max_seq_len + TILE - 1) / TILE;
+    chunking(B, nkv, tiles, device_sms(), p.chunk_tiles, p.num_chunks);
+    size_t o = STATUS_BYTES;
+    p.off_ms = o;
+    o = align_up(o + (size_t)B * nq * p.num_chunks * sizeof(float2), WS_ALIGN);
+    p.off_acc = o;
+    o = align_up(o + (size_t)B * nq * p.num_chunks * HD * sizeof(float), WS_ALIGN);
+    p.total = o;
+    return p;
+}
+
+Plan plan_sparse(int B, int nq, int nkv, int max_seq_len, int block, int topk) {
+    Plan p;
+    const int G = nq / nkv;
+    const int m = block / TILE;
+    const int64_t tiles = ((int64_t)max_seq_len + TILE - 1) / TILE;
+    p.max_nblk = (int)(((int64_t)max_seq_len + block - 1) / block);
+    int64_t cap = (int64_t)(p.max_nblk < (int64_t)G * topk ? p.max_nblk : (int64_t)G * topk) * m;
+    if (cap > tiles) cap = tiles;
+    if (cap < 2 * m && cap < tiles) cap = tiles < 2 * m ? tiles : 2 * m;
+    if (cap < 1) cap = 1;
+    p.list_cap = (int)cap;
+    chunking(B, nkv, p.list_cap, device_sms(), p.chunk_tiles, p.num_chunks);
+    size_t o = STATUS_BYTES;
+    p.off_scores = o;
+    o = align_up(o + (size_t)B * nq * p.max_nblk * sizeof(float), WS_ALIGN);
+    p.off_masks = o;
+    o = align_up(o + (size_t)B * nkv * p.max_nblk, WS_ALIGN);
+    p.off_list = o;
+    o = align_up(o + (size_t)B * nkv * p.list_cap * sizeof(int32_t), WS_ALIGN);
+    p.off_len = o;
+    o = align_up(o + (size_t)B * nkv * sizeof(int32_t), WS_ALIGN);
+    p.off_ms = o;
+    o = align_up(o + (size_t)B * nq * p.num_chunks * sizeof(float2), WS_ALIGN);
+    p.off_acc = o;
+    o = align_up(o + (size_t)B * nq * p.num_chunks * HD * sizeof(float), WS_ALIGN);
+    p.total = o;
+    return p;
+}
+
+int check_cache(const kq8_cache_t* c) {
+    if (!c) return KQ8_ERR_INVALID_ARG;
+    if (c->head_dim != HD) return KQ8_ERR_UNSUPPORTED;
+    if (c->kv_bs < TILE || c->kv_bs > 256 || c->kv_bs % TILE != 0) return KQ8_ERR_UNSUPPORTED;
+    if (c->num_kv_heads < 1 || c->num_pages < 1) return KQ8_ERR_INVALID_ARG;
+    if (!c->k || !c->v || !c->kscale || !c->vscale) return KQ8_ERR_INVALID_ARG;
+    if (!aligned(c->k, 16) || !aligned(c->v, 16) || !aligned(c->kscale, 16) ||
+        !aligned(c->vscale, 16))
+        return KQ8_ERR_INVALID_ARG;
+    return KQ8_OK;
+}
+
+int check_decode(float* out, const float* q, const kq8_cache_t* c, const int32_t* pt,
+                 int32_t max_pages, const int32_t* seq_lens, int32_t max_seq_len, int32_t B,
+                 int32_t nq) {
+    int rc = check_cache(c);
+    if (rc) return rc;
+    if (B < 0 || nq < 1 || max_seq_len < 0 || max_pages < 0) return KQ8_ERR_INVALID_ARG;
+    if (nq % c->num_kv_heads != 0) return KQ8_ERR_UNSUPPORTED;
+    const int G = nq / c->num_kv_heads;
+    if (G < 1 || G > MAX_G) return KQ8_ERR_UNSUPPORTED;
+    if ((int64_t)max_seq_len > (int64_t)max_pages * c->kv_bs) return KQ8_ERR_INVALID_ARG;
+    if (max_seq_len >= (1 << 29)) return KQ8_ERR_UNSUPPORTED;
+    if (B > 65535) return KQ8_ERR_UNSUPPORTED;
+    if (B > 0) {
+        if (!out || !q || !seq_lens || (max_seq_len > 0 && !pt)) return KQ8_ERR_INVALID_ARG;
+        if (!aligned(out, 16) || !aligned(q, 16)) return KQ8_ERR_INVALID_ARG;
+    }
+    return KQ8_OK;
+}
+
+int check_ws(void* ws, size_t bytes, size_t need) {
+    if (!ws || !aligned(ws, WS_ALIGN)) return KQ8_ERR_WORKSPACE;
+    if (bytes < need) return KQ8_ERR_WORKSPACE;
+    return KQ8_OK;
+}
+
+AttnParams attn_params(float* out, const float* q, const kq8_cache_t* c, const int32_t* pt,
+                       int32_t max_pages, const int32_t* seq_lens, int32_t max_seq_len, int32_t B,
+                       int32_t nq, float scale, const Plan& plan, void* ws) {
+    AttnParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.out = out;
+    p.q = q;
+    p.cache = *c;
+    p.page_table = pt;
+    p.max_pages = max_pages;
+    p.seq_lens = seq_lens;
+    p.max_seq_len = max_seq_len;
+    p.B = B;
+    p.nq = nq;
+    p.scale = scale;
+    p.chunk_tiles = plan.chunk_tiles;
+    p.num_chunks = plan.num_chunks;
+    p.part_ms = reinterpret_cast<float2*>(static_cast<char*>(ws) + plan.off_ms);
+    p.part_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + plan.off_acc);
+    p.status = static_cast<uint32_t*>(ws);
+    return p;
+}
+
+}  // namespace
+}  // namespace kq8
+
+using namespace kq8;
+
+extern "C" {
+
+int kq8_version(void) { return 10000; }
+
+const char* kq8_strerror(int code) {
+    switch (code) {
+        case KQ8_OK: return "ok";
+        case KQ8_ERR_INVALID_ARG: return "invalid argument";
+        case KQ8_ERR_UNSUPPORTED: return "unsupported shape";
+        case KQ8_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case KQ8_ERR_CUDA: return "CUDA error";
+        default: return "unknown error";
+    }
+}
+
+int kq8_append_kv(const kq8_cache_t* cache, const float* k, const float* v, const int32_t* slot,
+                  int32_t T, uint32_t* status, kq8_stream_t stream) {
+    int rc = check_cache(cache);
+    if (rc) return rc;
+    if (T < 0) return KQ8_ERR_INVALID_ARG;
+    if (T == 0) return KQ8_OK;
+    if (!k || !v || !slot || !aligned(k, 16) || !aligned(v, 16)) return KQ8_ERR_INVALID_ARG;
+    if (status && !aligned(status, 4)) return KQ8_ERR_INVALID_ARG;
+    return launch_append(*cache, k, v, slot, T, status, (cudaStream_t)stream);
+}
+
+size_t kq8_decode_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len) {
+    if (B < 0 || nq < 1 || nkv < 1 || max_seq_len < 0) return 0;
+    return plan_exact(B, nq, nkv, max_seq_len).total;
+}
+
+int kq8_decode_plan(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len, int32_t* chunk_tiles,
+                    int32_t* num_chunks) {
+    if (B < 0 || nq < 1 || nkv < 1 || max_seq_len < 0 || !chunk_tiles || !num_chunks)
+        return KQ8_ERR_INVALID_ARG;
+    const Plan p = plan_exact(B, nq, nkv, max_seq_len);
+    *chunk_tiles = p.chunk_tiles;
+    *num_chunks = p.num_chunks;
+    return KQ8_OK;
+}
+
+size_t kq8_sparse_decode_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len,
+                                         int32_t block, int32_t topk) {
+    if (B < 0 || nq < 1 || nkv < 1 || max_seq_len < 0 || block < TILE || block % TILE || topk < 1)
+        return 0;
+    return plan_sparse(B, nq, nkv, max_seq_len, block, topk).total;
+}
+
+int kq8_workspace_init(void* workspace, size_t workspace_bytes, kq8_stream_t stream) {
+    if (check_ws(workspace, workspace_bytes, STATUS_BYTES)) return KQ8_ERR_WORKSPACE;
+    return cudaMemsetAsync(workspace, 0, STATUS_BYTES, (cudaStream_t)stream) == cudaSuccess
+               ? KQ8_OK
+               : KQ8_ERR_CUDA;
+}
+
+int kq8_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
+                    const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                    int32_t max_seq_len, int32_t B, int32_t nq, float scale, void* workspace,
+                    size_t workspace_bytes, kq8_stream_t stream) {
+    int rc = check_decode(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq);
+    if (rc) return rc;
+    const int nkv = cache->num_kv_heads;
+    const Plan plan = plan_exact(B, nq, nkv, max_seq_len);
+    rc = check_ws(workspace, workspace_bytes, plan.total);
+    if (rc) return rc;
+    if (B == 0) return KQ8_OK;
+    AttnParams p = attn_params(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq,
+                               scale, plan, workspace);
+    return launch_attn(p, nq / nkv, false, B, nkv, (cudaStream_t)stream);
+}
+
+int kq8_sparse_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
+                           const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                           int32_t max_seq_len, int32_t B, int32_t nq, float scale, int32_t block,
+                           int32_t topk, int32_t probe, int32_t* sel_blocks, void* workspace,
+                           size_t workspace_bytes, kq8_stream_t stream) {
+    int rc = check_decode(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq);
+    if (rc) return rc;
+    if (block < TILE || block % TILE != 0 || topk < 1 || probe < 1 || probe > block)
+        return KQ8_ERR_UNSUPPORTED;
+    if (sel_blocks && !aligned(sel_blocks, 4)) return KQ8_ERR_INVALID_ARG;
+    const int nkv = cache->num_kv_heads;
+    const int G = nq / nkv;
+    const Plan plan = plan_sparse(B, nq, nkv, max_seq_len, block, topk);
+    rc = check_ws(workspace, workspace_bytes, plan.total);
+    if (rc) return rc;
+    if (B == 0) return KQ8_OK;
+    char* ws = static_cast<char*>(workspace);
+    SparseParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.q = q;
+    sp.cache = *cache;
+    sp.page_table = page_table;
+    sp.max_pages = max_pages;
+    sp.seq_lens = seq_lens;
+    sp.max_seq_len = max_seq_len;
+    sp.B = B;
+    sp.nq = nq;
+    sp.scale = scale;
+    sp.block = block;
+    sp.topk = topk;
+    sp.probe = probe;
+    sp.max_nblk = plan.max_nblk;
+    sp.scores = reinterpret_cast<float*>(ws + plan.off_scores);
+    sp.masks = reinterpret_cast<uint8_t*>(ws + plan.off_masks);
+    sp.tile_list = reinterpret_cast<int32_t*>(ws + plan.off_list);
+    sp.list_len = reinterpret_cast<int32_t*>(ws + plan.off_len);
+    sp.list_cap = plan.list_cap;
+    sp.sel_blocks = sel_blocks;
+    sp.status = reinterpret_cast<uint32_t*>(ws);
+    cudaStream_t s = (cudaStream_t)stream;
+    rc = launch_probe(sp, G, B, nkv, s);
+    if (rc) return rc;
+    rc = launch_topk(sp, G, B, nkv, s);
+    if (rc) return rc;
+    AttnParams p = attn_params(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq,
+                               scale, plan, workspace);
+    p.tile_list = sp.tile_list;
+    p.list_len = sp.list_len;
+    p.list_cap = sp.list_cap;
+    return launch_attn(p, G, true, B, nkv, s);
+}
+
+int kq8_read_status(void* status_word, uint32_t* status, kq8_stream_t stream) {
+    if (!status_word || !status || !aligned(status_word, 4)) return KQ8_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KQ8_ERR_CUDA;
+    if (cudaMemcpy(status, status_word, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KQ8_ERR_CUDA;
+    if (cudaMemsetAsync(status_word, 0, sizeof(uint32_t), s) != cudaSuccess) return KQ8_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+}
+
+int kq8_debug_quantize_q(int8_t* qi, float* qsc, const float* q, int32_t rows, int32_t hd,
+                         kq8_stream_t stream) {
+    if (hd != HD) return KQ8_ERR_UNSUPPORTED;
+    if (rows < 0 || (rows > 0 && (!qi || !qsc || !q || !aligned(q, 16) || !aligned(qi, 4))))
+        return KQ8_ERR_INVALID_ARG;
+    return launch_debug_quantize(qi, qsc, q, rows, (cudaStream_t)stream);
+}
+
+int kq8_debug_block_dots(int32_t* dots, const float* q, const kq8_cache_t* cache,
+                         const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                         int32_t max_seq_len, int32_t B, int32_t nq, kq8_stream_t stream) {
+    int rc = check_decode(reinterpret_cast<float*>(dots), q, cache, page_table, max_pages, seq_lens,
+                          max_seq_len, B, nq);
+    if (rc) return rc;
+    return launch_debug_dots(dots, q, *cache, page_table, max_pages, seq_lens, max_seq_len, B, nq,
+                             (cudaStream_t)stream);
+}
+
+int kq8_debug_probe_scores(float* scores, const float* q, const kq8_cache_t* cache,
+                           const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                           int32_t max_seq_len, int32_t B, int32_t nq, float scale, int32_t block,
+                           int32_t probe, kq8_stream_t stream) {
+    int rc = check_decode(scores, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq);
+    if (rc) return rc;
+    if (block < TILE || block % TILE != 0 || probe < 1 || probe > block) return KQ8_ERR_UNSUPPORTED;
+    SparseParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.q = q;
+    sp.cache = *cache;
+    sp.page_table = page_table;
+    sp.max_pages = max_pages;
+    sp.seq_lens = seq_lens;
+    sp.max_seq_len = max_seq_len;
+    sp.B = B;
+    sp.nq = nq;
+    sp.scale = scale;
+    sp.block = block;
+    sp.probe = probe;
+    sp.max_nblk = (int)(((int64_t)max_seq_len + block - 1) / block);
+    sp.scores = scores;
+    sp.status = nullptr;  // bad page ids are skipped without a status word
+    return launch_probe(sp, nq / cache->num_kv_heads, B, cache->num_kv_heads,
+                        (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// kq8_attn.cu -- launchers of the split-KV attention kernel and the merge.
+#include "kq8_attn.cuh"
+#include "kq8_internal.h"
+
+namespace kq8 {
+
+constexpr int ATTN_STAGES = 3;
+
+template <int G, bool SPARSE>
+static int launch_attn_g(const AttnParams& p, int B, int nkv, cudaStream_t s) {
+    auto kern = kq8_attn_kernel<G, ATTN_STAGES, SPARSE>;
+    const size_t smem = sizeof(AttnSmem<G, ATTN_STAGES>);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return KQ8_ERR_CUDA;
+    dim3 grid(p.num_chunks, nkv, B);
+    kern<<<grid, ATTN_THREADS, smem, s>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return KQ8_ERR_CUDA;
+    if (p.num_chunks > 1) {
+        kq8_merge_kernel<SPARSE><<<B * p.nq, HD, 0, s>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return KQ8_ERR_CUDA;
+    }
+    return KQ8_OK;
+}
+
+template <bool SPARSE>
+static int launch_attn_s(const AttnParams& p, int G, int B, int nkv, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_attn_g<1, SPARSE>(p, B, nkv, s);
+        case 2: return launch_attn_g<2, SPARSE>(p, B, nkv, s);
+        case 3: return launch_attn_g<3, SPARSE>(p, B, nkv, s);
+        case 4: return launch_attn_g<4, SPARSE>(p, B, nkv, s);
+        case 5: return launch_attn_g<5, SPARSE>(p, B, nkv, s);
+        case 6: return launch_attn_g<6, SPARSE>(p, B, nkv, s);
+        case 7: return launch_attn_g<7, SPARSE>(p, B, nkv, s);
+        case 8: return launch_attn_g<8, SPARSE>(p, B, nkv, s);
+        default: return KQ8_ERR_UNSUPPORTED;
+    }
+}
+
+int launch_attn(const AttnParams& p, int G, bool sparse, int B, int nkv, cudaStream_t s) {
+    if (B == 0) return KQ8_OK;
+    return sparse ? launch_attn_s<true>(p, G, B, nkv, s) : launch_attn_s<false>(p, G, B, nkv, s);
+}
+
+size_t attn_smem_bytes(int G) {
+    switch (G) {
+        case 1: return sizeof(AttnSmem<1, ATTN_STAGES>);
+        case 2: return sizeof(AttnSmem<2, ATTN_STAGES>);
+        case 3: return sizeof(AttnSmem<3, ATTN_STAGES>);
+        case 4: return sizeof(AttnSmem<4, ATTN_STAGES>);
+        case 5: return sizeof(AttnSmem<5, ATTN_STAGES>);
+        case 6: return sizeof(AttnSmem<6, ATTN_STAGES>);
+        case 7: return sizeof(AttnSmem<7, ATTN_STAGES>);
+        default: return sizeof(AttnSmem<8, ATTN_STAGES>);
+    }
+}
+
+}  // namespace kq8

@@ -1,0 +1,25 @@
+// kq8_internal.h -- launchers shared between the libkq8 translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "kq8.h"
+
+namespace kq8 {
+
+struct AttnParams;
+struct SparseParams;
+
+int launch_append(const kq8_cache_t& c, const float* k, const float* v, const int32_t* slot,
+                  int32_t T, uint32_t* status, cudaStream_t stream);
+int launch_debug_quantize(int8_t* qi, float* qsc, const float* q, int32_t rows, cudaStream_t s);
+int launch_debug_dots(int32_t* dots, const float* q, const kq8_cache_t& c,
+                      const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                      int32_t max_seq_len, int32_t B, int32_t nq, cudaStream_t s);
+
+// Attention over KV chunks (+ the merge when any sequence spans > 1 chunk).
+int launch_attn(const AttnParams& p, int G, bool sparse, int B, int nkv, cudaStream_t s);
+int launch_probe(const SparseParams& p, int G, int B, int nkv, cudaStream_t s);
+int launch_topk(const SparseParams& p, int G, int B, int nkv, cudaStream_t s);
+
+}  // namespace kq8

@@ -1,0 +1,155 @@
+// kq8_misc.cu -- the write path (article 9-3 §2, kv_quantize_per_head) and the
+// test-only kernels that expose the hot path's integer building blocks.
+#include "kq8_common.cuh"
+#include "kq8_internal.h"
+
+namespace kq8 {
+
+// One (token, KV head) row of K or V, one warp: lane l holds elements
+// 4l..4l+3.  m = max |x| (exact, order-free), stored as the scale; codes are
+// roundf(x / (m * (1/127))) clamped to [-127, 127] with an IEEE divide, as the
+// oracle does; an all-zero row gives zero codes.  Returns the lane's 4 codes.
+__device__ __forceinline__ uint32_t kv_quantize_lane(const float4 x, float& m_out) {
+    float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+    m = warp_max(m);
+    m_out = m;
+    if (m == 0.0f) return 0u;
+    const float d = __fmul_rn(m, inv127());
+    auto code = [&](float v) -> uint32_t {
+        float r = roundf(__fdiv_rn(v, d));
+        r = fminf(fmaxf(r, -127.0f), 127.0f);
+        return (uint32_t)((int)r & 0xff);
+    };
+    return code(x.x) | (code(x.y) << 8) | (code(x.z) << 16) | (code(x.w) << 24);
+}
+
+constexpr int APPEND_WARPS = 8;
+
+// grid: ceil(T * nkv / APPEND_WARPS) blocks of APPEND_WARPS warps; warp = one
+// (token, head) item, quantising its K and its V row.
+__global__ void __launch_bounds__(APPEND_WARPS * 32)
+    kq8_append_kernel(const kq8_cache_t c, const float* __restrict__ k, const float* __restrict__ v,
+                      const int32_t* __restrict__ slot, int32_t T, uint32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t item = (int64_t)blockIdx.x * APPEND_WARPS + (threadIdx.x >> 5);
+    const int nkv = c.num_kv_heads, kv_bs = c.kv_bs;
+    if (item >= (int64_t)T * nkv) return;
+    const int64_t t = item / nkv;
+    const int h = (int)(item % nkv);
+    const int32_t sl = slot[t];
+    if (sl < 0) return;
+    if ((int64_t)sl >= (int64_t)c.num_pages * kv_bs) {
+        if (lane == 0 && status) atomicOr(status, KQ8_STATUS_BAD_SLOT);
+        return;
+    }
+    const int32_t page = sl / kv_bs;
+    const int r = sl % kv_bs;
+    const size_t row = (size_t)item * HD;
+    const float4 xk = __ldcs(reinterpret_cast<const float4*>(k + row) + lane);
+    const float4 xv = __ldcs(reinterpret_cast<const float4*>(v + row) + lane);
+    float mk, mv;
+    const uint32_t ck = kv_quantize_lane(xk, mk);
+    const uint32_t cv = kv_quantize_lane(xv, mv);
+    // K: element i of row r at sub-tile r/32, block i/32, row r%32, byte i%32
+    const size_t ko = kv_sub_off(page, h, nkv, kv_bs, r / TILE) + (size_t)(lane >> 3) * 1024 +
+                      (size_t)(r % TILE) * 32 + (size_t)(lane & 7) * 4;
+    *reinterpret_cast<uint32_t*>(c.k + ko) = ck;
+    const size_t vo = page_head(page, h, nkv) * (size_t)kv_bs * HD + (size_t)r * HD + lane * 4;
+    *reinterpret_cast<uint32_t*>(c.v + vo) = cv;
+    if (lane == 0) {
+        const size_t so = page_head(page, h, nkv) * (size_t)kv_bs + r;
+        c.kscale[so] = mk;
+        c.vscale[so] = mv;
+    }
+}
+
+int launch_append(const kq8_cache_t& c, const float* k, const float* v, const int32_t* slot,
+                  int32_t T, uint32_t* status, cudaStream_t stream) {
+    const int64_t items = (int64_t)T * c.num_kv_heads;
+    if (items == 0) return KQ8_OK;
+    const int64_t blocks = (items + APPEND_WARPS - 1) / APPEND_WARPS;
+    kq8_append_kernel<<<(unsigned)blocks, APPEND_WARPS * 32, 0, stream>>>(c, k, v, slot, T, status);
+    return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Test-only: Q quantisation, one warp per row of 128.
+// ---------------------------------------------------------------------------
+__global__ void kq8_debug_quantize_kernel(int8_t* qi, float* qsc, const float* q, int32_t rows) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const float4 x = reinterpret_cast<const float4*>(q + row * HD)[lane];
+    float s;
+    const uint32_t codes = quantize_q_lane(x, s);
+    reinterpret_cast<uint32_t*>(qi + row * HD)[lane] = codes;
+    if ((lane & 7) == 0) qsc[row * NB + (lane >> 3)] = s;
+}
+
+int launch_debug_quantize(int8_t* qi, float* qsc, const float* q, int32_t rows, cudaStream_t s) {
+    if (rows == 0) return KQ8_OK;
+    kq8_debug_quantize_kernel<<<(rows + 3) / 4, 128, 0, s>>>(qi, qsc, q, rows);
+    return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Test-only: int32 block dots of every token with every query head, with the
+// same data path as the attention kernel's score phase (K sub-tile in shared
+// memory, lane = token, half-swizzled 16-byte loads, dp4a).
+// grid (ceil(max_seq_len/32), nkv, B), 1 warp.
+// ---------------------------------------------------------------------------
+__global__ void kq8_debug_dots_kernel(int32_t* dots, const float* q, const kq8_cache_t c,
+                                      const int32_t* page_table, int32_t max_pages,
+                                      const int32_t* seq_lens, int32_t max_seq_len, int32_t nq) {
+    __shared__ __align__(16) int8_t kt[SUB_K_BYTES];
+    __shared__ __align__(16) int8_t qi[MAX_G][HD];
+    const int lane = threadIdx.x;
+    const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int nkv = c.num_kv_heads, G = nq / nkv;
+    const int n = seq_lens[b];
+    if (n < 0 || n > max_seq_len || tile * TILE >= n) return;
+    const int32_t pg = page_table[(size_t)b * max_pages + tile / (c.kv_bs / TILE)];
+    if (pg < 0 || pg >= c.num_pages) return;
+    for (int g = 0; g < G; g++) {
+        const float4 x = reinterpret_cast<const float4*>(q + ((size_t)b * nq + h * G + g) * HD)[lane];
+        float s;
+        reinterpret_cast<uint32_t*>(qi[g])[lane] = quantize_q_lane(x, s);
+    }
+    const int8_t* src = c.k + kv_sub_off(pg, h, nkv, c.kv_bs, tile % (c.kv_bs / TILE));
+    for (int i = lane; i < SUB_K_BYTES / 16; i += 32)
+        reinterpret_cast<uint4*>(kt)[i] = reinterpret_cast<const uint4*>(src)[i];
+    __syncwarp();
+    const int t = lane;
+    const int hs = (t >> 2) & 1;
+    for (int g = 0; g < G; g++) {
+        for (int bb = 0; bb < NB; bb++) {
+            const uint4 kA = *reinterpret_cast<const uint4*>(kt + bb * 1024 + t * 32 + hs * 16);
+            const uint4 kB = *reinterpret_cast<const uint4*>(kt + bb * 1024 + t * 32 + (hs ^ 1) * 16);
+            const uint4 qA = *reinterpret_cast<const uint4*>(qi[g] + bb * 32 + hs * 16);
+            const uint4 qB = *reinterpret_cast<const uint4*>(qi[g] + bb * 32 + (hs ^ 1) * 16);
+            int d = __dp4a((int)kA.x, (int)qA.x, 0);
+            d = __dp4a((int)kA.y, (int)qA.y, d);
+            d = __dp4a((int)kA.z, (int)qA.z, d);
+            d = __dp4a((int)kA.w, (int)qA.w, d);
+            d = __dp4a((int)kB.x, (int)qB.x, d);
+            d = __dp4a((int)kB.y, (int)qB.y, d);
+            d = __dp4a((int)kB.z, (int)qB.z, d);
+            d = __dp4a((int)kB.w, (int)qB.w, d);
+            const int tok = tile * TILE + t;
+            if (tok < n)
+                dots[(((size_t)b * nq + h * G + g) * max_seq_len + tok) * NB + bb] = d;
+        }
+    }
+}
+
+int launch_debug_dots(int32_t* dots, const float* q, const kq8_cache_t& c,
+                      const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                      int32_t max_seq_len, int32_t B, int32_t nq, cudaStream_t s) {
+    if (B == 0 || max_seq_len == 0) return KQ8_OK;
+    dim3 grid((max_seq_len + TILE - 1) / TILE, c.num_kv_heads, B);
+    kq8_debug_dots_kernel<<<grid, 32, 0, s>>>(dots, q, c, page_table, max_pages, seq_lens,
+                                               max_seq_len, nq);
+    return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+}
+
+}  // namespace kq8

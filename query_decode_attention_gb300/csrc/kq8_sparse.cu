@@ -1,0 +1,44 @@
+// kq8_sparse.cu -- launchers of the block-sparse probe and top-k kernels.
+#include "kq8_internal.h"
+#include "kq8_sparse.cuh"
+
+namespace kq8 {
+
+template <int G>
+static int launch_probe_g(const SparseParams& p, int B, int nkv, cudaStream_t s) {
+    dim3 grid((p.max_nblk + PROBE_BLOCKS_PER_CTA - 1) / PROBE_BLOCKS_PER_CTA, nkv, B);
+    kq8_probe_kernel<G><<<grid, PROBE_WARPS * 32, 0, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+}
+
+template <int G>
+static int launch_topk_g(const SparseParams& p, int B, int nkv, cudaStream_t s) {
+    dim3 grid(nkv, B);
+    kq8_topk_kernel<G><<<grid, TOPK_THREADS, 0, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+}
+
+#define KQ8_SWITCH_G(F, ...)                 \
+    switch (G) {                             \
+        case 1: return F<1>(__VA_ARGS__);    \
+        case 2: return F<2>(__VA_ARGS__);    \
+        case 3: return F<3>(__VA_ARGS__);    \
+        case 4: return F<4>(__VA_ARGS__);    \
+        case 5: return F<5>(__VA_ARGS__);    \
+        case 6: return F<6>(__VA_ARGS__);    \
+        case 7: return F<7>(__VA_ARGS__);    \
+        case 8: return F<8>(__VA_ARGS__);    \
+        default: return KQ8_ERR_UNSUPPORTED; \
+    }
+
+int launch_probe(const SparseParams& p, int G, int B, int nkv, cudaStream_t s) {
+    if (B == 0 || p.max_nblk == 0) return KQ8_OK;
+    KQ8_SWITCH_G(launch_probe_g, p, B, nkv, s)
+}
+
+int launch_topk(const SparseParams& p, int G, int B, int nkv, cudaStream_t s) {
+    if (B == 0) return KQ8_OK;
+    KQ8_SWITCH_G(launch_topk_g, p, B, nkv, s)
+}
+
+}  // namespace kq8

@@ -1,0 +1,295 @@
+// kq8_sparse.cuh -- block-sparse decode (article 10-1 §1-§2): probe kernel,
+// top-k selection and the per-KV-head union tile lists that the attention
+// kernel then walks in SPARSE mode.
+//
+// Readings taken where the pages are silent (the page that details the
+// probe is not available): probe p of block j reads token
+// j*block + p*(block/probe) if < seq_len; the block score is the max of the
+// one-pass scores there; per query head the topk highest blocks are kept,
+// equal scores going to the lower block index; topk >= nblk keeps all;
+// attention runs over the kept blocks in ascending order.
+#pragma once
+
+#include "kq8_common.cuh"
+
+namespace kq8 {
+
+struct SparseParams {
+    const float* q;
+    kq8_cache_t cache;
+    const int32_t* page_table;
+    int32_t max_pages;
+    const int32_t* seq_lens;
+    int32_t max_seq_len;
+    int32_t B, nq;
+    float scale;
+    int32_t block, topk, probe;
+    int32_t max_nblk;        // ceil(max_seq_len / block)
+    float* scores;           // [B][nq][max_nblk]
+    uint8_t* masks;          // [B][nkv][max_nblk]
+    int32_t* tile_list;      // [B][nkv][list_cap]
+    int32_t* list_len;       // [B][nkv]
+    int32_t list_cap;
+    int32_t* sel_blocks;     // optional [B][nq][topk]
+    uint32_t* status;
+};
+
+__device__ __forceinline__ int sparse_seq_len(const SparseParams& P, int b) {
+    int n = P.seq_lens[b];
+    if (n < 0 || n > P.max_seq_len) return -1;
+    return n;
+}
+
+// ---------------------------------------------------------------------------
+// Probe: grid (ceil(max_nblk / PROBE_BLOCKS_PER_CTA), nkv, B), 8 warps.  Lane
+// (row pr = lane/4, 32-element block bb = lane%4) of a warp loads the 32 bytes
+// of block bb of probe row pr, forms G int32 dots, and the 4 lanes of a row
+// combine them in the method's order (bb = 0, 1, 2, 3) into the exact score.
+// ---------------------------------------------------------------------------
+constexpr int PROBE_WARPS = 8;
+constexpr int PROBE_BLOCKS_PER_CTA = 64;
+
+template <int G>
+__global__ void __launch_bounds__(PROBE_WARPS * 32) kq8_probe_kernel(const SparseParams P) {
+    __shared__ __align__(16) int8_t qi[G][HD];
+    __shared__ float qsc[G][NB];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int nkv = P.cache.num_kv_heads, kv_bs = P.cache.kv_bs;
+    const int n = sparse_seq_len(P, b);
+    if (n < 0 || n <= 2 * P.block) return;  // gate: the exact path needs no probe
+    const int nblk = (n + P.block - 1) / P.block;
+    const int j0 = blockIdx.x * PROBE_BLOCKS_PER_CTA;
+    if (j0 >= nblk) return;
+    const int j1 = min(j0 + PROBE_BLOCKS_PER_CTA, nblk);
+
+    for (int g = warp; g < G; g += PROBE_WARPS) {
+        const float4 x =
+            reinterpret_cast<const float4*>(P.q + ((size_t)b * P.nq + (size_t)h * G + g) * HD)[lane];
+        float qs;
+        const uint32_t codes = quantize_q_lane(x, qs);
+        reinterpret_cast<uint32_t*>(qi[g])[lane] = codes;
+        if ((lane & 7) == 0) qsc[g][lane >> 3] = qs;
+    }
+    __syncthreads();
+
+    const int pr = lane >> 2, bb = lane & 3;
+    const int stride = P.block / P.probe;
+    uint4 qa[G], qb[G];
+    float qs[G];
+#pragma unroll
+    for (int g = 0; g < G; g++) {
+        qa[g] = *reinterpret_cast<const uint4*>(qi[g] + bb * 32);
+        qb[g] = *reinterpret_cast<const uint4*>(qi[g] + bb * 32 + 16);
+        qs[g] = qsc[g][bb];
+    }
+    const float scale = P.scale;
+
+    for (int j = j0 + warp; j < j1; j += PROBE_WARPS) {
+        float best[G];
+#pragma unroll
+        for (int g = 0; g < G; g++) best[g] = -INFINITY;
+        for (int p0 = 0; p0 < P.probe; p0 += 8) {
+            const int p = p0 + pr;
+            const int t = j * P.block + p * stride;
+            bool valid = (p < P.probe) && (t < n);
+            uint4 ka = make_uint4(0, 0, 0, 0), kb = ka;
+            float kst = 0.0f;
+            if (valid) {
+                const int32_t pg = P.page_table[(size_t)b * P.max_pages + t / kv_bs];
+                if (pg >= 0 && pg < P.cache.num_pages) {
+                    const int r = t % kv_bs;
+                    const int8_t* src = P.cache.k + kv_sub_off(pg, h, nkv, kv_bs, r / TILE) +
+                                        bb * 1024 + (r % TILE) * 32;
+                    ka = __ldg(reinterpret_cast<const uint4*>(src));
+                    kb = __ldg(reinterpret_cast<const uint4*>(src + 16));
+                    kst = __ldg(P.cache.kscale + scale_sub_off(pg, h, nkv, kv_bs, r / TILE) + r % TILE);
+                } else {
+                    valid = false;
+                    if (bb == 0 && P.status) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
+                }
+            }
+#pragma unroll
+            for (int g = 0; g < G; g++) {
+                int d = __dp4a((int)ka.x, (int)qa[g].x, 0);
+                d = __dp4a((int)ka.y, (int)qa[g].y, d);
+                d = __dp4a((int)ka.z, (int)qa[g].z, d);
+                d = __dp4a((int)ka.w, (int)qa[g].w, d);
+                d = __dp4a((int)kb.x, (int)qb[g].x, d);
+                d = __dp4a((int)kb.y, (int)qb[g].y, d);
+                d = __dp4a((int)kb.z, (int)qb[g].z, d);
+                d = __dp4a((int)kb.w, (int)qb[g].w, d);
+                const float x = __fmul_rn(i2f_exact(d), qs[g]);
+                // lanes 4pr+1..3 hand their block terms to lane 4pr, summed in order
+                const float x1 = __shfl_down_sync(0xffffffffu, x, 1);
+                const float x2 = __shfl_down_sync(0xffffffffu, x, 2);
+                const float x3 = __shfl_down_sync(0xffffffffu, x, 3);
+                float s = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(0.0f, x), x1), x2), x3);
+                s = __fmul_rn(__fmul_rn(s, __fmul_rn(kst, inv127())), scale);
+                if (!valid) s = -INFINITY;
+                // max over the 8 rows held by lanes 0, 4, ..., 28
+                s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 4));
+                s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 8));
+                s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 16));
+                // lanes with bb != 0 carried partial terms; only lane 0's row max counts
+                best[g] = fmaxf(best[g], __shfl_sync(0xffffffffu, s, 0));
+            }
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int g = 0; g < G; g++)
+                P.scores[((size_t)b * P.nq + (size_t)h * G + g) * P.max_nblk + j] = best[g];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Top-k + union: one CTA of 256 threads per (KV head, sequence).
+// ---------------------------------------------------------------------------
+constexpr int TOPK_THREADS = 256;
+
+// Order-preserving map of a float to uint32 (larger float -> larger key);
+// -0 and +0 map to the same key, so ties follow float equality.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t u = __float_as_uint(f == 0.0f ? 0.0f : f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive block-wide prefix sum of v over 256 threads; returns the prefix
+// and writes the total.  Uses `tmp` (>= 8 ints).
+__device__ __forceinline__ int block_excl_scan(int v, int* tmp, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) tmp[warp] = x;
+    __syncthreads();
+    int base = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < TOPK_THREADS / 32; w++) {
+        const int t = tmp[w];
+        if (w < warp) base += t;
+        tot += t;
+    }
+    __syncthreads();
+    total = tot;
+    return base + x - v;
+}
+
+template <int G>
+__global__ void __launch_bounds__(TOPK_THREADS) kq8_topk_kernel(const SparseParams P) {
+    __shared__ int hist[256];
+    __shared__ int scan_tmp[TOPK_THREADS / 32];
+    __shared__ uint32_t s_prefix;
+    __shared__ int s_kk;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int nkv = P.cache.num_kv_heads;
+    const int tid = threadIdx.x;
+    int n = sparse_seq_len(P, b);
+    if (n < 0) {
+        if (tid == 0 && h == 0) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
+        n = 0;
+    }
+    const int ntiles = (n + TILE - 1) / TILE;
+    const int m = P.block / TILE;  // tiles per block
+    int32_t* list = P.tile_list + (size_t)(b * nkv + h) * P.list_cap;
+    const bool gated = n <= 2 * P.block;
+
+    if (P.sel_blocks) {
+        for (int g = 0; g < G; g++) {
+            int32_t* sel = P.sel_blocks + ((size_t)b * P.nq + (size_t)h * G + g) * P.topk;
+            for (int i = tid; i < P.topk; i += TOPK_THREADS) sel[i] = -1;
+        }
+    }
+    if (gated) {  // exact path: every tile, every head
+        const int32_t all = (int32_t)(((1u << G) - 1u) << 24);
+        for (int i = tid; i < ntiles; i += TOPK_THREADS) list[i] = i | all;
+        if (tid == 0) P.list_len[b * nkv + h] = ntiles;
+        return;
+    }
+    const int nblk = (n + P.block - 1) / P.block;
+    uint8_t* masks = P.masks + (size_t)(b * nkv + h) * P.max_nblk;
+    for (int j = tid; j < nblk; j += TOPK_THREADS) masks[j] = 0;
+    __syncthreads();
+
+    for (int g = 0; g < G; g++) {
+        const float* sc = P.scores + ((size_t)b * P.nq + (size_t)h * G + g) * P.max_nblk;
+        int32_t* sel = P.sel_blocks ? P.sel_blocks + ((size_t)b * P.nq + (size_t)h * G + g) * P.topk
+                                    : nullptr;
+        const int k = min(P.topk, nblk);
+        uint32_t thr = 0;  // keys > thr are kept, plus the first kk keys == thr
+        int kk = 0;
+        if (k == nblk) {
+            thr = 0;
+            kk = nblk;  // every key >= 0: take all ties at key 0 too
+        } else {
+            // radix select of the k-th largest key, 8 bits at a time from the top
+            uint32_t prefix = 0, pmask = 0;
+            int rem = k;
+            for (int pass = 0; pass < 4; pass++) {
+                const int shift = 24 - 8 * pass;
+                hist[tid] = 0;
+                __syncthreads();
+                for (int j = tid; j < nblk; j += TOPK_THREADS) {
+                    const uint32_t u = order_key(sc[j]);
+                    if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255], 1);
+                }
+                __syncthreads();
+                // inclusive count from digit 255 downwards: thread t holds digit 255 - t
+                const int cnt = hist[255 - tid];
+                int tot;
+                const int excl = block_excl_scan(cnt, scan_tmp, tot);
+                if (excl < rem && excl + cnt >= rem) {
+                    s_prefix = prefix | ((uint32_t)(255 - tid) << shift);
+                    s_kk = rem - excl;
+                }
+                __syncthreads();
+                prefix = s_prefix;
+                rem = s_kk;
+                pmask |= 0xFFu << shift;
+                __syncthreads();
+            }
+            thr = prefix;
+            kk = rem;
+        }
+        // mark: key > thr, or key == thr among the first kk such keys by index
+        int ties_before = 0, kept_before = 0;
+        for (int base = 0; base < nblk; base += TOPK_THREADS) {
+            const int j = base + tid;
+            const uint32_t u = (j < nblk) ? order_key(sc[j]) : 0u;
+            const bool in = j < nblk;
+            const bool gt = in && (k == nblk || u > thr);
+            const bool eq = in && !gt && u == thr;
+            int tie_tot;
+            const int tie_rank = block_excl_scan(eq ? 1 : 0, scan_tmp, tie_tot) + ties_before;
+            const bool keep = gt || (eq && tie_rank < kk);
+            int keep_tot;
+            const int pos = block_excl_scan(keep ? 1 : 0, scan_tmp, keep_tot) + kept_before;
+            if (keep) {
+                masks[j] |= (uint8_t)(1u << g);
+                if (sel) sel[pos] = j;
+            }
+            ties_before += tie_tot;
+            kept_before += keep_tot;
+        }
+        __syncthreads();
+    }
+
+    // union over the G heads -> ascending tile list with per-entry head masks
+    int written = 0;
+    for (int base = 0; base < nblk; base += TOPK_THREADS) {
+        const int j = base + tid;
+        const uint32_t mk = (j < nblk) ? masks[j] : 0u;
+        const int cnt = mk ? min(m, ntiles - j * m) : 0;
+        int tot;
+        const int pos = block_excl_scan(cnt, scan_tmp, tot) + written;
+        for (int s = 0; s < cnt; s++) list[pos + s] = (j * m + s) | (int32_t)(mk << 24);
+        written += tot;
+    }
+    if (tid == 0) P.list_len[b * nkv + h] = written;
+}
+
+}  // namespace kq8

@@ -190,13 +190,13 @@ def _plant(wl: Workload, b: int, K: np.ndarray, qb: np.ndarray, n: int) -> None:
         u = qb[kh * G:(kh + 1) * G].astype(np.float64).sum(0)
         u /= np.linalg.norm(u)
         rr = _rng(_layer_seed(wl, 0, 12, b * 64 + kh))
-        for j in _planted_blocks(wl, b, kh, n):
-            t0, t1 = j * wl.block, min((j + 1) * wl.block, n)
-            for t in range(t0, t1):
-                x = rr.standard_normal(wl.hd)
-                x -= x.dot(u) * u
-                x /= np.linalg.norm(x)
-                K[t, kh] = (math.sqrt(wl.hd) * (0.8 * u + 0.6 * x)).astype(np.float32)
+        blocks = _planted_blocks(wl, b, kh, n)
+        rows = np.concatenate([np.arange(j * wl.block, min((j + 1) * wl.block, n))
+                               for j in blocks])
+        x = rr.standard_normal((rows.size, wl.hd))
+        x -= (x @ u)[:, None] * u[None, :]
+        x /= np.linalg.norm(x, axis=1, keepdims=True)
+        K[rows, kh] = (math.sqrt(wl.hd) * (0.8 * u[None, :] + 0.6 * x)).astype(np.float32)
 
 
 def planted_blocks(wl: Workload, b: int, kh: int) -> np.ndarray:

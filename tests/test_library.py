@@ -1,0 +1,109 @@
+"""Host-side checks of libkq8 that need no GPU: the library loads, exports
+every entry point include/kq8.h declares, and rejects bad arguments before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from query_decode_attention_gb300 import build
+    build.build()
+    from query_decode_attention_gb300 import kq8
+    return kq8
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "kq8.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kq8_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("kq8_append_kv", "kq8_decode_attn", "kq8_sparse_decode_attn",
+              "kq8_decode_workspace_bytes", "kq8_sparse_decode_workspace_bytes",
+              "kq8_workspace_init", "kq8_read_status", "kq8_strerror", "kq8_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib._build.LIB)
+    for n in declared_functions():
+        assert hasattr(so, n), n
+
+
+def test_strerror_and_version(lib):
+    assert lib.kq8_version() >= 10000
+    assert lib.kq8_strerror(0) == "ok"
+    assert "workspace" in lib.kq8_strerror(lib.KQ8_ERR_WORKSPACE)
+    assert lib.kq8_strerror(-99) == "unknown error"
+
+
+def test_workspace_sizes_are_sane(lib):
+    small = lib.kq8_decode_workspace_bytes(1, 16, 8, 256)
+    assert small >= 256 and small % 256 == 0
+    big = lib.kq8_decode_workspace_bytes(64, 32, 8, 32768)
+    assert big > small
+    assert lib.kq8_decode_workspace_bytes(-1, 16, 8, 256) == 0
+    sp = lib.kq8_sparse_decode_workspace_bytes(16, 16, 8, 65536, 32, 32)
+    # scores of every block per query head fit
+    assert sp >= 16 * 16 * (65536 // 32) * 4
+    assert lib.kq8_sparse_decode_workspace_bytes(16, 16, 8, 65536, 48, 32) == 0  # block % 32
+
+
+def _cache_struct(lib, **kw):
+    c = dict(k=16, v=16, kscale=16, vscale=16, num_pages=4, kv_bs=32, num_kv_heads=8,
+             head_dim=128)
+    c.update(kw)
+    return lib.kq8_cache_t(c["k"], c["v"], c["kscale"], c["vscale"], c["num_pages"], c["kv_bs"],
+                           c["num_kv_heads"], c["head_dim"])
+
+
+def _decode(lib, cache, B=1, nq=16, max_seq_len=64, max_pages=2, ws=None, ws_bytes=1 << 20,
+            out=256, q=256, pt=256, sl=256):
+    so = lib._lib
+    return so.kq8_decode_attn(out, q, ctypes.byref(cache), pt, max_pages, sl, max_seq_len, B, nq,
+                              0.1, ws, ws_bytes, None)
+
+
+def test_argument_validation_without_device(lib):
+    ok = _cache_struct(lib)
+    # fake 256-aligned addresses: validation fails before any launch
+    assert _decode(lib, _cache_struct(lib, head_dim=64)) == lib.KQ8_ERR_UNSUPPORTED
+    assert _decode(lib, _cache_struct(lib, kv_bs=48)) == lib.KQ8_ERR_UNSUPPORTED
+    assert _decode(lib, _cache_struct(lib, k=17)) == lib.KQ8_ERR_INVALID_ARG
+    assert _decode(lib, _cache_struct(lib, v=0)) == lib.KQ8_ERR_INVALID_ARG
+    assert _decode(lib, ok, nq=12) == lib.KQ8_ERR_UNSUPPORTED          # nq % nkv
+    assert _decode(lib, ok, nq=8 * 9) == lib.KQ8_ERR_UNSUPPORTED       # G = 9
+    assert _decode(lib, ok, max_seq_len=100, max_pages=2) == lib.KQ8_ERR_INVALID_ARG
+    assert _decode(lib, ok, B=-1) == lib.KQ8_ERR_INVALID_ARG
+    assert _decode(lib, ok, q=260) == lib.KQ8_ERR_INVALID_ARG          # q not 16-B aligned
+    assert _decode(lib, ok, ws=None) == lib.KQ8_ERR_WORKSPACE
+    assert _decode(lib, ok, ws=512 + 16) == lib.KQ8_ERR_WORKSPACE      # misaligned
+    assert _decode(lib, ok, ws=512, ws_bytes=64) == lib.KQ8_ERR_WORKSPACE
+    assert _decode(lib, ok, B=0, ws=512) == lib.KQ8_OK                 # nothing to do
+    so = lib._lib
+    assert so.kq8_append_kv(ctypes.byref(ok), 256, 256, 256, -1, None, None) == lib.KQ8_ERR_INVALID_ARG
+    assert so.kq8_append_kv(ctypes.byref(ok), 256, 256, 256, 0, None, None) == lib.KQ8_OK
+    assert so.kq8_append_kv(None, 256, 256, 256, 1, None, None) == lib.KQ8_ERR_INVALID_ARG
+    sp = so.kq8_sparse_decode_attn
+    args = (256, 256, ctypes.byref(ok), 256, 2, 256, 64, 1, 16, ctypes.c_float(0.1))
+    assert sp(*args, 32, 32, 33, None, 512, 1 << 20, None) == lib.KQ8_ERR_UNSUPPORTED  # probe > block
+    assert sp(*args, 16, 32, 8, None, 512, 1 << 20, None) == lib.KQ8_ERR_UNSUPPORTED   # block < 32
+    assert sp(*args, 32, 0, 8, None, 512, 1 << 20, None) == lib.KQ8_ERR_UNSUPPORTED    # topk 0
+
+
+def test_product_path_has_no_oracle_or_cpu_fallback():
+    pkg = os.path.join(ROOT, "query_decode_attention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "kq8o_" not in text, f
