@@ -40,7 +40,7 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kq8", choices=["kq8", "reference"])
     ap.add_argument("--layers", type=int, default=36)
@@ -90,7 +90,9 @@ def committed_traffic(kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling.  Started before the warm-up (NVML
+    start-up can stall GPU submission); only the samples taken between
+    mark_start() and mark_end() -- the timed region -- are summarised."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -100,6 +102,8 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.start = 0
+        self.end = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(prefix="kq8_clocks_", suffix=".csv")
@@ -107,12 +111,23 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
-        time.sleep(0.3)
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < 20:
+            if os.path.getsize(self.path) > 0 or self.proc.poll() is not None:
+                break
+            time.sleep(0.05)
         return self
+
+    def mark_start(self):
+        self.start = os.path.getsize(self.path) if self.path else 0
+
+    def mark_end(self):
+        time.sleep(0.06)  # let the sample covering the end land
+        self.end = os.path.getsize(self.path) if self.path else 0
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -125,80 +140,96 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons = [], None, set()
-        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
-                 "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    smax = float(parts[2])
-                except ValueError:
-                    continue
-                for nm, val in zip(names[1:], parts[5:9]):
-                    if val.lower() == "active":
-                        reasons.add(nm)
+            text = f.read()
         os.unlink(self.path)
+        region = text[self.start:self.end] if self.end is not None else text[self.start:]
+        sm, smax, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in region.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
 
 
 # ---------------------------------------------------------------------------
 # CPU oracle timing (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample_gbs(wl, seqs, nthreads):
-    """Time the oracle's exact decode over sequences `seqs` of layer 0 (all
-    query heads).  Returns (GB/s, seconds, bytes)."""
-    import oracle
-    from query_decode_attention_gb300 import workloads as W
-    q = W.host_q(wl)[seqs]
-    k8s, kss, v8s, vss = [], [], [], []
-    nbytes = 0
-    for b in seqs:
-        K, V = W.host_kv(wl, b)
-        k8, ks = oracle.kv_quantize_rows(K)
-        v8, vs = oracle.kv_quantize_rows(V)
-        k8s.append(k8)
-        kss.append(ks)
-        v8s.append(v8)
-        vss.append(vs)
-        nbytes += int(wl.seq_lens[b]) * wl.nkv * (2 * wl.hd + 8)
-    t0 = time.perf_counter()
-    oracle.decode_batch(q, k8s, kss, v8s, vss, wl.scale, kv_bs=wl.kv_bs, nthreads=nthreads)
-    dt = time.perf_counter() - t0
-    return nbytes / dt / 1e9, dt, nbytes
+class OracleSample:
+    """Sequences `seqs` of layer 0 of a workload, quantised by the oracle, ready
+    to time the oracle's exact decode over them (all query heads)."""
+
+    def __init__(self, wl, seqs):
+        import oracle
+        from query_decode_attention_gb300 import workloads as W
+        oracle.build()
+        self.oracle = oracle
+        self.wl = wl
+        self.seqs = list(seqs)
+        self.q = W.host_q(wl)[self.seqs]
+        self.k8, self.ks, self.v8, self.vs = [], [], [], []
+        self.nbytes = 0
+        for b in self.seqs:
+            K, V = W.host_kv(wl, b)
+            k8, ks = oracle.kv_quantize_rows(K)
+            v8, vs = oracle.kv_quantize_rows(V)
+            self.k8.append(k8)
+            self.ks.append(ks)
+            self.v8.append(v8)
+            self.vs.append(vs)
+            self.nbytes += int(wl.seq_lens[b]) * wl.nkv * (2 * wl.hd + 8)
+
+    def run(self, nthreads):
+        """One pass; returns seconds."""
+        t0 = time.perf_counter()
+        self.oracle.decode_batch(self.q, self.k8, self.ks, self.v8, self.vs, self.wl.scale,
+                                 kv_bs=self.wl.kv_bs, nthreads=nthreads)
+        return time.perf_counter() - t0
+
+    def describe(self):
+        lens = [int(self.wl.seq_lens[b]) for b in self.seqs]
+        return (f"oracle exact decode of sequences {self.seqs[0]}..{self.seqs[-1]} of the "
+                f"{self.wl.B} (n = {min(lens)}..{max(lens)}, all {self.wl.nq} query heads, "
+                f"layer 0, {self.nbytes / 1e6:.0f} MB of KV), OpenMP over (sequence, head)")
+
+
+def oracle_threads():
+    return max(1, os.cpu_count() or 1)
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the CPU oracle, as it stands, on a bounded sample."""
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample of
+    the same workload per step."""
     if rank != 0:
         return
     from query_decode_attention_gb300 import workloads as W
-    import oracle
-    oracle.build()
     wl = W.serving_8b(B=args.batch, layers=args.layers)
-    threads = max(1, os.cpu_count() or 1)
-    order = np.argsort(wl.seq_lens)[: max(1, min(4, wl.B))]  # shortest: bounded work
-    seqs = [int(order[i % len(order)]) for i in range(1)]
+    threads = oracle_threads()
+    smp = OracleSample(wl, range(min(4, wl.B)))
     for _ in range(args.warmup):
-        oracle_sample_gbs(wl, seqs, threads)
-    vals, secs = [], 0.0
-    for _ in range(args.steps):
-        g, dt, nb = oracle_sample_gbs(wl, seqs, threads)
-        vals.append(g)
-        secs += dt
-    v = statistics.median(vals)
-    sample = (f"exact decode of {len(seqs)} sequence(s) x 32 query heads (n={int(wl.seq_lens[seqs[0]])}),"
-              f" layer 0 of the {wl.name} workload, per step")
+        smp.run(threads)
+    secs = sum(smp.run(threads) for _ in range(args.steps))
+    v = smp.nbytes * args.steps / secs / 1e9
+    sample = smp.describe() + ", one pass per step"
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1e3 * secs / max(1, args.steps), 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "int8xint8->int32, fp32 softmax",
-            "data": "synthetic", "config": {"workload": wl.name, "sample": sample},
+            "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8xint8->int32 scores, fp32 softmax/accumulate", "data": "synthetic",
+            "config": {"workload": wl.name, "sample": sample},
             "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -276,6 +307,7 @@ def main():
             if timers is not None:
                 timers[l][1].record(stream)
 
+    clk = ClockSampler(local).__enter__()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -286,17 +318,19 @@ def main():
     timers = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(L)] for _ in range(args.steps)]
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        if pg:
-            pg.barrier()
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        for s in range(args.steps):
-            step(timers[s])
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        if pg:
-            pg.barrier()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    clk.mark_start()
+    ev0.record(stream)
+    for s in range(args.steps):
+        step(timers[s])
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk.mark_end()
+    if pg:
+        pg.barrier()
+    clk.__exit__(None, None, None)
     clocks = clk.summary()
     elapsed_ms = ev0.elapsed_time(ev1)
     if pg:
@@ -489,23 +523,18 @@ def extras(dev, kq8, paged, W, peak):
     return res
 
 
-def cpu_baseline(wl):
-    import oracle
-    oracle.build()
-    threads = max(1, os.cpu_count() or 1)
-    order = list(np.argsort(wl.seq_lens))
-    seqs, total_s = [], 0.0
-    g, dt, nb = 0.0, 0.0, 0
-    # grow the sample until ~10 s of CPU time (bounded to 8 sequences)
-    for b in order[:8]:
-        seqs.append(int(b))
-        g, dt, nb = oracle_sample_gbs(wl, seqs, threads)
-        if dt > 3.0:
-            break
-    return {"value": round(g, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"exact decode of {len(seqs)} of the {wl.B} sequences (all 32 query heads, "
-                      f"layer 0, {nb / 1e6:.1f} MB of KV), OpenMP over (sequence, head)",
-            "seconds": round(dt, 2)}
+def cpu_baseline(wl, seconds=10.0):
+    """The oracle timed on the host cores on a bounded sample of the workload:
+    the first 8 sequences of layer 0, passes repeated for about `seconds`."""
+    threads = oracle_threads()
+    smp = OracleSample(wl, range(min(8, wl.B)))
+    smp.run(threads)
+    passes, secs = 0, 0.0
+    while secs < seconds and passes < 1000:
+        secs += smp.run(threads)
+        passes += 1
+    return {"value": round(smp.nbytes * passes / secs / 1e9, 4), "unit": UNIT, "cores": threads,
+            "kind": "oracle", "sample": smp.describe() + f", {passes} passes in {secs:.1f} s"}
 
 
 if __name__ == "__main__":
