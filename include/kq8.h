@@ -146,6 +146,30 @@ int kq8_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
                     size_t workspace_bytes, kq8_stream_t stream);
 
 /*
+ * Allocation-free variant of kq8_decode_attn, for callers that may not allocate
+ * device memory: code running inside another runtime's allocator or launch path
+ * (a cudaMalloc there can re-enter that runtime, and it may synchronise the
+ * device and stall every other stream), or serving loops that forbid device
+ * allocation after start-up.  The method's pages have no counterpart: this is a
+ * deployment convenience.
+ * Same arguments and result as kq8_decode_attn, without the workspace: the
+ * partials go to a scratch array of KQ8_NOALLOC_SCRATCH_BYTES compiled into the
+ * library, which every GPU that loads the library holds until the process exits.
+ * Returns KQ8_ERR_WORKSPACE when these sizes need more scratch than that (see
+ * kq8_decode_workspace_bytes).  Calls no allocating routine.
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream capture.
+ * Every call uses the same array: calls that overlap on the GPU (other streams,
+ * other threads, the same device) race and corrupt each other's results.
+ * Device-side status bits are not reported by this entry point.
+ */
+#define KQ8_NOALLOC_SCRATCH_BYTES (32u << 20)
+int kq8_decode_attn_noalloc(float* out, const float* q, const kq8_cache_t* cache,
+                            const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                            int32_t max_seq_len, int32_t B, int32_t nq, float scale,
+                            kq8_stream_t stream);
+
+/*
  * Bytes of workspace kq8_sparse_decode_attn needs (>= 256).
  */
 size_t kq8_sparse_decode_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len,

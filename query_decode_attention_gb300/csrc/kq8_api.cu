@@ -338,3 +338,66 @@ int kq8_debug_probe_scores(float* scores, const float* q, const kq8_cache_t* cac
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free exact decode.  Some callers may not allocate device memory at
+// all: plugins that run inside another runtime's allocator or launch path
+// (cudaMalloc there can re-enter that runtime, and it may synchronise the
+// device, stalling every other stream), and serving loops that forbid device
+// allocation once they have started.  For them, kq8_decode_attn_noalloc uses a
+// fixed scratch array compiled into this library instead of a caller-provided
+// workspace.  The array lives in every device's global memory from the moment
+// the library is loaded until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace kq8 {
+namespace {
+
+constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)KQ8_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+
+// Device address of the scratch array on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device, with that device current, and cached.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KQ8_ERR_CUDA;
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return KQ8_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return KQ8_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return KQ8_OK;
+}
+
+}  // namespace
+}  // namespace kq8
+
+extern "C" int kq8_decode_attn_noalloc(float* out, const float* q, const kq8_cache_t* cache,
+                                       const int32_t* page_table, int32_t max_pages,
+                                       const int32_t* seq_lens, int32_t max_seq_len, int32_t B,
+                                       int32_t nq, float scale, kq8_stream_t stream) {
+    int rc = check_decode(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq);
+    if (rc) return rc;
+    const int nkv = cache->num_kv_heads;
+    const Plan plan = plan_exact(B, nq, nkv, max_seq_len);
+    if (plan.total > NOALLOC_SCRATCH_BYTES) return KQ8_ERR_WORKSPACE;  // sizes beyond the array
+    if (B == 0) return KQ8_OK;
+    void* ws = nullptr;
+    rc = noalloc_scratch(&ws);
+    if (rc) return rc;
+    // Nothing in the scratch has to start at zero: every partial is written
+    // before the merge reads it, and the status word only collects error bits
+    // that this entry point does not report.
+    AttnParams p = attn_params(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq,
+                               scale, plan, ws);
+    return launch_attn(p, nq / nkv, false, B, nkv, (cudaStream_t)stream);
+}

@@ -64,6 +64,8 @@ _lib.kq8_decode_attn.argtypes = [_P, _P, _CP, _P, _I32, _P, _I32, _I32, _I32, ct
                                  _SZ, _P]
 _lib.kq8_sparse_decode_attn.argtypes = [_P, _P, _CP, _P, _I32, _P, _I32, _I32, _I32,
                                         ctypes.c_float, _I32, _I32, _I32, _P, _P, _SZ, _P]
+_lib.kq8_decode_attn_noalloc.argtypes = [_P, _P, _CP, _P, _I32, _P, _I32, _I32, _I32,
+                                         ctypes.c_float, _P]
 _lib.kq8_read_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), _P]
 _lib.kq8_strerror.argtypes = [ctypes.c_int]
 _lib.kq8_strerror.restype = ctypes.c_char_p
@@ -211,6 +213,19 @@ def kq8_decode_attn(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
                                 max_pages, _ptr(seq_lens), int(max_seq_len), B, nq, float(scale),
                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 _stream(stream)), "kq8_decode_attn")
+
+
+def kq8_decode_attn_noalloc(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
+                            page_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                            scale: float, stream=None) -> None:
+    """kq8_decode_attn without a workspace, for callers that may not allocate
+    device memory (the library's fixed scratch array is used instead; calls
+    that overlap on the GPU race)."""
+    B, nq, max_pages = _decode_args(out, q, cache, page_table, seq_lens)
+    _check(_lib.kq8_decode_attn_noalloc(_ptr(out), _ptr(q), ctypes.byref(cache.struct),
+                                        _ptr(page_table), max_pages, _ptr(seq_lens),
+                                        int(max_seq_len), B, nq, float(scale), _stream(stream)),
+           "kq8_decode_attn_noalloc")
 
 
 def kq8_sparse_decode_attn(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
