@@ -30,11 +30,11 @@ int device_sms() {
 
 // Split of each (sequence, KV head) list of `tiles_max` 32-token tiles into
 // chunks of `chunk_tiles` tiles (a multiple of the CTA's 4 warps).  The chunk
-// is sized so that B * nkv * (chunks) CTAs give about four waves of two CTAs
+// is sized so that B * nkv * (chunks) CTAs give about four waves of three CTAs
 // per SM, between 4 and 64 tiles (128 to 2048 tokens).
 void chunking(int64_t B, int64_t nkv, int64_t tiles_max, int sms, int& ct, int& nch) {
     const int64_t total = B * nkv * tiles_max;
-    const int64_t target = (int64_t)sms * 2 * 4;
+    const int64_t target = (int64_t)sms * 3 * 4;
     int64_t c = (total + target - 1) / (target > 0 ? target : 1);
     c = (c + ATTN_WARPS - 1) / ATTN_WARPS * ATTN_WARPS;
     if (c < ATTN_WARPS) c = ATTN_WARPS;

@@ -4,12 +4,10 @@
 
 namespace kq8 {
 
-constexpr int ATTN_STAGES = 3;
-
 template <int G, bool SPARSE>
 static int launch_attn_g(const AttnParams& p, int B, int nkv, cudaStream_t s) {
-    auto kern = kq8_attn_kernel<G, ATTN_STAGES, SPARSE>;
-    const size_t smem = sizeof(AttnSmem<G, ATTN_STAGES>);
+    auto kern = kq8_attn_kernel<G, SPARSE>;
+    const size_t smem = sizeof(AttnSmem<G>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return KQ8_ERR_CUDA;
@@ -45,14 +43,14 @@ int launch_attn(const AttnParams& p, int G, bool sparse, int B, int nkv, cudaStr
 
 size_t attn_smem_bytes(int G) {
     switch (G) {
-        case 1: return sizeof(AttnSmem<1, ATTN_STAGES>);
-        case 2: return sizeof(AttnSmem<2, ATTN_STAGES>);
-        case 3: return sizeof(AttnSmem<3, ATTN_STAGES>);
-        case 4: return sizeof(AttnSmem<4, ATTN_STAGES>);
-        case 5: return sizeof(AttnSmem<5, ATTN_STAGES>);
-        case 6: return sizeof(AttnSmem<6, ATTN_STAGES>);
-        case 7: return sizeof(AttnSmem<7, ATTN_STAGES>);
-        default: return sizeof(AttnSmem<8, ATTN_STAGES>);
+        case 1: return sizeof(AttnSmem<1>);
+        case 2: return sizeof(AttnSmem<2>);
+        case 3: return sizeof(AttnSmem<3>);
+        case 4: return sizeof(AttnSmem<4>);
+        case 5: return sizeof(AttnSmem<5>);
+        case 6: return sizeof(AttnSmem<6>);
+        case 7: return sizeof(AttnSmem<7>);
+        default: return sizeof(AttnSmem<8>);
     }
 }
 

@@ -5,20 +5,26 @@
 // the chunk's tiles w, w+4, ...  All G query heads of KV head h are handled by
 // the same warp, so each K/V byte is read from HBM once for the whole group.
 //
-// Per warp, a ring of NS shared-memory stages is filled by bulk-async copies
-// (one elected lane issues them, completion on an mbarrier per stage) while
-// the warp computes on older stages.  Per tile:
+// Per warp, a ring of ATTN_STAGES shared-memory stages is filled by bulk-async
+// copies (one lane issues them; completion on an mbarrier per stage) while the
+// warp computes on the previous stage.  The page ids of the warp's tiles are
+// fetched once, one per lane, so issuing a copy never waits on memory.  Per
+// tile:
 //   score phase (lane = token): int32 block dots of the token's K row with
-//     the G int8 query rows (dp4a), the fp32 score in the exact order of the
-//     method, tile max across the warp, online-softmax rescale when the
-//     running max grows, w = exp(s - M);
+//     the G int8 query rows (dp4a), the fp32 score in the method's order on
+//     pairs of heads (packed fp32 ops, each lane still rounded separately),
+//     moved to base 2; a warp vote checks whether any score exceeds the
+//     running max by more than RESCALE_SLACK and only then reduces the tile
+//     max and rescales the warp's state (the online-softmax rescale of
+//     article 9-2 §1, done lazily: between rescales the weights may exceed 1
+//     by at most 2^RESCALE_SLACK, which fp32 absorbs); w = 2^(s - M);
 //   value phase (lane = 16 bytes of a V row, 4 rows per instruction): int8 ->
 //     fp32 by byte permutes and a packed subtract, acc += v * (w * vs) with
 //     packed FMAs.
 // The 4 warps' (M, S, acc) are merged in shared memory; a chunk that covers
 // the whole sequence writes out = acc / S directly, others write an
 // unnormalised partial (M, S, acc) that kq8_merge_kernel combines by its
-// log-sum-exp (the same algebra as the online rescale, article 9-2 §1).
+// log-sum-exp (the same algebra as the online rescale).
 #pragma once
 
 #include "kq8_common.cuh"
@@ -27,6 +33,11 @@ namespace kq8 {
 
 constexpr int ATTN_WARPS = 4;
 constexpr int ATTN_THREADS = ATTN_WARPS * 32;
+constexpr int ATTN_STAGES = 2;
+constexpr int MAX_WARP_TILES = 32;     // tiles per warp per chunk, one per lane
+constexpr int MAX_CHUNK_TILES = ATTN_WARPS * MAX_WARP_TILES;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float RESCALE_SLACK = 8.0f;  // base-2 units
 
 struct AttnParams {
     float* out;
@@ -38,10 +49,10 @@ struct AttnParams {
     int32_t max_seq_len;
     int32_t B, nq;
     float scale;
-    int32_t chunk_tiles;   // multiple of ATTN_WARPS
+    int32_t chunk_tiles;   // multiple of ATTN_WARPS, <= MAX_CHUNK_TILES
     int32_t num_chunks;    // grid.x
     float* part_acc;       // [B][nq][num_chunks][HD]
-    float2* part_ms;       // [B][nq][num_chunks] (M, S)
+    float2* part_ms;       // [B][nq][num_chunks] (M in base 2, S)
     uint32_t* status;
     // block-sparse tile lists (SPARSE only): entry = tile | head_mask << 24
     const int32_t* tile_list;  // [B][nkv][list_cap]
@@ -51,20 +62,48 @@ struct AttnParams {
 
 template <int G>
 struct AttnShape {
-    static constexpr int E = (G <= 4) ? 16 : 8;        // V elements per lane
-    static constexpr int NC = HD / E;                   // lanes per V row
-    static constexpr int TG = 32 / NC;                  // V rows per instruction
-    static constexpr int GP = (G <= 4) ? 4 : 8;         // padded heads in p rows
+    static constexpr int E = (G <= 4) ? 16 : 8;  // V elements per lane
+    static constexpr int NC = HD / E;            // lanes per V row
+    static constexpr int TG = 32 / NC;           // V rows per instruction
+    static constexpr int GP = (G + 1) / 2;       // head pairs
+    static constexpr int MIN_CTAS = (G <= 4) ? 3 : 2;
 };
 
-template <int G, int NS>
+template <int G>
 struct AttnSmem {
-    alignas(128) uint8_t stage[ATTN_WARPS][NS][STAGE_BYTES];
-    alignas(16) float p[ATTN_WARPS][TILE][AttnShape<G>::GP];
+    alignas(128) uint8_t stage[ATTN_WARPS][ATTN_STAGES][STAGE_BYTES];
+    // per token: (p_g, p_g, p_g+1, p_g+1) for each head pair, p = w * vs
+    alignas(16) float4 p[ATTN_WARPS][TILE][AttnShape<G>::GP];
     alignas(16) int8_t qi[G][HD];
     alignas(16) float qsc[G][NB];
-    alignas(8) uint64_t bar[ATTN_WARPS][NS];
+    alignas(8) uint64_t bar[ATTN_WARPS][ATTN_STAGES];
 };
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Four int8 codes in one word -> two float pairs, exactly: flip the sign bits
+// (offset binary u = c + 128), drop each byte into the mantissa of 2^23 with a
+// byte permute and subtract 2^23 + 128 with one packed add per pair.
+__device__ __forceinline__ void i8x4_to_f2(uint32_t w, float2& a, float2& b) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float2 bias = make_float2(-8388736.0f, -8388736.0f);
+    a = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
+                               __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541))),
+                   bias);
+    b = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
+                               __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543))),
+                   bias);
+}
+
+// Two int32 dots (|d| < 2^22) -> a float pair, exactly.
+__device__ __forceinline__ float2 i2f_pair(int d0, int d1) {
+    return __fadd2_rn(make_float2(__int_as_float(0x4B400000 + d0), __int_as_float(0x4B400000 + d1)),
+                      make_float2(-12582912.0f, -12582912.0f));
+}
 
 // Number of list entries (tiles) of sequence b / KV head h.
 template <bool SPARSE>
@@ -79,13 +118,15 @@ __device__ __forceinline__ int valid_seq_len(const AttnParams& P, int b) {
     return n;
 }
 
-template <int G, int NS, bool SPARSE>
-__global__ void __launch_bounds__(ATTN_THREADS, 2) kq8_attn_kernel(const AttnParams P) {
+template <int G, bool SPARSE>
+__global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
+    kq8_attn_kernel(const AttnParams P) {
     using Sh = AttnShape<G>;
     constexpr int E = Sh::E, NC = Sh::NC, TG = Sh::TG, GP = Sh::GP;
     constexpr int EP = E / 2;  // float2 pairs per head per lane
+    constexpr int NS = ATTN_STAGES;
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    AttnSmem<G, NS>& S = *reinterpret_cast<AttnSmem<G, NS>*>(smem_raw);
+    AttnSmem<G>& S = *reinterpret_cast<AttnSmem<G>*>(smem_raw);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -102,7 +143,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2) kq8_attn_kernel(const AttnPar
     if (chunk >= nch) return;
     const int e0 = chunk * P.chunk_tiles;
     const int e1 = min(e0 + P.chunk_tiles, entries);
-    const int32_t* list = SPARSE ? P.tile_list + (size_t)(b * nkv + h) * P.list_cap : nullptr;
+    const int mine = (e1 - e0 > warp) ? (e1 - e0 - warp + ATTN_WARPS - 1) / ATTN_WARPS : 0;
 
     // ---- prologue: quantise the G query heads once (article 9-2 §2 seg. 1)
     for (int g = warp; g < G; g += ATTN_WARPS) {
@@ -113,84 +154,86 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2) kq8_attn_kernel(const AttnPar
         reinterpret_cast<uint32_t*>(S.qi[g])[lane] = codes;
         if ((lane & 7) == 0) S.qsc[g][lane >> 3] = qs;
     }
+    // ---- this warp's tiles, one per lane: tile index, head mask, page (-1 if bad)
+    int my_tile = 0;
+    uint32_t my_mask = 0;
+    int32_t my_page = -1;
+    if (lane < mine) {
+        const int e = e0 + warp + ATTN_WARPS * lane;
+        if (SPARSE) {
+            const int32_t v = P.tile_list[(size_t)(b * nkv + h) * P.list_cap + e];
+            my_tile = v & 0xFFFFFF;
+            my_mask = (uint32_t)v >> 24;
+        } else {
+            my_tile = e;
+            my_mask = 0xFFu;
+        }
+        const int32_t pg = P.page_table[(size_t)b * P.max_pages + my_tile / subs];
+        if (pg >= 0 && pg < P.cache.num_pages) {
+            my_page = pg;
+        } else {
+            atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
+        }
+    }
     if (lane == 0)
         for (int s = 0; s < NS; s++) mbar_init(&S.bar[warp][s], 1);
     fence_barrier_init();
     __syncthreads();
 
-    const int mine = (e1 - e0 > warp) ? (e1 - e0 - warp + ATTN_WARPS - 1) / ATTN_WARPS : 0;
     const uint64_t pol = l2_evict_first_policy();
-
-    // entry i of this warp -> (tile, head mask, page); page < 0 when invalid
-    auto entry_of = [&](int i, int& tile, uint32_t& mask) {
-        const int e = e0 + warp + ATTN_WARPS * i;
-        if (SPARSE) {
-            const int32_t v = list[e];
-            tile = v & 0xFFFFFF;
-            mask = (uint32_t)v >> 24;
-        } else {
-            tile = e;
-            mask = 0xFFu;
+    // all lanes call this (it shuffles); lane 0 issues the stage's copies
+    auto issue = [&](int i) {
+        const int tile = __shfl_sync(0xffffffffu, my_tile, i);
+        const int32_t pg = __shfl_sync(0xffffffffu, my_page, i);
+        if (lane == 0) {
+            uint64_t* bar = &S.bar[warp][i % NS];
+            if (pg < 0) {
+                mbar_arrive_expect_tx(bar, 0);  // completes the phase with no data
+            } else {
+                const int sub = tile % subs;
+                uint8_t* st = S.stage[warp][i % NS];
+                const size_t kvo = kv_sub_off(pg, h, nkv, kv_bs, sub);
+                const size_t so = scale_sub_off(pg, h, nkv, kv_bs, sub);
+                mbar_arrive_expect_tx(bar, STAGE_BYTES);
+                bulk_g2s(st, P.cache.k + kvo, SUB_K_BYTES, bar, pol);
+                bulk_g2s(st + SUB_K_BYTES, P.cache.v + kvo, SUB_V_BYTES, bar, pol);
+                bulk_g2s(st + SUB_K_BYTES + SUB_V_BYTES, P.cache.kscale + so, SUB_S_BYTES, bar,
+                         pol);
+                bulk_g2s(st + SUB_K_BYTES + SUB_V_BYTES + SUB_S_BYTES, P.cache.vscale + so,
+                         SUB_S_BYTES, bar, pol);
+            }
         }
     };
-    auto page_of = [&](int tile) -> int32_t {
-        const int32_t pg = P.page_table[(size_t)b * P.max_pages + tile / subs];
-        return (pg >= 0 && pg < P.cache.num_pages) ? pg : -1;
-    };
-    auto issue = [&](int i) {  // lane 0 only
-        int tile;
-        uint32_t mask;
-        entry_of(i, tile, mask);
-        const int32_t pg = page_of(tile);
-        uint64_t* bar = &S.bar[warp][i % NS];
-        if (pg < 0) {
-            atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
-            mbar_arrive_expect_tx(bar, 0);  // completes the phase with no data
-            return;
-        }
-        const int sub = tile % subs;
-        uint8_t* st = S.stage[warp][i % NS];
-        const size_t kvo = kv_sub_off(pg, h, nkv, kv_bs, sub);
-        const size_t so = scale_sub_off(pg, h, nkv, kv_bs, sub);
-        mbar_arrive_expect_tx(bar, STAGE_BYTES);
-        bulk_g2s(st, P.cache.k + kvo, SUB_K_BYTES, bar, pol);
-        bulk_g2s(st + SUB_K_BYTES, P.cache.v + kvo, SUB_V_BYTES, bar, pol);
-        bulk_g2s(st + SUB_K_BYTES + SUB_V_BYTES, P.cache.kscale + so, SUB_S_BYTES, bar, pol);
-        bulk_g2s(st + SUB_K_BYTES + SUB_V_BYTES + SUB_S_BYTES, P.cache.vscale + so, SUB_S_BYTES,
-                 bar, pol);
-    };
+    for (int i = 0; i < NS && i < mine; i++) issue(i);
 
-    if (lane == 0)
-        for (int i = 0; i < NS && i < mine; i++) issue(i);
-
-    float M[G], Sl[G];
+    float M2[G], Sl[G];
     float2 acc[G][EP];
 #pragma unroll
     for (int g = 0; g < G; g++) {
-        M[g] = M_INIT;
+        M2[g] = M_INIT;
         Sl[g] = 0.0f;
 #pragma unroll
         for (int e = 0; e < EP; e++) acc[g][e] = make_float2(0.0f, 0.0f);
     }
-    float qsc_r[G][NB];
+    float2 qsc2[GP][NB];  // block scales of head pairs (2gp, 2gp+1)
 #pragma unroll
-    for (int g = 0; g < G; g++)
+    for (int gp = 0; gp < GP; gp++)
 #pragma unroll
-        for (int bb = 0; bb < NB; bb++) qsc_r[g][bb] = S.qsc[g][bb];
+        for (int bb = 0; bb < NB; bb++)
+            qsc2[gp][bb] = make_float2(S.qsc[2 * gp][bb], S.qsc[min(2 * gp + 1, G - 1)][bb]);
+    const float sc2 = P.scale * LOG2E;  // softmax scale and the move to base 2
 
-    const float scale = P.scale;
     bool failed = false;
     int i = 0;
     for (; i < mine; i++) {
-        int tile;
-        uint32_t mask;
-        entry_of(i, tile, mask);
-        const bool ok_page = page_of(tile) >= 0;
+        const int tile = __shfl_sync(0xffffffffu, my_tile, i);
+        const uint32_t mask = __shfl_sync(0xffffffffu, my_mask, i);
+        const int32_t pg = __shfl_sync(0xffffffffu, my_page, i);
         if (!mbar_wait_bounded(&S.bar[warp][i % NS], (i / NS) & 1)) {
             failed = true;
             break;
         }
-        if (ok_page) {
+        if (pg >= 0) {
             const uint8_t* st = S.stage[warp][i % NS];
             const int8_t* kst = reinterpret_cast<const int8_t*>(st);
             const int8_t* vst = reinterpret_cast<const int8_t*>(st + SUB_K_BYTES);
@@ -225,76 +268,92 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2) kq8_attn_kernel(const AttnPar
                     dot[g][bb] = d;
                 }
             }
-            const float ksv = kss[t];
+            const float ks = __fmul_rn(kss[t], inv127());
             const float vstep = __fmul_rn(vss[t], inv127());
-            float pw[GP];
+            float s2[2 * GP];
 #pragma unroll
-            for (int g = 0; g < GP; g++) pw[g] = 0.0f;
+            for (int gp = 0; gp < GP; gp++) {
+                const int g1 = min(2 * gp + 1, G - 1);
+                // s = sum_b dot_b * qsc_b in block order (the first add, 0 + x, is exact)
+                float2 s = __fmul2_rn(i2f_pair(dot[2 * gp][0], dot[g1][0]), qsc2[gp][0]);
+#pragma unroll
+                for (int bb = 1; bb < NB; bb++)
+                    s = __fadd2_rn(s, __fmul2_rn(i2f_pair(dot[2 * gp][bb], dot[g1][bb]),
+                                                 qsc2[gp][bb]));
+                s = __fmul2_rn(__fmul2_rn(s, make_float2(ks, ks)), make_float2(sc2, sc2));
+                s2[2 * gp] = s.x;
+                s2[2 * gp + 1] = s.y;
+            }
+            float w[2 * GP];
 #pragma unroll
             for (int g = 0; g < G; g++) {
                 const bool on = live && ((mask >> g) & 1u);
-                const float s = on ? score_exact(dot[g], qsc_r[g], ksv, scale) : -INFINITY;
-                const float mt = warp_max(s);
-                const float mn = fmaxf(M[g], mt);
-                if (mn > M[g]) {  // warp-uniform: rescale what was accumulated
-                    const float c = expf(M[g] - mn);
+                const float sv = on ? s2[g] : -INFINITY;
+                if (__any_sync(0xffffffffu, sv > M2[g] + RESCALE_SLACK)) {
+                    // rare: a new maximum by a wide margin -> rescale the state
+                    const float mn = fmaxf(M2[g], warp_max(sv));
+                    const float c = ex2(M2[g] - mn);
                     Sl[g] *= c;
 #pragma unroll
-                    for (int e = 0; e < EP; e++) fmul2(acc[g][e], c);
-                    M[g] = mn;
+                    for (int e = 0; e < EP; e++) acc[g][e] = __fmul2_rn(acc[g][e], make_float2(c, c));
+                    M2[g] = mn;
                 }
-                const float w = on ? expf(s - mn) : 0.0f;
-                Sl[g] += w;
-                pw[g] = on ? w * vstep : 0.0f;
+                w[g] = on ? ex2(sv - M2[g]) : 0.0f;
+                Sl[g] += w[g];
             }
-            float* prow = S.p[warp][t];
+            if constexpr ((G & 1) != 0) w[G] = 0.0f;
 #pragma unroll
-            for (int g4 = 0; g4 < GP; g4 += 4)
-                *reinterpret_cast<float4*>(prow + g4) =
-                    make_float4(pw[g4], pw[g4 + 1], pw[g4 + 2], pw[g4 + 3]);
+            for (int gp = 0; gp < GP; gp++) {
+                const float2 pp = __fmul2_rn(make_float2(w[2 * gp], w[2 * gp + 1]),
+                                             make_float2(vstep, vstep));
+                // masked tokens have w = 0; their (possibly stale) scale must not leak in
+                const float p0 = (w[2 * gp] != 0.0f) ? pp.x : 0.0f;
+                const float p1 = (w[2 * gp + 1] != 0.0f) ? pp.y : 0.0f;
+                S.p[warp][t][gp] = make_float4(p0, p0, p1, p1);
+            }
             __syncwarp();
 
             // ---- value phase: lane (tg, c) covers elements c*E.. of rows tg, tg+TG, ...
             const int tg = lane / NC, c = lane % NC;
 #pragma unroll 2
             for (int r = tg; r < TILE; r += TG) {
-                float f[E];
+                float2 f[EP];
                 if (E == 16) {
                     const uint4 vv = *reinterpret_cast<const uint4*>(vst + r * HD + c * 16);
-                    i8x4_to_f32(vv.x, f[0], f[1], f[2], f[3]);
-                    i8x4_to_f32(vv.y, f[4], f[5], f[6], f[7]);
-                    i8x4_to_f32(vv.z, f[8], f[9], f[10], f[11]);
-                    i8x4_to_f32(vv.w, f[12], f[13], f[14], f[15]);
+                    i8x4_to_f2(vv.x, f[0], f[1]);
+                    i8x4_to_f2(vv.y, f[2], f[3]);
+                    i8x4_to_f2(vv.z, f[4], f[5]);
+                    i8x4_to_f2(vv.w, f[6], f[7]);
                 } else {
                     const uint2 vv = *reinterpret_cast<const uint2*>(vst + r * HD + c * 8);
-                    i8x4_to_f32(vv.x, f[0], f[1], f[2], f[3]);
-                    i8x4_to_f32(vv.y, f[4], f[5], f[6], f[7]);
-                }
-                float pr[GP];
-#pragma unroll
-                for (int g4 = 0; g4 < GP; g4 += 4) {
-                    const float4 pp = *reinterpret_cast<const float4*>(&S.p[warp][r][g4]);
-                    pr[g4] = pp.x;
-                    pr[g4 + 1] = pp.y;
-                    pr[g4 + 2] = pp.z;
-                    pr[g4 + 3] = pp.w;
+                    i8x4_to_f2(vv.x, f[0], f[1]);
+                    i8x4_to_f2(vv.y, f[2], f[3]);
                 }
 #pragma unroll
-                for (int g = 0; g < G; g++)
+                for (int gp = 0; gp < GP; gp++) {
+                    const float4 pp = S.p[warp][r][gp];
+                    const float2 pa = make_float2(pp.x, pp.y);
+                    const float2 pb = make_float2(pp.z, pp.w);
 #pragma unroll
-                    for (int e = 0; e < EP; e++) ffma2(acc[g][e], f[2 * e], f[2 * e + 1], pr[g]);
+                    for (int e = 0; e < EP; e++) {
+                        acc[2 * gp][e] = __ffma2_rn(f[e], pa, acc[2 * gp][e]);
+                        if (2 * gp + 1 < G)
+                            acc[2 * gp + 1][e] = __ffma2_rn(f[e], pb, acc[2 * gp + 1][e]);
+                    }
+                }
             }
         }
         __syncwarp();
-        if (lane == 0 && i + NS < mine) issue(i + NS);
+        if (i + NS < mine) issue(i + NS);
     }
     if (failed) {
         if (lane == 0) atomicOr(P.status, KQ8_STATUS_TIMEOUT);
         // let the copies this warp still has in flight land before leaving
-        for (int j = i; j < mine && j < i + NS; j++) mbar_wait_bounded(&S.bar[warp][j % NS], (j / NS) & 1);
+        for (int j = i; j < mine && j < i + NS; j++)
+            mbar_wait_bounded(&S.bar[warp][j % NS], (j / NS) & 1);
 #pragma unroll
         for (int g = 0; g < G; g++) {
-            M[g] = M_INIT;
+            M2[g] = M_INIT;
             Sl[g] = 0.0f;
 #pragma unroll
             for (int e = 0; e < EP; e++) acc[g][e] = make_float2(0.0f, 0.0f);
@@ -316,7 +375,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2) kq8_attn_kernel(const AttnPar
 
     // ---- merge the 4 warps in shared memory (reuses the stage buffers)
     __syncthreads();
-    float* macc = reinterpret_cast<float*>(S.stage);                  // [W][G][HD]
+    float* macc = reinterpret_cast<float*>(S.stage);                      // [W][G][HD]
     float2* mms = reinterpret_cast<float2*>(macc + ATTN_WARPS * G * HD);  // [W][G]
     if (lane < NC) {
 #pragma unroll
@@ -328,7 +387,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2) kq8_attn_kernel(const AttnPar
     }
     if (lane == 0)
 #pragma unroll
-        for (int g = 0; g < G; g++) mms[warp * G + g] = make_float2(M[g], Sl[g]);
+        for (int g = 0; g < G; g++) mms[warp * G + g] = make_float2(M2[g], Sl[g]);
     __syncthreads();
 
     const int d = threadIdx.x;  // output element
@@ -340,7 +399,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2) kq8_attn_kernel(const AttnPar
 #pragma unroll
         for (int w = 0; w < ATTN_WARPS; w++) {
             const float2 ms = mms[w * G + g];
-            const float f = expf(ms.x - mx);
+            const float f = ex2(ms.x - mx);
             ssum += ms.y * f;
             a += macc[(w * G + g) * HD + d] * f;
         }
@@ -355,8 +414,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 2) kq8_attn_kernel(const AttnPar
     }
 }
 
-// Combine the partials of sequences split over several chunks:
-//   M = max_c m_c, out = sum_c acc_c e^(m_c - M) / sum_c S_c e^(m_c - M).
+// Combine the partials of sequences split over several chunks (base-2 maxima):
+//   M = max_c m_c, out = sum_c acc_c 2^(m_c - M) / sum_c S_c 2^(m_c - M).
 template <bool SPARSE>
 __global__ void __launch_bounds__(HD) kq8_merge_kernel(const AttnParams P) {
     const int row = blockIdx.x;  // b * nq + hq
@@ -374,7 +433,7 @@ __global__ void __launch_bounds__(HD) kq8_merge_kernel(const AttnParams P) {
     float ssum = 0.0f, a = 0.0f;
     for (int c = 0; c < nch; c++) {
         const float2 ms = P.part_ms[base + c];
-        const float f = expf(ms.x - mx);
+        const float f = ex2(ms.x - mx);
         ssum += ms.y * f;
         a += P.part_acc[(base + c) * HD + threadIdx.x] * f;
     }
