@@ -35,6 +35,7 @@ import numpy as np  # noqa: E402
 METRIC = "q8-KV decode attention: effective KV GB/s and % of GB300 HBM peak"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+WORKLOADS = ("serving", "long", "sparse", "qwen2b")
 
 
 def parse():
@@ -43,8 +44,14 @@ def parse():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kq8", choices=["kq8", "reference"])
+    ap.add_argument("--workload", default="serving", choices=WORKLOADS,
+                    help="serving: B=64 ragged 1K-32K, 36 layers (default); long: B=8 n=131072; "
+                         "sparse: block-sparse B=16 n=65536; qwen2b: B=1 n=4059, 28 layers")
     ap.add_argument("--layers", type=int, default=36)
     ap.add_argument("--batch", type=int, default=64)
+    ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],
+                    help="replay the step as a captured CUDA graph (auto: for qwen2b, whose "
+                         "per-layer GPU work is shorter than its host-side launch path)")
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -170,20 +177,23 @@ class ClockSampler:
 
 class OracleSample:
     """Sequences `seqs` of layer 0 of a workload, quantised by the oracle, ready
-    to time the oracle's exact decode over them (all query heads)."""
+    to time the oracle's decode over them (all query heads; block-sparse for
+    the sparse workload)."""
 
-    def __init__(self, wl, seqs):
+    def __init__(self, wl, seqs, sparse=False):
         import oracle
         from query_decode_attention_gb300 import workloads as W
         oracle.build()
         self.oracle = oracle
         self.wl = wl
+        self.sparse = sparse
         self.seqs = list(seqs)
-        self.q = W.host_q(wl)[self.seqs]
+        qall = W.host_q(wl)
+        self.q = qall[self.seqs]
         self.k8, self.ks, self.v8, self.vs = [], [], [], []
         self.nbytes = 0
         for b in self.seqs:
-            K, V = W.host_kv(wl, b)
+            K, V = W.host_kv(wl, b, q=qall)
             k8, ks = oracle.kv_quantize_rows(K)
             v8, vs = oracle.kv_quantize_rows(V)
             self.k8.append(k8)
@@ -194,14 +204,17 @@ class OracleSample:
 
     def run(self, nthreads):
         """One pass; returns seconds."""
+        wl = self.wl
         t0 = time.perf_counter()
-        self.oracle.decode_batch(self.q, self.k8, self.ks, self.v8, self.vs, self.wl.scale,
-                                 kv_bs=self.wl.kv_bs, nthreads=nthreads)
+        self.oracle.decode_batch(self.q, self.k8, self.ks, self.v8, self.vs, wl.scale,
+                                 kv_bs=wl.kv_bs, sparse=self.sparse, block=wl.block,
+                                 topk=wl.topk, probe=wl.probe, nthreads=nthreads)
         return time.perf_counter() - t0
 
     def describe(self):
         lens = [int(self.wl.seq_lens[b]) for b in self.seqs]
-        return (f"oracle exact decode of sequences {self.seqs[0]}..{self.seqs[-1]} of the "
+        kind = "block-sparse" if self.sparse else "exact"
+        return (f"oracle {kind} decode of sequences {self.seqs[0]}..{self.seqs[-1]} of the "
                 f"{self.wl.B} (n = {min(lens)}..{max(lens)}, all {self.wl.nq} query heads, "
                 f"layer 0, {self.nbytes / 1e6:.0f} MB of KV), OpenMP over (sequence, head)")
 
@@ -212,13 +225,13 @@ def oracle_threads():
 
 def run_reference(args, rank, world):
     """The reference arm: the CPU oracle, as it stands, on a bounded sample of
-    the same workload per step."""
+    the same workload per step (value: the same exact-equivalent KV GB/s)."""
     if rank != 0:
         return
-    from query_decode_attention_gb300 import workloads as W
-    wl = W.serving_8b(B=args.batch, layers=args.layers)
+    wl, sparse = make_workload(args, 0)
     threads = oracle_threads()
-    smp = OracleSample(wl, range(min(4, wl.B)))
+    nseq = {"serving": 4, "long": 1, "sparse": 2, "qwen2b": 1}[args.workload]
+    smp = OracleSample(wl, range(min(nseq, wl.B)), sparse=sparse)
     for _ in range(args.warmup):
         smp.run(threads)
     secs = sum(smp.run(threads) for _ in range(args.steps))
@@ -237,9 +250,126 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-# ---------------------------------------------------------------------------
-# GPU arm
-# ---------------------------------------------------------------------------
+def make_workload(args, rank):
+    """The bench workload (each rank draws its own batch: weak scaling)."""
+    from query_decode_attention_gb300 import workloads as W
+    if args.workload == "serving":
+        return W.serving_8b(B=args.batch, layers=args.layers, seed=3000 + rank), False
+    if args.workload == "long":
+        return W.long_context(seed=4000 + rank), False
+    if args.workload == "sparse":
+        return W.sparse_planted(65536, B=16, seed=5000 + rank), True
+    return W.qwen3vl_2b(4059, seed=2000 + rank), False
+
+
+class Scenario:
+    """A workload resident on the device: one paged q8 pool per layer (round
+    robin over fewer pools when memory is short), per-step inputs and the
+    step itself -- per layer, append each sequence's new token and run decode
+    attention (exact, or block-sparse for the sparse workload)."""
+
+    def __init__(self, args, rank, dev):
+        import torch
+        from query_decode_attention_gb300 import kq8, paged
+        from query_decode_attention_gb300 import workloads as W
+        self.kq8, self.W = kq8, W
+        self.wl, self.sparse = make_workload(args, rank)
+        wl = self.wl
+        self.dev = dev
+        self.L = wl.layers
+        free, _ = torch.cuda.mem_get_info(dev)
+        t0 = time.time()
+        self.caches = []
+        n_pools, self.per_layer = self.L, None
+        for layer in range(self.L):
+            if self.sparse:
+                q = W.host_q(wl, layer)
+                Ks, Vs = zip(*[W.host_kv(wl, b, layer, q=q) for b in range(wl.B)])
+                case = paged.fill_from_host(wl, list(Ks), list(Vs), dev, q_host=q)
+                del Ks, Vs
+            else:
+                case = paged.fill_cache(wl, layer, dev)
+            if self.per_layer is None:
+                self.per_layer = case.cache.nbytes()
+                n_pools = max(1, min(self.L, (int(free * 0.80) - 8 * self.per_layer) // self.per_layer))
+            self.caches.append(case)
+            if len(self.caches) >= n_pools:
+                break
+        torch.cuda.synchronize()
+        self.setup_s = time.time() - t0
+        B, nq, nkv, hd, L = wl.B, wl.nq, wl.nkv, wl.hd, self.L
+        self.q_all = torch.stack([self.caches[l % len(self.caches)].q if self.sparse
+                                  else W.device_q(wl, l, dev) for l in range(L)])
+        g = W.device_generator(dev, 77 + rank)
+        self.k_new = torch.randn((L, B, nkv, hd), generator=g, device=dev)
+        self.v_new = torch.randn((L, B, nkv, hd), generator=g, device=dev)
+        last = [W.slots_for(wl, self.caches[0].page_table_np, b, int(n) - 1, int(n))[0]
+                for b, n in enumerate(wl.seq_lens)]
+        self.slots = torch.tensor(np.array(last, np.int32), device=dev)
+        self.out_all = torch.empty((L, B, nq, hd), dtype=torch.float32, device=dev)
+        if self.sparse:
+            nb = kq8.kq8_sparse_decode_workspace_bytes(B, nq, nkv, wl.max_seq_len, wl.block, wl.topk)
+            self.chunk_tiles, self.num_chunks = kq8.kq8_sparse_decode_plan(
+                B, nq, nkv, wl.max_seq_len, wl.block, wl.topk)
+            self.sel = torch.empty((B, nq, wl.topk), dtype=torch.int32, device=dev)
+            self.launches_per_layer = 4 + (1 if self.num_chunks > 1 else 0)
+        else:
+            nb = kq8.kq8_decode_workspace_bytes(B, nq, nkv, wl.max_seq_len)
+            self.chunk_tiles, self.num_chunks = kq8.kq8_decode_plan(B, nq, nkv, wl.max_seq_len)
+            self.sel = None
+            self.launches_per_layer = 2 + (1 if self.num_chunks > 1 else 0)
+        self.ws = kq8.new_workspace(nb, dev)
+
+    def decode(self, l, out, q, stream):
+        wl, case = self.wl, self.caches[l % len(self.caches)]
+        if self.sparse:
+            self.kq8.kq8_sparse_decode_attn(out, q, case.cache, case.page_table, case.seq_lens,
+                                            wl.max_seq_len, wl.scale, wl.block, wl.topk,
+                                            wl.probe, self.ws, sel_blocks=self.sel, stream=stream)
+        else:
+            self.kq8.kq8_decode_attn(out, q, case.cache, case.page_table, case.seq_lens,
+                                     wl.max_seq_len, wl.scale, self.ws, stream=stream)
+
+    def step(self, stream, timers=None, q=None, k=None, v=None, slots=None, out=None):
+        q = self.q_all if q is None else q
+        k = self.k_new if k is None else k
+        v = self.v_new if v is None else v
+        slots = self.slots if slots is None else slots
+        out = self.out_all if out is None else out
+        for l in range(self.L):
+            case = self.caches[l % len(self.caches)]
+            self.kq8.kq8_append_kv(case.cache, k[l], v[l], slots, stream=stream)
+            if timers is not None:
+                timers[l][0].record(stream)
+            self.decode(l, out[l], q[l], stream)
+            if timers is not None:
+                timers[l][1].record(stream)
+
+    def kv_bytes_per_layer(self):
+        """KV bytes exact decode reads per layer (264 B per token and KV head)."""
+        return self.wl.kv_bytes_per_layer()
+
+    def sparse_bytes_per_layer(self):
+        """Bytes the sparse call must read per layer: probe rows (K row +
+        scale) of every probed block plus whole 32-token tiles (K, V, scales)
+        of the per-KV-head union of kept blocks; gated sequences read all."""
+        wl = self.wl
+        sel = self.sel.cpu().numpy()
+        total = 0
+        for b in range(wl.B):
+            n = int(wl.seq_lens[b])
+            if n <= 2 * wl.block:
+                total += -(-n // 32) * wl.nkv * 8448
+                continue
+            nblk = -(-n // wl.block)
+            rows = sum(len(range(j * wl.block, min((j + 1) * wl.block, n), wl.block // wl.probe)[:wl.probe])
+                       for j in range(nblk))
+            total += rows * wl.nkv * (wl.hd + 4)
+            for h in range(wl.nkv):
+                blocks = set(sel[b, h * wl.G:(h + 1) * wl.G].ravel().tolist()) - {-1}
+                total += len(blocks) * (wl.block // 32) * 8448
+        return total
+
 
 def main():
     args = parse()
@@ -262,59 +392,28 @@ def main():
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
         pg = dist
 
-    # ---- workload: each rank serves its own batch (weak scaling, no collective)
-    wl = W.serving_8b(B=args.batch, layers=args.layers, seed=3000 + rank)
-    free, total_mem = torch.cuda.mem_get_info(dev)
-    per_layer = None
-    caches = []
-    n_pools = wl.layers
-    t_setup = time.time()
-    for layer in range(wl.layers):
-        case = paged.fill_cache(wl, layer, dev)
-        if per_layer is None:
-            per_layer = case.cache.nbytes()
-            budget = int(free * 0.80) - 8 * per_layer
-            n_pools = max(2, min(wl.layers, budget // per_layer))
-        caches.append(case)
-        if len(caches) >= n_pools:
-            break
-    torch.cuda.synchronize()
-    setup_s = time.time() - t_setup
-    L = wl.layers
-    B, nq, nkv, hd = wl.B, wl.nq, wl.nkv, wl.hd
-
-    # per-step inputs (resident): q per layer, new K/V per layer, write slots
-    q_all = torch.stack([W.device_q(wl, l, dev) for l in range(L)])            # [L,B,nq,hd]
-    gk = W.device_generator(dev, 77 + rank)
-    k_new = torch.randn((L, B, nkv, hd), generator=gk, device=dev)
-    v_new = torch.randn((L, B, nkv, hd), generator=gk, device=dev)
-    last = np.array([W.slots_for(wl, caches[0].page_table_np, b, int(n) - 1, int(n))[0]
-                     for b, n in enumerate(wl.seq_lens)], np.int32)
-    slots = torch.tensor(last, dtype=torch.int32, device=dev)
-    out_all = torch.empty((L, B, nq, hd), dtype=torch.float32, device=dev)
-    ws_bytes = kq8.kq8_decode_workspace_bytes(B, nq, nkv, wl.max_seq_len)
-    ws = kq8.new_workspace(ws_bytes, dev)
+    sc = Scenario(args, rank, dev)
+    wl, L = sc.wl, sc.L
     stream = torch.cuda.current_stream(dev)
-
-    def step(timers=None):
-        for l in range(L):
-            case = caches[l % len(caches)]
-            kq8.kq8_append_kv(case.cache, k_new[l], v_new[l], slots, stream=stream)
-            if timers is not None:
-                timers[l][0].record(stream)
-            kq8.kq8_decode_attn(out_all[l], q_all[l], case.cache, case.page_table, case.seq_lens,
-                                wl.max_seq_len, wl.scale, ws, stream=stream)
-            if timers is not None:
-                timers[l][1].record(stream)
 
     clk = ClockSampler(local).__enter__()
     for _ in range(args.warmup):
-        step()
+        sc.step(stream)
     torch.cuda.synchronize()
-    status = kq8.kq8_read_status(ws)
+    status = kq8.kq8_read_status(sc.ws)
+
+    use_graph = args.graph == "on" or (args.graph == "auto" and args.workload == "qwen2b")
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            sc.step(torch.cuda.current_stream(dev))
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
 
     # ---- timed region
-    bytes_per_step = wl.kv_bytes_per_layer() * L
+    bytes_per_step = sc.kv_bytes_per_layer() * L
     timers = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(L)] for _ in range(args.steps)]
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -324,12 +423,20 @@ def main():
     clk.mark_start()
     ev0.record(stream)
     for s in range(args.steps):
-        step(timers[s])
+        if graph is not None:
+            graph.replay()
+        else:
+            sc.step(stream, timers[s])
     ev1.record(stream)
     torch.cuda.synchronize()
     clk.mark_end()
     if pg:
         pg.barrier()
+    if graph is not None:
+        # per-call decode durations for the roofline: the same steps, eagerly
+        for s in range(args.steps):
+            sc.step(stream, timers[s])
+        torch.cuda.synchronize()
     clk.__exit__(None, None, None)
     clocks = clk.summary()
     elapsed_ms = ev0.elapsed_time(ev1)
@@ -343,45 +450,54 @@ def main():
                  for s in range(args.steps) for l in range(L)]
     dec_avg_ms = sum(decode_ms) / len(decode_ms)
     peak, peak_kind = measured_peaks()
-    achieved = wl.kv_bytes_per_layer() / (dec_avg_ms * 1e-3) / 1e9
-    traffic_per_token_head, _ = committed_traffic("kq8_attn_kernel")
-    traffic = None
-    if traffic_per_token_head is not None:
-        traffic = int(traffic_per_token_head * wl.total_tokens * nkv)
-    chunk_tiles, num_chunks = kq8.kq8_decode_plan(B, nq, nkv, wl.max_seq_len)
-    launches_per_layer = 2 + (1 if num_chunks > 1 else 0)  # append, attention, merge
-    status |= kq8.kq8_read_status(ws)
+    status |= kq8.kq8_read_status(sc.ws)
+    if sc.sparse:
+        algo = sc.sparse_bytes_per_layer()
+        kernel = "kq8_sparse_decode_attn call (probe + top-k + attention + merge)"
+        traffic = None
+    else:
+        algo = sc.kv_bytes_per_layer()
+        kernel = "kq8_attn_kernel + kq8_merge_kernel (one decode call)"
+        per_unit, _ = committed_traffic("kq8_attn_kernel")
+        traffic = int(per_unit * wl.total_tokens * wl.nkv) if per_unit is not None else None
+    achieved = algo / (dec_avg_ms * 1e-3) / 1e9
 
     # ---- end to end through the public API from pinned host buffers
-    e2e = e2e_measure(args, wl, caches, dev, stream, kq8, L, bytes_per_step, world, pg)
+    e2e = e2e_measure(args, sc, stream, bytes_per_step, world, pg)
 
+    mode = "block-sparse" if sc.sparse else "exact"
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8xint8->int32 scores, fp32 softmax/accumulate", "data": "synthetic",
         "config": {**W.describe(wl), "workload": wl.name,
-                   "step": f"{L} layers x (append {B} tokens + exact decode attention)",
-                   "distinct_layer_pools": len(caches),
-                   "l2": f"no flush: each layer pool is {per_layer / 1e9:.2f} GB (> 129 MB L2)",
+                   "step": f"{L} layers x (append {wl.B} tokens + {mode} decode attention)",
+                   "value_bytes": ("exact-equivalent KV bytes (264 B per token and KV head)"
+                                   if sc.sparse else "KV bytes read (264 B per token and KV head)"),
+                   "distinct_layer_pools": len(sc.caches),
+                   "l2": f"no flush: each layer pool is {sc.per_layer / 1e9:.2f} GB (> 129 MB L2)",
                    "bytes_per_step": bytes_per_step, "parallelism": f"replicas x{world}",
-                   "chunk_tiles": chunk_tiles, "num_chunks": num_chunks},
+                   "chunk_tiles": sc.chunk_tiles, "num_chunks": sc.num_chunks},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "kq8_attn_kernel + kq8_merge_kernel (one decode call)",
-                     "peak_kind": f"{peak_kind} hbm_gbs",
-                     "bytes_per_launch": wl.kv_bytes_per_layer(),
-                     "launch_ms": round(dec_avg_ms, 5)},
+                     "kernel": kernel, "peak_kind": f"{peak_kind} hbm_gbs",
+                     "bytes_per_launch": algo, "launch_ms": round(dec_avg_ms, 5),
+                     "launch_ms_source": ("eager calls after the graph-replayed timed region"
+                                          if graph is not None else "the timed region")},
         "e2e": e2e,
-        "gpu_launches": args.steps * L * launches_per_layer,
+        "gpu_launches": args.steps * L * sc.launches_per_layer,
+        "cuda_graph": graph is not None,
         "clocks": clocks,
         "status_word": status,
-        "setup_s": round(setup_s, 1),
+        "setup_s": round(sc.setup_s, 1),
     }
-    if rank == 0 and not args.no_extras:
+    del sc
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_extras and args.workload == "serving":
         line["extras"] = extras(dev, kq8, paged, W, peak)
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl)
+        line["cpu_baseline"] = cpu_baseline(wl, sparse=(args.workload == "sparse"))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg:
@@ -389,34 +505,26 @@ def main():
         pg.destroy_process_group()
 
 
-def e2e_measure(args, wl, caches, dev, stream, kq8, L, bytes_per_step, world, pg):
-    """Same step with its inputs copied from pinned host memory every step and
-    the outputs read back, all inside the timed region."""
+def e2e_measure(args, sc, stream, bytes_per_step, world, pg):
+    """The same step through the public API with its inputs (q, the new K/V
+    token of every sequence, write slots) copied from pinned host memory every
+    step and the outputs read back, all inside the timed region."""
     import torch
-    B, nq, nkv, hd = wl.B, wl.nq, wl.nkv, wl.hd
-    h_q = torch.randn((L, B, nq, hd), dtype=torch.float32).pin_memory()
-    h_k = torch.randn((L, B, nkv, hd), dtype=torch.float32).pin_memory()
-    h_v = torch.randn((L, B, nkv, hd), dtype=torch.float32).pin_memory()
-    h_out = torch.empty((L, B, nq, hd), dtype=torch.float32).pin_memory()
-    d_q = torch.empty_like(h_q, device=dev)
-    d_k = torch.empty_like(h_k, device=dev)
-    d_v = torch.empty_like(h_v, device=dev)
-    d_out = torch.empty_like(h_out, device=dev)
-    last = np.array([W_slot(wl, caches[0].page_table_np, b) for b in range(B)], np.int32)
-    h_slots = torch.tensor(last, dtype=torch.int32).pin_memory()
-    d_slots = torch.empty_like(h_slots, device=dev)
-    ws = kq8.new_workspace(kq8.kq8_decode_workspace_bytes(B, nq, nkv, wl.max_seq_len), dev)
+    h_q = sc.q_all.cpu().pin_memory()
+    h_k = sc.k_new.cpu().pin_memory()
+    h_v = sc.v_new.cpu().pin_memory()
+    h_slots = sc.slots.cpu().pin_memory()
+    h_out = torch.empty(sc.out_all.shape, dtype=torch.float32).pin_memory()
+    d_q, d_k, d_v = (torch.empty_like(x, device=sc.dev) for x in (h_q, h_k, h_v))
+    d_slots = torch.empty_like(h_slots, device=sc.dev)
+    d_out = torch.empty_like(h_out, device=sc.dev)
 
     def step():
         d_q.copy_(h_q, non_blocking=True)
         d_k.copy_(h_k, non_blocking=True)
         d_v.copy_(h_v, non_blocking=True)
         d_slots.copy_(h_slots, non_blocking=True)
-        for l in range(L):
-            case = caches[l % len(caches)]
-            kq8.kq8_append_kv(case.cache, d_k[l], d_v[l], d_slots, stream=stream)
-            kq8.kq8_decode_attn(d_out[l], d_q[l], case.cache, case.page_table, case.seq_lens,
-                                wl.max_seq_len, wl.scale, ws, stream=stream)
+        sc.step(stream, q=d_q, k=d_k, v=d_v, slots=d_slots, out=d_out)
         h_out.copy_(d_out, non_blocking=True)
 
     for _ in range(max(1, args.warmup)):
@@ -433,20 +541,14 @@ def e2e_measure(args, wl, caches, dev, stream, kq8, L, bytes_per_step, world, pg
     torch.cuda.synchronize()
     ms = ev0.elapsed_time(ev1)
     if pg:
-        t = torch.tensor([ms], device=dev)
+        t = torch.tensor([ms], device=sc.dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms = float(t.item())
-    h2d = (h_q.numel() + h_k.numel() + h_v.numel()) * 4 + h_slots.numel() * 4
-    d2h = h_out.numel() * 4
+    h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_slots))
+    d2h = h_out.numel() * h_out.element_size()
     return {"value": round(bytes_per_step * steps * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(ms / steps, 4)}
-
-
-def W_slot(wl, pt, b):
-    from query_decode_attention_gb300 import workloads as W
-    n = int(wl.seq_lens[b])
-    return int(W.slots_for(wl, pt, b, n - 1, n)[0])
 
 
 def _time_calls(fn, reps, stream):
@@ -523,11 +625,12 @@ def extras(dev, kq8, paged, W, peak):
     return res
 
 
-def cpu_baseline(wl, seconds=10.0):
+def cpu_baseline(wl, sparse=False, seconds=10.0):
     """The oracle timed on the host cores on a bounded sample of the workload:
-    the first 8 sequences of layer 0, passes repeated for about `seconds`."""
+    up to 8 sequences of layer 0, passes repeated for about `seconds`."""
     threads = oracle_threads()
-    smp = OracleSample(wl, range(min(8, wl.B)))
+    nseq = 8 if wl.B >= 8 and int(wl.seq_lens.max()) <= 32768 else min(2, wl.B)
+    smp = OracleSample(wl, range(nseq), sparse=sparse)
     smp.run(threads)
     passes, secs = 0, 0.0
     while secs < seconds and passes < 1000:

@@ -59,9 +59,11 @@ enum {
  * kv_bs consecutive tokens of one sequence for all `num_kv_heads` KV heads.
  *   k      : int8 [num_pages][nkv][kv_bs/32][hd/32][32][32]
  *            page p, head h, token row r, element i lives at
- *            ((p*nkv + h)*kv_bs*hd) + (r/32)*32*hd + (i/32)*1024 + (r%32)*32 + i%32
- *            (each token's 32-element block is 32 contiguous bytes, the same
- *            block of 32 tokens is 1 KB contiguous).
+ *            ((p*nkv + h)*kv_bs*hd) + (r/32)*32*hd + (i/32)*1024 + kpos*32 + i%32
+ *            with kpos = (r%32 % 4)*8 + (r%32)/4: each token's 32-element
+ *            block is 32 contiguous bytes, the same block of a 32-token
+ *            sub-tile is 1 KB contiguous, and rows 0, 4, 8, ... of a sub-tile
+ *            are adjacent (a block probe every 4 rows reads whole lines).
  *   v      : int8 [num_pages][nkv][kv_bs][hd], token rows contiguous.
  *   kscale : float [num_pages][nkv][kv_bs], the row's max |k| (the stored
  *            scale of [9-3] §2; readers multiply by 1/127 as on [9-2] §2).
@@ -174,6 +176,13 @@ int kq8_decode_attn_noalloc(float* out, const float* q, const kq8_cache_t* cache
  */
 size_t kq8_sparse_decode_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len,
                                          int32_t block, int32_t topk);
+
+/*
+ * The split kq8_sparse_decode_attn uses for its bounded attention (as
+ * kq8_decode_plan).  num_chunks > 1 means a merge kernel runs after it.
+ */
+int kq8_sparse_decode_plan(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len, int32_t block,
+                           int32_t topk, int32_t* chunk_tiles, int32_t* num_chunks);
 
 /*
  * Block-sparse decode attention ([10-1] §1-§2).  Per sequence the gate of

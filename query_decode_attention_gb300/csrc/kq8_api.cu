@@ -207,6 +207,17 @@ size_t kq8_sparse_decode_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int
     return plan_sparse(B, nq, nkv, max_seq_len, block, topk).total;
 }
 
+int kq8_sparse_decode_plan(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len, int32_t block,
+                           int32_t topk, int32_t* chunk_tiles, int32_t* num_chunks) {
+    if (B < 0 || nq < 1 || nkv < 1 || nq % nkv || max_seq_len < 0 || block < TILE ||
+        block % TILE || topk < 1 || !chunk_tiles || !num_chunks)
+        return KQ8_ERR_INVALID_ARG;
+    const Plan p = plan_sparse(B, nq, nkv, max_seq_len, block, topk);
+    *chunk_tiles = p.chunk_tiles;
+    *num_chunks = p.num_chunks;
+    return KQ8_OK;
+}
+
 int kq8_workspace_init(void* workspace, size_t workspace_bytes, kq8_stream_t stream) {
     if (check_ws(workspace, workspace_bytes, STATUS_BYTES)) return KQ8_ERR_WORKSPACE;
     return cudaMemsetAsync(workspace, 0, STATUS_BYTES, (cudaStream_t)stream) == cudaSuccess
@@ -262,6 +273,7 @@ int kq8_sparse_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
     sp.topk = topk;
     sp.probe = probe;
     sp.max_nblk = plan.max_nblk;
+    sp.probe_bpc = probe_blocks_per_cta(block, cache->kv_bs);
     sp.scores = reinterpret_cast<float*>(ws + plan.off_scores);
     sp.masks = reinterpret_cast<uint8_t*>(ws + plan.off_masks);
     sp.tile_list = reinterpret_cast<int32_t*>(ws + plan.off_list);
@@ -331,6 +343,7 @@ int kq8_debug_probe_scores(float* scores, const float* q, const kq8_cache_t* cac
     sp.block = block;
     sp.probe = probe;
     sp.max_nblk = (int)(((int64_t)max_seq_len + block - 1) / block);
+    sp.probe_bpc = probe_blocks_per_cta(block, cache->kv_bs);
     sp.scores = scores;
     sp.status = nullptr;  // bad page ids are skipped without a status word
     return launch_probe(sp, nq / cache->num_kv_heads, B, cache->num_kv_heads,

@@ -72,7 +72,7 @@ struct AttnShape {
 template <int G>
 struct AttnSmem {
     alignas(128) uint8_t stage[ATTN_WARPS][ATTN_STAGES][STAGE_BYTES];
-    // per token: (p_g, p_g, p_g+1, p_g+1) for each head pair, p = w * vs
+    // per K position: (p_g, p_g, p_g+1, p_g+1) for each head pair, p = w * vs
     alignas(16) float4 p[ATTN_WARPS][TILE][AttnShape<G>::GP];
     alignas(16) int8_t qi[G][HD];
     alignas(16) float qsc[G][NB];
@@ -240,17 +240,19 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             const float* kss = reinterpret_cast<const float*>(st + SUB_K_BYTES + SUB_V_BYTES);
             const float* vss = kss + TILE;
 
-            // ---- score phase: lane t scores token tile*32 + t for all G heads
-            const int t = lane;
+            // ---- score phase: lane q reads K position q, i.e. token row
+            // t = krow(q) of the tile, and scores it for all G heads
+            const int q = lane;
+            const int t = krow(q);
             const bool live = tile * TILE + t < n;
             int dot[G][NB];
-            const int hs = (t >> 2) & 1;  // half order that keeps the loads conflict-free
+            const int hs = (q >> 2) & 1;  // half order that keeps the loads conflict-free
 #pragma unroll
             for (int bb = 0; bb < NB; bb++) {
                 const uint4 kA =
-                    *reinterpret_cast<const uint4*>(kst + bb * 1024 + t * 32 + hs * 16);
+                    *reinterpret_cast<const uint4*>(kst + bb * 1024 + q * 32 + hs * 16);
                 const uint4 kB =
-                    *reinterpret_cast<const uint4*>(kst + bb * 1024 + t * 32 + (hs ^ 1) * 16);
+                    *reinterpret_cast<const uint4*>(kst + bb * 1024 + q * 32 + (hs ^ 1) * 16);
 #pragma unroll
                 for (int g = 0; g < G; g++) {
                     const uint4 qA =
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                 // masked tokens have w = 0; their (possibly stale) scale must not leak in
                 const float p0 = (w[2 * gp] != 0.0f) ? pp.x : 0.0f;
                 const float p1 = (w[2 * gp + 1] != 0.0f) ? pp.y : 0.0f;
-                S.p[warp][t][gp] = make_float4(p0, p0, p1, p1);
+                S.p[warp][q][gp] = make_float4(p0, p0, p1, p1);  // by K position
             }
             __syncwarp();
 
@@ -331,7 +333,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                 }
 #pragma unroll
                 for (int gp = 0; gp < GP; gp++) {
-                    const float4 pp = S.p[warp][r][gp];
+                    const float4 pp = S.p[warp][kpos(r)][gp];
                     const float2 pa = make_float2(pp.x, pp.y);
                     const float2 pb = make_float2(pp.z, pp.w);
 #pragma unroll

@@ -2,7 +2,10 @@
 //
 // Cache layout, per (page p, KV head h), head_dim 128, kv_bs a multiple of 32:
 //   K: kv_bs/32 sub-tiles of 4 KB; sub-tile = 4 blocks (32 elements each) x
-//      32 tokens x 32 B  -> byte (r, i) at (r/32)*4096 + (i/32)*1024 + (r%32)*32 + i%32
+//      32 row positions x 32 B -> byte (r, i) at
+//      (r/32)*4096 + (i/32)*1024 + kpos(r%32)*32 + i%32, where row r of a
+//      sub-tile sits at position kpos(r) = (r%4)*8 + r/4: rows 0, 4, 8, ...
+//      are adjacent, so a block probe at a stride of 4 rows reads whole lines
 //   V: kv_bs rows of 128 B (token-major)
 //   kscale, vscale: kv_bs floats (the row's max |x|)
 // One 32-token sub-tile of one head is therefore 4096 B of K + 4096 B of V +
@@ -34,6 +37,9 @@ __host__ __device__ constexpr float inv127() { return 1.0f / 127.0f; }
 // ---------------------------------------------------------------------------
 // Cache addressing
 // ---------------------------------------------------------------------------
+// Position of row r (0..31) of a K sub-tile, and the row held at position q.
+__host__ __device__ __forceinline__ int kpos(int r) { return (r & 3) * 8 + (r >> 2); }
+__host__ __device__ __forceinline__ int krow(int q) { return (q & 7) * 4 + (q >> 3); }
 __device__ __forceinline__ size_t page_head(int32_t page, int h, int nkv) {
     return (size_t)page * (size_t)nkv + (size_t)h;
 }

@@ -50,9 +50,9 @@ __global__ void __launch_bounds__(APPEND_WARPS * 32)
     float mk, mv;
     const uint32_t ck = kv_quantize_lane(xk, mk);
     const uint32_t cv = kv_quantize_lane(xv, mv);
-    // K: element i of row r at sub-tile r/32, block i/32, row r%32, byte i%32
+    // K: element i of row r at sub-tile r/32, block i/32, position kpos(r%32), byte i%32
     const size_t ko = kv_sub_off(page, h, nkv, kv_bs, r / TILE) + (size_t)(lane >> 3) * 1024 +
-                      (size_t)(r % TILE) * 32 + (size_t)(lane & 7) * 4;
+                      (size_t)kpos(r % TILE) * 32 + (size_t)(lane & 7) * 4;
     *reinterpret_cast<uint32_t*>(c.k + ko) = ck;
     const size_t vo = page_head(page, h, nkv) * (size_t)kv_bs * HD + (size_t)r * HD + lane * 4;
     *reinterpret_cast<uint32_t*>(c.v + vo) = cv;
@@ -119,12 +119,13 @@ __global__ void kq8_debug_dots_kernel(int32_t* dots, const float* q, const kq8_c
     for (int i = lane; i < SUB_K_BYTES / 16; i += 32)
         reinterpret_cast<uint4*>(kt)[i] = reinterpret_cast<const uint4*>(src)[i];
     __syncwarp();
-    const int t = lane;
-    const int hs = (t >> 2) & 1;
+    const int kq = lane;       // K position read by this lane
+    const int t = krow(kq);    // token row it holds
+    const int hs = (kq >> 2) & 1;
     for (int g = 0; g < G; g++) {
         for (int bb = 0; bb < NB; bb++) {
-            const uint4 kA = *reinterpret_cast<const uint4*>(kt + bb * 1024 + t * 32 + hs * 16);
-            const uint4 kB = *reinterpret_cast<const uint4*>(kt + bb * 1024 + t * 32 + (hs ^ 1) * 16);
+            const uint4 kA = *reinterpret_cast<const uint4*>(kt + bb * 1024 + kq * 32 + hs * 16);
+            const uint4 kB = *reinterpret_cast<const uint4*>(kt + bb * 1024 + kq * 32 + (hs ^ 1) * 16);
             const uint4 qA = *reinterpret_cast<const uint4*>(qi[g] + bb * 32 + hs * 16);
             const uint4 qB = *reinterpret_cast<const uint4*>(qi[g] + bb * 32 + (hs ^ 1) * 16);
             int d = __dp4a((int)kA.x, (int)qA.x, 0);

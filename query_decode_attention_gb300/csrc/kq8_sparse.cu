@@ -6,7 +6,7 @@ namespace kq8 {
 
 template <int G>
 static int launch_probe_g(const SparseParams& p, int B, int nkv, cudaStream_t s) {
-    dim3 grid((p.max_nblk + PROBE_BLOCKS_PER_CTA - 1) / PROBE_BLOCKS_PER_CTA, nkv, B);
+    dim3 grid((p.max_nblk + p.probe_bpc - 1) / p.probe_bpc, nkv, B);
     kq8_probe_kernel<G><<<grid, PROBE_WARPS * 32, 0, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
 }
@@ -31,8 +31,17 @@ static int launch_topk_g(const SparseParams& p, int B, int nkv, cudaStream_t s) 
         default: return KQ8_ERR_UNSUPPORTED; \
     }
 
+// Blocks per probe CTA: as many as keep the pages they span within the CTA's
+// staged page ids (a CTA's blocks span at most bpc * block / kv_bs + 1 pages).
+int probe_blocks_per_cta(int block, int kv_bs) {
+    const long long bpc = (long long)(PROBE_MAX_PAGES - 1) * kv_bs / block;
+    return (int)(bpc < 1 ? 1 : (bpc > PROBE_MAX_BPC ? PROBE_MAX_BPC : bpc));
+}
+
 int launch_probe(const SparseParams& p, int G, int B, int nkv, cudaStream_t s) {
     if (B == 0 || p.max_nblk == 0) return KQ8_OK;
+    if (p.probe_bpc < 1 || (long long)p.probe_bpc * p.block / p.cache.kv_bs + 1 > PROBE_MAX_PAGES)
+        return KQ8_ERR_INVALID_ARG;
     KQ8_SWITCH_G(launch_probe_g, p, B, nkv, s)
 }
 

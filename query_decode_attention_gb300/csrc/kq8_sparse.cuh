@@ -25,6 +25,7 @@ struct SparseParams {
     float scale;
     int32_t block, topk, probe;
     int32_t max_nblk;        // ceil(max_seq_len / block)
+    int32_t probe_bpc;       // probe blocks per CTA (its pages fit PROBE_MAX_PAGES)
     float* scores;           // [B][nq][max_nblk]
     uint8_t* masks;          // [B][nkv][max_nblk]
     int32_t* tile_list;      // [B][nkv][list_cap]
@@ -41,28 +42,54 @@ __device__ __forceinline__ int sparse_seq_len(const SparseParams& P, int b) {
 }
 
 // ---------------------------------------------------------------------------
-// Probe: grid (ceil(max_nblk / PROBE_BLOCKS_PER_CTA), nkv, B), 8 warps.  Lane
-// (row pr = lane/4, 32-element block bb = lane%4) of a warp loads the 32 bytes
-// of block bb of probe row pr, forms G int32 dots, and the 4 lanes of a row
-// combine them in the method's order (bb = 0, 1, 2, 3) into the exact score.
+// Probe: grid (ceil(max_nblk / probe_bpc), nkv, B), 8 warps.  The CTA's page
+// ids are read once into shared memory (no K load waits on a page-table load).
+// Warp w owns blocks j0 + w + 8i; it walks units = (pass of 8 probe rows,
+// group of PROBE_UNROLL of its blocks) and issues the next unit's loads
+// before computing the current one, so loads stay in flight.  Lane (row
+// pr = lane/4, 32-element block bb = lane%4) loads the 32 bytes of block bb
+// of probe row pr, forms G int32 dots, and the 4 lanes of a row combine them
+// in the method's order (bb = 0, 1, 2, 3) into the exact score; block maxima
+// collect in shared memory across passes.
 // ---------------------------------------------------------------------------
 constexpr int PROBE_WARPS = 8;
-constexpr int PROBE_BLOCKS_PER_CTA = 64;
+constexpr int PROBE_MAX_BPC = 128;     // blocks per CTA
+constexpr int PROBE_MAX_PAGES = 256;   // page ids a CTA stages
+constexpr int PROBE_UNROLL = 4;
+
+struct ProbeUnit {
+    uint4 ka[PROBE_UNROLL], kb[PROBE_UNROLL];
+    float kst[PROBE_UNROLL];
+    bool valid[PROBE_UNROLL];
+};
 
 template <int G>
 __global__ void __launch_bounds__(PROBE_WARPS * 32) kq8_probe_kernel(const SparseParams P) {
+    constexpr int U = PROBE_UNROLL;
     __shared__ __align__(16) int8_t qi[G][HD];
     __shared__ float qsc[G][NB];
+    __shared__ int32_t pages[PROBE_MAX_PAGES];
+    __shared__ float best[PROBE_MAX_BPC][G];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y, b = blockIdx.z;
     const int nkv = P.cache.num_kv_heads, kv_bs = P.cache.kv_bs;
     const int n = sparse_seq_len(P, b);
     if (n < 0 || n <= 2 * P.block) return;  // gate: the exact path needs no probe
     const int nblk = (n + P.block - 1) / P.block;
-    const int j0 = blockIdx.x * PROBE_BLOCKS_PER_CTA;
+    const int j0 = blockIdx.x * P.probe_bpc;
     if (j0 >= nblk) return;
-    const int j1 = min(j0 + PROBE_BLOCKS_PER_CTA, nblk);
+    const int j1 = min(j0 + P.probe_bpc, nblk);
+    const int pg0 = (j0 * P.block) / kv_bs;
+    const int pg1 = (min(j1 * P.block, n) - 1) / kv_bs;
 
+    for (int i = threadIdx.x; i <= pg1 - pg0; i += PROBE_WARPS * 32) {
+        const int32_t pg = P.page_table[(size_t)b * P.max_pages + pg0 + i];
+        const bool ok = pg >= 0 && pg < P.cache.num_pages;
+        if (!ok && P.status) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
+        pages[i] = ok ? pg : -1;
+    }
+    for (int i = threadIdx.x; i < (j1 - j0) * G; i += PROBE_WARPS * 32)
+        best[i / G][i % G] = -INFINITY;
     for (int g = warp; g < G; g += PROBE_WARPS) {
         const float4 x =
             reinterpret_cast<const float4*>(P.q + ((size_t)b * P.nq + (size_t)h * G + g) * HD)[lane];
@@ -85,61 +112,83 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32) kq8_probe_kernel(const Spars
     }
     const float scale = P.scale;
 
-    for (int j = j0 + warp; j < j1; j += PROBE_WARPS) {
-        float best[G];
+    // this warp's units: (pass, group of U of its blocks)
+    const int my_blocks = (j1 - j0 > warp) ? (j1 - j0 - warp + PROBE_WARPS - 1) / PROBE_WARPS : 0;
+    const int ngroups = (my_blocks + U - 1) / U;
+    const int npass = (P.probe + 7) / 8;
+    const int nunits = ngroups * npass;
+    auto block_of = [&](int group, int u) { return j0 + warp + PROBE_WARPS * (group * U + u); };
+    auto load = [&](ProbeUnit& L, int k) {
+        const int group = k % ngroups, p = (k / ngroups) * 8 + pr;
 #pragma unroll
-        for (int g = 0; g < G; g++) best[g] = -INFINITY;
-        for (int p0 = 0; p0 < P.probe; p0 += 8) {
-            const int p = p0 + pr;
-            const int t = j * P.block + p * stride;
-            bool valid = (p < P.probe) && (t < n);
-            uint4 ka = make_uint4(0, 0, 0, 0), kb = ka;
-            float kst = 0.0f;
-            if (valid) {
-                const int32_t pg = P.page_table[(size_t)b * P.max_pages + t / kv_bs];
-                if (pg >= 0 && pg < P.cache.num_pages) {
+        for (int u = 0; u < U; u++) {
+            const int jj = block_of(group, u);
+            const int t = jj * P.block + p * stride;
+            L.valid[u] = (jj < j1) && (p < P.probe) && (t < n);
+            L.ka[u] = make_uint4(0, 0, 0, 0);
+            L.kb[u] = L.ka[u];
+            L.kst[u] = 0.0f;
+            if (L.valid[u]) {
+                const int32_t pg = pages[t / kv_bs - pg0];
+                if (pg >= 0) {
                     const int r = t % kv_bs;
                     const int8_t* src = P.cache.k + kv_sub_off(pg, h, nkv, kv_bs, r / TILE) +
-                                        bb * 1024 + (r % TILE) * 32;
-                    ka = __ldg(reinterpret_cast<const uint4*>(src));
-                    kb = __ldg(reinterpret_cast<const uint4*>(src + 16));
-                    kst = __ldg(P.cache.kscale + scale_sub_off(pg, h, nkv, kv_bs, r / TILE) + r % TILE);
+                                        bb * 1024 + kpos(r % TILE) * 32;
+                    L.ka[u] = __ldg(reinterpret_cast<const uint4*>(src));
+                    L.kb[u] = __ldg(reinterpret_cast<const uint4*>(src + 16));
+                    L.kst[u] = __ldg(P.cache.kscale + scale_sub_off(pg, h, nkv, kv_bs, r / TILE) +
+                                     r % TILE);
                 } else {
-                    valid = false;
-                    if (bb == 0 && P.status) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
+                    L.valid[u] = false;
                 }
             }
+        }
+    };
+    auto compute = [&](const ProbeUnit& L, int k) {
+        const int group = k % ngroups;
+#pragma unroll
+        for (int u = 0; u < U; u++) {
 #pragma unroll
             for (int g = 0; g < G; g++) {
-                int d = __dp4a((int)ka.x, (int)qa[g].x, 0);
-                d = __dp4a((int)ka.y, (int)qa[g].y, d);
-                d = __dp4a((int)ka.z, (int)qa[g].z, d);
-                d = __dp4a((int)ka.w, (int)qa[g].w, d);
-                d = __dp4a((int)kb.x, (int)qb[g].x, d);
-                d = __dp4a((int)kb.y, (int)qb[g].y, d);
-                d = __dp4a((int)kb.z, (int)qb[g].z, d);
-                d = __dp4a((int)kb.w, (int)qb[g].w, d);
+                int d = __dp4a((int)L.ka[u].x, (int)qa[g].x, 0);
+                d = __dp4a((int)L.ka[u].y, (int)qa[g].y, d);
+                d = __dp4a((int)L.ka[u].z, (int)qa[g].z, d);
+                d = __dp4a((int)L.ka[u].w, (int)qa[g].w, d);
+                d = __dp4a((int)L.kb[u].x, (int)qb[g].x, d);
+                d = __dp4a((int)L.kb[u].y, (int)qb[g].y, d);
+                d = __dp4a((int)L.kb[u].z, (int)qb[g].z, d);
+                d = __dp4a((int)L.kb[u].w, (int)qb[g].w, d);
                 const float x = __fmul_rn(i2f_exact(d), qs[g]);
                 // lanes 4pr+1..3 hand their block terms to lane 4pr, summed in order
                 const float x1 = __shfl_down_sync(0xffffffffu, x, 1);
                 const float x2 = __shfl_down_sync(0xffffffffu, x, 2);
                 const float x3 = __shfl_down_sync(0xffffffffu, x, 3);
                 float s = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(0.0f, x), x1), x2), x3);
-                s = __fmul_rn(__fmul_rn(s, __fmul_rn(kst, inv127())), scale);
-                if (!valid) s = -INFINITY;
+                s = __fmul_rn(__fmul_rn(s, __fmul_rn(L.kst[u], inv127())), scale);
+                if (!L.valid[u]) s = -INFINITY;
                 // max over the 8 rows held by lanes 0, 4, ..., 28
                 s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 4));
                 s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 8));
                 s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 16));
-                // lanes with bb != 0 carried partial terms; only lane 0's row max counts
-                best[g] = fmaxf(best[g], __shfl_sync(0xffffffffu, s, 0));
+                const int jj = block_of(group, u);
+                // lanes with bb != 0 carried partial terms; lane 0 holds the rows' max
+                if (lane == 0 && jj < j1) best[jj - j0][g] = fmaxf(best[jj - j0][g], s);
             }
         }
-        if (lane == 0) {
-#pragma unroll
-            for (int g = 0; g < G; g++)
-                P.scores[((size_t)b * P.nq + (size_t)h * G + g) * P.max_nblk + j] = best[g];
-        }
+    };
+    ProbeUnit A, Bu;
+    if (nunits > 0) load(A, 0);
+    for (int k = 0; k < nunits; k += 2) {
+        if (k + 1 < nunits) load(Bu, k + 1);
+        compute(A, k);
+        if (k + 1 >= nunits) break;
+        if (k + 2 < nunits) load(A, k + 2);
+        compute(Bu, k + 1);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < (j1 - j0) * G; i += PROBE_WARPS * 32) {
+        const int jj = j0 + i / G, g = i % G;
+        P.scores[((size_t)b * P.nq + (size_t)h * G + g) * P.max_nblk + jj] = best[i / G][g];
     }
 }
 

@@ -59,6 +59,8 @@ _lib.kq8_sparse_decode_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32,
 _lib.kq8_sparse_decode_workspace_bytes.restype = _SZ
 _lib.kq8_decode_plan.argtypes = [_I32, _I32, _I32, _I32, ctypes.POINTER(_I32),
                                  ctypes.POINTER(_I32)]
+_lib.kq8_sparse_decode_plan.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32, ctypes.POINTER(_I32),
+                                        ctypes.POINTER(_I32)]
 _lib.kq8_workspace_init.argtypes = [_P, _SZ, _P]
 _lib.kq8_decode_attn.argtypes = [_P, _P, _CP, _P, _I32, _P, _I32, _I32, _I32, ctypes.c_float, _P,
                                  _SZ, _P]
@@ -171,6 +173,14 @@ def kq8_decode_plan(B: int, nq: int, nkv: int, max_seq_len: int):
     ct, nc = _I32(0), _I32(0)
     _check(_lib.kq8_decode_plan(B, nq, nkv, max_seq_len, ctypes.byref(ct), ctypes.byref(nc)),
            "kq8_decode_plan")
+    return int(ct.value), int(nc.value)
+
+
+def kq8_sparse_decode_plan(B: int, nq: int, nkv: int, max_seq_len: int, block: int, topk: int):
+    """(chunk_tiles, num_chunks) of the sparse decode's bounded attention."""
+    ct, nc = _I32(0), _I32(0)
+    _check(_lib.kq8_sparse_decode_plan(B, nq, nkv, max_seq_len, block, topk, ctypes.byref(ct),
+                                       ctypes.byref(nc)), "kq8_sparse_decode_plan")
     return int(ct.value), int(nc.value)
 
 

@@ -91,9 +91,11 @@ def unpack(cache: kq8.PagedKVCache, slots: np.ndarray):
     (k8 [T, nkv, 128], ks [T, nkv], v8 [T, nkv, 128], vs [T, nkv]) numpy."""
     s = torch.as_tensor(np.asarray(slots, np.int64), device=cache.k.device)
     page, r = s // cache.kv_bs, s % cache.kv_bs
-    # k: [P, nkv, sub, 4, 32, 32] -> token r is [.., r//32, :, r%32, :]
+    # k: [P, nkv, sub, 4, 32, 32] -> row r is [.., r//32, :, kpos(r%32), :] with
+    # kpos(x) = (x%4)*8 + x//4 (rows 0, 4, 8, ... adjacent)
+    pos = (r % 32 % 4) * 8 + (r % 32) // 4
     k = cache.k[page, :, r // 32]                     # [T, nkv, 4, 32, 32]
-    k = k[torch.arange(len(s), device=s.device), :, :, r % 32, :]  # [T, nkv, 4, 32]
+    k = k[torch.arange(len(s), device=s.device), :, :, pos, :]  # [T, nkv, 4, 32]
     k8 = k.reshape(len(s), cache.num_kv_heads, 128)
     v8 = cache.v[page, :, r]                          # [T, nkv, 128]
     ks = cache.kscale[page, :, r]
