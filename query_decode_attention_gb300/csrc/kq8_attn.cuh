@@ -221,7 +221,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
 #pragma unroll
         for (int bb = 0; bb < NB; bb++)
             qsc2[gp][bb] = make_float2(S.qsc[2 * gp][bb], S.qsc[min(2 * gp + 1, G - 1)][bb]);
-    const float sc2 = P.scale * LOG2E;  // softmax scale and the move to base 2
+    // stored K max -> step (1/127), softmax scale and the move to base 2
+    const float kscale_mul = inv127() * P.scale * LOG2E;
+    float Mhi[G];  // rescale threshold: running max + RESCALE_SLACK
+#pragma unroll
+    for (int g = 0; g < G; g++) Mhi[g] = M_INIT + RESCALE_SLACK;
 
     bool failed = false;
     int i = 0;
@@ -270,37 +274,54 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                     dot[g][bb] = d;
                 }
             }
-            const float ks = __fmul_rn(kss[t], inv127());
+            // (s * ks) * scale * log2(e) with ks = kscale / 127: one multiplier per token
+            const float kmul = __fmul_rn(kss[t], kscale_mul);
             const float vstep = __fmul_rn(vss[t], inv127());
-            float s2[2 * GP];
+            float sv[2 * GP];
 #pragma unroll
             for (int gp = 0; gp < GP; gp++) {
                 const int g1 = min(2 * gp + 1, G - 1);
-                // s = sum_b dot_b * qsc_b in block order (the first add, 0 + x, is exact)
-                float2 s = __fmul2_rn(i2f_pair(dot[2 * gp][0], dot[g1][0]), qsc2[gp][0]);
+                // s = sum_b dot_b * qsc_b in block order (the first add, 0 + x, is exact);
+                // the int32 dots are < 2^22 in magnitude, so the conversions are exact
+                float2 s = __fmul2_rn(make_float2(__int2float_rn(dot[2 * gp][0]),
+                                                  __int2float_rn(dot[g1][0])),
+                                      qsc2[gp][0]);
 #pragma unroll
                 for (int bb = 1; bb < NB; bb++)
-                    s = __fadd2_rn(s, __fmul2_rn(i2f_pair(dot[2 * gp][bb], dot[g1][bb]),
+                    s = __fadd2_rn(s, __fmul2_rn(make_float2(__int2float_rn(dot[2 * gp][bb]),
+                                                             __int2float_rn(dot[g1][bb])),
                                                  qsc2[gp][bb]));
-                s = __fmul2_rn(__fmul2_rn(s, make_float2(ks, ks)), make_float2(sc2, sc2));
-                s2[2 * gp] = s.x;
-                s2[2 * gp + 1] = s.y;
+                s = __fmul2_rn(s, make_float2(kmul, kmul));
+                sv[2 * gp] = s.x;
+                sv[2 * gp + 1] = s.y;
+            }
+            bool grow = false;
+#pragma unroll
+            for (int g = 0; g < G; g++) {
+                const bool on = live && ((mask >> g) & 1u);
+                sv[g] = on ? sv[g] : -INFINITY;
+                grow |= sv[g] > Mhi[g];
+            }
+            if (__any_sync(0xffffffffu, grow)) {
+                // rare: some head's maximum grew by a wide margin -> rescale its state
+#pragma unroll
+                for (int g = 0; g < G; g++) {
+                    const float mn = fmaxf(M2[g], warp_max(sv[g]));
+                    if (mn > M2[g]) {
+                        const float c = ex2(M2[g] - mn);
+                        Sl[g] *= c;
+#pragma unroll
+                        for (int e = 0; e < EP; e++)
+                            acc[g][e] = __fmul2_rn(acc[g][e], make_float2(c, c));
+                        M2[g] = mn;
+                        Mhi[g] = mn + RESCALE_SLACK;
+                    }
+                }
             }
             float w[2 * GP];
 #pragma unroll
             for (int g = 0; g < G; g++) {
-                const bool on = live && ((mask >> g) & 1u);
-                const float sv = on ? s2[g] : -INFINITY;
-                if (__any_sync(0xffffffffu, sv > M2[g] + RESCALE_SLACK)) {
-                    // rare: a new maximum by a wide margin -> rescale the state
-                    const float mn = fmaxf(M2[g], warp_max(sv));
-                    const float c = ex2(M2[g] - mn);
-                    Sl[g] *= c;
-#pragma unroll
-                    for (int e = 0; e < EP; e++) acc[g][e] = __fmul2_rn(acc[g][e], make_float2(c, c));
-                    M2[g] = mn;
-                }
-                w[g] = on ? ex2(sv - M2[g]) : 0.0f;
+                w[g] = ex2(sv[g] - M2[g]);  // masked: ex2(-inf) = 0
                 Sl[g] += w[g];
             }
             if constexpr ((G & 1) != 0) w[G] = 0.0f;
@@ -317,7 +338,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
 
             // ---- value phase: lane (tg, c) covers elements c*E.. of rows tg, tg+TG, ...
             const int tg = lane / NC, c = lane % NC;
-#pragma unroll 2
+#pragma unroll
             for (int r = tg; r < TILE; r += TG) {
                 float2 f[EP];
                 if (E == 16) {
@@ -356,6 +377,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
 #pragma unroll
         for (int g = 0; g < G; g++) {
             M2[g] = M_INIT;
+            Mhi[g] = M_INIT + RESCALE_SLACK;
             Sl[g] = 0.0f;
 #pragma unroll
             for (int e = 0; e < EP; e++) acc[g][e] = make_float2(0.0f, 0.0f);
