@@ -312,13 +312,19 @@ class Scenario:
             self.chunk_tiles, self.num_chunks = kq8.kq8_sparse_decode_plan(
                 B, nq, nkv, wl.max_seq_len, wl.block, wl.topk)
             self.sel = torch.empty((B, nq, wl.topk), dtype=torch.int32, device=dev)
-            self.launches_per_layer = 4 + (1 if self.num_chunks > 1 else 0)
+            self.launches_per_layer = 4 + (1 if self._merge_kernel() else 0)
         else:
             nb = kq8.kq8_decode_workspace_bytes(B, nq, nkv, wl.max_seq_len)
             self.chunk_tiles, self.num_chunks = kq8.kq8_decode_plan(B, nq, nkv, wl.max_seq_len)
             self.sel = None
-            self.launches_per_layer = 2 + (1 if self.num_chunks > 1 else 0)
+            self.launches_per_layer = 2 + (1 if self._merge_kernel() else 0)
         self.ws = kq8.new_workspace(nb, dev)
+
+    def _merge_kernel(self):
+        """The separate merge kernel runs only when chunks split a sequence and
+        the batch has more (sequence, KV head) pairs than the in-kernel merge's
+        16384 counters."""
+        return self.num_chunks > 1 and self.wl.B * self.wl.nkv > 16384
 
     def decode(self, l, out, q, stream):
         wl, case = self.wl, self.caches[l % len(self.caches)]
@@ -457,7 +463,8 @@ def main():
         traffic = None
     else:
         algo = sc.kv_bytes_per_layer()
-        kernel = "kq8_attn_kernel + kq8_merge_kernel (one decode call)"
+        kernel = ("kq8_attn_kernel + kq8_merge_kernel (one decode call)" if sc._merge_kernel()
+                  else "kq8_attn_kernel with its in-kernel chunk merge (one decode call)")
         per_unit, _ = committed_traffic("kq8_attn_kernel")
         traffic = int(per_unit * wl.total_tokens * wl.nkv) if per_unit is not None else None
     achieved = algo / (dec_avg_ms * 1e-3) / 1e9

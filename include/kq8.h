@@ -100,7 +100,10 @@ int kq8_append_kv(const kq8_cache_t* cache, const float* k, const float* v, cons
 
 /*
  * Bytes of workspace kq8_decode_attn needs for these sizes on the current
- * device (>= 256).  The first 256 bytes hold the status word.
+ * device.  The first 256 bytes hold the status word, the next 64 KB the
+ * per-(sequence, KV head) chunk counters of the in-kernel merge; both must be
+ * zero before the first call (kq8_workspace_init) and every completed call
+ * leaves the counters at zero.  Re-initialise a workspace after a failed call.
  */
 size_t kq8_decode_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len);
 
@@ -114,8 +117,9 @@ int kq8_decode_plan(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len, int
                     int32_t* num_chunks);
 
 /*
- * Clears the status word of a workspace (one 256-byte memset on `stream`).
- * Call once after allocating a workspace.
+ * Clears the status word and the chunk counters of a workspace (one memset of
+ * up to 64 KB + 256 bytes on `stream`).  Call once after allocating a
+ * workspace: an uninitialised workspace gives wrong results.
  */
 int kq8_workspace_init(void* workspace, size_t workspace_bytes, kq8_stream_t stream);
 

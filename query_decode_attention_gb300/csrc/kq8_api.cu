@@ -16,6 +16,12 @@ namespace {
 
 constexpr size_t WS_ALIGN = 256;
 constexpr size_t STATUS_BYTES = 256;
+// Chunk counters for the merge folded into the attention kernel: one per
+// (sequence, KV head), in a fixed region right after the status word, zero
+// between calls (kq8_workspace_init clears them, the merging CTA resets its
+// own).  Larger batches fall back to the separate merge kernel.
+constexpr size_t MAX_COUNTERS = 16384;
+constexpr size_t HEADER_BYTES = STATUS_BYTES + MAX_COUNTERS * sizeof(uint32_t);
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
@@ -49,14 +55,14 @@ struct Plan {
     size_t off_ms = 0, off_acc = 0;
     int max_nblk = 0, list_cap = 0;
     size_t off_scores = 0, off_masks = 0, off_list = 0, off_len = 0;
-    size_t total = STATUS_BYTES;
+    size_t total = HEADER_BYTES;
 };
 
 Plan plan_exact(int B, int nq, int nkv, int max_seq_len) {
     Plan p;
     const int64_t tiles = ((int64_t)max_seq_len + TILE - 1) / TILE;
     chunking(B, nkv, tiles, device_sms(), p.chunk_tiles, p.num_chunks);
-    size_t o = STATUS_BYTES;
+    size_t o = HEADER_BYTES;
     p.off_ms = o;
     o = align_up(o + (size_t)B * nq * p.num_chunks * sizeof(float2), WS_ALIGN);
     p.off_acc = o;
@@ -77,7 +83,7 @@ Plan plan_sparse(int B, int nq, int nkv, int max_seq_len, int block, int topk) {
     if (cap < 1) cap = 1;
     p.list_cap = (int)cap;
     chunking(B, nkv, p.list_cap, device_sms(), p.chunk_tiles, p.num_chunks);
-    size_t o = STATUS_BYTES;
+    size_t o = HEADER_BYTES;
     p.off_scores = o;
     o = align_up(o + (size_t)B * nq * p.max_nblk * sizeof(float), WS_ALIGN);
     p.off_masks = o;
@@ -151,6 +157,9 @@ AttnParams attn_params(float* out, const float* q, const kq8_cache_t* c, const i
     p.part_ms = reinterpret_cast<float2*>(static_cast<char*>(ws) + plan.off_ms);
     p.part_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + plan.off_acc);
     p.status = static_cast<uint32_t*>(ws);
+    p.counters = ((size_t)B * (size_t)c->num_kv_heads <= MAX_COUNTERS)
+                     ? reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + STATUS_BYTES)
+                     : nullptr;
     return p;
 }
 
@@ -220,7 +229,8 @@ int kq8_sparse_decode_plan(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_l
 
 int kq8_workspace_init(void* workspace, size_t workspace_bytes, kq8_stream_t stream) {
     if (check_ws(workspace, workspace_bytes, STATUS_BYTES)) return KQ8_ERR_WORKSPACE;
-    return cudaMemsetAsync(workspace, 0, STATUS_BYTES, (cudaStream_t)stream) == cudaSuccess
+    const size_t n = workspace_bytes < HEADER_BYTES ? workspace_bytes : HEADER_BYTES;
+    return cudaMemsetAsync(workspace, 0, n, (cudaStream_t)stream) == cudaSuccess
                ? KQ8_OK
                : KQ8_ERR_CUDA;
 }
@@ -407,9 +417,10 @@ extern "C" int kq8_decode_attn_noalloc(float* out, const float* q, const kq8_cac
     void* ws = nullptr;
     rc = noalloc_scratch(&ws);
     if (rc) return rc;
-    // Nothing in the scratch has to start at zero: every partial is written
-    // before the merge reads it, and the status word only collects error bits
-    // that this entry point does not report.
+    // Only the chunk counters must start at zero: a __device__ array is zeroed
+    // when the library loads and every call leaves its counters at zero again.
+    // Partials are written before they are read, and the status word only
+    // collects error bits that this entry point does not report.
     AttnParams p = attn_params(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq,
                                scale, plan, ws);
     return launch_attn(p, nq / nkv, false, B, nkv, (cudaStream_t)stream);

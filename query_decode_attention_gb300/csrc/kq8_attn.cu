@@ -14,7 +14,7 @@ static int launch_attn_g(const AttnParams& p, int B, int nkv, cudaStream_t s) {
     dim3 grid(p.num_chunks, nkv, B);
     kern<<<grid, ATTN_THREADS, smem, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return KQ8_ERR_CUDA;
-    if (p.num_chunks > 1) {
+    if (p.num_chunks > 1 && p.counters == nullptr) {
         kq8_merge_kernel<SPARSE><<<B * p.nq, HD, 0, s>>>(p);
         if (cudaGetLastError() != cudaSuccess) return KQ8_ERR_CUDA;
     }

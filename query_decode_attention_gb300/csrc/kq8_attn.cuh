@@ -23,8 +23,10 @@
 //     packed FMAs.
 // The 4 warps' (M, S, acc) are merged in shared memory; a chunk that covers
 // the whole sequence writes out = acc / S directly, others write an
-// unnormalised partial (M, S, acc) that kq8_merge_kernel combines by its
-// log-sum-exp (the same algebra as the online rescale).
+// unnormalised partial (M, S, acc), and the last of a sequence's chunk CTAs to
+// finish (an atomic ticket per (sequence, KV head)) combines them by their
+// log-sum-exp -- the same algebra as the online rescale.  Without ticket
+// counters (very large batches) kq8_merge_kernel does that step instead.
 #pragma once
 
 #include "kq8_common.cuh"
@@ -54,6 +56,7 @@ struct AttnParams {
     float* part_acc;       // [B][nq][num_chunks][HD]
     float2* part_ms;       // [B][nq][num_chunks] (M in base 2, S)
     uint32_t* status;
+    uint32_t* counters;    // [B][nkv] chunk tickets, zero between calls; null: merge kernel
     // block-sparse tile lists (SPARSE only): entry = tile | head_mask << 24
     const int32_t* tile_list;  // [B][nkv][list_cap]
     const int32_t* list_len;   // [B][nkv]
@@ -77,6 +80,7 @@ struct AttnSmem {
     alignas(16) int8_t qi[G][HD];
     alignas(16) float qsc[G][NB];
     alignas(8) uint64_t bar[ATTN_WARPS][ATTN_STAGES];
+    int last;  // this CTA drew the last ticket of its (sequence, KV head)
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -436,6 +440,43 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             if (d == 0) P.part_ms[pr] = make_float2(mx, ssum);
         }
     }
+    if (nch == 1 || P.counters == nullptr) return;
+
+    // ---- the last CTA of this (sequence, KV head) to finish merges the chunks
+    //   M = max_c m_c, out = sum_c acc_c 2^(m_c - M) / sum_c S_c 2^(m_c - M)
+    __threadfence();  // this thread's partials are visible before the ticket
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned ticket = atomicAdd(&P.counters[b * nkv + h], 1u);
+        S.last = (ticket == (unsigned)(nch - 1));
+    }
+    __syncthreads();
+    if (!S.last) return;
+    __threadfence();
+    // one warp per query head, 4 output elements per lane, one online pass over
+    // the chunks with their loads issued in batches
+    for (int g = warp; g < G; g += ATTN_WARPS) {
+        const size_t base = ((size_t)b * P.nq + (size_t)h * G + g) * P.num_chunks;
+        float mx = M_INIT, ssum = 0.0f;
+        float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 8
+        for (int c = 0; c < nch; c++) {
+            const float2 ms = __ldcg(&P.part_ms[base + c]);
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(P.part_acc + (base + c) * HD) + lane);
+            const float mn = fmaxf(mx, ms.x);
+            const float fo = ex2(mx - mn), fn = ex2(ms.x - mn);
+            ssum = ssum * fo + ms.y * fn;
+            a.x = a.x * fo + x.x * fn;
+            a.y = a.y * fo + x.y * fn;
+            a.z = a.z * fo + x.z * fn;
+            a.w = a.w * fo + x.w * fn;
+            mx = mn;
+        }
+        float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (ssum > 0.0f) o = make_float4(a.x / ssum, a.y / ssum, a.z / ssum, a.w / ssum);
+        reinterpret_cast<float4*>(P.out + ((size_t)b * P.nq + (size_t)h * G + g) * HD)[lane] = o;
+    }
+    if (threadIdx.x == 0) P.counters[b * nkv + h] = 0;  // ready for the next call
 }
 
 // Combine the partials of sequences split over several chunks (base-2 maxima):
