@@ -72,6 +72,10 @@ def lib():
             L.kq8o_score.restype = _F
             L.kq8o_attn_single_q.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F,
                                              _P, _I, _P, _P]
+            L.kq8o_stream_reset.argtypes = [_P, _P, _P, _I]
+            L.kq8o_attn_stream.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                           _I, _F]
+            L.kq8o_stream_output.argtypes = [_P, _F, _P, _I]
             L.kq8o_attn_two_pass_f64.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                                  _F, _P, _I]
             L.kq8o_attn_ref_f64.argtypes = [_P, _P, _P, _P, _I, _I, _D]
@@ -226,6 +230,35 @@ def attn_single_q(q, cache: SeqCache, kh, scale, tokens=None, trace=False):
     if trace:
         return out, mtr[:n_list], nv.value
     return out
+
+
+class StreamState:
+    """Running one-pass state (M, S, acc[hd]) of one query head, kept between
+    calls (article 9-2 §3, streaming form)."""
+
+    def __init__(self, hd=128):
+        self.M = np.zeros(1, np.float32)
+        self.S = np.zeros(1, np.float32)
+        self.acc = np.zeros(hd, np.float32)
+        lib().kq8o_stream_reset(self.M.ctypes.data_as(_P), self.S.ctypes.data_as(_P),
+                                self.acc.ctypes.data_as(_P), hd)
+
+    def output(self):
+        out = np.empty_like(self.acc)
+        lib().kq8o_stream_output(out.ctypes.data_as(_P), float(self.S[0]),
+                                 self.acc.ctypes.data_as(_P), self.acc.shape[0])
+        return out
+
+
+def attn_stream(state: StreamState, q, cache: SeqCache, kh, scale, t_begin, t_end):
+    """Continue the one-pass loop of `state` over tokens [t_begin, t_end)."""
+    q, pq = _c(q, np.float32)
+    kp, vp = cache.scale_ptrs(kh)
+    lib().kq8o_attn_stream(state.M.ctypes.data_as(_P), state.S.ctypes.data_as(_P),
+                           state.acc.ctypes.data_as(_P), pq, cache.k_ptrs, cache.v_ptrs, kp, vp,
+                           int(t_begin), int(t_end), cache.kv_dim, cache.kv_bs, cache.nkv,
+                           kh * cache.hd, cache.hd, float(np.float32(scale)))
+    return state
 
 
 def attn_two_pass_f64(q, cache: SeqCache, kh, scale, tokens=None):

@@ -199,6 +199,59 @@ void kq8o_attn_single_q(float* out, const float* q,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Streaming form ([9-2] §3: the one-pass kernel "can compute while KV blocks */
+/* arrive one by one", the two-pass one cannot).  The running state (M, S,    */
+/* acc[hd]) of the loop above is kept by the caller between calls; one call   */
+/* continues the loop over tokens [t_begin, t_end) exactly as the one-pass    */
+/* kernel would, so feeding a sequence in pieces reproduces the one-call      */
+/* result bit for bit.  A fresh state is M = -1e9, S = 0, acc = 0; the output */
+/* is acc / S (0 for an empty state), the single divide of [9-2] segment 3.   */
+/* ------------------------------------------------------------------------ */
+void kq8o_stream_reset(float* M, float* S, float* acc, int hd) {
+    *M = M_INIT;
+    *S = 0.0f;
+    for (int i = 0; i < hd; i++) acc[i] = 0.0f;
+}
+
+void kq8o_attn_stream(float* M_io, float* S_io, float* acc, const float* q,
+                      int8_t* const* k_blocks, int8_t* const* v_blocks,
+                      const float* kscale, const float* vscale, int t_begin, int t_end,
+                      int kv_dim, int kv_bs, int nkv, int kh_off, int hd, float scale) {
+    int nblk = hd / 32;
+    int8_t qi[KQ8O_MAX_HD];
+    float qsc[KQ8O_MAX_HD / 32];
+    int32_t dots[KQ8O_MAX_HD / 32];
+    kq8o_quantize_q(q, hd, qi, qsc);
+    float M = *M_io, S = *S_io;
+    for (int t = t_begin; t < t_end; t++) {
+        const int8_t* kt = row_ptr(k_blocks, t, kv_bs, kv_dim, kh_off);
+        const int8_t* vt = row_ptr(v_blocks, t, kv_bs, kv_dim, kh_off);
+        kq8o_block_dots(qi, kt, hd, dots);
+        float s = kq8o_score(dots, qsc, nblk, kscale[(size_t)t * nkv], scale);
+        float w;
+        if (s > M) {
+            float c = expf(M - s);
+            S *= c;
+            for (int i = 0; i < hd; i++) acc[i] *= c;
+            M = s;
+            w = 1.0f;
+        } else {
+            w = expf(s - M);
+        }
+        S += w;
+        float vs = vscale[(size_t)t * nkv] * KVQ_INV;
+        float pv = w * vs;
+        for (int i = 0; i < hd; i++) acc[i] += (float)vt[i] * pv;
+    }
+    *M_io = M;
+    *S_io = S;
+}
+
+void kq8o_stream_output(float* out, float S, const float* acc, int hd) {
+    for (int i = 0; i < hd; i++) out[i] = (S > 0.0f) ? acc[i] / S : 0.0f;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Naive two-pass attention over the same quantised data, in fp64 ([9-2] §3: */
 /* store every score, take the max, exponentiate, weight V -- "functionally   */
 /* equivalent" to the one-pass kernel).  Q, K and V enter through their codes */

@@ -24,6 +24,12 @@ void kq8o_attn_single_q(float* out, const float* q, int8_t* const* k_blocks,
                         int seq_len, int kv_dim, int kv_bs, int nkv, int kh_off, int hd,
                         float scale, const int32_t* tokens, int n_tokens, float* m_trace,
                         int* n_visited);
+void kq8o_stream_reset(float* M, float* S, float* acc, int hd);
+void kq8o_attn_stream(float* M_io, float* S_io, float* acc, const float* q, int8_t* const* k_blocks,
+                      int8_t* const* v_blocks, const float* kscale, const float* vscale,
+                      int t_begin, int t_end, int kv_dim, int kv_bs, int nkv, int kh_off, int hd,
+                      float scale);
+void kq8o_stream_output(float* out, float S, const float* acc, int hd);
 void kq8o_attn_two_pass_f64(double* out, const float* q, int8_t* const* k_blocks,
                             int8_t* const* v_blocks, const float* kscale, const float* vscale,
                             int seq_len, int kv_dim, int kv_bs, int nkv, int kh_off, int hd,

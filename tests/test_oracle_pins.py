@@ -518,3 +518,33 @@ def test_planted_blocks_are_recalled():
                                                    wl.topk, wl.probe)
             assert used
             assert set(sel.tolist()) == set(W.planted_blocks(wl, b, kh).tolist())
+
+
+# ---------------------------------------------------------------------------
+# Streaming form (article 9-2 §3): KV fed in pieces through a carried state
+# ---------------------------------------------------------------------------
+
+def test_streaming_in_pieces_equals_one_call():
+    # the carried (M, S, acc) continues the same loop, so any split of the
+    # sequence gives the one-call result bit for bit
+    n = 700
+    cache, (k8, ks, v8, vs) = _cache(n, seed=95)
+    q = np.random.default_rng(96).standard_normal(128).astype(np.float32)
+    one = oracle.attn_single_q(q, cache, 1, 0.1)
+    for cuts in ([0, n], [0, 1, 2, n], [0, 31, 32, 33, 400, 699, n], [0, 350, 350, n]):
+        st = oracle.StreamState()
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            oracle.attn_stream(st, q, cache, 1, 0.1, a, b)
+        assert np.array_equal(st.output(), one), cuts
+    # the state itself is the textbook pair: acc / S is softmax-weighted V
+    ref = _textbook(q, k8, ks, v8, vs, 1, np.float32(0.1))
+    assert np.abs(one - ref).max() < 1e-5 * np.abs(ref).max()
+
+
+def test_streaming_empty_state_and_empty_pieces():
+    cache, _ = _cache(10, seed=97)
+    q = np.ones(128, np.float32)
+    st = oracle.StreamState()
+    assert not st.output().any()
+    oracle.attn_stream(st, q, cache, 0, 0.1, 5, 5)  # empty piece changes nothing
+    assert st.S[0] == 0 and st.M[0] == np.float32(-1e9)
