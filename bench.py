@@ -591,6 +591,23 @@ def extras(dev, kq8, paged, W, peak):
     gbs = wl.kv_bytes_per_layer() / (ms * 1e-3) / 1e9
     res["long_context_exact"] = {"workload": wl.name, "ms": round(ms, 4), "GB/s": round(gbs, 1),
                                  "frac_of_peak": round(gbs / peak, 4)}
+    # streaming form: the same cache folded into running states in 8 pieces
+    pieces = 8
+    state = kq8.AttnState(wl.B, wl.nq, dev)
+    bounds = [torch.full((wl.B,), (wl.max_seq_len * k) // pieces, dtype=torch.int32, device=dev)
+              for k in range(pieces + 1)]
+
+    def stream_all():
+        kq8.kq8_state_reset(state, stream=stream)
+        for k in range(pieces):
+            kq8.kq8_decode_attn_update(state, case.q, case.cache, case.page_table, bounds[k],
+                                       bounds[k + 1], wl.max_seq_len, wl.scale, ws, stream=stream)
+        kq8.kq8_state_finalize(out, state, stream=stream)
+    ms_s = _time_calls(stream_all, 10, stream)
+    gbs_s = wl.kv_bytes_per_layer() / (ms_s * 1e-3) / 1e9
+    res["long_context_streamed_8_pieces"] = {"ms": round(ms_s, 4), "GB/s": round(gbs_s, 1),
+                                             "frac_of_peak": round(gbs_s / peak, 4),
+                                             "vs_one_call": round(ms / ms_s, 3)}
     # write path: 8 x 4096 new tokens into that cache
     T = 8 * 4096
     g = W.device_generator(dev, 99)

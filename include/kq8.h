@@ -213,6 +213,34 @@ int kq8_sparse_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
                            size_t workspace_bytes, kq8_stream_t stream);
 
 /*
+ * Streaming form ([9-2] §3: the one-pass kernel can compute while KV arrives
+ * piece by piece).  A running state per (sequence, query head) is kept in
+ * caller memory between calls: state_acc float [rows][hd] (16-byte aligned)
+ * and state_ms float [rows][2] (8-byte aligned), rows = B * nq in the layout
+ * of `out`.  Its contents are this library's unnormalised online-softmax state
+ * (running max in base-2 units of the scaled score, running sum, accumulator);
+ * treat them as opaque.
+ *   kq8_state_reset        : makes every row empty.
+ *   kq8_decode_attn_update : attends tokens [seq_begin[b], seq_end[b]) of each
+ *                            sequence (seq_begin optional: NULL = 0; each in
+ *                            [0, seq_end[b]], else KQ8_STATUS_BAD_SEQLEN and the
+ *                            sequence is skipped) and folds the result into the
+ *                            state by its log-sum-exp.  Other arguments as
+ *                            kq8_decode_attn (workspace from
+ *                            kq8_decode_workspace_bytes).  Feeding a sequence in
+ *                            pieces gives the one-call result up to rounding.
+ *   kq8_state_finalize     : out = acc / sum per row (0 for an empty row).
+ */
+int kq8_state_reset(float* state_acc, float* state_ms, int32_t rows, kq8_stream_t stream);
+int kq8_decode_attn_update(float* state_acc, float* state_ms, const float* q,
+                           const kq8_cache_t* cache, const int32_t* page_table, int32_t max_pages,
+                           const int32_t* seq_begin, const int32_t* seq_end, int32_t max_seq_len,
+                           int32_t B, int32_t nq, float scale, void* workspace,
+                           size_t workspace_bytes, kq8_stream_t stream);
+int kq8_state_finalize(float* out, const float* state_acc, const float* state_ms, int32_t rows,
+                       kq8_stream_t stream);
+
+/*
  * Copies the status word of `workspace` (or of a kq8_append_kv status word) to
  * *status (host), then clears it; synchronises `stream`.
  */

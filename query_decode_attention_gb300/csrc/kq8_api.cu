@@ -304,6 +304,43 @@ int kq8_sparse_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
     return launch_attn(p, G, true, B, nkv, s);
 }
 
+int kq8_state_reset(float* state_acc, float* state_ms, int32_t rows, kq8_stream_t stream) {
+    if (rows < 0 || (rows > 0 && (!state_acc || !state_ms || !aligned(state_acc, 16) ||
+                                  !aligned(state_ms, 8))))
+        return KQ8_ERR_INVALID_ARG;
+    return launch_state_reset(state_acc, reinterpret_cast<float2*>(state_ms), rows,
+                              (cudaStream_t)stream);
+}
+
+int kq8_decode_attn_update(float* state_acc, float* state_ms, const float* q,
+                           const kq8_cache_t* cache, const int32_t* page_table, int32_t max_pages,
+                           const int32_t* seq_begin, const int32_t* seq_end, int32_t max_seq_len,
+                           int32_t B, int32_t nq, float scale, void* workspace,
+                           size_t workspace_bytes, kq8_stream_t stream) {
+    int rc = check_decode(state_acc, q, cache, page_table, max_pages, seq_end, max_seq_len, B, nq);
+    if (rc) return rc;
+    if (B > 0 && (!state_ms || !aligned(state_ms, 8))) return KQ8_ERR_INVALID_ARG;
+    const int nkv = cache->num_kv_heads;
+    const Plan plan = plan_exact(B, nq, nkv, max_seq_len);
+    rc = check_ws(workspace, workspace_bytes, plan.total);
+    if (rc) return rc;
+    if (B == 0) return KQ8_OK;
+    AttnParams p = attn_params(nullptr, q, cache, page_table, max_pages, seq_end, max_seq_len, B,
+                               nq, scale, plan, workspace);
+    p.seq_begin = seq_begin;
+    p.state_acc = state_acc;
+    p.state_ms = reinterpret_cast<float2*>(state_ms);
+    return launch_attn(p, nq / nkv, false, B, nkv, (cudaStream_t)stream);
+}
+
+int kq8_state_finalize(float* out, const float* state_acc, const float* state_ms, int32_t rows,
+                       kq8_stream_t stream) {
+    if (rows < 0 || (rows > 0 && (!out || !state_acc || !state_ms || !aligned(state_ms, 8))))
+        return KQ8_ERR_INVALID_ARG;
+    return launch_state_finalize(out, state_acc, reinterpret_cast<const float2*>(state_ms), rows,
+                                 (cudaStream_t)stream);
+}
+
 int kq8_read_status(void* status_word, uint32_t* status, kq8_stream_t stream) {
     if (!status_word || !status || !aligned(status_word, 4)) return KQ8_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;

@@ -41,6 +41,31 @@ int launch_attn(const AttnParams& p, int G, bool sparse, int B, int nkv, cudaStr
     return sparse ? launch_attn_s<true>(p, G, B, nkv, s) : launch_attn_s<false>(p, G, B, nkv, s);
 }
 
+// Running states: reset to empty (max -1e9, sum 0, acc 0) and finalise to
+// out = acc / S (0 for an empty state), one block of HD threads per row.
+__global__ void __launch_bounds__(HD) kq8_state_reset_kernel(float* acc, float2* ms) {
+    acc[(size_t)blockIdx.x * HD + threadIdx.x] = 0.0f;
+    if (threadIdx.x == 0) ms[blockIdx.x] = make_float2(M_INIT, 0.0f);
+}
+__global__ void __launch_bounds__(HD) kq8_state_finalize_kernel(float* out, const float* acc,
+                                                                const float2* ms) {
+    const float s = ms[blockIdx.x].y;
+    const size_t i = (size_t)blockIdx.x * HD + threadIdx.x;
+    out[i] = (s > 0.0f) ? acc[i] / s : 0.0f;
+}
+
+int launch_state_reset(float* acc, float2* ms, int rows, cudaStream_t s) {
+    if (rows == 0) return KQ8_OK;
+    kq8_state_reset_kernel<<<rows, HD, 0, s>>>(acc, ms);
+    return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+}
+
+int launch_state_finalize(float* out, const float* acc, const float2* ms, int rows, cudaStream_t s) {
+    if (rows == 0) return KQ8_OK;
+    kq8_state_finalize_kernel<<<rows, HD, 0, s>>>(out, acc, ms);
+    return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+}
+
 size_t attn_smem_bytes(int G) {
     switch (G) {
         case 1: return sizeof(AttnSmem<1>);

@@ -57,6 +57,11 @@ struct AttnParams {
     float2* part_ms;       // [B][nq][num_chunks] (M in base 2, S)
     uint32_t* status;
     uint32_t* counters;    // [B][nkv] chunk tickets, zero between calls; null: merge kernel
+    // streaming form (exact mode only): attend tokens [seq_begin[b], seq_lens[b])
+    // and fold the result into a caller-held running state instead of `out`
+    const int32_t* seq_begin;  // optional [B]
+    float* state_acc;          // optional [B][nq][HD] unnormalised accumulator
+    float2* state_ms;          // optional [B][nq] (running max in base 2, running sum)
     // block-sparse tile lists (SPARSE only): entry = tile | head_mask << 24
     const int32_t* tile_list;  // [B][nkv][list_cap]
     const int32_t* list_len;   // [B][nkv]
@@ -109,17 +114,50 @@ __device__ __forceinline__ float2 i2f_pair(int d0, int d1) {
                       make_float2(-12582912.0f, -12582912.0f));
 }
 
-// Number of list entries (tiles) of sequence b / KV head h.
-template <bool SPARSE>
-__device__ __forceinline__ int attn_entries(const AttnParams& P, int b, int h, int n) {
-    if (SPARSE) return P.list_len[b * P.cache.num_kv_heads + h];
-    return (n + TILE - 1) / TILE;
-}
-
 __device__ __forceinline__ int valid_seq_len(const AttnParams& P, int b) {
     int n = P.seq_lens[b];
     if (n < 0 || n > P.max_seq_len) return -1;
     return n;
+}
+
+// The tokens of sequence b one call attends: [begin, n), as list entries
+// (tiles) starting at tile first_tile; bad lengths/starts give an empty range.
+struct SeqRange {
+    int n, begin, first_tile, entries;
+    bool bad;
+};
+template <bool SPARSE>
+__device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h) {
+    SeqRange r;
+    r.n = valid_seq_len(P, b);
+    r.bad = r.n < 0;
+    if (r.bad) r.n = 0;
+    r.begin = 0;
+    if (!SPARSE && P.seq_begin) {
+        r.begin = P.seq_begin[b];
+        if (r.begin < 0 || r.begin > r.n) {
+            r.bad = true;
+            r.begin = r.n;
+        }
+    }
+    r.first_tile = r.begin / TILE;
+    if (r.n == r.begin)
+        r.entries = 0;
+    else if (SPARSE)
+        r.entries = P.list_len[b * P.cache.num_kv_heads + h];
+    else
+        r.entries = (r.n + TILE - 1) / TILE - r.first_tile;
+    return r;
+}
+
+// Folds a result (m, s, a) into a running state (mo, so, ao), base-2 maxima:
+// M = max, then both sides are scaled by 2^(their max - M) and added.
+__device__ __forceinline__ void fold_state(float mo, float so, float m, float s, float& M,
+                                           float& S, float& fo, float& fn) {
+    M = fmaxf(mo, m);
+    fo = ex2(mo - M);
+    fn = ex2(m - M);
+    S = so * fo + s * fn;
 }
 
 template <int G, bool SPARSE>
@@ -137,12 +175,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     const int nkv = P.cache.num_kv_heads, kv_bs = P.cache.kv_bs;
     const int subs = kv_bs / TILE;
 
-    int n = valid_seq_len(P, b);
-    if (n < 0) {
-        if (threadIdx.x == 0 && chunk == 0 && h == 0) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
-        n = 0;
-    }
-    const int entries = (n == 0) ? 0 : attn_entries<SPARSE>(P, b, h, n);
+    const SeqRange rng = seq_range<SPARSE>(P, b, h);
+    if (rng.bad && threadIdx.x == 0 && chunk == 0 && h == 0) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
+    const int n = rng.n, begin = rng.begin;
+    const int entries = rng.entries;
     const int nch = max(1, (entries + P.chunk_tiles - 1) / P.chunk_tiles);
     if (chunk >= nch) return;
     const int e0 = chunk * P.chunk_tiles;
@@ -169,7 +205,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             my_tile = v & 0xFFFFFF;
             my_mask = (uint32_t)v >> 24;
         } else {
-            my_tile = e;
+            my_tile = rng.first_tile + e;
             my_mask = 0xFFu;
         }
         const int32_t pg = P.page_table[(size_t)b * P.max_pages + my_tile / subs];
@@ -252,7 +288,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             // t = krow(q) of the tile, and scores it for all G heads
             const int q = lane;
             const int t = krow(q);
-            const bool live = tile * TILE + t < n;
+            const bool live = tile * TILE + t < n && tile * TILE + t >= begin;
             int dot[G][NB];
             const int hs = (q >> 2) & 1;  // half order that keeps the loads conflict-free
 #pragma unroll
@@ -432,7 +468,15 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             a += macc[(w * G + g) * HD + d] * f;
         }
         const size_t row = (size_t)b * P.nq + (size_t)h * G + g;
-        if (nch == 1) {
+        if (nch == 1 && P.state_acc) {
+            const float2 old = P.state_ms[row];
+            float M, Sn, fo, fn;
+            fold_state(old.x, old.y, mx, ssum, M, Sn, fo, fn);
+            const float an = P.state_acc[row * HD + d] * fo + a * fn;
+            __syncthreads();  // every thread has read the old state row
+            P.state_acc[row * HD + d] = an;
+            if (d == 0) P.state_ms[row] = make_float2(M, Sn);
+        } else if (nch == 1) {
             P.out[row * HD + d] = (ssum > 0.0f) ? a / ssum : 0.0f;
         } else {
             const size_t pr = row * P.num_chunks + chunk;
@@ -472,9 +516,22 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             a.w = a.w * fo + x.w * fn;
             mx = mn;
         }
-        float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (ssum > 0.0f) o = make_float4(a.x / ssum, a.y / ssum, a.z / ssum, a.w / ssum);
-        reinterpret_cast<float4*>(P.out + ((size_t)b * P.nq + (size_t)h * G + g) * HD)[lane] = o;
+        const size_t row = (size_t)b * P.nq + (size_t)h * G + g;
+        if (P.state_acc) {  // fold into the caller's running state (this warp owns the row)
+            const float2 old = P.state_ms[row];
+            float M, Sn, fo, fn;
+            fold_state(old.x, old.y, mx, ssum, M, Sn, fo, fn);
+            float4* sa = reinterpret_cast<float4*>(P.state_acc + row * HD) + lane;
+            const float4 ao = *sa;
+            __syncwarp();
+            *sa = make_float4(ao.x * fo + a.x * fn, ao.y * fo + a.y * fn, ao.z * fo + a.z * fn,
+                              ao.w * fo + a.w * fn);
+            if (lane == 0) P.state_ms[row] = make_float2(M, Sn);
+        } else {
+            float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (ssum > 0.0f) o = make_float4(a.x / ssum, a.y / ssum, a.z / ssum, a.w / ssum);
+            reinterpret_cast<float4*>(P.out + row * HD)[lane] = o;
+        }
     }
     if (threadIdx.x == 0) P.counters[b * nkv + h] = 0;  // ready for the next call
 }
@@ -487,9 +544,7 @@ __global__ void __launch_bounds__(HD) kq8_merge_kernel(const AttnParams P) {
     const int b = row / P.nq, hq = row % P.nq;
     const int G = P.nq / P.cache.num_kv_heads;
     const int h = hq / G;
-    const int n = valid_seq_len(P, b);
-    if (n <= 0) return;
-    const int entries = attn_entries<SPARSE>(P, b, h, n);
+    const int entries = seq_range<SPARSE>(P, b, h).entries;
     const int nch = (entries + P.chunk_tiles - 1) / P.chunk_tiles;
     if (nch <= 1) return;
     const size_t base = (size_t)row * P.num_chunks;
@@ -502,7 +557,17 @@ __global__ void __launch_bounds__(HD) kq8_merge_kernel(const AttnParams P) {
         ssum += ms.y * f;
         a += P.part_acc[(base + c) * HD + threadIdx.x] * f;
     }
-    P.out[(size_t)row * HD + threadIdx.x] = (ssum > 0.0f) ? a / ssum : 0.0f;
+    if (P.state_acc) {
+        const float2 old = P.state_ms[row];
+        float M, Sn, fo, fn;
+        fold_state(old.x, old.y, mx, ssum, M, Sn, fo, fn);
+        const float an = P.state_acc[(size_t)row * HD + threadIdx.x] * fo + a * fn;
+        __syncthreads();  // every thread has read the old state row
+        P.state_acc[(size_t)row * HD + threadIdx.x] = an;
+        if (threadIdx.x == 0) P.state_ms[row] = make_float2(M, Sn);
+    } else {
+        P.out[(size_t)row * HD + threadIdx.x] = (ssum > 0.0f) ? a / ssum : 0.0f;
+    }
 }
 
 }  // namespace kq8

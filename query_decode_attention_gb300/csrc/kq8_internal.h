@@ -20,6 +20,8 @@ int launch_debug_dots(int32_t* dots, const float* q, const kq8_cache_t& c,
 // Attention over KV chunks (+ the merge when any sequence spans > 1 chunk).
 int launch_attn(const AttnParams& p, int G, bool sparse, int B, int nkv, cudaStream_t s);
 int launch_probe(const SparseParams& p, int G, int B, int nkv, cudaStream_t s);
+int launch_state_reset(float* acc, float2* ms, int rows, cudaStream_t s);
+int launch_state_finalize(float* out, const float* acc, const float2* ms, int rows, cudaStream_t s);
 int probe_blocks_per_cta(int block, int kv_bs);
 int launch_topk(const SparseParams& p, int G, int B, int nkv, cudaStream_t s);
 

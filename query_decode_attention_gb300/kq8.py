@@ -68,6 +68,10 @@ _lib.kq8_sparse_decode_attn.argtypes = [_P, _P, _CP, _P, _I32, _P, _I32, _I32, _
                                         ctypes.c_float, _I32, _I32, _I32, _P, _P, _SZ, _P]
 _lib.kq8_decode_attn_noalloc.argtypes = [_P, _P, _CP, _P, _I32, _P, _I32, _I32, _I32,
                                          ctypes.c_float, _P]
+_lib.kq8_state_reset.argtypes = [_P, _P, _I32, _P]
+_lib.kq8_decode_attn_update.argtypes = [_P, _P, _P, _CP, _P, _I32, _P, _P, _I32, _I32, _I32,
+                                        ctypes.c_float, _P, _SZ, _P]
+_lib.kq8_state_finalize.argtypes = [_P, _P, _P, _I32, _P]
 _lib.kq8_read_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), _P]
 _lib.kq8_strerror.argtypes = [ctypes.c_int]
 _lib.kq8_strerror.restype = ctypes.c_char_p
@@ -255,6 +259,49 @@ def kq8_sparse_decode_attn(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCac
                                        int(topk), int(probe), _ptr(sel_blocks), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(),
                                        _stream(stream)), "kq8_sparse_decode_attn")
+
+
+class AttnState:
+    """A running attention state for B sequences x nq query heads (the
+    streaming form): acc float32 [B, nq, 128], ms float32 [B, nq, 2]."""
+
+    def __init__(self, B: int, nq: int, device="cuda", stream=None):
+        self.acc = torch.empty((B, nq, HEAD_DIM), dtype=torch.float32, device=device)
+        self.ms = torch.empty((B, nq, 2), dtype=torch.float32, device=device)
+        kq8_state_reset(self, stream)
+
+
+def kq8_state_reset(state: AttnState, stream=None) -> None:
+    rows = state.acc.numel() // HEAD_DIM
+    _check(_lib.kq8_state_reset(_ptr(state.acc), _ptr(state.ms), rows, _stream(stream)),
+           "kq8_state_reset")
+
+
+def kq8_decode_attn_update(state: AttnState, q: torch.Tensor, cache: PagedKVCache,
+                           page_table: torch.Tensor, seq_begin: Optional[torch.Tensor],
+                           seq_end: torch.Tensor, max_seq_len: int, scale: float,
+                           workspace: torch.Tensor, stream=None) -> None:
+    """Fold tokens [seq_begin, seq_end) of each sequence into `state`."""
+    B, nq, max_pages = _decode_args(state.acc, q, cache, page_table, seq_end)
+    if seq_begin is not None:
+        _dtype(seq_begin, torch.int32, "seq_begin")
+        if seq_begin.numel() != B:
+            raise ValueError("seq_begin must be [B]")
+    _check(_lib.kq8_decode_attn_update(_ptr(state.acc), _ptr(state.ms), _ptr(q),
+                                       ctypes.byref(cache.struct), _ptr(page_table), max_pages,
+                                       _ptr(seq_begin), _ptr(seq_end), int(max_seq_len), B, nq,
+                                       float(scale), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream)), "kq8_decode_attn_update")
+
+
+def kq8_state_finalize(out: torch.Tensor, state: AttnState, stream=None) -> None:
+    _dtype(out, torch.float32, "out")
+    if out.shape != state.acc.shape:
+        raise ValueError("out must match the state's [B, nq, 128]")
+    rows = state.acc.numel() // HEAD_DIM
+    _check(_lib.kq8_state_finalize(_ptr(out), _ptr(state.acc), _ptr(state.ms), rows,
+                                   _stream(stream)), "kq8_state_finalize")
 
 
 def kq8_read_status(word: torch.Tensor, stream=None) -> int:
