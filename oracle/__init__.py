@@ -89,6 +89,9 @@ def lib():
             L.kq8o_decode_batch.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                             _F, _I, _I, _I, _I, _P, _I]
             L.kq8o_decode_batch.restype = _I
+            L.kq8o_prefill_batch.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                             _I, _F, _I, _I, _I, _I, _P, _I]
+            L.kq8o_prefill_batch.restype = _I
             L.kq8o_has_openmp.restype = _I
             _lib = L
     return _lib
@@ -324,16 +327,10 @@ def sparse_attn_head(q, cache: SeqCache, kh, scale, block, topk, probe):
 # Batch driver (OpenMP over (sequence, query head) when available)
 # --------------------------------------------------------------------------
 
-def decode_batch(q, k8_list, ks_list, v8_list, vs_list, scale, kv_bs=32, sparse=False, block=32,
-                 topk=32, probe=8, nthreads=0):
-    """Exact (or block-sparse) decode for B sequences of one layer.
-
-    q: float32 [B, nq, hd]; k8_list[b]: int8 [n_b, nkv, hd]; ks_list[b]:
-    float32 [n_b, nkv] (same for V).  Returns out float32 [B, nq, hd] and,
-    for sparse, sel int32 [B, nq, topk] (-1 padded)."""
-    q = np.ascontiguousarray(q, np.float32)
-    B, nq, hd = q.shape
-    nkv = k8_list[0].shape[1] if len(k8_list) else 1
+def _pack_layer(k8_list, ks_list, v8_list, vs_list, hd, kv_bs):
+    """One layer's sequences as the token-major rows the C drivers walk."""
+    B = len(k8_list)
+    nkv = k8_list[0].shape[1] if B else 1
     lens = np.array([k.shape[0] for k in k8_list], np.int32)
     offs = np.zeros(B, np.int64)
     offs[1:] = np.cumsum(lens.astype(np.int64))[:-1]
@@ -349,6 +346,20 @@ def decode_batch(q, k8_list, ks_list, v8_list, vs_list, scale, kv_bs=32, sparse=
         v_rows[o:o + n] = v8_list[b].reshape(n, nkv * hd)
         ks[o:o + n] = ks_list[b]
         vs[o:o + n] = vs_list[b]
+    return k_rows, v_rows, ks, vs, offs, lens, nkv
+
+
+def decode_batch(q, k8_list, ks_list, v8_list, vs_list, scale, kv_bs=32, sparse=False, block=32,
+                 topk=32, probe=8, nthreads=0):
+    """Exact (or block-sparse) decode for B sequences of one layer.
+
+    q: float32 [B, nq, hd]; k8_list[b]: int8 [n_b, nkv, hd]; ks_list[b]:
+    float32 [n_b, nkv] (same for V).  Returns out float32 [B, nq, hd] and,
+    for sparse, sel int32 [B, nq, topk] (-1 padded)."""
+    q = np.ascontiguousarray(q, np.float32)
+    B, nq, hd = q.shape
+    k_rows, v_rows, ks, vs, offs, lens, nkv = _pack_layer(k8_list, ks_list, v8_list, vs_list, hd,
+                                                          kv_bs)
     out = np.empty((B, nq, hd), np.float32)
     sel = np.full((B, nq, max(1, topk)), -1, np.int32) if sparse else None
     rc = lib().kq8o_decode_batch(out.ctypes.data_as(_P), q.ctypes.data_as(_P),
@@ -359,6 +370,35 @@ def decode_batch(q, k8_list, ks_list, v8_list, vs_list, scale, kv_bs=32, sparse=
                                  sel.ctypes.data_as(_P) if sparse else None, int(nthreads))
     if rc != 0:
         raise ValueError("oracle: unsupported shape")
+    return (out, sel[:, :, :topk]) if sparse else out
+
+
+def prefill_batch(q, q_lens, k8_list, ks_list, v8_list, vs_list, scale, kv_bs=32, sparse=False,
+                  block=32, topk=32, probe=8, nthreads=0):
+    """Batched causal prefill for B sequences of one layer (see kq8o_prefill_batch).
+
+    q: float32 [total_q, nq, hd], packed by sequence; q_lens[b] = nb_b new
+    tokens of sequence b, the last nb_b of its cache (k8_list[b] etc. as in
+    decode_batch).  Returns out float32 [total_q, nq, hd] and, for sparse,
+    sel int32 [total_q, nq, topk] (-1 padded)."""
+    q = np.ascontiguousarray(q, np.float32)
+    T, nq, hd = q.shape
+    q_off = np.zeros(len(k8_list) + 1, np.int32)
+    q_off[1:] = np.cumsum(np.asarray(q_lens, np.int64))
+    assert int(q_off[-1]) == T
+    k_rows, v_rows, ks, vs, offs, lens, nkv = _pack_layer(k8_list, ks_list, v8_list, vs_list, hd,
+                                                          kv_bs)
+    out = np.empty((T, nq, hd), np.float32)
+    sel = np.full((T, nq, max(1, topk)), -1, np.int32) if sparse else None
+    rc = lib().kq8o_prefill_batch(out.ctypes.data_as(_P), q.ctypes.data_as(_P),
+                                  k_rows.ctypes.data_as(_P), v_rows.ctypes.data_as(_P),
+                                  ks.ctypes.data_as(_P), vs.ctypes.data_as(_P),
+                                  offs.ctypes.data_as(_P), lens.ctypes.data_as(_P),
+                                  q_off.ctypes.data_as(_P), len(k8_list), nq, nkv, hd, kv_bs,
+                                  float(np.float32(scale)), int(sparse), block, topk, probe,
+                                  sel.ctypes.data_as(_P) if sparse else None, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle: unsupported shape or q_lens")
     return (out, sel[:, :, :topk]) if sparse else out
 
 

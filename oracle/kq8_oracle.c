@@ -494,6 +494,65 @@ int kq8o_decode_batch(float* out, const float* q, int8_t* k_rows, int8_t* v_rows
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Batched prefill over the same layout ([10-1] §1: a batch of nb new tokens */
+/* scores against the whole history, O(nb*n) exact or O(nb*k*block) sparse;  */
+/* §2: the prefill gate picks the exact or the block-sparse batched kernel).  */
+/* Queries are packed: sequence b owns query rows q_off[b] .. q_off[b+1]-1,   */
+/* nb_b = q_off[b+1] - q_off[b] of them, and its cache already holds those    */
+/* tokens, so seq_lens[b] >= nb_b.                                            */
+/* READING (the pages give no formula for the batched kernel): query i of     */
+/* sequence b is the token at position p = seq_lens[b] - nb_b + i and sees    */
+/* tokens 0..p (causal), each query handled exactly as one decode query with  */
+/* seq_len = p + 1 -- same Q quantisation, score, one-pass online softmax and */
+/* single divide; with sparse set, the block-sparse head over that prefix,    */
+/* whose own gate (n <= 2*block -> exact) applies per query.                  */
+/* out: [total_q][nq][hd]; sel_out (sparse, optional): [total_q][nq][topk].   */
+/* ------------------------------------------------------------------------ */
+int kq8o_prefill_batch(float* out, const float* q, int8_t* k_rows, int8_t* v_rows,
+                       const float* kscale, const float* vscale, const int64_t* row_offset,
+                       const int32_t* seq_lens, const int32_t* q_off, int B, int nq, int nkv,
+                       int hd, int kv_bs, float scale, int sparse, int block, int topk, int probe,
+                       int32_t* sel_out, int nthreads) {
+    if (hd > KQ8O_MAX_HD || hd % 32 != 0 || nkv <= 0 || nq % nkv != 0) return -1;
+    for (int b = 0; b < B; b++) {
+        int nb = q_off[b + 1] - q_off[b];
+        if (nb < 0 || nb > seq_lens[b]) return -1;
+    }
+    int G = nq / nkv;
+    int kv_dim = nkv * hd;
+    int64_t units = (int64_t)q_off[B] * nq;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t u = 0; u < units; u++) {
+        int r = (int)(u / nq), h = (int)(u % nq);
+        int b = 0;
+        while (q_off[b + 1] <= r) b++;
+        int nb = q_off[b + 1] - q_off[b];
+        int n = seq_lens[b] - nb + (r - q_off[b]) + 1; /* visible prefix */
+        int kh = h / G;
+        int8_t** kb = make_block_ptrs(k_rows, row_offset[b], seq_lens[b], kv_bs, kv_dim);
+        int8_t** vb = make_block_ptrs(v_rows, row_offset[b], seq_lens[b], kv_bs, kv_dim);
+        const float* ks = kscale + (size_t)row_offset[b] * nkv + kh;
+        const float* vs = vscale + (size_t)row_offset[b] * nkv + kh;
+        float* o = out + (size_t)u * hd;
+        const float* qq = q + (size_t)u * hd;
+        if (sparse)
+            kq8o_sparse_attn_head(o, qq, kb, vb, ks, vs, n, kv_dim, kv_bs, nkv, kh * hd, hd, scale,
+                                  block, topk, probe, sel_out ? sel_out + (size_t)u * topk : NULL);
+        else
+            kq8o_attn_single_q(o, qq, kb, vb, ks, vs, n, kv_dim, kv_bs, nkv, kh * hd, hd, scale,
+                               NULL, 0, NULL, NULL);
+        free(kb);
+        free(vb);
+    }
+    return 0;
+}
+
 /* Write path over a batch of rows: x[T][nkv][hd] -> codes[T][nkv][hd] and
  * stored maxima[T][nkv] ([9-3] §2, applied per (token, head)). */
 void kq8o_kv_quantize_rows(const float* x, int64_t T, int nkv, int hd, int8_t* codes, float* maxima) {

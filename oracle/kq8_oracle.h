@@ -51,6 +51,11 @@ int kq8o_decode_batch(float* out, const float* q, int8_t* k_rows, int8_t* v_rows
                       const int32_t* seq_lens, int B, int nq, int nkv, int hd, int kv_bs,
                       float scale, int sparse, int block, int topk, int probe, int32_t* sel_out,
                       int nthreads);
+int kq8o_prefill_batch(float* out, const float* q, int8_t* k_rows, int8_t* v_rows,
+                       const float* kscale, const float* vscale, const int64_t* row_offset,
+                       const int32_t* seq_lens, const int32_t* q_off, int B, int nq, int nkv,
+                       int hd, int kv_bs, float scale, int sparse, int block, int topk, int probe,
+                       int32_t* sel_out, int nthreads);
 int kq8o_has_openmp(void);
 
 #endif
