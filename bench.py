@@ -73,10 +73,11 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources) -> str:
+    """Hash of the csrc files a kernel and its launch plan are built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "query_decode_attention_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(sources):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -91,7 +92,7 @@ def committed_traffic(kernel: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(kernel)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(e.get("sources", [])):
         return None, None
     return e.get("bytes_per_unit"), e.get("unit")
 
