@@ -241,6 +241,41 @@ int kq8_state_finalize(float* out, const float* state_acc, const float* state_ms
                        kq8_stream_t stream);
 
 /*
+ * Batched causal prefill attention over the q8 cache ([10-1] §1: a batch of nb
+ * new tokens scores against the whole history, O(nb*n); §2: the exact batched
+ * kernel of the prefill gate).  Reading (the page gives no formula for the
+ * batched kernel): each new token is one decode query of [9-2] §2 over the
+ * tokens up to and including itself.
+ *   out, q      : float [total_q][nq][128] (device, 16-byte aligned); the new
+ *                 tokens' queries packed by sequence: sequence b owns rows
+ *                 q_offsets[b] .. q_offsets[b+1]-1.
+ *   q_offsets   : int32 [B+1] (device), non-decreasing, q_offsets[B] <= total_q.
+ *   seq_lens    : int32 [B] (device): tokens in the cache for sequence b,
+ *                 INCLUDING its nb_b = q_offsets[b+1] - q_offsets[b] new ones
+ *                 (append them with kq8_append_kv first).  New token i sits at
+ *                 position seq_lens[b] - nb_b + i and attends tokens 0 .. that
+ *                 position.
+ *   max_seq_len, max_q_len : host bounds on seq_lens[b] and nb_b (grid size).
+ *   cache, page_table, max_pages, scale : as kq8_decode_attn.
+ *   workspace   : >= kq8_prefill_workspace_bytes(...) bytes, 256-byte aligned,
+ *                 its status word cleared by kq8_workspace_init.
+ * A sequence whose bounds are inconsistent (nb_b > seq_lens[b], seq_lens[b] >
+ * max_seq_len, nb_b > max_q_len, rows outside total_q) sets
+ * KQ8_STATUS_BAD_SEQLEN and is skipped (its outputs are not written); a page
+ * id outside the pool sets KQ8_STATUS_BAD_PAGE and its 32-token sub-tiles are
+ * left out.  Results match one kq8_decode_attn per new token to fp32
+ * rounding.  Runs on the tcgen05 tensor cores: 128 (token, query head) rows
+ * per CTA, exact integer block dots in fp32 TMEM accumulators.
+ */
+size_t kq8_prefill_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len,
+                                   int32_t max_q_len);
+int kq8_prefill_attn(float* out, const float* q, int32_t total_q, const kq8_cache_t* cache,
+                     const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                     const int32_t* q_offsets, int32_t max_seq_len, int32_t max_q_len, int32_t B,
+                     int32_t nq, float scale, void* workspace, size_t workspace_bytes,
+                     kq8_stream_t stream);
+
+/*
  * Copies the status word of `workspace` (or of a kq8_append_kv status word) to
  * *status (host), then clears it; synchronises `stream`.
  */

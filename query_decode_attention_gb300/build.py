@@ -1,6 +1,6 @@
 """Builds libkq8.so in-tree with nvcc for sm_103a (GB300).
 
-The four translation units compile in parallel; the result is
+The translation units compile in parallel; the result is
 ``query_decode_attention_gb300/_build/libkq8.so``.  No CMake, no torch
 extension machinery: a plain shared library with a C ABI (include/kq8.h).
 """
@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libkq8.so")
 
-SOURCES = ["kq8_attn.cu", "kq8_sparse.cu", "kq8_misc.cu", "kq8_api.cu"]
+SOURCES = ["kq8_attn.cu", "kq8_sparse.cu", "kq8_misc.cu", "kq8_api.cu", "kq8_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I" + INCLUDE,
               "-I" + CSRC]

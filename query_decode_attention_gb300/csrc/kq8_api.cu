@@ -100,22 +100,10 @@ Plan plan_sparse(int B, int nq, int nkv, int max_seq_len, int block, int topk) {
     return p;
 }
 
-int check_cache(const kq8_cache_t* c) {
-    if (!c) return KQ8_ERR_INVALID_ARG;
-    if (c->head_dim != HD) return KQ8_ERR_UNSUPPORTED;
-    if (c->kv_bs < TILE || c->kv_bs > 256 || c->kv_bs % TILE != 0) return KQ8_ERR_UNSUPPORTED;
-    if (c->num_kv_heads < 1 || c->num_pages < 1) return KQ8_ERR_INVALID_ARG;
-    if (!c->k || !c->v || !c->kscale || !c->vscale) return KQ8_ERR_INVALID_ARG;
-    if (!aligned(c->k, 16) || !aligned(c->v, 16) || !aligned(c->kscale, 16) ||
-        !aligned(c->vscale, 16))
-        return KQ8_ERR_INVALID_ARG;
-    return KQ8_OK;
-}
-
 int check_decode(float* out, const float* q, const kq8_cache_t* c, const int32_t* pt,
                  int32_t max_pages, const int32_t* seq_lens, int32_t max_seq_len, int32_t B,
                  int32_t nq) {
-    int rc = check_cache(c);
+    int rc = check_cache_args(c);
     if (rc) return rc;
     if (B < 0 || nq < 1 || max_seq_len < 0 || max_pages < 0) return KQ8_ERR_INVALID_ARG;
     if (nq % c->num_kv_heads != 0) return KQ8_ERR_UNSUPPORTED;
@@ -164,6 +152,19 @@ AttnParams attn_params(float* out, const float* q, const kq8_cache_t* c, const i
 }
 
 }  // namespace
+
+int check_cache_args(const kq8_cache_t* c) {
+    if (!c) return KQ8_ERR_INVALID_ARG;
+    if (c->head_dim != HD) return KQ8_ERR_UNSUPPORTED;
+    if (c->kv_bs < TILE || c->kv_bs > 256 || c->kv_bs % TILE != 0) return KQ8_ERR_UNSUPPORTED;
+    if (c->num_kv_heads < 1 || c->num_pages < 1) return KQ8_ERR_INVALID_ARG;
+    if (!c->k || !c->v || !c->kscale || !c->vscale) return KQ8_ERR_INVALID_ARG;
+    if (!aligned(c->k, 16) || !aligned(c->v, 16) || !aligned(c->kscale, 16) ||
+        !aligned(c->vscale, 16))
+        return KQ8_ERR_INVALID_ARG;
+    return KQ8_OK;
+}
+
 }  // namespace kq8
 
 using namespace kq8;
@@ -185,7 +186,7 @@ const char* kq8_strerror(int code) {
 
 int kq8_append_kv(const kq8_cache_t* cache, const float* k, const float* v, const int32_t* slot,
                   int32_t T, uint32_t* status, kq8_stream_t stream) {
-    int rc = check_cache(cache);
+    int rc = check_cache_args(cache);
     if (rc) return rc;
     if (T < 0) return KQ8_ERR_INVALID_ARG;
     if (T == 0) return KQ8_OK;

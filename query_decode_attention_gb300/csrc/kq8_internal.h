@@ -9,6 +9,11 @@ namespace kq8 {
 
 struct AttnParams;
 struct SparseParams;
+struct PrefillParams;
+
+// Shared argument checks of a kq8_cache_t (head_dim 128, kv_bs a multiple of
+// 32 up to 256, 16-byte aligned arrays); returns a KQ8_ERR_* code or KQ8_OK.
+int check_cache_args(const kq8_cache_t* c);
 
 int launch_append(const kq8_cache_t& c, const float* k, const float* v, const int32_t* slot,
                   int32_t T, uint32_t* status, cudaStream_t stream);
@@ -23,6 +28,7 @@ int launch_probe(const SparseParams& p, int G, int B, int nkv, cudaStream_t s);
 int launch_state_reset(float* acc, float2* ms, int rows, cudaStream_t s);
 int launch_state_finalize(float* out, const float* acc, const float2* ms, int rows, cudaStream_t s);
 int probe_blocks_per_cta(int block, int kv_bs);
+int launch_prefill(const PrefillParams& p, int G, int nkv, cudaStream_t s);
 int launch_topk(const SparseParams& p, int G, int B, int nkv, cudaStream_t s);
 
 }  // namespace kq8

@@ -1,0 +1,523 @@
+// kq8_prefill.cu -- batched causal prefill attention over the q8 cache on the
+// 5th-generation tensor cores.
+//
+// Article 10-1 §1 ("why long context must be sparse"): a batch of nb new
+// tokens scores against the whole history, an nb x n score matrix; §2 names
+// the exact batched kernel the prefill gate falls back to.  Each query is
+// computed like one decode query (article 9-2 §2): Q quantised once in
+// 32-element max-abs blocks, score = ((sum_b dot_b * qsc_b) * ks) * scale with
+// int32 block dots, one-pass online softmax, one divide at the end.  Query i
+// of a sequence with nb new tokens and n cached tokens sits at position
+// n - nb + i and sees tokens 0 .. n - nb + i.
+//
+// GB300 mapping.  A CTA takes 128 (token, query head) rows of one sequence and
+// one KV head -- 128 / G consecutive new tokens x the G query heads sharing
+// the KV head -- and walks the KV history in 32-token cache sub-tiles:
+//   1. K and V codes are read once per CTA and widened exactly to 16-bit
+//      (K -> fp16, V -> bf16; every int8 is exact in both) into the
+//      tensor-core operand layout in shared memory.
+//   2. S: four MMAs pairs (M = 128, N = 32, K = 16) per sub-tile, one per
+//      32-element quantisation block, each into its own TMEM accumulator, so
+//      every block dot is the exact integer (|sum| < 2^19 in fp32).
+//   3. Each thread owns one row (one TMEM lane): it forms the scores from the
+//      four block dots exactly as a decode query does, runs the online
+//      softmax (rescaling its O row in TMEM only when the running max grows
+//      by more than 2^8), and writes the weights w = p * vscale / 127 as a bf16
+//      high part and a bf16 remainder (w = hi + lo to 2^-17 relative).
+//   4. O += W_hi V + W_lo V: four MMAs (M = 128, N = 128, K = 16) into a
+//      128-column TMEM accumulator that lives for the whole CTA.
+// One thread issues every MMA; completion comes back through mbarriers.
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kq8_internal.h"
+#include "kq8_tc.cuh"
+
+namespace kq8 {
+namespace {
+
+constexpr int PF_THREADS = 128;
+constexpr int PF_ROWS = 128;             // MMA M: (token, head) rows per CTA
+constexpr int PF_NT = TILE;              // KV tokens per step: one cache sub-tile
+constexpr uint32_t PF_TMEM_COLS = 256;   // O (128 columns) + 4 block-dot accumulators (32 each)
+constexpr uint32_t PF_COL_D = 128;       // first block-dot column
+
+// Shared memory map (bytes).  Every operand is K-major without swizzle: 8-row
+// x 16-byte core matrices, 128 B each, rows of a core matrix adjacent.
+constexpr uint32_t SM_Q = 0;             // fp16 Q codes: 128 rows x 128 dims (32 KB)
+constexpr uint32_t SM_K = 32768;         // fp16 K codes: 32 tokens x 128 dims (8 KB)
+constexpr uint32_t SM_V = 40960;         // bf16 V codes: 128 dims x 32 tokens (8 KB)
+constexpr uint32_t SM_WHI = 49152;       // bf16 weights, high part: 128 rows x 32 tokens (8 KB)
+constexpr uint32_t SM_WLO = 57344;       // bf16 weights, remainder (8 KB)
+constexpr uint32_t SM_KS = 65536;        // 32 floats: kscale / 127 of the sub-tile's tokens
+constexpr uint32_t SM_VS = 65664;        // 32 floats: vscale / 127
+constexpr uint32_t SM_BAR = 65792;       // two mbarriers: S done, PV done
+constexpr uint32_t SM_TMEM = 65808;      // TMEM base address written by the allocator
+// 96 KB per CTA: two CTAs per SM, which is what two 256-column TMEM
+// allocations allow (a third would wait in the allocator).
+constexpr uint32_t PF_SMEM = 98304;
+
+constexpr size_t PF_STATUS_BYTES = 256;  // workspace: the status word (256-byte slot)
+
+constexpr float PF_LOG2E = 1.4426950408889634f;
+constexpr float PF_RESCALE_SLACK = 8.0f;  // log2 units: rescale O when the max grows > 2^8
+
+// Byte offset of the 16-byte chunk holding elements 8*kc .. 8*kc+7 of row r in
+// a K-major operand of R rows: core matrices adjacent along K are R*16 B apart
+// (leading byte offset), along the rows 128 B apart (stride byte offset).
+__device__ __forceinline__ uint32_t cm_off(int r, int kc, int R) {
+    return (uint32_t)(kc * R * 16 + (r >> 3) * 128 + (r & 7) * 16);
+}
+
+__device__ __forceinline__ float pf_ex2(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Two int8 codes (bytes 2*which, 2*which+1 of w) -> two exact fp16 values:
+// offset-binary byte u = c + 128 in the mantissa of 1024, minus 1152.
+__device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t w, int which) {
+    const uint32_t u = w ^ 0x80808080u;
+    uint32_t x = __byte_perm(u, 0x64646464u, which ? 0x4342u : 0x4140u);
+    __half2 hv = *reinterpret_cast<__half2*>(&x);
+    hv = __hsub2(hv, __float2half2_rn(1152.0f));
+    return *reinterpret_cast<uint32_t*>(&hv);
+}
+
+__device__ __forceinline__ uint32_t bf2_bits(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t h2_bits(int lo, int hi) {
+    __half2 v = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// One 32-token sub-tile of one KV head as this thread holds it in registers
+// between the global loads and the shared-memory stores.
+struct Raw {
+    uint4 k0, k1;     // K codes of token `lane`, dims 32*warp .. 32*warp+31
+    uint32_t v[8];    // V codes of tokens 8*warp .. +7, dims 4*lane .. +3
+    float sc;         // kscale (threads 0-31) or vscale (32-63) of token tid % 32
+    bool ok;          // page id in range
+};
+
+}  // namespace
+
+struct PrefillParams {
+    float* out;
+    const float* q;
+    kq8_cache_t cache;
+    const int32_t* page_table;
+    int32_t max_pages;
+    const int32_t* seq_lens;
+    const int32_t* q_off;
+    int32_t total_q;
+    int32_t max_seq_len;
+    int32_t max_q_len;
+    int32_t B;
+    int32_t nq;
+    float scale;
+    uint32_t* status;
+};
+
+template <int G>
+__global__ void __launch_bounds__(PF_THREADS, 2) kq8_prefill_kernel(const PrefillParams P) {
+    constexpr int TQ = PF_ROWS / G;  // new tokens per CTA
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int nkv = P.cache.num_kv_heads, kv_bs = P.cache.kv_bs;
+    const int qt = gridDim.x - 1 - blockIdx.x;  // the longest query tiles start first
+
+    const int n = P.seq_lens[b];
+    const int q0 = P.q_off[b];
+    const int nb = P.q_off[b + 1] - q0;
+    if (n < 0 || n > P.max_seq_len || nb < 0 || nb > n || nb > P.max_q_len || q0 < 0 ||
+        (int64_t)q0 + nb > P.total_q) {
+        if (tid == 0 && blockIdx.x == 0 && h == 0) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
+        return;
+    }
+    const int i0 = qt * TQ;
+    if (i0 >= nb) return;
+    const int ntok = min(TQ, nb - i0);
+    const int tq = tid / G, g = tid % G;
+    const bool valid = tid < TQ * G && tq < ntok;
+    const int pos = valid ? n - nb + i0 + tq : -1;  // this row sees tokens 0 .. pos
+    const int ntiles = (n - nb + i0 + ntok - 1) / PF_NT + 1;
+
+    uint64_t* bar_s = reinterpret_cast<uint64_t*>(sm + SM_BAR);
+    uint64_t* bar_pv = bar_s + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SM_TMEM);
+    if (warp == 0) {
+        __syncwarp();
+        tc::tmem_alloc(tslot, PF_TMEM_COLS);
+    }
+    if (tid == 0) {
+        mbar_init(bar_s, 1);
+        mbar_init(bar_pv, 1);
+        fence_barrier_init();
+    }
+
+    // ---- Q: quantise this row once (article 9-2 §2 segment 1) -> fp16 codes
+    float qsc[NB];
+    {
+        uint8_t* Qs = sm + SM_Q;
+        const float4* src = reinterpret_cast<const float4*>(
+            P.q + ((size_t)(q0 + i0 + tq) * P.nq + (size_t)h * G + g) * HD);
+#pragma unroll
+        for (int blk = 0; blk < NB; blk++) {
+            float4 x[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                if (valid)
+                    x[i] = src[blk * 8 + i];
+                else
+                    x[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(x[i].x), fabsf(x[i].y)),
+                                   fmaxf(fabsf(x[i].z), fabsf(x[i].w))));
+            if (m < 1e-6f) m = 1.0f;
+            qsc[blk] = __fmul_rn(m, inv127());
+            const float iq = __fdiv_rn(127.0f, m);
+            auto code = [&](float v) -> int {
+                float t = __fmul_rn(v, iq);
+                t = fminf(fmaxf(t, -128.0f), 127.0f);
+                return __float2int_rz(t);
+            };
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                const float4 a = x[2 * c], e = x[2 * c + 1];
+                const uint4 w = make_uint4(h2_bits(code(a.x), code(a.y)),
+                                           h2_bits(code(a.z), code(a.w)),
+                                           h2_bits(code(e.x), code(e.y)),
+                                           h2_bits(code(e.z), code(e.w)));
+                *reinterpret_cast<uint4*>(Qs + cm_off(tid, blk * 4 + c, PF_ROWS)) = w;
+            }
+        }
+    }
+    tc::fence_smem_to_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tbase = *tslot;
+    const uint32_t t_lane = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
+
+    // ---- KV sub-tile loads (global -> registers), one tile ahead
+    const float* ks_s = reinterpret_cast<const float*>(sm + SM_KS);
+    const float* vs_s = reinterpret_cast<const float*>(sm + SM_VS);
+    auto load = [&](int j, Raw& r) {
+        const int t0 = j * PF_NT;
+        const int32_t pg = P.page_table[(size_t)b * P.max_pages + t0 / kv_bs];
+        r.ok = pg >= 0 && pg < P.cache.num_pages;
+        r.sc = 0.0f;
+        if (!r.ok) {
+            r.k0 = r.k1 = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int tt = 0; tt < 8; tt++) r.v[tt] = 0;
+            return;
+        }
+        const int sub = (t0 % kv_bs) / PF_NT;
+        const size_t kvo = kv_sub_off(pg, h, nkv, kv_bs, sub);
+        const uint4* kp =
+            reinterpret_cast<const uint4*>(P.cache.k + kvo + warp * 1024 + kpos(lane) * 32);
+        r.k0 = __ldg(kp);
+        r.k1 = __ldg(kp + 1);
+        const uint32_t* vp =
+            reinterpret_cast<const uint32_t*>(P.cache.v + kvo + (size_t)warp * 8 * HD) + lane;
+#pragma unroll
+        for (int tt = 0; tt < 8; tt++) r.v[tt] = __ldg(vp + tt * (HD / 4));
+        if (tid < 64 && t0 + (tid & 31) < n) {
+            const size_t so = scale_sub_off(pg, h, nkv, kv_bs, sub) + (tid & 31);
+            r.sc = tid < 32 ? __ldg(P.cache.kscale + so) : __ldg(P.cache.vscale + so);
+        }
+    };
+    // registers -> 16-bit operands in shared memory
+    auto stage = [&](const Raw& r) {
+        uint8_t* Ks = sm + SM_K;
+        const uint32_t kw[8] = {r.k0.x, r.k0.y, r.k0.z, r.k0.w, r.k1.x, r.k1.y, r.k1.z, r.k1.w};
+#pragma unroll
+        for (int c = 0; c < 4; c++)
+            *reinterpret_cast<uint4*>(Ks + cm_off(lane, warp * 4 + c, PF_NT)) =
+                make_uint4(i8x2_to_h2(kw[2 * c], 0), i8x2_to_h2(kw[2 * c], 1),
+                           i8x2_to_h2(kw[2 * c + 1], 0), i8x2_to_h2(kw[2 * c + 1], 1));
+        // V is stored transposed (dims as rows, tokens along K): one 16-byte
+        // chunk = 8 tokens of one dim.  The dim order is rotated per lane pair
+        // so that the eight lanes of each store phase hit eight bank groups.
+        uint8_t* Vs = sm + SM_V;
+        uint32_t u[8];
+#pragma unroll
+        for (int tt = 0; tt < 8; tt++) u[tt] = r.v[tt] ^ 0x80808080u;
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            const int ee = (e + (lane >> 1)) & 3;
+            const uint32_t sel = 0x7540u | (uint32_t)ee;
+            float f[8];
+#pragma unroll
+            for (int tt = 0; tt < 8; tt++)
+                f[tt] = __fsub_rn(__uint_as_float(__byte_perm(u[tt], 0x4B000000u, sel)),
+                                  8388736.0f);
+            *reinterpret_cast<uint4*>(Vs + cm_off(4 * lane + ee, warp, PF_ROWS)) =
+                make_uint4(bf2_bits(f[0], f[1]), bf2_bits(f[2], f[3]), bf2_bits(f[4], f[5]),
+                           bf2_bits(f[6], f[7]));
+        }
+        if (tid < 64)
+            reinterpret_cast<float*>(sm + (tid < 32 ? SM_KS : SM_VS))[tid & 31] =
+                __fmul_rn(r.sc, inv127());
+    };
+
+    float M2 = M_INIT, Mhi = M_INIT + PF_RESCALE_SLACK, S = 0.0f;
+    bool alive = true;
+    uint64_t* fail_bar = nullptr;
+    uint32_t fail_par = 0;
+    Raw raw;
+    load(0, raw);
+    for (int j = 0; j < ntiles; j++) {
+        bool ok = true;
+        if (j > 0) {
+            ok = mbar_wait_bounded(bar_pv, (j - 1) & 1);  // W and V buffers free again
+            fail_bar = bar_pv;
+            fail_par = (j - 1) & 1;
+        }
+        if (ok) stage(raw);
+        const bool tile_ok = raw.ok;
+        if (j + 1 < ntiles) load(j + 1, raw);
+        tc::fence_smem_to_async();
+        if (!__syncthreads_and(ok)) {
+            alive = false;
+            break;
+        }
+        if (tid == 0) {
+            if (!tile_ok) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
+            tc::fence_after_sync();
+            const uint32_t qa = smem_u32(sm + SM_Q), ka = smem_u32(sm + SM_K);
+            constexpr uint32_t ID = tc::IDesc<128, PF_NT, false>::value;
+#pragma unroll
+            for (int blk = 0; blk < NB; blk++)
+#pragma unroll
+                for (int kk = 0; kk < 2; kk++) {
+                    const int kc = blk * 4 + kk * 2;
+                    tc::mma_f16(tbase + PF_COL_D + 32 * blk,
+                                tc::sdesc(qa + kc * PF_ROWS * 16, PF_ROWS * 16, 128),
+                                tc::sdesc(ka + kc * PF_NT * 16, PF_NT * 16, 128), ID, kk > 0);
+                }
+            tc::mma_commit(bar_s);
+        }
+        ok = mbar_wait_bounded(bar_s, j & 1);
+        if (!__syncthreads_and(ok)) {
+            fail_bar = bar_s;
+            fail_par = j & 1;
+            alive = false;
+            break;
+        }
+        tc::fence_after_sync();
+        __syncwarp();  // tcgen05.ld/st are warp-collective (.sync.aligned)
+
+        // ---- scores of this row against the sub-tile (article 9-2 §2 seg. 2)
+        float s[PF_NT];
+        {
+            float d[PF_NT];
+            tc::tmem_ld32(tbase + t_lane + PF_COL_D, d);
+#pragma unroll
+            for (int t = 0; t < PF_NT; t++) s[t] = __fmul_rn(d[t], qsc[0]);
+#pragma unroll
+            for (int blk = 1; blk < NB; blk++) {
+                tc::tmem_ld32(tbase + t_lane + PF_COL_D + 32 * blk, d);
+#pragma unroll
+                for (int t = 0; t < PF_NT; t++) s[t] = __fadd_rn(s[t], __fmul_rn(d[t], qsc[blk]));
+            }
+        }
+        const int t0 = j * PF_NT;
+        const int nvis = tile_ok ? max(0, min(PF_NT, pos - t0 + 1)) : 0;
+        float mt = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < PF_NT; t++) {
+            s[t] = __fmul_rn(__fmul_rn(__fmul_rn(s[t], ks_s[t]), P.scale), PF_LOG2E);
+            if (t < nvis) mt = fmaxf(mt, s[t]);
+        }
+        // ---- lazy rescale of S and of this row of O (the online-softmax max)
+        const bool need = mt > Mhi;
+        float cf = 1.0f;
+        if (need) {
+            cf = pf_ex2(M2 - mt);
+            S = __fmul_rn(S, cf);
+            M2 = mt;
+            Mhi = mt + PF_RESCALE_SLACK;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+            for (int c = 0; c < HD / 32; c++) {
+                float o[32];
+                tc::tmem_ld32(tbase + t_lane + 32 * c, o);
+#pragma unroll
+                for (int i = 0; i < 32; i++) o[i] = __fmul_rn(o[i], cf);
+                tc::tmem_st32(tbase + t_lane + 32 * c, o);
+            }
+        }
+        // ---- weights w = p * vscale / 127 as bf16 hi + lo
+        uint8_t* Wh = sm + SM_WHI;
+        uint8_t* Wl = sm + SM_WLO;
+#pragma unroll
+        for (int c = 0; c < PF_NT / 8; c++) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int u2 = 0; u2 < 4; u2++) {
+                const int t = 8 * c + 2 * u2;
+                const float p0 = (t < nvis) ? pf_ex2(s[t] - M2) : 0.0f;
+                const float p1 = (t + 1 < nvis) ? pf_ex2(s[t + 1] - M2) : 0.0f;
+                S = __fadd_rn(S, p0);
+                S = __fadd_rn(S, p1);
+                const float w0 = __fmul_rn(p0, vs_s[t]), w1 = __fmul_rn(p1, vs_s[t + 1]);
+                __nv_bfloat162 hv = __floats2bfloat162_rn(w0, w1);
+                const float2 hf = __bfloat1622float2(hv);
+                hi[u2] = *reinterpret_cast<uint32_t*>(&hv);
+                lo[u2] = bf2_bits(__fsub_rn(w0, hf.x), __fsub_rn(w1, hf.y));
+            }
+            *reinterpret_cast<uint4*>(Wh + cm_off(tid, c, PF_ROWS)) =
+                make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(Wl + cm_off(tid, c, PF_ROWS)) =
+                make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        tc::fence_before_sync();
+        tc::fence_smem_to_async();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint32_t va = smem_u32(sm + SM_V), ha = smem_u32(sm + SM_WHI),
+                           la = smem_u32(sm + SM_WLO);
+            constexpr uint32_t ID = tc::IDesc<128, HD, true>::value;
+#pragma unroll
+            for (int kk = 0; kk < PF_NT / 16; kk++) {
+                const uint32_t off = (uint32_t)(kk * 2) * PF_ROWS * 16;
+                const uint64_t vd = tc::sdesc(va + off, PF_ROWS * 16, 128);
+                tc::mma_f16(tbase, tc::sdesc(ha + off, PF_ROWS * 16, 128), vd, ID, j > 0 || kk > 0);
+                tc::mma_f16(tbase, tc::sdesc(la + off, PF_ROWS * 16, 128), vd, ID, true);
+            }
+            tc::mma_commit(bar_pv);
+        }
+    }
+
+    if (alive) {
+        const bool ok = mbar_wait_bounded(bar_pv, (ntiles - 1) & 1);
+        if (!__syncthreads_and(ok)) {
+            alive = false;
+            fail_bar = bar_pv;
+            fail_par = (ntiles - 1) & 1;
+        }
+    }
+    if (alive) {
+        tc::fence_after_sync();
+        __syncwarp();
+        const float inv_ok = S > 0.0f ? 1.0f : 0.0f;  // no visible token: 0 (pages' empty case)
+        const float Sd = S > 0.0f ? S : 1.0f;
+        float* dst = P.out + ((size_t)(q0 + i0 + tq) * P.nq + (size_t)h * G + g) * HD;
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; c++) {
+            float o[32];
+            tc::tmem_ld32(tbase + t_lane + 32 * c, o);
+            if (valid) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<float4*>(dst + 32 * c + i) =
+                        make_float4(__fdiv_rn(o[i], Sd) * inv_ok, __fdiv_rn(o[i + 1], Sd) * inv_ok,
+                                    __fdiv_rn(o[i + 2], Sd) * inv_ok,
+                                    __fdiv_rn(o[i + 3], Sd) * inv_ok);
+            }
+        }
+    } else {
+        // a completion never came: record it, give the tensor core one more
+        // bounded wait, then release TMEM without touching the outputs
+        if (tid == 0) atomicOr(P.status, KQ8_STATUS_TIMEOUT);
+        if (fail_bar) mbar_wait_bounded(fail_bar, fail_par);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tbase, PF_TMEM_COLS);
+    }
+}
+
+template <int G>
+int launch_prefill_g(const PrefillParams& p, int nkv, cudaStream_t s) {
+    constexpr int TQ = PF_ROWS / G;
+    if (cudaFuncSetAttribute(kq8_prefill_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PF_SMEM) != cudaSuccess)
+        return KQ8_ERR_CUDA;
+    const dim3 grid((unsigned)((p.max_q_len + TQ - 1) / TQ), (unsigned)nkv, (unsigned)p.B);
+    kq8_prefill_kernel<G><<<grid, PF_THREADS, PF_SMEM, s>>>(p);
+    return cudaPeekAtLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+}
+
+int launch_prefill(const PrefillParams& p, int G, int nkv, cudaStream_t s) {
+    switch (G) {
+        case 1: return launch_prefill_g<1>(p, nkv, s);
+        case 2: return launch_prefill_g<2>(p, nkv, s);
+        case 3: return launch_prefill_g<3>(p, nkv, s);
+        case 4: return launch_prefill_g<4>(p, nkv, s);
+        case 5: return launch_prefill_g<5>(p, nkv, s);
+        case 6: return launch_prefill_g<6>(p, nkv, s);
+        case 7: return launch_prefill_g<7>(p, nkv, s);
+        case 8: return launch_prefill_g<8>(p, nkv, s);
+        default: return KQ8_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace kq8
+
+using namespace kq8;
+
+extern "C" {
+
+size_t kq8_prefill_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len,
+                                   int32_t max_q_len) {
+    (void)B, (void)nq, (void)nkv, (void)max_seq_len, (void)max_q_len;
+    return PF_STATUS_BYTES;
+}
+
+int kq8_prefill_attn(float* out, const float* q, int32_t total_q, const kq8_cache_t* cache,
+                     const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                     const int32_t* q_offsets, int32_t max_seq_len, int32_t max_q_len, int32_t B,
+                     int32_t nq, float scale, void* workspace, size_t workspace_bytes,
+                     kq8_stream_t stream) {
+    int rc = check_cache_args(cache);
+    if (rc) return rc;
+    if (B < 0 || nq < 1 || total_q < 0 || max_seq_len < 0 || max_q_len < 0 || max_pages < 0)
+        return KQ8_ERR_INVALID_ARG;
+    const int nkv = cache->num_kv_heads;
+    if (nq % nkv != 0 || nq / nkv > MAX_G) return KQ8_ERR_UNSUPPORTED;
+    if ((int64_t)max_seq_len > (int64_t)max_pages * cache->kv_bs) return KQ8_ERR_INVALID_ARG;
+    if (max_q_len > max_seq_len) return KQ8_ERR_INVALID_ARG;
+    if (max_seq_len >= (1 << 29) || B > 65535) return KQ8_ERR_UNSUPPORTED;
+    if (!workspace || (uintptr_t)workspace % 256 != 0 ||
+        workspace_bytes < kq8_prefill_workspace_bytes(B, nq, nkv, max_seq_len, max_q_len))
+        return KQ8_ERR_WORKSPACE;
+    if (B == 0 || max_q_len == 0) return KQ8_OK;
+    if (!out || !q || !seq_lens || !q_offsets || !page_table) return KQ8_ERR_INVALID_ARG;
+    if ((uintptr_t)out % 16 != 0 || (uintptr_t)q % 16 != 0) return KQ8_ERR_INVALID_ARG;
+    PrefillParams p;
+    p.out = out;
+    p.q = q;
+    p.cache = *cache;
+    p.page_table = page_table;
+    p.max_pages = max_pages;
+    p.seq_lens = seq_lens;
+    p.q_off = q_offsets;
+    p.total_q = total_q;
+    p.max_seq_len = max_seq_len;
+    p.max_q_len = max_q_len;
+    p.B = B;
+    p.nq = nq;
+    p.scale = scale;
+    p.status = static_cast<uint32_t*>(workspace);
+    return launch_prefill(p, nq / nkv, nkv, (cudaStream_t)stream);
+}
+
+}  // extern "C"

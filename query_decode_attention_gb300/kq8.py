@@ -72,6 +72,10 @@ _lib.kq8_state_reset.argtypes = [_P, _P, _I32, _P]
 _lib.kq8_decode_attn_update.argtypes = [_P, _P, _P, _CP, _P, _I32, _P, _P, _I32, _I32, _I32,
                                         ctypes.c_float, _P, _SZ, _P]
 _lib.kq8_state_finalize.argtypes = [_P, _P, _P, _I32, _P]
+_lib.kq8_prefill_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32]
+_lib.kq8_prefill_workspace_bytes.restype = _SZ
+_lib.kq8_prefill_attn.argtypes = [_P, _P, _I32, _CP, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
+                                  ctypes.c_float, _P, _SZ, _P]
 _lib.kq8_read_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), _P]
 _lib.kq8_strerror.argtypes = [ctypes.c_int]
 _lib.kq8_strerror.restype = ctypes.c_char_p
@@ -302,6 +306,36 @@ def kq8_state_finalize(out: torch.Tensor, state: AttnState, stream=None) -> None
     rows = state.acc.numel() // HEAD_DIM
     _check(_lib.kq8_state_finalize(_ptr(out), _ptr(state.acc), _ptr(state.ms), rows,
                                    _stream(stream)), "kq8_state_finalize")
+
+
+def kq8_prefill_workspace_bytes(B: int, nq: int, nkv: int, max_seq_len: int,
+                                max_q_len: int) -> int:
+    return int(_lib.kq8_prefill_workspace_bytes(B, nq, nkv, max_seq_len, max_q_len))
+
+
+def kq8_prefill_attn(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
+                     page_table: torch.Tensor, seq_lens: torch.Tensor, q_offsets: torch.Tensor,
+                     max_seq_len: int, max_q_len: int, scale: float, workspace: torch.Tensor,
+                     stream=None) -> None:
+    """Batched causal prefill attention (include/kq8.h): q and out are
+    [total_q, nq, 128], packed by sequence per q_offsets [B+1]; seq_lens
+    counts each sequence's cached tokens including its new ones."""
+    _dtype(out, torch.float32, "out")
+    _dtype(q, torch.float32, "q")
+    _dtype(page_table, torch.int32, "page_table")
+    _dtype(seq_lens, torch.int32, "seq_lens")
+    _dtype(q_offsets, torch.int32, "q_offsets")
+    if q.dim() != 3 or q.shape[2] != HEAD_DIM or out.shape != q.shape:
+        raise ValueError("q and out must be [total_q, nq, 128]")
+    B = seq_lens.numel()
+    if q_offsets.numel() != B + 1 or page_table.dim() != 2 or page_table.shape[0] != B:
+        raise ValueError("q_offsets must be [B+1] and page_table [B, max_pages]")
+    _check(_lib.kq8_prefill_attn(_ptr(out), _ptr(q), q.shape[0], ctypes.byref(cache.struct),
+                                 _ptr(page_table), page_table.shape[1], _ptr(seq_lens),
+                                 _ptr(q_offsets), int(max_seq_len), int(max_q_len), B, q.shape[1],
+                                 float(scale), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)),
+           "kq8_prefill_attn")
 
 
 def kq8_read_status(word: torch.Tensor, stream=None) -> int:

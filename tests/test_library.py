@@ -99,6 +99,31 @@ def test_argument_validation_without_device(lib):
     assert sp(*args, 32, 0, 8, None, 512, 1 << 20, None) == lib.KQ8_ERR_UNSUPPORTED    # topk 0
 
 
+def _prefill(lib, cache, B=1, nq=16, total_q=8, max_seq_len=64, max_q_len=8, max_pages=2,
+             ws=512, ws_bytes=1 << 20, out=256, q=256, pt=256, sl=256, qo=256):
+    return lib._lib.kq8_prefill_attn(out, q, total_q, ctypes.byref(cache), pt, max_pages, sl, qo,
+                                     max_seq_len, max_q_len, B, nq, 0.1, ws, ws_bytes, None)
+
+
+def test_prefill_argument_validation_without_device(lib):
+    ok = _cache_struct(lib)
+    assert lib.kq8_prefill_workspace_bytes(4, 16, 8, 4096, 512) >= 256
+    assert _prefill(lib, _cache_struct(lib, head_dim=64)) == lib.KQ8_ERR_UNSUPPORTED
+    assert _prefill(lib, _cache_struct(lib, kv_bs=40)) == lib.KQ8_ERR_UNSUPPORTED
+    assert _prefill(lib, ok, nq=12) == lib.KQ8_ERR_UNSUPPORTED         # nq % nkv
+    assert _prefill(lib, ok, nq=72) == lib.KQ8_ERR_UNSUPPORTED         # G = 9
+    assert _prefill(lib, ok, max_seq_len=100) == lib.KQ8_ERR_INVALID_ARG  # > max_pages * kv_bs
+    assert _prefill(lib, ok, max_q_len=65) == lib.KQ8_ERR_INVALID_ARG  # more new than cached
+    assert _prefill(lib, ok, total_q=-1) == lib.KQ8_ERR_INVALID_ARG
+    assert _prefill(lib, ok, out=264) == lib.KQ8_ERR_INVALID_ARG        # 8-B aligned only
+    assert _prefill(lib, ok, qo=None) == lib.KQ8_ERR_INVALID_ARG
+    assert _prefill(lib, ok, ws=None) == lib.KQ8_ERR_WORKSPACE
+    assert _prefill(lib, ok, ws=512 + 64) == lib.KQ8_ERR_WORKSPACE     # not 256-B aligned
+    assert _prefill(lib, ok, ws_bytes=16) == lib.KQ8_ERR_WORKSPACE
+    assert _prefill(lib, ok, B=0) == lib.KQ8_OK                        # nothing to do
+    assert _prefill(lib, ok, max_q_len=0) == lib.KQ8_OK
+
+
 def test_product_path_has_no_oracle_or_cpu_fallback():
     pkg = os.path.join(ROOT, "query_decode_attention_gb300")
     for dirpath, _, files in os.walk(pkg):
