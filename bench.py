@@ -35,7 +35,8 @@ import numpy as np  # noqa: E402
 METRIC = "q8-KV decode attention: effective KV GB/s and % of GB300 HBM peak"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-WORKLOADS = ("serving", "long", "sparse", "qwen2b")
+FALLBACK_BF16_TFLOPS = 1900.0
+WORKLOADS = ("serving", "long", "sparse", "qwen2b", "prefill")
 
 
 def parse():
@@ -46,7 +47,8 @@ def parse():
     ap.add_argument("--impl", default="kq8", choices=["kq8", "reference"])
     ap.add_argument("--workload", default="serving", choices=WORKLOADS,
                     help="serving: B=64 ragged 1K-32K, 36 layers (default); long: B=8 n=131072; "
-                         "sparse: block-sparse B=16 n=65536; qwen2b: B=1 n=4059, 28 layers")
+                         "sparse: block-sparse B=16 n=65536; qwen2b: B=1 n=4059, 28 layers; "
+                         "prefill: the causal prefill kernel alone (Qwen3-VL prompts, TFLOP/s)")
     ap.add_argument("--layers", type=int, default=36)
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],
@@ -71,6 +73,17 @@ def measured_peaks():
             d = json.load(f)
         return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_peak():
+    """Dense bf16 tensor peak (burst) for kernels timed alone."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured bf16_tflops (burst)"
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def kernel_source_hash(sources) -> str:
@@ -384,6 +397,9 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
+    if args.workload == "prefill":
+        run_prefill_bench(args)
+        return
 
     import torch
     from query_decode_attention_gb300 import build as kbuild
@@ -574,10 +590,76 @@ def _time_calls(fn, reps, stream):
     return statistics.median(a.elapsed_time(b) for a, b in evs)
 
 
+PREFILL_CASES = (
+    # (name, nq, nkv, prompt tokens): whole prompts in one call -- the longest
+    # Qwen3-VL-2B prompt of the prefill table and an 8K Qwen3-VL-8B prompt
+    ("qwen3vl2b_prompt_n4059", 16, 8, 4059),
+    ("qwen3vl8b_prompt_n8192", 32, 8, 8192),
+)
+
+
+def prefill_flops(nq, n, nb):
+    """Algorithmic FLOPs of one causal prefill call: per (query head, new
+    token, visible token) a 128-long Q.K dot and a 128-wide P.V update,
+    2 * 128 FLOPs each (the kernel's bf16 hi + lo split of P is not counted)."""
+    vis = nb * (n - nb) + nb * (nb + 1) // 2
+    return nq * vis * 4 * 128
+
+
+def prefill_measure(dev, kq8, paged, W, peak_tflops, reps=10, cases=PREFILL_CASES):
+    """Causal prefill of whole prompts, one layer per call, timed alone with
+    CUDA events (median of reps).  The layer's KV (<= 17 MB) stays in L2: the
+    kernel is bound by the tensor and CUDA cores, not by HBM."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for name, nq, nkv, n in cases:
+        wl = W.Workload(name, 1, nq, nkv, np.array([n], np.int32), kind="sigma", seed=2100 + n)
+        case = paged.fill_cache(wl, 0, dev)
+        g = W.device_generator(dev, 7 + n)
+        q = torch.randn((n, nq, wl.hd), generator=g, device=dev)
+        out = torch.empty_like(q)
+        q_off = torch.tensor([0, n], dtype=torch.int32, device=dev)
+        ws = kq8.new_workspace(kq8.kq8_prefill_workspace_bytes(1, nq, nkv, n, n), dev)
+        ms = _time_calls(lambda: kq8.kq8_prefill_attn(out, q, case.cache, case.page_table,
+                                                      case.seq_lens, q_off, n, n, wl.scale, ws,
+                                                      stream=stream), reps, stream)
+        tf = prefill_flops(nq, n, n) / (ms * 1e-3) / 1e12
+        res[name] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                     "frac_of_bf16_peak": round(tf / peak_tflops, 4),
+                     "flops": prefill_flops(nq, n, n), "status_word": kq8.kq8_read_status(ws)}
+        del case, q, out
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_prefill_bench(args):
+    """--workload prefill: the prefill kernel alone, one JSON line."""
+    import torch
+    from query_decode_attention_gb300 import build as kbuild
+    kbuild.build()
+    from query_decode_attention_gb300 import kq8, paged
+    from query_decode_attention_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak, kind = measured_bf16_peak()
+    res = prefill_measure(dev, kq8, paged, W, peak, reps=max(3, args.steps))
+    name, r = next(iter(res.items()))
+    print(json.dumps({"metric": "q8-KV causal prefill attention TFLOP/s", "value": r["TFLOP/s"],
+                      "unit": "TFLOP/s", "n_gpus": 1, "higher_is_better": True,
+                      "dtype": "int8 codes as fp16/bf16 operands, fp32 TMEM accumulators",
+                      "config": {"workload": name, "cases": list(res)},
+                      "roofline": {"bound": "tensor", "achieved": r["TFLOP/s"], "peak": peak,
+                                   "unit": "TFLOP/s", "frac": r["frac_of_bf16_peak"],
+                                   "peak_kind": kind},
+                      "cases": res}))
+
+
 def extras(dev, kq8, paged, W, peak):
-    """Secondary measurements: long-context exact decode, the write path and
-    the block-sparse path (each timed alone with CUDA events, median of reps;
-    every working set exceeds L2)."""
+    """Secondary measurements: long-context exact decode, the streaming form,
+    the write path and the block-sparse path (each timed alone with CUDA
+    events, median of reps; every working set exceeds L2), then the causal
+    prefill kernel (compute-bound; its per-layer KV stays in L2)."""
     import torch
     stream = torch.cuda.current_stream(dev)
     res = {}
@@ -647,6 +729,10 @@ def extras(dev, kq8, paged, W, peak):
                             "speedup_vs_exact": round(ms_ex / ms, 2),
                             "probe_plus_selected_bytes": probe_bytes + sel_bytes,
                             "exact_GB/s": round(wl.kv_bytes_per_layer() / (ms_ex * 1e-3) / 1e9, 1)}
+    del case, out, ws, wsx
+    torch.cuda.empty_cache()
+    # causal prefill of whole prompts on the tensor cores
+    res["prefill"] = prefill_measure(dev, kq8, paged, W, measured_bf16_peak()[0])
     return res
 
 

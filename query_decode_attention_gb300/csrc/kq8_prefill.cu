@@ -50,7 +50,7 @@ constexpr uint32_t SM_K = 32768;         // fp16 K codes: 32 tokens x 128 dims (
 constexpr uint32_t SM_V = 40960;         // bf16 V codes: 128 dims x 32 tokens (8 KB)
 constexpr uint32_t SM_WHI = 49152;       // bf16 weights, high part: 128 rows x 32 tokens (8 KB)
 constexpr uint32_t SM_WLO = 57344;       // bf16 weights, remainder (8 KB)
-constexpr uint32_t SM_KS = 65536;        // 32 floats: kscale / 127 of the sub-tile's tokens
+constexpr uint32_t SM_KS = 65536;        // 32 floats: kscale / 127 * scale * log2(e) per token
 constexpr uint32_t SM_VS = 65664;        // 32 floats: vscale / 127
 constexpr uint32_t SM_BAR = 65792;       // two mbarriers: S done, PV done
 constexpr uint32_t SM_TMEM = 65808;      // TMEM base address written by the allocator
@@ -210,8 +210,8 @@ __global__ void __launch_bounds__(PF_THREADS, 2) kq8_prefill_kernel(const Prefil
     const uint32_t t_lane = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
 
     // ---- KV sub-tile loads (global -> registers), one tile ahead
-    const float* ks_s = reinterpret_cast<const float*>(sm + SM_KS);
-    const float* vs_s = reinterpret_cast<const float*>(sm + SM_VS);
+    // per-token score multiplier kscale * (1/127) * scale * log2(e)
+    const float kmul = inv127() * P.scale * PF_LOG2E;
     auto load = [&](int j, Raw& r) {
         const int t0 = j * PF_NT;
         const int32_t pg = P.page_table[(size_t)b * P.max_pages + t0 / kv_bs];
@@ -258,21 +258,26 @@ __global__ void __launch_bounds__(PF_THREADS, 2) kq8_prefill_kernel(const Prefil
         for (int e = 0; e < 4; e++) {
             const int ee = (e + (lane >> 1)) & 3;
             const uint32_t sel = 0x7540u | (uint32_t)ee;
-            float f[8];
+            const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+            float2 f[4];
 #pragma unroll
-            for (int tt = 0; tt < 8; tt++)
-                f[tt] = __fsub_rn(__uint_as_float(__byte_perm(u[tt], 0x4B000000u, sel)),
-                                  8388736.0f);
+            for (int q2 = 0; q2 < 4; q2++)
+                f[q2] = __fadd2_rn(
+                    make_float2(__uint_as_float(__byte_perm(u[2 * q2], 0x4B000000u, sel)),
+                                __uint_as_float(__byte_perm(u[2 * q2 + 1], 0x4B000000u, sel))),
+                    bias);
             *reinterpret_cast<uint4*>(Vs + cm_off(4 * lane + ee, warp, PF_ROWS)) =
-                make_uint4(bf2_bits(f[0], f[1]), bf2_bits(f[2], f[3]), bf2_bits(f[4], f[5]),
-                           bf2_bits(f[6], f[7]));
+                make_uint4(bf2_bits(f[0].x, f[0].y), bf2_bits(f[1].x, f[1].y),
+                           bf2_bits(f[2].x, f[2].y), bf2_bits(f[3].x, f[3].y));
         }
         if (tid < 64)
             reinterpret_cast<float*>(sm + (tid < 32 ? SM_KS : SM_VS))[tid & 31] =
-                __fmul_rn(r.sc, inv127());
+                __fmul_rn(r.sc, tid < 32 ? kmul : inv127());
     };
 
-    float M2 = M_INIT, Mhi = M_INIT + PF_RESCALE_SLACK, S = 0.0f;
+    float M2 = M_INIT, Mhi = M_INIT + PF_RESCALE_SLACK;
+    float2 S2 = make_float2(0.0f, 0.0f);  // running sum, even and odd tokens
+    const int pos_first = n - nb + i0;    // position of the CTA's first new token
     bool alive = true;
     uint64_t* fail_bar = nullptr;
     uint32_t fail_par = 0;
@@ -319,34 +324,48 @@ __global__ void __launch_bounds__(PF_THREADS, 2) kq8_prefill_kernel(const Prefil
         tc::fence_after_sync();
         __syncwarp();  // tcgen05.ld/st are warp-collective (.sync.aligned)
 
-        // ---- scores of this row against the sub-tile (article 9-2 §2 seg. 2)
-        float s[PF_NT];
+        // ---- scores of this row against the sub-tile (article 9-2 §2 seg. 2):
+        // s = sum_b dot_b * qsc_b, then times kscale * (1/127) * scale, in log2
+        // units for ex2 (one multiplier per token, staged with the tile)
+        float2 x[PF_NT / 2];
         {
             float d[PF_NT];
             tc::tmem_ld32(tbase + t_lane + PF_COL_D, d);
+            const float2 c0 = make_float2(qsc[0], qsc[0]);
 #pragma unroll
-            for (int t = 0; t < PF_NT; t++) s[t] = __fmul_rn(d[t], qsc[0]);
+            for (int i = 0; i < PF_NT / 2; i++) x[i] = __fmul2_rn(make_float2(d[2 * i], d[2 * i + 1]), c0);
 #pragma unroll
             for (int blk = 1; blk < NB; blk++) {
                 tc::tmem_ld32(tbase + t_lane + PF_COL_D + 32 * blk, d);
+                const float2 cb = make_float2(qsc[blk], qsc[blk]);
 #pragma unroll
-                for (int t = 0; t < PF_NT; t++) s[t] = __fadd_rn(s[t], __fmul_rn(d[t], qsc[blk]));
+                for (int i = 0; i < PF_NT / 2; i++)
+                    x[i] = __ffma2_rn(make_float2(d[2 * i], d[2 * i + 1]), cb, x[i]);
             }
         }
+        const float2* km2 = reinterpret_cast<const float2*>(sm + SM_KS);
+#pragma unroll
+        for (int i = 0; i < PF_NT / 2; i++) x[i] = __fmul2_rn(x[i], km2[i]);
         const int t0 = j * PF_NT;
+        // every row of the CTA sees every token of this sub-tile: no masking
+        const bool full = tile_ok && t0 + PF_NT - 1 <= pos_first;
         const int nvis = tile_ok ? max(0, min(PF_NT, pos - t0 + 1)) : 0;
+        if (!full) {
+#pragma unroll
+            for (int i = 0; i < PF_NT / 2; i++) {
+                if (2 * i >= nvis) x[i].x = -INFINITY;
+                if (2 * i + 1 >= nvis) x[i].y = -INFINITY;
+            }
+        }
         float mt = -INFINITY;
 #pragma unroll
-        for (int t = 0; t < PF_NT; t++) {
-            s[t] = __fmul_rn(__fmul_rn(__fmul_rn(s[t], ks_s[t]), P.scale), PF_LOG2E);
-            if (t < nvis) mt = fmaxf(mt, s[t]);
-        }
+        for (int i = 0; i < PF_NT / 2; i++) mt = fmaxf(mt, fmaxf(x[i].x, x[i].y));
         // ---- lazy rescale of S and of this row of O (the online-softmax max)
         const bool need = mt > Mhi;
         float cf = 1.0f;
         if (need) {
             cf = pf_ex2(M2 - mt);
-            S = __fmul_rn(S, cf);
+            S2 = __fmul2_rn(S2, make_float2(cf, cf));
             M2 = mt;
             Mhi = mt + PF_RESCALE_SLACK;
         }
@@ -360,24 +379,28 @@ __global__ void __launch_bounds__(PF_THREADS, 2) kq8_prefill_kernel(const Prefil
                 tc::tmem_st32(tbase + t_lane + 32 * c, o);
             }
         }
-        // ---- weights w = p * vscale / 127 as bf16 hi + lo
+        // ---- weights w = p * vscale / 127 = hi + lo: hi is w cut to bf16
+        // (its top 16 bits), lo = w - hi (exact) rounded to bf16
         uint8_t* Wh = sm + SM_WHI;
         uint8_t* Wl = sm + SM_WLO;
+        const float2* vs2 = reinterpret_cast<const float2*>(sm + SM_VS);
+        const float2 negm = make_float2(-M2, -M2);
 #pragma unroll
         for (int c = 0; c < PF_NT / 8; c++) {
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int u2 = 0; u2 < 4; u2++) {
-                const int t = 8 * c + 2 * u2;
-                const float p0 = (t < nvis) ? pf_ex2(s[t] - M2) : 0.0f;
-                const float p1 = (t + 1 < nvis) ? pf_ex2(s[t + 1] - M2) : 0.0f;
-                S = __fadd_rn(S, p0);
-                S = __fadd_rn(S, p1);
-                const float w0 = __fmul_rn(p0, vs_s[t]), w1 = __fmul_rn(p1, vs_s[t + 1]);
-                __nv_bfloat162 hv = __floats2bfloat162_rn(w0, w1);
-                const float2 hf = __bfloat1622float2(hv);
-                hi[u2] = *reinterpret_cast<uint32_t*>(&hv);
-                lo[u2] = bf2_bits(__fsub_rn(w0, hf.x), __fsub_rn(w1, hf.y));
+                const int i = 4 * c + u2;
+                const float2 y = __fadd2_rn(x[i], negm);  // -inf (masked) -> ex2 = 0
+                const float2 pr = make_float2(pf_ex2(y.x), pf_ex2(y.y));
+                S2 = __fadd2_rn(S2, pr);
+                const float2 w = __fmul2_rn(pr, vs2[i]);
+                const uint32_t wx = __float_as_uint(w.x), wy = __float_as_uint(w.y);
+                hi[u2] = __byte_perm(wx, wy, 0x7632);
+                const float2 hf = make_float2(__uint_as_float(wx & 0xFFFF0000u),
+                                              __uint_as_float(wy & 0xFFFF0000u));
+                const float2 r = __fadd2_rn(w, make_float2(-hf.x, -hf.y));
+                lo[u2] = bf2_bits(r.x, r.y);
             }
             *reinterpret_cast<uint4*>(Wh + cm_off(tid, c, PF_ROWS)) =
                 make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -414,6 +437,7 @@ __global__ void __launch_bounds__(PF_THREADS, 2) kq8_prefill_kernel(const Prefil
     if (alive) {
         tc::fence_after_sync();
         __syncwarp();
+        const float S = S2.x + S2.y;
         const float inv_ok = S > 0.0f ? 1.0f : 0.0f;  // no visible token: 0 (pages' empty case)
         const float Sd = S > 0.0f ? S : 1.0f;
         float* dst = P.out + ((size_t)(q0 + i0 + tq) * P.nq + (size_t)h * G + g) * HD;
