@@ -44,19 +44,27 @@ constexpr uint32_t PF_TMEM_COLS = 256;   // O (128 columns) + 4 block-dot accumu
 constexpr uint32_t PF_COL_D = 128;       // first block-dot column
 
 // Shared memory map (bytes).  Every operand is K-major without swizzle: 8-row
-// x 16-byte core matrices, 128 B each, rows of a core matrix adjacent.
+// x 16-byte core matrices, 128 B each, rows of a core matrix adjacent.  K, V,
+// the weights and the per-token scales are double-buffered by sub-tile parity
+// so that the tensor core works on one sub-tile while the CUDA cores prepare
+// the next.
 constexpr uint32_t SM_Q = 0;             // fp16 Q codes: 128 rows x 128 dims (32 KB)
-constexpr uint32_t SM_K = 32768;         // fp16 K codes: 32 tokens x 128 dims (8 KB)
-constexpr uint32_t SM_V = 40960;         // bf16 V codes: 128 dims x 32 tokens (8 KB)
-constexpr uint32_t SM_WHI = 49152;       // bf16 weights, high part: 128 rows x 32 tokens (8 KB)
-constexpr uint32_t SM_WLO = 57344;       // bf16 weights, remainder (8 KB)
-constexpr uint32_t SM_KS = 65536;        // 32 floats: kscale / 127 * scale * log2(e) per token
-constexpr uint32_t SM_VS = 65664;        // 32 floats: vscale / 127
-constexpr uint32_t SM_BAR = 65792;       // two mbarriers: S done, PV done
-constexpr uint32_t SM_TMEM = 65808;      // TMEM base address written by the allocator
-// 96 KB per CTA: two CTAs per SM, which is what two 256-column TMEM
+constexpr uint32_t SM_K = 32768;         // 2 x fp16 K codes: 32 tokens x 128 dims (8 KB each)
+constexpr uint32_t SM_V = 49152;         // 2 x bf16 V codes: 128 dims x 32 tokens (8 KB each)
+constexpr uint32_t SM_W = 65536;         // 2 x (bf16 weights hi, lo): 128 rows x 32 tokens (16 KB)
+constexpr uint32_t SM_SC = 98304;        // 2 x (32 score multipliers, 32 value steps) (256 B)
+constexpr uint32_t SM_BAR = 98816;       // two mbarriers: S done, PV done
+constexpr uint32_t SM_TMEM = 98832;      // TMEM base address written by the allocator
+// 97 KB per CTA: two CTAs per SM, which is what two 256-column TMEM
 // allocations allow (a third would wait in the allocator).
-constexpr uint32_t PF_SMEM = 98304;
+constexpr uint32_t PF_SMEM = 99328;
+
+__device__ __forceinline__ uint32_t sm_k(int p) { return SM_K + 8192u * p; }
+__device__ __forceinline__ uint32_t sm_v(int p) { return SM_V + 8192u * p; }
+__device__ __forceinline__ uint32_t sm_whi(int p) { return SM_W + 16384u * p; }
+__device__ __forceinline__ uint32_t sm_wlo(int p) { return SM_W + 16384u * p + 8192u; }
+__device__ __forceinline__ uint32_t sm_km(int p) { return SM_SC + 256u * p; }
+__device__ __forceinline__ uint32_t sm_vs(int p) { return SM_SC + 256u * p + 128u; }
 
 constexpr size_t PF_STATUS_BYTES = 256;  // workspace: the status word (256-byte slot)
 
@@ -97,12 +105,16 @@ __device__ __forceinline__ uint32_t h2_bits(int lo, int hi) {
 }
 
 // One 32-token sub-tile of one KV head as this thread holds it in registers
-// between the global loads and the shared-memory stores.
-struct Raw {
+// between the global loads and the shared-memory stores: the K half (with
+// the page lookup and the scales) and the V half are loaded one sub-tile
+// apart in the pipeline, so each has a whole step to arrive.
+struct RawK {
     uint4 k0, k1;     // K codes of token `lane`, dims 32*warp .. 32*warp+31
-    uint32_t v[8];    // V codes of tokens 8*warp .. +7, dims 4*lane .. +3
     float sc;         // kscale (threads 0-31) or vscale (32-63) of token tid % 32
-    bool ok;          // page id in range
+    int32_t pg;       // page id (-1 when out of range)
+};
+struct RawV {
+    uint32_t v[8];    // V codes of tokens 8*warp .. +7, dims 4*lane .. +3
 };
 
 }  // namespace
@@ -209,56 +221,69 @@ __global__ void __launch_bounds__(PF_THREADS, 2) kq8_prefill_kernel(const Prefil
     const uint32_t tbase = *tslot;
     const uint32_t t_lane = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
 
-    // ---- KV sub-tile loads (global -> registers), one tile ahead
+    // ---- KV sub-tile loads (global -> registers)
     // per-token score multiplier kscale * (1/127) * scale * log2(e)
     const float kmul = inv127() * P.scale * PF_LOG2E;
-    auto load = [&](int j, Raw& r) {
+    auto load_k = [&](int j, RawK& r) {
         const int t0 = j * PF_NT;
         const int32_t pg = P.page_table[(size_t)b * P.max_pages + t0 / kv_bs];
-        r.ok = pg >= 0 && pg < P.cache.num_pages;
         r.sc = 0.0f;
-        if (!r.ok) {
+        if (pg < 0 || pg >= P.cache.num_pages) {
+            r.pg = -1;
             r.k0 = r.k1 = make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int tt = 0; tt < 8; tt++) r.v[tt] = 0;
             return;
         }
+        r.pg = pg;
         const int sub = (t0 % kv_bs) / PF_NT;
         const size_t kvo = kv_sub_off(pg, h, nkv, kv_bs, sub);
         const uint4* kp =
             reinterpret_cast<const uint4*>(P.cache.k + kvo + warp * 1024 + kpos(lane) * 32);
         r.k0 = __ldg(kp);
         r.k1 = __ldg(kp + 1);
-        const uint32_t* vp =
-            reinterpret_cast<const uint32_t*>(P.cache.v + kvo + (size_t)warp * 8 * HD) + lane;
-#pragma unroll
-        for (int tt = 0; tt < 8; tt++) r.v[tt] = __ldg(vp + tt * (HD / 4));
         if (tid < 64 && t0 + (tid & 31) < n) {
             const size_t so = scale_sub_off(pg, h, nkv, kv_bs, sub) + (tid & 31);
             r.sc = tid < 32 ? __ldg(P.cache.kscale + so) : __ldg(P.cache.vscale + so);
         }
     };
-    // registers -> 16-bit operands in shared memory
-    auto stage = [&](const Raw& r) {
-        uint8_t* Ks = sm + SM_K;
+    auto load_v = [&](int j, int32_t pg, RawV& r) {
+        if (pg < 0) {
+#pragma unroll
+            for (int tt = 0; tt < 8; tt++) r.v[tt] = 0;
+            return;
+        }
+        const int t0 = j * PF_NT;
+        const size_t kvo = kv_sub_off(pg, h, nkv, kv_bs, (t0 % kv_bs) / PF_NT);
+        const uint32_t* vp =
+            reinterpret_cast<const uint32_t*>(P.cache.v + kvo + (size_t)warp * 8 * HD) + lane;
+#pragma unroll
+        for (int tt = 0; tt < 8; tt++) r.v[tt] = __ldg(vp + tt * (HD / 4));
+    };
+    // registers -> 16-bit operands of buffer p in shared memory
+    auto stage_k = [&](const RawK& r, int p) {
+        uint8_t* Ks = sm + sm_k(p);
         const uint32_t kw[8] = {r.k0.x, r.k0.y, r.k0.z, r.k0.w, r.k1.x, r.k1.y, r.k1.z, r.k1.w};
 #pragma unroll
         for (int c = 0; c < 4; c++)
             *reinterpret_cast<uint4*>(Ks + cm_off(lane, warp * 4 + c, PF_NT)) =
                 make_uint4(i8x2_to_h2(kw[2 * c], 0), i8x2_to_h2(kw[2 * c], 1),
                            i8x2_to_h2(kw[2 * c + 1], 0), i8x2_to_h2(kw[2 * c + 1], 1));
-        // V is stored transposed (dims as rows, tokens along K): one 16-byte
-        // chunk = 8 tokens of one dim.  The dim order is rotated per lane pair
-        // so that the eight lanes of each store phase hit eight bank groups.
-        uint8_t* Vs = sm + SM_V;
+        if (tid < 64)
+            reinterpret_cast<float*>(sm + (tid < 32 ? sm_km(p) : sm_vs(p)))[tid & 31] =
+                __fmul_rn(r.sc, tid < 32 ? kmul : inv127());
+    };
+    // V is stored transposed (dims as rows, tokens along K): one 16-byte chunk
+    // = 8 tokens of one dim.  The dim order is rotated per lane pair so that
+    // the eight lanes of each store phase hit eight bank groups.
+    auto stage_v = [&](const RawV& r, int p) {
+        uint8_t* Vs = sm + sm_v(p);
         uint32_t u[8];
 #pragma unroll
         for (int tt = 0; tt < 8; tt++) u[tt] = r.v[tt] ^ 0x80808080u;
+        const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
 #pragma unroll
         for (int e = 0; e < 4; e++) {
             const int ee = (e + (lane >> 1)) & 3;
             const uint32_t sel = 0x7540u | (uint32_t)ee;
-            const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
             float2 f[4];
 #pragma unroll
             for (int q2 = 0; q2 < 4; q2++)
@@ -270,160 +295,200 @@ __global__ void __launch_bounds__(PF_THREADS, 2) kq8_prefill_kernel(const Prefil
                 make_uint4(bf2_bits(f[0].x, f[0].y), bf2_bits(f[1].x, f[1].y),
                            bf2_bits(f[2].x, f[2].y), bf2_bits(f[3].x, f[3].y));
         }
-        if (tid < 64)
-            reinterpret_cast<float*>(sm + (tid < 32 ? SM_KS : SM_VS))[tid & 31] =
-                __fmul_rn(r.sc, tid < 32 ? kmul : inv127());
+    };
+    // one thread issues the MMAs of a step
+    auto issue_s = [&](int p) {  // D_blk = Q_blk K_blk^T, blk = 0..3 (exact block dots)
+        const uint32_t qa = smem_u32(sm + SM_Q), ka = smem_u32(sm + sm_k(p));
+        constexpr uint32_t ID = tc::IDesc<128, PF_NT, false>::value;
+#pragma unroll
+        for (int blk = 0; blk < NB; blk++)
+#pragma unroll
+            for (int kk = 0; kk < 2; kk++) {
+                const int kc = blk * 4 + kk * 2;
+                tc::mma_f16(tbase + PF_COL_D + 32 * blk,
+                            tc::sdesc(qa + kc * PF_ROWS * 16, PF_ROWS * 16, 128),
+                            tc::sdesc(ka + kc * PF_NT * 16, PF_NT * 16, 128), ID, kk > 0);
+            }
+        tc::mma_commit(bar_s);
+    };
+    auto issue_pv = [&](int p, bool accumulate) {  // O (+)= W_hi V + W_lo V
+        const uint32_t va = smem_u32(sm + sm_v(p)), ha = smem_u32(sm + sm_whi(p)),
+                       la = smem_u32(sm + sm_wlo(p));
+        constexpr uint32_t ID = tc::IDesc<128, HD, true>::value;
+#pragma unroll
+        for (int kk = 0; kk < PF_NT / 16; kk++) {
+            const uint32_t off = (uint32_t)(kk * 2) * PF_ROWS * 16;
+            const uint64_t vd = tc::sdesc(va + off, PF_ROWS * 16, 128);
+            tc::mma_f16(tbase, tc::sdesc(ha + off, PF_ROWS * 16, 128), vd, ID,
+                        accumulate || kk > 0);
+            tc::mma_f16(tbase, tc::sdesc(la + off, PF_ROWS * 16, 128), vd, ID, true);
+        }
+        tc::mma_commit(bar_pv);
     };
 
+    // ---- pipeline.  Step j (buffer cur = j & 1, nxt = cur ^ 1):
+    //   0. K half of sub-tile j+1 -> buffer nxt (its last reader S(j-1) is done)
+    //   1. wait S(j)
+    //   2. softmax of sub-tile j -> weights in buffer cur (while PV(j-1) runs)
+    //   3. wait PV(j-1); V half of sub-tile j+1 -> buffer nxt
+    //   4. barrier; issue S(j+1), then PV(j)
+    // Global loads run one step ahead of the stores that consume them.
     float M2 = M_INIT, Mhi = M_INIT + PF_RESCALE_SLACK;
     float2 S2 = make_float2(0.0f, 0.0f);  // running sum, even and odd tokens
     const int pos_first = n - nb + i0;    // position of the CTA's first new token
     bool alive = true;
     uint64_t* fail_bar = nullptr;
     uint32_t fail_par = 0;
-    Raw raw;
-    load(0, raw);
-    for (int j = 0; j < ntiles; j++) {
-        bool ok = true;
-        if (j > 0) {
-            ok = mbar_wait_bounded(bar_pv, (j - 1) & 1);  // W and V buffers free again
-            fail_bar = bar_pv;
-            fail_par = (j - 1) & 1;
-        }
-        if (ok) stage(raw);
-        const bool tile_ok = raw.ok;
-        if (j + 1 < ntiles) load(j + 1, raw);
-        tc::fence_smem_to_async();
-        if (!__syncthreads_and(ok)) {
-            alive = false;
-            break;
-        }
-        if (tid == 0) {
-            if (!tile_ok) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
-            tc::fence_after_sync();
-            const uint32_t qa = smem_u32(sm + SM_Q), ka = smem_u32(sm + SM_K);
-            constexpr uint32_t ID = tc::IDesc<128, PF_NT, false>::value;
-#pragma unroll
-            for (int blk = 0; blk < NB; blk++)
-#pragma unroll
-                for (int kk = 0; kk < 2; kk++) {
-                    const int kc = blk * 4 + kk * 2;
-                    tc::mma_f16(tbase + PF_COL_D + 32 * blk,
-                                tc::sdesc(qa + kc * PF_ROWS * 16, PF_ROWS * 16, 128),
-                                tc::sdesc(ka + kc * PF_NT * 16, PF_NT * 16, 128), ID, kk > 0);
-                }
-            tc::mma_commit(bar_s);
-        }
-        ok = mbar_wait_bounded(bar_s, j & 1);
-        if (!__syncthreads_and(ok)) {
-            fail_bar = bar_s;
-            fail_par = j & 1;
-            alive = false;
-            break;
-        }
+    RawK rk;
+    RawV rv;
+    load_k(0, rk);
+    load_v(0, rk.pg, rv);
+    stage_k(rk, 0);
+    stage_v(rv, 0);
+    bool ok_cur = rk.pg >= 0, ok_nxt = false;
+    if (ntiles > 1) {
+        load_k(1, rk);
+        load_v(1, rk.pg, rv);
+    }
+    tc::fence_smem_to_async();
+    __syncthreads();
+    if (tid == 0) {
+        if (!ok_cur) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
         tc::fence_after_sync();
-        __syncwarp();  // tcgen05.ld/st are warp-collective (.sync.aligned)
-
-        // ---- scores of this row against the sub-tile (article 9-2 §2 seg. 2):
-        // s = sum_b dot_b * qsc_b, then times kscale * (1/127) * scale, in log2
-        // units for ex2 (one multiplier per token, staged with the tile)
-        float2 x[PF_NT / 2];
-        {
-            float d[PF_NT];
-            tc::tmem_ld32(tbase + t_lane + PF_COL_D, d);
-            const float2 c0 = make_float2(qsc[0], qsc[0]);
-#pragma unroll
-            for (int i = 0; i < PF_NT / 2; i++) x[i] = __fmul2_rn(make_float2(d[2 * i], d[2 * i + 1]), c0);
-#pragma unroll
-            for (int blk = 1; blk < NB; blk++) {
-                tc::tmem_ld32(tbase + t_lane + PF_COL_D + 32 * blk, d);
-                const float2 cb = make_float2(qsc[blk], qsc[blk]);
+        issue_s(0);
+    }
+    for (int j = 0; j < ntiles; j++) {
+        const int cur = j & 1, nxt = cur ^ 1;
+        const bool more = j + 1 < ntiles;
+        // step 0
+        int32_t pg_after = -1;
+        if (more) {
+            stage_k(rk, nxt);
+            ok_nxt = rk.pg >= 0;
+            if (j + 2 < ntiles) {
+                load_k(j + 2, rk);
+                pg_after = rk.pg;
+            }
+        }
+        // step 1
+        const bool ok_s = __all_sync(0xffffffffu, mbar_wait_bounded(bar_s, j & 1));
+        bool ok_pv = true;
+        if (ok_s) {
+            tc::fence_after_sync();
+            // ---- step 2: scores of this row against the sub-tile (article
+            // 9-2 §2 seg. 2): s = sum_b dot_b * qsc_b, times the token's
+            // kscale / 127 * scale, in log2 units for ex2
+            float2 x[PF_NT / 2];
+            {
+                float d[PF_NT];
+                tc::tmem_ld32(tbase + t_lane + PF_COL_D, d);
+                const float2 c0 = make_float2(qsc[0], qsc[0]);
 #pragma unroll
                 for (int i = 0; i < PF_NT / 2; i++)
-                    x[i] = __ffma2_rn(make_float2(d[2 * i], d[2 * i + 1]), cb, x[i]);
+                    x[i] = __fmul2_rn(make_float2(d[2 * i], d[2 * i + 1]), c0);
+#pragma unroll
+                for (int blk = 1; blk < NB; blk++) {
+                    tc::tmem_ld32(tbase + t_lane + PF_COL_D + 32 * blk, d);
+                    const float2 cb = make_float2(qsc[blk], qsc[blk]);
+#pragma unroll
+                    for (int i = 0; i < PF_NT / 2; i++)
+                        x[i] = __ffma2_rn(make_float2(d[2 * i], d[2 * i + 1]), cb, x[i]);
+                }
             }
-        }
-        const float2* km2 = reinterpret_cast<const float2*>(sm + SM_KS);
+            const float2* km2 = reinterpret_cast<const float2*>(sm + sm_km(cur));
 #pragma unroll
-        for (int i = 0; i < PF_NT / 2; i++) x[i] = __fmul2_rn(x[i], km2[i]);
-        const int t0 = j * PF_NT;
-        // every row of the CTA sees every token of this sub-tile: no masking
-        const bool full = tile_ok && t0 + PF_NT - 1 <= pos_first;
-        const int nvis = tile_ok ? max(0, min(PF_NT, pos - t0 + 1)) : 0;
-        if (!full) {
+            for (int i = 0; i < PF_NT / 2; i++) x[i] = __fmul2_rn(x[i], km2[i]);
+            const int t0 = j * PF_NT;
+            // every row of the CTA sees every token of this sub-tile: no masking
+            const bool full = ok_cur && t0 + PF_NT - 1 <= pos_first;
+            if (!full) {
+                const int nvis = ok_cur ? max(0, min(PF_NT, pos - t0 + 1)) : 0;
 #pragma unroll
-            for (int i = 0; i < PF_NT / 2; i++) {
-                if (2 * i >= nvis) x[i].x = -INFINITY;
-                if (2 * i + 1 >= nvis) x[i].y = -INFINITY;
+                for (int i = 0; i < PF_NT / 2; i++) {
+                    if (2 * i >= nvis) x[i].x = -INFINITY;
+                    if (2 * i + 1 >= nvis) x[i].y = -INFINITY;
+                }
             }
-        }
-        float mt = -INFINITY;
+            float mt = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < PF_NT / 2; i++) mt = fmaxf(mt, fmaxf(x[i].x, x[i].y));
-        // ---- lazy rescale of S and of this row of O (the online-softmax max)
-        const bool need = mt > Mhi;
-        float cf = 1.0f;
-        if (need) {
-            cf = pf_ex2(M2 - mt);
-            S2 = __fmul2_rn(S2, make_float2(cf, cf));
-            M2 = mt;
-            Mhi = mt + PF_RESCALE_SLACK;
-        }
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
+            for (int i = 0; i < PF_NT / 2; i++) mt = fmaxf(mt, fmaxf(x[i].x, x[i].y));
+            // lazy rescale of S and of this row of O (online-softmax max);
+            // O is read only after PV(j-1) has landed
+            const bool need = mt > Mhi;
+            float cf = 1.0f;
+            if (need) {
+                cf = pf_ex2(M2 - mt);
+                S2 = __fmul2_rn(S2, make_float2(cf, cf));
+                M2 = mt;
+                Mhi = mt + PF_RESCALE_SLACK;
+            }
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                ok_pv = __all_sync(0xffffffffu, mbar_wait_bounded(bar_pv, (j - 1) & 1));
+                if (ok_pv) {
+                    tc::fence_after_sync();
 #pragma unroll 1
-            for (int c = 0; c < HD / 32; c++) {
-                float o[32];
-                tc::tmem_ld32(tbase + t_lane + 32 * c, o);
+                    for (int c = 0; c < HD / 32; c++) {
+                        float o[32];
+                        tc::tmem_ld32(tbase + t_lane + 32 * c, o);
 #pragma unroll
-                for (int i = 0; i < 32; i++) o[i] = __fmul_rn(o[i], cf);
-                tc::tmem_st32(tbase + t_lane + 32 * c, o);
+                        for (int i = 0; i < 32; i++) o[i] = __fmul_rn(o[i], cf);
+                        tc::tmem_st32(tbase + t_lane + 32 * c, o);
+                    }
+                }
+            }
+            // weights w = p * vscale / 127 = hi + lo: hi is w cut to bf16 (its
+            // top 16 bits), lo = w - hi (exact) rounded to bf16
+            uint8_t* Wh = sm + sm_whi(cur);
+            uint8_t* Wl = sm + sm_wlo(cur);
+            const float2* vs2 = reinterpret_cast<const float2*>(sm + sm_vs(cur));
+            const float2 negm = make_float2(-M2, -M2);
+#pragma unroll
+            for (int c = 0; c < PF_NT / 8; c++) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int u2 = 0; u2 < 4; u2++) {
+                    const int i = 4 * c + u2;
+                    const float2 y = __fadd2_rn(x[i], negm);  // -inf (masked) -> ex2 = 0
+                    const float2 pr = make_float2(pf_ex2(y.x), pf_ex2(y.y));
+                    S2 = __fadd2_rn(S2, pr);
+                    const float2 w = __fmul2_rn(pr, vs2[i]);
+                    const uint32_t wx = __float_as_uint(w.x), wy = __float_as_uint(w.y);
+                    hi[u2] = __byte_perm(wx, wy, 0x7632);
+                    const float2 r = __fadd2_rn(w, make_float2(-__uint_as_float(wx & 0xFFFF0000u),
+                                                               -__uint_as_float(wy & 0xFFFF0000u)));
+                    lo[u2] = bf2_bits(r.x, r.y);
+                }
+                *reinterpret_cast<uint4*>(Wh + cm_off(tid, c, PF_ROWS)) =
+                    make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(Wl + cm_off(tid, c, PF_ROWS)) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
         }
-        // ---- weights w = p * vscale / 127 = hi + lo: hi is w cut to bf16
-        // (its top 16 bits), lo = w - hi (exact) rounded to bf16
-        uint8_t* Wh = sm + SM_WHI;
-        uint8_t* Wl = sm + SM_WLO;
-        const float2* vs2 = reinterpret_cast<const float2*>(sm + SM_VS);
-        const float2 negm = make_float2(-M2, -M2);
-#pragma unroll
-        for (int c = 0; c < PF_NT / 8; c++) {
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int u2 = 0; u2 < 4; u2++) {
-                const int i = 4 * c + u2;
-                const float2 y = __fadd2_rn(x[i], negm);  // -inf (masked) -> ex2 = 0
-                const float2 pr = make_float2(pf_ex2(y.x), pf_ex2(y.y));
-                S2 = __fadd2_rn(S2, pr);
-                const float2 w = __fmul2_rn(pr, vs2[i]);
-                const uint32_t wx = __float_as_uint(w.x), wy = __float_as_uint(w.y);
-                hi[u2] = __byte_perm(wx, wy, 0x7632);
-                const float2 hf = make_float2(__uint_as_float(wx & 0xFFFF0000u),
-                                              __uint_as_float(wy & 0xFFFF0000u));
-                const float2 r = __fadd2_rn(w, make_float2(-hf.x, -hf.y));
-                lo[u2] = bf2_bits(r.x, r.y);
-            }
-            *reinterpret_cast<uint4*>(Wh + cm_off(tid, c, PF_ROWS)) =
-                make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(Wl + cm_off(tid, c, PF_ROWS)) =
-                make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        // step 3
+        if (ok_s && ok_pv && j > 0)
+            ok_pv = __all_sync(0xffffffffu, mbar_wait_bounded(bar_pv, (j - 1) & 1));
+        if (ok_s && ok_pv && more) {
+            stage_v(rv, nxt);
+            if (j + 2 < ntiles) load_v(j + 2, pg_after, rv);
         }
+        // step 4
         tc::fence_before_sync();
         tc::fence_smem_to_async();
-        __syncthreads();
+        if (!__syncthreads_and(ok_s && ok_pv)) {
+            alive = false;
+            fail_bar = ok_s ? bar_pv : bar_s;
+            fail_par = ok_s ? (uint32_t)((j - 1) & 1) : (uint32_t)(j & 1);
+            break;
+        }
         if (tid == 0) {
             tc::fence_after_sync();
-            const uint32_t va = smem_u32(sm + SM_V), ha = smem_u32(sm + SM_WHI),
-                           la = smem_u32(sm + SM_WLO);
-            constexpr uint32_t ID = tc::IDesc<128, HD, true>::value;
-#pragma unroll
-            for (int kk = 0; kk < PF_NT / 16; kk++) {
-                const uint32_t off = (uint32_t)(kk * 2) * PF_ROWS * 16;
-                const uint64_t vd = tc::sdesc(va + off, PF_ROWS * 16, 128);
-                tc::mma_f16(tbase, tc::sdesc(ha + off, PF_ROWS * 16, 128), vd, ID, j > 0 || kk > 0);
-                tc::mma_f16(tbase, tc::sdesc(la + off, PF_ROWS * 16, 128), vd, ID, true);
+            if (more) {
+                if (!ok_nxt) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
+                issue_s(nxt);
             }
-            tc::mma_commit(bar_pv);
+            issue_pv(cur, j > 0);
         }
+        ok_cur = ok_nxt;
     }
 
     if (alive) {
