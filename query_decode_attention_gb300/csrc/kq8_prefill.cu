@@ -94,6 +94,22 @@ __device__ __forceinline__ uint32_t i8x2_to_h2(uint32_t w, int which) {
     return *reinterpret_cast<uint32_t*>(&hv);
 }
 
+// Read-only global loads kept where they are written (volatile asm): the
+// pipeline issues them a whole step before their data is needed, and a
+// compiler under register pressure would otherwise sink them next to the use.
+__device__ __forceinline__ uint4 ldg_pinned_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint32_t ldg_pinned_u32(const void* p) {
+    uint32_t r;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t bf2_bits(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -224,11 +240,28 @@ __global__ void __launch_bounds__(PF_THREADS, 2) kq8_prefill_kernel(const Prefil
     // ---- KV sub-tile loads (global -> registers)
     // per-token score multiplier kscale * (1/127) * scale * log2(e)
     const float kmul = inv127() * P.scale * PF_LOG2E;
+    // page ids: lane l of every warp holds the page of sub-tile 32*w + l for
+    // the current window w and the next one, so that a page id is a shuffle
+    // away and its global load is a whole window ahead of its use
+    auto load_window = [&](int w) -> int32_t {
+        const int t = 32 * w + lane;
+        if (t >= ntiles) return -1;
+        const int32_t pg = P.page_table[(size_t)b * P.max_pages + (t * PF_NT) / kv_bs];
+        return (pg >= 0 && pg < P.cache.num_pages) ? pg : -1;
+    };
+    int32_t pw_cur = load_window(0), pw_nxt = load_window(1);
+    auto page_of = [&](int t) -> int32_t {  // t = 0, 1, 2, ... in order, warp-uniform
+        if ((t & 31) == 0 && t > 0) {
+            pw_cur = pw_nxt;
+            pw_nxt = load_window((t >> 5) + 1);
+        }
+        return __shfl_sync(0xffffffffu, pw_cur, t & 31);
+    };
     auto load_k = [&](int j, RawK& r) {
         const int t0 = j * PF_NT;
-        const int32_t pg = P.page_table[(size_t)b * P.max_pages + t0 / kv_bs];
+        const int32_t pg = page_of(j);
         r.sc = 0.0f;
-        if (pg < 0 || pg >= P.cache.num_pages) {
+        if (pg < 0) {
             r.pg = -1;
             r.k0 = r.k1 = make_uint4(0, 0, 0, 0);
             return;
@@ -238,11 +271,13 @@ __global__ void __launch_bounds__(PF_THREADS, 2) kq8_prefill_kernel(const Prefil
         const size_t kvo = kv_sub_off(pg, h, nkv, kv_bs, sub);
         const uint4* kp =
             reinterpret_cast<const uint4*>(P.cache.k + kvo + warp * 1024 + kpos(lane) * 32);
-        r.k0 = __ldg(kp);
-        r.k1 = __ldg(kp + 1);
+        r.k0 = ldg_pinned_v4(kp);
+        r.k1 = ldg_pinned_v4(kp + 1);
         if (tid < 64 && t0 + (tid & 31) < n) {
             const size_t so = scale_sub_off(pg, h, nkv, kv_bs, sub) + (tid & 31);
-            r.sc = tid < 32 ? __ldg(P.cache.kscale + so) : __ldg(P.cache.vscale + so);
+            r.sc = __uint_as_float(
+                ldg_pinned_u32(tid < 32 ? (const void*)(P.cache.kscale + so)
+                                        : (const void*)(P.cache.vscale + so)));
         }
     };
     auto load_v = [&](int j, int32_t pg, RawV& r) {
@@ -256,7 +291,7 @@ __global__ void __launch_bounds__(PF_THREADS, 2) kq8_prefill_kernel(const Prefil
         const uint32_t* vp =
             reinterpret_cast<const uint32_t*>(P.cache.v + kvo + (size_t)warp * 8 * HD) + lane;
 #pragma unroll
-        for (int tt = 0; tt < 8; tt++) r.v[tt] = __ldg(vp + tt * (HD / 4));
+        for (int tt = 0; tt < 8; tt++) r.v[tt] = ldg_pinned_u32(vp + tt * (HD / 4));
     };
     // registers -> 16-bit operands of buffer p in shared memory
     auto stage_k = [&](const RawK& r, int p) {
@@ -297,31 +332,34 @@ __global__ void __launch_bounds__(PF_THREADS, 2) kq8_prefill_kernel(const Prefil
         }
     };
     // one thread issues the MMAs of a step
+    // Matrix descriptors of every operand buffer, built once; an MMA at K
+    // chunk kc adds kc * leading-byte-offset / 16 to the start-address field.
+    const uint64_t d_q = tc::sdesc(smem_u32(sm + SM_Q), PF_ROWS * 16, 128);
+    const uint64_t d_k0 = tc::sdesc(smem_u32(sm + sm_k(0)), PF_NT * 16, 128);
+    const uint64_t d_v0 = tc::sdesc(smem_u32(sm + sm_v(0)), PF_ROWS * 16, 128);
+    const uint64_t d_w0 = tc::sdesc(smem_u32(sm + sm_whi(0)), PF_ROWS * 16, 128);
     auto issue_s = [&](int p) {  // D_blk = Q_blk K_blk^T, blk = 0..3 (exact block dots)
-        const uint32_t qa = smem_u32(sm + SM_Q), ka = smem_u32(sm + sm_k(p));
+        const uint64_t dk = d_k0 + (uint64_t)p * (8192u >> 4);
         constexpr uint32_t ID = tc::IDesc<128, PF_NT, false>::value;
 #pragma unroll
         for (int blk = 0; blk < NB; blk++)
 #pragma unroll
             for (int kk = 0; kk < 2; kk++) {
                 const int kc = blk * 4 + kk * 2;
-                tc::mma_f16(tbase + PF_COL_D + 32 * blk,
-                            tc::sdesc(qa + kc * PF_ROWS * 16, PF_ROWS * 16, 128),
-                            tc::sdesc(ka + kc * PF_NT * 16, PF_NT * 16, 128), ID, kk > 0);
+                tc::mma_f16(tbase + PF_COL_D + 32 * blk, d_q + (uint64_t)(kc * PF_ROWS),
+                            dk + (uint64_t)(kc * PF_NT), ID, kk > 0);
             }
         tc::mma_commit(bar_s);
     };
     auto issue_pv = [&](int p, bool accumulate) {  // O (+)= W_hi V + W_lo V
-        const uint32_t va = smem_u32(sm + sm_v(p)), ha = smem_u32(sm + sm_whi(p)),
-                       la = smem_u32(sm + sm_wlo(p));
+        const uint64_t dv = d_v0 + (uint64_t)p * (8192u >> 4);
+        const uint64_t dh = d_w0 + (uint64_t)p * (16384u >> 4), dl = dh + (8192u >> 4);
         constexpr uint32_t ID = tc::IDesc<128, HD, true>::value;
 #pragma unroll
         for (int kk = 0; kk < PF_NT / 16; kk++) {
-            const uint32_t off = (uint32_t)(kk * 2) * PF_ROWS * 16;
-            const uint64_t vd = tc::sdesc(va + off, PF_ROWS * 16, 128);
-            tc::mma_f16(tbase, tc::sdesc(ha + off, PF_ROWS * 16, 128), vd, ID,
-                        accumulate || kk > 0);
-            tc::mma_f16(tbase, tc::sdesc(la + off, PF_ROWS * 16, 128), vd, ID, true);
+            const uint64_t off = (uint64_t)(kk * 2 * PF_ROWS);  // 2 K chunks, in 16-byte units
+            tc::mma_f16(tbase, dh + off, dv + off, ID, accumulate || kk > 0);
+            tc::mma_f16(tbase, dl + off, dv + off, ID, true);
         }
         tc::mma_commit(bar_pv);
     };
