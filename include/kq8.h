@@ -276,6 +276,28 @@ int kq8_prefill_attn(float* out, const float* q, int32_t total_q, const kq8_cach
                      kq8_stream_t stream);
 
 /*
+ * Block-sparse batched prefill ([10-1] §1: the sparse prefill costs
+ * O(nb*k*block) instead of O(nb*n); §2: the prefill gate).  Reading: each new
+ * token is one block-sparse decode query (kq8_sparse_decode_attn) over the
+ * tokens up to and including itself, the gate seq_len <= 2*block applied per
+ * token to that prefix length; selection stays per query head.
+ * Arguments as kq8_prefill_attn plus block, topk, probe and sel_blocks
+ * (optional int32 [total_q][nq][topk], -1 padded) as kq8_sparse_decode_attn;
+ * total_q <= 65535 rows per call.  Rows outside every sequence are written as
+ * zeros; the rows of an inconsistent sequence set KQ8_STATUS_BAD_SEQLEN.
+ * workspace: kq8_sparse_prefill_workspace_bytes(total_q, ...) bytes, status
+ * word cleared by kq8_workspace_init.
+ */
+size_t kq8_sparse_prefill_workspace_bytes(int32_t total_q, int32_t nq, int32_t nkv,
+                                          int32_t max_seq_len, int32_t block, int32_t topk);
+int kq8_sparse_prefill_attn(float* out, const float* q, int32_t total_q, const kq8_cache_t* cache,
+                            const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                            const int32_t* q_offsets, int32_t max_seq_len, int32_t max_q_len,
+                            int32_t B, int32_t nq, float scale, int32_t block, int32_t topk,
+                            int32_t probe, int32_t* sel_blocks, void* workspace,
+                            size_t workspace_bytes, kq8_stream_t stream);
+
+/*
  * Copies the status word of `workspace` (or of a kq8_append_kv status word) to
  * *status (host), then clears it; synchronises `stream`.
  */

@@ -151,6 +151,53 @@ AttnParams attn_params(float* out, const float* q, const kq8_cache_t* c, const i
     return p;
 }
 
+// Probe, top-k and bounded attention over `rows` decode rows (article 10-1
+// §1-§2); row_seq (optional) maps each row to its page-table row.
+int run_sparse(float* out, const float* q, const kq8_cache_t* cache, const int32_t* page_table,
+               int32_t max_pages, const int32_t* row_len, const int32_t* row_seq,
+               int32_t max_seq_len, int32_t rows, int32_t nq, float scale, int32_t block,
+               int32_t topk, int32_t probe, int32_t* sel_blocks, const Plan& plan,
+               void* workspace, cudaStream_t s) {
+    const int nkv = cache->num_kv_heads;
+    const int G = nq / nkv;
+    char* ws = static_cast<char*>(workspace);
+    SparseParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.q = q;
+    sp.cache = *cache;
+    sp.page_table = page_table;
+    sp.max_pages = max_pages;
+    sp.seq_lens = row_len;
+    sp.max_seq_len = max_seq_len;
+    sp.B = rows;
+    sp.nq = nq;
+    sp.scale = scale;
+    sp.block = block;
+    sp.topk = topk;
+    sp.probe = probe;
+    sp.max_nblk = plan.max_nblk;
+    sp.probe_bpc = probe_blocks_per_cta(block, cache->kv_bs);
+    sp.scores = reinterpret_cast<float*>(ws + plan.off_scores);
+    sp.masks = reinterpret_cast<uint8_t*>(ws + plan.off_masks);
+    sp.tile_list = reinterpret_cast<int32_t*>(ws + plan.off_list);
+    sp.list_len = reinterpret_cast<int32_t*>(ws + plan.off_len);
+    sp.list_cap = plan.list_cap;
+    sp.sel_blocks = sel_blocks;
+    sp.status = reinterpret_cast<uint32_t*>(ws);
+    sp.row_seq = row_seq;
+    int rc = launch_probe(sp, G, rows, nkv, s);
+    if (rc) return rc;
+    rc = launch_topk(sp, G, rows, nkv, s);
+    if (rc) return rc;
+    AttnParams p = attn_params(out, q, cache, page_table, max_pages, row_len, max_seq_len, rows,
+                               nq, scale, plan, workspace);
+    p.tile_list = sp.tile_list;
+    p.list_len = sp.list_len;
+    p.list_cap = sp.list_cap;
+    p.row_seq = row_seq;
+    return launch_attn(p, G, true, rows, nkv, s);
+}
+
 }  // namespace
 
 int check_cache_args(const kq8_cache_t* c) {
@@ -262,47 +309,49 @@ int kq8_sparse_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
     if (block < TILE || block % TILE != 0 || topk < 1 || probe < 1 || probe > block)
         return KQ8_ERR_UNSUPPORTED;
     if (sel_blocks && !aligned(sel_blocks, 4)) return KQ8_ERR_INVALID_ARG;
-    const int nkv = cache->num_kv_heads;
-    const int G = nq / nkv;
-    const Plan plan = plan_sparse(B, nq, nkv, max_seq_len, block, topk);
+    const Plan plan = plan_sparse(B, nq, cache->num_kv_heads, max_seq_len, block, topk);
     rc = check_ws(workspace, workspace_bytes, plan.total);
     if (rc) return rc;
     if (B == 0) return KQ8_OK;
-    char* ws = static_cast<char*>(workspace);
-    SparseParams sp;
-    std::memset(&sp, 0, sizeof(sp));
-    sp.q = q;
-    sp.cache = *cache;
-    sp.page_table = page_table;
-    sp.max_pages = max_pages;
-    sp.seq_lens = seq_lens;
-    sp.max_seq_len = max_seq_len;
-    sp.B = B;
-    sp.nq = nq;
-    sp.scale = scale;
-    sp.block = block;
-    sp.topk = topk;
-    sp.probe = probe;
-    sp.max_nblk = plan.max_nblk;
-    sp.probe_bpc = probe_blocks_per_cta(block, cache->kv_bs);
-    sp.scores = reinterpret_cast<float*>(ws + plan.off_scores);
-    sp.masks = reinterpret_cast<uint8_t*>(ws + plan.off_masks);
-    sp.tile_list = reinterpret_cast<int32_t*>(ws + plan.off_list);
-    sp.list_len = reinterpret_cast<int32_t*>(ws + plan.off_len);
-    sp.list_cap = plan.list_cap;
-    sp.sel_blocks = sel_blocks;
-    sp.status = reinterpret_cast<uint32_t*>(ws);
+    return run_sparse(out, q, cache, page_table, max_pages, seq_lens, nullptr, max_seq_len, B, nq,
+                      scale, block, topk, probe, sel_blocks, plan, workspace, (cudaStream_t)stream);
+}
+
+size_t kq8_sparse_prefill_workspace_bytes(int32_t total_q, int32_t nq, int32_t nkv,
+                                          int32_t max_seq_len, int32_t block, int32_t topk) {
+    const size_t base = kq8_sparse_decode_workspace_bytes(total_q, nq, nkv, max_seq_len, block, topk);
+    if (base == 0) return 0;
+    return base + align_up(2 * sizeof(int32_t) * (size_t)total_q, WS_ALIGN);
+}
+
+int kq8_sparse_prefill_attn(float* out, const float* q, int32_t total_q, const kq8_cache_t* cache,
+                            const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                            const int32_t* q_offsets, int32_t max_seq_len, int32_t max_q_len,
+                            int32_t B, int32_t nq, float scale, int32_t block, int32_t topk,
+                            int32_t probe, int32_t* sel_blocks, void* workspace,
+                            size_t workspace_bytes, kq8_stream_t stream) {
+    // the rows are the packed queries: total_q plays the decode batch
+    int rc = check_decode(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, total_q, nq);
+    if (rc) return rc;
+    if (B < 0 || B > 65535 || max_q_len < 0 || max_q_len > max_seq_len) return KQ8_ERR_INVALID_ARG;
+    if (block < TILE || block % TILE != 0 || topk < 1 || probe < 1 || probe > block)
+        return KQ8_ERR_UNSUPPORTED;
+    if (sel_blocks && !aligned(sel_blocks, 4)) return KQ8_ERR_INVALID_ARG;
+    const Plan plan = plan_sparse(total_q, nq, cache->num_kv_heads, max_seq_len, block, topk);
+    rc = check_ws(workspace, workspace_bytes,
+                  kq8_sparse_prefill_workspace_bytes(total_q, nq, cache->num_kv_heads,
+                                                     max_seq_len, block, topk));
+    if (rc) return rc;
+    if (total_q == 0) return KQ8_OK;
+    if (B > 0 && !q_offsets) return KQ8_ERR_INVALID_ARG;
+    int32_t* row_seq = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + plan.total);
+    int32_t* row_len = row_seq + total_q;
     cudaStream_t s = (cudaStream_t)stream;
-    rc = launch_probe(sp, G, B, nkv, s);
+    rc = launch_prefill_rows(row_seq, row_len, q_offsets, seq_lens, B, total_q, max_seq_len,
+                             max_q_len, s);
     if (rc) return rc;
-    rc = launch_topk(sp, G, B, nkv, s);
-    if (rc) return rc;
-    AttnParams p = attn_params(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq,
-                               scale, plan, workspace);
-    p.tile_list = sp.tile_list;
-    p.list_len = sp.list_len;
-    p.list_cap = sp.list_cap;
-    return launch_attn(p, G, true, B, nkv, s);
+    return run_sparse(out, q, cache, page_table, max_pages, row_len, row_seq, max_seq_len, total_q,
+                      nq, scale, block, topk, probe, sel_blocks, plan, workspace, s);
 }
 
 int kq8_state_reset(float* state_acc, float* state_ms, int32_t rows, kq8_stream_t stream) {

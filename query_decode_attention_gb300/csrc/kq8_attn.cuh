@@ -66,6 +66,9 @@ struct AttnParams {
     const int32_t* tile_list;  // [B][nkv][list_cap]
     const int32_t* list_len;   // [B][nkv]
     int32_t list_cap;
+    // optional [B]: the page-table row of each row b (prefill: the query
+    // token's sequence); null = row b
+    const int32_t* row_seq;
 };
 
 template <int G>
@@ -208,7 +211,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             my_tile = rng.first_tile + e;
             my_mask = 0xFFu;
         }
-        const int32_t pg = P.page_table[(size_t)b * P.max_pages + my_tile / subs];
+        const int32_t pg =
+            P.page_table[(size_t)(P.row_seq ? P.row_seq[b] : b) * P.max_pages + my_tile / subs];
         if (pg >= 0 && pg < P.cache.num_pages) {
             my_page = pg;
         } else {

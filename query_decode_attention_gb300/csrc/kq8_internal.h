@@ -29,6 +29,9 @@ int launch_state_reset(float* acc, float2* ms, int rows, cudaStream_t s);
 int launch_state_finalize(float* out, const float* acc, const float2* ms, int rows, cudaStream_t s);
 int probe_blocks_per_cta(int block, int kv_bs);
 int launch_prefill(const PrefillParams& p, int G, int nkv, cudaStream_t s);
+int launch_prefill_rows(int32_t* row_seq, int32_t* row_len, const int32_t* q_off,
+                        const int32_t* seq_lens, int32_t B, int32_t total_q, int32_t max_seq_len,
+                        int32_t max_q_len, cudaStream_t s);
 int launch_topk(const SparseParams& p, int G, int B, int nkv, cudaStream_t s);
 
 }  // namespace kq8

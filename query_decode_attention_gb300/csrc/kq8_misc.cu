@@ -73,6 +73,47 @@ int launch_append(const kq8_cache_t& c, const float* k, const float* v, const in
 }
 
 // ---------------------------------------------------------------------------
+// Batched prefill as per-token rows (article 10-1 §1): packed query row r of
+// sequence b, the i-th of its nb new tokens, sits at position
+// seq_lens[b] - nb + i and attends the prefix of length position + 1 of b's
+// pages.  Writes row_seq[r] = b and row_len[r] = that length; rows outside
+// every sequence get length 0, rows of an inconsistent sequence -1 (skipped
+// by the attention kernels, which set KQ8_STATUS_BAD_SEQLEN).
+// ---------------------------------------------------------------------------
+__global__ void kq8_prefill_rows_kernel(int32_t* row_seq, int32_t* row_len, const int32_t* q_off,
+                                        const int32_t* seq_lens, int32_t B, int32_t total_q,
+                                        int32_t max_seq_len, int32_t max_q_len) {
+    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < total_q; r += gridDim.x * blockDim.x) {
+        int lo = 0, hi = B + 1;  // first k in [0, B] with q_off[k] > r
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (q_off[mid] > r) hi = mid; else lo = mid + 1;
+        }
+        const int b = lo - 1;
+        int32_t seq = 0, len = 0;
+        if (b >= 0 && b < B && q_off[b] <= r && r < q_off[b + 1]) {
+            const int n = seq_lens[b], nb = q_off[b + 1] - q_off[b];
+            seq = b;
+            const bool bad = n < 0 || n > max_seq_len || nb > n || nb > max_q_len ||
+                             q_off[b] < 0 || q_off[b + 1] > total_q;
+            len = bad ? -1 : n - nb + (r - q_off[b]) + 1;
+        }
+        row_seq[r] = seq;
+        row_len[r] = len;
+    }
+}
+
+int launch_prefill_rows(int32_t* row_seq, int32_t* row_len, const int32_t* q_off,
+                        const int32_t* seq_lens, int32_t B, int32_t total_q, int32_t max_seq_len,
+                        int32_t max_q_len, cudaStream_t s) {
+    if (total_q == 0) return KQ8_OK;
+    const int blocks = (int)((total_q + 255) / 256 < 1024 ? (total_q + 255) / 256 : 1024);
+    kq8_prefill_rows_kernel<<<blocks, 256, 0, s>>>(row_seq, row_len, q_off, seq_lens, B, total_q,
+                                                   max_seq_len, max_q_len);
+    return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
 // Test-only: Q quantisation, one warp per row of 128.
 // ---------------------------------------------------------------------------
 __global__ void kq8_debug_quantize_kernel(int8_t* qi, float* qsc, const float* q, int32_t rows) {

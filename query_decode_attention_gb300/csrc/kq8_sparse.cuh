@@ -33,6 +33,7 @@ struct SparseParams {
     int32_t list_cap;
     int32_t* sel_blocks;     // optional [B][nq][topk]
     uint32_t* status;
+    const int32_t* row_seq;  // optional [B]: page-table row of row b (null = b)
 };
 
 __device__ __forceinline__ int sparse_seq_len(const SparseParams& P, int b) {
@@ -82,8 +83,9 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32) kq8_probe_kernel(const Spars
     const int pg0 = (j0 * P.block) / kv_bs;
     const int pg1 = (min(j1 * P.block, n) - 1) / kv_bs;
 
+    const size_t pt_row = (size_t)(P.row_seq ? P.row_seq[b] : b) * P.max_pages;
     for (int i = threadIdx.x; i <= pg1 - pg0; i += PROBE_WARPS * 32) {
-        const int32_t pg = P.page_table[(size_t)b * P.max_pages + pg0 + i];
+        const int32_t pg = P.page_table[pt_row + pg0 + i];
         const bool ok = pg >= 0 && pg < P.cache.num_pages;
         if (!ok && P.status) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
         pages[i] = ok ? pg : -1;

@@ -76,6 +76,10 @@ _lib.kq8_prefill_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32]
 _lib.kq8_prefill_workspace_bytes.restype = _SZ
 _lib.kq8_prefill_attn.argtypes = [_P, _P, _I32, _CP, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
                                   ctypes.c_float, _P, _SZ, _P]
+_lib.kq8_sparse_prefill_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32]
+_lib.kq8_sparse_prefill_workspace_bytes.restype = _SZ
+_lib.kq8_sparse_prefill_attn.argtypes = [_P, _P, _I32, _CP, _P, _I32, _P, _P, _I32, _I32, _I32,
+                                         _I32, ctypes.c_float, _I32, _I32, _I32, _P, _P, _SZ, _P]
 _lib.kq8_read_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), _P]
 _lib.kq8_strerror.argtypes = [ctypes.c_int]
 _lib.kq8_strerror.restype = ctypes.c_char_p
@@ -336,6 +340,42 @@ def kq8_prefill_attn(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
                                  float(scale), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream)),
            "kq8_prefill_attn")
+
+
+def kq8_sparse_prefill_workspace_bytes(total_q: int, nq: int, nkv: int, max_seq_len: int,
+                                       block: int, topk: int) -> int:
+    return int(_lib.kq8_sparse_prefill_workspace_bytes(total_q, nq, nkv, max_seq_len, block, topk))
+
+
+def kq8_sparse_prefill_attn(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
+                            page_table: torch.Tensor, seq_lens: torch.Tensor,
+                            q_offsets: torch.Tensor, max_seq_len: int, max_q_len: int,
+                            scale: float, block: int, topk: int, probe: int,
+                            workspace: torch.Tensor, sel_blocks: Optional[torch.Tensor] = None,
+                            stream=None) -> None:
+    """Block-sparse batched prefill (include/kq8.h); arguments as
+    kq8_prefill_attn plus the block-sparse knobs of kq8_sparse_decode_attn."""
+    _dtype(out, torch.float32, "out")
+    _dtype(q, torch.float32, "q")
+    _dtype(page_table, torch.int32, "page_table")
+    _dtype(seq_lens, torch.int32, "seq_lens")
+    _dtype(q_offsets, torch.int32, "q_offsets")
+    if q.dim() != 3 or q.shape[2] != HEAD_DIM or out.shape != q.shape:
+        raise ValueError("q and out must be [total_q, nq, 128]")
+    B = seq_lens.numel()
+    if q_offsets.numel() != B + 1 or page_table.dim() != 2 or page_table.shape[0] != B:
+        raise ValueError("q_offsets must be [B+1] and page_table [B, max_pages]")
+    if sel_blocks is not None:
+        _dtype(sel_blocks, torch.int32, "sel_blocks")
+        if sel_blocks.numel() != q.shape[0] * q.shape[1] * topk:
+            raise ValueError("sel_blocks must be [total_q, nq, topk]")
+    _check(_lib.kq8_sparse_prefill_attn(_ptr(out), _ptr(q), q.shape[0], ctypes.byref(cache.struct),
+                                        _ptr(page_table), page_table.shape[1], _ptr(seq_lens),
+                                        _ptr(q_offsets), int(max_seq_len), int(max_q_len), B,
+                                        q.shape[1], float(scale), int(block), int(topk),
+                                        int(probe), _ptr(sel_blocks), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream(stream)), "kq8_sparse_prefill_attn")
 
 
 def kq8_read_status(word: torch.Tensor, stream=None) -> int:

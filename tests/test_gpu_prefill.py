@@ -137,3 +137,53 @@ def test_prefill_qwen2b_prompt_sampled_rows():
         ref = oracle.prefill_batch(qp[i:i + 1], [1], [k8s[0][:p]], [kss[0][:p]], [v8s[0][:p]],
                                    [vss[0][:p]], wl.scale)
         assert_out_close(got[i:i + 1], ref, f"token {i}")
+
+
+# ---------------------------------------------------------------------------
+# Block-sparse prefill (article 10-1 §1-§2): per token, the block-sparse decode
+# query over its own prefix; selections bit-exact, outputs within tolerance.
+# ---------------------------------------------------------------------------
+
+def _run_sparse(wl, q_lens, block, topk, probe, seed=0):
+    q_lens = np.asarray(q_lens, np.int32)
+    _, Ks, Vs = host_inputs(wl)
+    T = int(q_lens.sum())
+    qp = np.random.default_rng(seed).standard_normal((T, wl.nq, wl.hd)).astype(np.float32)
+    case = paged.fill_from_host(wl, Ks, Vs, DEV)
+    q_off = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    out = torch.full((T, wl.nq, wl.hd), float("nan"), device=DEV)
+    sel = torch.full((T, wl.nq, topk), -7, dtype=torch.int32, device=DEV)
+    mq = int(q_lens.max(initial=0))
+    ws = kq8.new_workspace(kq8.kq8_sparse_prefill_workspace_bytes(T, wl.nq, wl.nkv, wl.max_seq_len,
+                                                                  block, topk), DEV)
+    kq8.kq8_sparse_prefill_attn(out, torch.tensor(qp, device=DEV), case.cache, case.page_table,
+                                case.seq_lens, torch.tensor(q_off, device=DEV), wl.max_seq_len, mq,
+                                wl.scale, block, topk, probe, ws, sel_blocks=sel)
+    status = kq8.kq8_read_status(ws)
+    k8s, kss, v8s, vss = oracle_quantized(Ks, Vs)
+    ref, ref_sel = oracle.prefill_batch(qp, q_lens, k8s, kss, v8s, vss, wl.scale, kv_bs=wl.kv_bs,
+                                        sparse=True, block=block, topk=topk, probe=probe)
+    return out.cpu().numpy(), sel.cpu().numpy(), ref, ref_sel, status
+
+
+@pytest.mark.parametrize("nq,nkv,lens,q_lens,block,topk,probe", [
+    (16, 8, [600], [600], 32, 4, 8),             # every prefix: gated (<= 64) and pruned rows
+    (32, 8, [1500, 90], [128, 90], 32, 8, 8),    # history + chunk, G = 4
+    (8, 2, [700], [64], 64, 3, 16),              # block 64 (two sub-tiles per block)
+])
+def test_sparse_prefill_matches_oracle(nq, nkv, lens, q_lens, block, topk, probe):
+    wl = W.custom(len(lens), nq, nkv, lens, seed=sum(lens) + block)
+    got, sel, ref, ref_sel, status = _run_sparse(wl, q_lens, block, topk, probe, seed=topk)
+    assert status == 0
+    assert np.array_equal(sel, ref_sel), "block selections differ"
+    assert_out_close(got, ref, "sparse prefill")
+
+
+def test_sparse_prefill_full_cover_equals_exact_prefill():
+    # k * block >= n: nothing is pruned, so the sparse path is the exact one
+    wl = W.custom(1, 16, 8, [500], seed=23)
+    got, sel, ref, _, status = _run_sparse(wl, [500], 32, 32, 8, seed=24)
+    exact, _, status2 = _run(wl, [500], seed=24)
+    assert status == 0 and status2 == 0
+    assert_out_close(got, exact, "sparse (all blocks kept) vs exact prefill")
+    assert_out_close(got, ref, "sparse vs oracle")

@@ -132,3 +132,24 @@ def test_product_path_has_no_oracle_or_cpu_fallback():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "kq8o_" not in text, f
+
+
+def test_sparse_prefill_argument_validation_without_device(lib):
+    ok = _cache_struct(lib)
+    so = lib._lib
+    assert lib.kq8_sparse_prefill_workspace_bytes(100, 16, 8, 4096, 32, 32) > \
+        lib.kq8_sparse_decode_workspace_bytes(100, 16, 8, 4096, 32, 32)
+    assert lib.kq8_sparse_prefill_workspace_bytes(100, 16, 8, 4096, 48, 32) == 0   # block % 32
+
+    def call(block=32, topk=4, probe=8, total_q=8, B=1, mq=8, ws=512, ws_bytes=1 << 24):
+        return so.kq8_sparse_prefill_attn(256, 256, total_q, ctypes.byref(ok), 256, 2, 256, 256,
+                                          64, mq, B, 16, ctypes.c_float(0.1), block, topk, probe,
+                                          None, ws, ws_bytes, None)
+    assert call(block=16) == lib.KQ8_ERR_UNSUPPORTED
+    assert call(probe=33) == lib.KQ8_ERR_UNSUPPORTED
+    assert call(topk=0) == lib.KQ8_ERR_UNSUPPORTED
+    assert call(mq=65) == lib.KQ8_ERR_INVALID_ARG          # more new tokens than cached
+    assert call(total_q=70000) == lib.KQ8_ERR_UNSUPPORTED  # rows > 65535
+    assert call(ws=None) == lib.KQ8_ERR_WORKSPACE
+    assert call(ws_bytes=1024) == lib.KQ8_ERR_WORKSPACE
+    assert call(total_q=0) == lib.KQ8_OK
