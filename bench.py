@@ -628,6 +628,16 @@ def prefill_measure(dev, kq8, paged, W, peak_tflops, reps=10, cases=PREFILL_CASE
         res[name] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
                      "frac_of_bf16_peak": round(tf / peak_tflops, 4),
                      "flops": prefill_flops(nq, n, n), "status_word": kq8.kq8_read_status(ws)}
+        # the block-sparse prefill of the same prompt (block 32, k 32, probe 8):
+        # per token O(n / block * probe + k * block) instead of O(n)
+        wss = kq8.new_workspace(kq8.kq8_sparse_prefill_workspace_bytes(n, nq, nkv, n, 32, 32), dev)
+        ms_sp = _time_calls(lambda: kq8.kq8_sparse_prefill_attn(
+            out, q, case.cache, case.page_table, case.seq_lens, q_off, n, n, wl.scale, 32, 32, 8,
+            wss, stream=stream), reps, stream)
+        res[name].update({"sparse_ms": round(ms_sp, 4),
+                          "sparse_speedup_vs_exact": round(ms / ms_sp, 3),
+                          "sparse_status_word": kq8.kq8_read_status(wss)})
+        del wss
         del case, q, out
         torch.cuda.empty_cache()
     return res
