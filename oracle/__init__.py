@@ -92,6 +92,12 @@ def lib():
             L.kq8o_prefill_batch.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                              _I, _F, _I, _I, _I, _I, _P, _I]
             L.kq8o_prefill_batch.restype = _I
+            L.kq8o_kv_quantize_rows_q4.argtypes = [_P, _I64, _I, _I, _P, _P]
+            L.kq8o_attn_single_q_q4.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                                _F]
+            L.kq8o_decode_batch_q4.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                               _I, _F, _I]
+            L.kq8o_decode_batch_q4.restype = _I
             L.kq8o_has_openmp.restype = _I
             _lib = L
     return _lib
@@ -116,6 +122,20 @@ def kv_quantize_rows(x):
     maxima = np.empty(rows.shape[0], np.float32)
     lib().kq8o_kv_quantize_rows(rows.ctypes.data_as(_P), rows.shape[0], 1, hd,
                                 codes.ctypes.data_as(_P), maxima.ctypes.data_as(_P))
+    return codes.reshape(x.shape), maxima.reshape(x.shape[:-1])
+
+
+def kv_quantize_rows_q4(x):
+    """q4 write path (the q8 rule with 7 for 127; the pages name --kv-q4 but
+    give no format): x[..., hd] float32 -> (codes int8 in [-7, 7] [..., hd],
+    stored max float32 [...])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    hd = x.shape[-1]
+    rows = x.reshape(-1, hd)
+    codes = np.empty(rows.shape, np.int8)
+    maxima = np.empty(rows.shape[0], np.float32)
+    lib().kq8o_kv_quantize_rows_q4(rows.ctypes.data_as(_P), rows.shape[0], 1, hd,
+                                   codes.ctypes.data_as(_P), maxima.ctypes.data_as(_P))
     return codes.reshape(x.shape), maxima.reshape(x.shape[:-1])
 
 
@@ -327,6 +347,17 @@ def sparse_attn_head(q, cache: SeqCache, kh, scale, block, topk, probe):
 # Batch driver (OpenMP over (sequence, query head) when available)
 # --------------------------------------------------------------------------
 
+def attn_single_q_q4(q, cache: SeqCache, kh, scale):
+    """One-pass attention of one query head over a q4 cache (codes in [-7, 7])."""
+    q, pq = _c(q, np.float32)
+    out = np.empty(cache.hd, np.float32)
+    kp, vp = cache.scale_ptrs(kh)
+    lib().kq8o_attn_single_q_q4(out.ctypes.data_as(_P), pq, cache.k_ptrs, cache.v_ptrs, kp, vp,
+                                cache.n, cache.kv_dim, cache.kv_bs, cache.nkv, kh * cache.hd,
+                                cache.hd, float(np.float32(scale)))
+    return out
+
+
 def _pack_layer(k8_list, ks_list, v8_list, vs_list, hd, kv_bs):
     """One layer's sequences as the token-major rows the C drivers walk."""
     B = len(k8_list)
@@ -371,6 +402,23 @@ def decode_batch(q, k8_list, ks_list, v8_list, vs_list, scale, kv_bs=32, sparse=
     if rc != 0:
         raise ValueError("oracle: unsupported shape")
     return (out, sel[:, :, :topk]) if sparse else out
+
+
+def decode_batch_q4(q, k4_list, ks_list, v4_list, vs_list, scale, kv_bs=32, nthreads=0):
+    """Exact decode over q4 caches (codes int8 in [-7, 7]); as decode_batch."""
+    q = np.ascontiguousarray(q, np.float32)
+    B, nq, hd = q.shape
+    k_rows, v_rows, ks, vs, offs, lens, nkv = _pack_layer(k4_list, ks_list, v4_list, vs_list, hd,
+                                                          kv_bs)
+    out = np.empty((B, nq, hd), np.float32)
+    rc = lib().kq8o_decode_batch_q4(out.ctypes.data_as(_P), q.ctypes.data_as(_P),
+                                    k_rows.ctypes.data_as(_P), v_rows.ctypes.data_as(_P),
+                                    ks.ctypes.data_as(_P), vs.ctypes.data_as(_P),
+                                    offs.ctypes.data_as(_P), lens.ctypes.data_as(_P), B, nq, nkv,
+                                    hd, kv_bs, float(np.float32(scale)), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle: unsupported shape")
+    return out
 
 
 def prefill_batch(q, q_lens, k8_list, ks_list, v8_list, vs_list, scale, kv_bs=32, sparse=False,

@@ -43,6 +43,12 @@
  * "KVQ_INV = 1/127" of [9-2] name this same constant. */
 static const float KVQ_INV = 1.0f / 127.0f;
 
+/* q4 KV ([10-1] §2 names the --kv-q4 switch and excludes it from the sparse
+ * path; no page gives its format).  READING: the q8 rule with 7 in place of
+ * 127 -- stored max m, step m * (1/7), codes roundf(x / step) clamped to
+ * [-7, 7], readers multiply the stored max by 1/7; Q stays int8 ([9-2] §2). */
+static const float Q4_INV = 1.0f / 7.0f;
+
 /* READING: the online-softmax running max starts at -1e9 ([9-2] §2 seg. 2). */
 static const float M_INIT = -1e9f;
 
@@ -78,6 +84,26 @@ void kq8o_kv_quantize_row(const float* v, int hd, int8_t* q, float* stored_max) 
     for (int i = 0; i < hd; i++) {
         float r = roundf(v[i] / d);
         r = clampf(r, -127.0f, 127.0f);
+        q[i] = (int8_t)(int)r;
+    }
+}
+
+/* q4 write path: the same steps with the q4 step and clamp (reading above). */
+void kq8o_kv_quantize_row_q4(const float* v, int hd, int8_t* q, float* stored_max) {
+    float m = 0.0f;
+    for (int i = 0; i < hd; i++) {
+        float a = fabsf(v[i]);
+        if (a > m) m = a;
+    }
+    *stored_max = m;
+    if (m == 0.0f) {
+        for (int i = 0; i < hd; i++) q[i] = 0;
+        return;
+    }
+    float d = m * Q4_INV;
+    for (int i = 0; i < hd; i++) {
+        float r = roundf(v[i] / d);
+        r = clampf(r, -7.0f, 7.0f);
         q[i] = (int8_t)(int)r;
     }
 }
@@ -126,6 +152,15 @@ void kq8o_block_dots(const int8_t* qi, const int8_t* krow, int hd, int32_t* dots
 /* Score of one token ([9-2] §2 segment 2 and its point 1): s starts at 0,
  * s += dot_b * qsc[b] block by block in order, then s = s * ks * scale with
  * ks = kscale * KVQ_INV.  Evaluated left to right in fp32. */
+static float score_steps(const int32_t* dots, const float* qsc, int nblk, float kscale_stored,
+                         float scale, float kv_inv) {
+    float ks = kscale_stored * kv_inv;
+    float s = 0.0f;
+    for (int b = 0; b < nblk; b++) s += (float)dots[b] * qsc[b];
+    s = s * ks * scale;
+    return s;
+}
+
 float kq8o_score(const int32_t* dots, const float* qsc, int nblk, float kscale_stored, float scale) {
     float ks = kscale_stored * KVQ_INV;
     float s = 0.0f;
@@ -153,12 +188,37 @@ static const int8_t* row_ptr(int8_t* const* blocks, int t, int kv_bs, int kv_dim
 /* m_trace (optional, [n]) receives M after each token; *n_visited (optional) */
 /* the number of tokens the loop visited (the [9-2] §4 debug invariants).     */
 /* ------------------------------------------------------------------------ */
+static void attn_one_pass(float* out, const float* q, int8_t* const* k_blocks,
+                          int8_t* const* v_blocks, const float* kscale, const float* vscale,
+                          int seq_len, int kv_dim, int kv_bs, int nkv, int kh_off, int hd,
+                          float scale, const int32_t* tokens, int n_tokens, float* m_trace,
+                          int* n_visited, float kv_inv);
+
 void kq8o_attn_single_q(float* out, const float* q,
                         int8_t* const* k_blocks, int8_t* const* v_blocks,
                         const float* kscale, const float* vscale,
                         int seq_len, int kv_dim, int kv_bs, int nkv, int kh_off, int hd,
                         float scale, const int32_t* tokens, int n_tokens,
                         float* m_trace, int* n_visited) {
+    attn_one_pass(out, q, k_blocks, v_blocks, kscale, vscale, seq_len, kv_dim, kv_bs, nkv, kh_off,
+                  hd, scale, tokens, n_tokens, m_trace, n_visited, KVQ_INV);
+}
+
+/* The same one pass over a q4 cache: codes in [-7, 7] held as int8, scales
+ * read with 1/7 (reading above). */
+void kq8o_attn_single_q_q4(float* out, const float* q, int8_t* const* k_blocks,
+                           int8_t* const* v_blocks, const float* kscale, const float* vscale,
+                           int seq_len, int kv_dim, int kv_bs, int nkv, int kh_off, int hd,
+                           float scale) {
+    attn_one_pass(out, q, k_blocks, v_blocks, kscale, vscale, seq_len, kv_dim, kv_bs, nkv, kh_off,
+                  hd, scale, NULL, 0, NULL, NULL, Q4_INV);
+}
+
+static void attn_one_pass(float* out, const float* q, int8_t* const* k_blocks,
+                          int8_t* const* v_blocks, const float* kscale, const float* vscale,
+                          int seq_len, int kv_dim, int kv_bs, int nkv, int kh_off, int hd,
+                          float scale, const int32_t* tokens, int n_tokens, float* m_trace,
+                          int* n_visited, float kv_inv) {
     int nblk = hd / 32;
     int8_t qi[KQ8O_MAX_HD];
     float qsc[KQ8O_MAX_HD / 32];
@@ -176,7 +236,7 @@ void kq8o_attn_single_q(float* out, const float* q,
         const int8_t* kt = row_ptr(k_blocks, t, kv_bs, kv_dim, kh_off);
         const int8_t* vt = row_ptr(v_blocks, t, kv_bs, kv_dim, kh_off);
         kq8o_block_dots(qi, kt, hd, dots);
-        float s = kq8o_score(dots, qsc, nblk, kscale[(size_t)t * nkv], scale);
+        float s = score_steps(dots, qsc, nblk, kscale[(size_t)t * nkv], scale, kv_inv);
         float w;
         if (s > M) {
             float c = expf(M - s);
@@ -188,7 +248,7 @@ void kq8o_attn_single_q(float* out, const float* q,
             w = expf(s - M);
         }
         S += w;
-        float vs = vscale[(size_t)t * nkv] * KVQ_INV;
+        float vs = vscale[(size_t)t * nkv] * kv_inv;
         float pv = w * vs;
         for (int i = 0; i < hd; i++) acc[i] += (float)vt[i] * pv;
         if (m_trace) m_trace[j] = M;
@@ -561,6 +621,48 @@ void kq8o_kv_quantize_rows(const float* x, int64_t T, int nkv, int hd, int8_t* c
             size_t r = (size_t)t * nkv + h;
             kq8o_kv_quantize_row(x + r * hd, hd, codes + r * hd, maxima + r);
         }
+}
+
+/* q4 write path over a batch of rows (reading above). */
+void kq8o_kv_quantize_rows_q4(const float* x, int64_t T, int nkv, int hd, int8_t* codes,
+                              float* maxima) {
+    for (int64_t t = 0; t < T; t++)
+        for (int h = 0; h < nkv; h++) {
+            size_t r = (size_t)t * nkv + h;
+            kq8o_kv_quantize_row_q4(x + r * hd, hd, codes + r * hd, maxima + r);
+        }
+}
+
+/* Exact decode over a q4 cache (codes as int8 in [-7, 7]), the batch driver
+ * of kq8o_decode_batch with the q4 one pass.  The block-sparse path is not
+ * offered for q4 ([10-1] §2: sparse attention is unavailable with --kv-q4). */
+int kq8o_decode_batch_q4(float* out, const float* q, int8_t* k_rows, int8_t* v_rows,
+                         const float* kscale, const float* vscale, const int64_t* row_offset,
+                         const int32_t* seq_lens, int B, int nq, int nkv, int hd, int kv_bs,
+                         float scale, int nthreads) {
+    if (hd > KQ8O_MAX_HD || hd % 32 != 0 || nkv <= 0 || nq % nkv != 0) return -1;
+    int G = nq / nkv;
+    int kv_dim = nkv * hd;
+    int64_t units = (int64_t)B * nq;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t u = 0; u < units; u++) {
+        int b = (int)(u / nq), h = (int)(u % nq);
+        int kh = h / G;
+        int8_t** kb = make_block_ptrs(k_rows, row_offset[b], seq_lens[b], kv_bs, kv_dim);
+        int8_t** vb = make_block_ptrs(v_rows, row_offset[b], seq_lens[b], kv_bs, kv_dim);
+        kq8o_attn_single_q_q4(out + (size_t)u * hd, q + (size_t)u * hd, kb, vb,
+                              kscale + (size_t)row_offset[b] * nkv + kh,
+                              vscale + (size_t)row_offset[b] * nkv + kh, seq_lens[b], kv_dim,
+                              kv_bs, nkv, kh * hd, hd, scale);
+        free(kb);
+        free(vb);
+    }
+    return 0;
 }
 
 int kq8o_has_openmp(void) {

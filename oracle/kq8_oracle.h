@@ -56,6 +56,17 @@ int kq8o_prefill_batch(float* out, const float* q, int8_t* k_rows, int8_t* v_row
                        const int32_t* seq_lens, const int32_t* q_off, int B, int nq, int nkv,
                        int hd, int kv_bs, float scale, int sparse, int block, int topk, int probe,
                        int32_t* sel_out, int nthreads);
+void kq8o_kv_quantize_row_q4(const float* v, int hd, int8_t* q, float* stored_max);
+void kq8o_kv_quantize_rows_q4(const float* x, int64_t T, int nkv, int hd, int8_t* codes,
+                              float* maxima);
+void kq8o_attn_single_q_q4(float* out, const float* q, int8_t* const* k_blocks,
+                           int8_t* const* v_blocks, const float* kscale, const float* vscale,
+                           int seq_len, int kv_dim, int kv_bs, int nkv, int kh_off, int hd,
+                           float scale);
+int kq8o_decode_batch_q4(float* out, const float* q, int8_t* k_rows, int8_t* v_rows,
+                         const float* kscale, const float* vscale, const int64_t* row_offset,
+                         const int32_t* seq_lens, int B, int nq, int nkv, int hd, int kv_bs,
+                         float scale, int nthreads);
 int kq8o_has_openmp(void);
 
 #endif
