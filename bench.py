@@ -714,6 +714,22 @@ def extras(dev, kq8, paged, W, peak):
                             "bytes": ab, "frac_of_peak": round(ab / (ms * 1e-3) / 1e9 / peak, 4)}
     del case, out, kn, vn
     torch.cuda.empty_cache()
+    # q4 cache: the serving shape (B = 64, ragged 1K-32K, one layer) read through
+    # kq8_decode_attn_q4; per (token, KV head) 64 + 64 B of codes + 8 B of scales
+    wl4 = W.serving_8b(layers=1)
+    case4 = paged.fill_cache(wl4, 0, dev, bits=4)
+    out4 = torch.empty((wl4.B, wl4.nq, wl4.hd), device=dev)
+    ws4 = kq8.new_workspace(kq8.kq8_decode_workspace_bytes(wl4.B, wl4.nq, wl4.nkv,
+                                                           wl4.max_seq_len), dev)
+    ms4 = _time_calls(lambda: kq8.kq8_decode_attn_q4(out4, case4.q, case4.cache, case4.page_table,
+                                                     case4.seq_lens, wl4.max_seq_len, wl4.scale,
+                                                     ws4, stream=stream), 10, stream)
+    b4 = wl4.total_tokens * wl4.nkv * (wl4.hd + 8)
+    res["q4_serving8b_B64"] = {"ms": round(ms4, 4), "GB/s": round(b4 / (ms4 * 1e-3) / 1e9, 1),
+                               "frac_of_peak": round(b4 / (ms4 * 1e-3) / 1e9 / peak, 4),
+                               "bytes": b4, "status_word": kq8.kq8_read_status(ws4)}
+    del case4, out4, ws4
+    torch.cuda.empty_cache()
     # block-sparse: B = 16, n = 65536, block 32, k 32, probe 8 (host-drawn planted inputs)
     wl = W.sparse_planted(65536, B=16)
     q = W.host_q(wl)

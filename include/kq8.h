@@ -298,6 +298,30 @@ int kq8_sparse_prefill_attn(float* out, const float* q, int32_t total_q, const k
                             size_t workspace_bytes, kq8_stream_t stream);
 
 /*
+ * q4 KV cache ([10-1] §2 names the --kv-q4 switch and keeps it out of the
+ * block-sparse path; no page gives the format).  Reading: the q8 write rule of
+ * [9-3] §2 with 7 levels a side -- per (token, head) m = max|x| is stored,
+ * codes round(x / (m * (1/7))) clamped to [-7, 7] -- and readers multiply the
+ * stored max by 1/7; Q is quantised to int8 exactly as in kq8_decode_attn.
+ * A q4 cache uses the same kq8_cache_t with half-size code arrays, per
+ * (page, head): K kv_bs/32 sub-tiles of 2 KB = [4 blocks][32 positions (as
+ * for q8)][16 B], V [kv_bs][64 B]; codes are 4-bit offset binary (code + 8),
+ * and in every 4-byte word of a row byte i holds element i (low nibble) and
+ * element i + 4 (high nibble).  k and v point to num_pages * nkv * kv_bs * 64
+ * bytes each; kscale and vscale as for q8.
+ *   kq8_append_kv_q4   : as kq8_append_kv, writing q4 codes.
+ *   kq8_decode_attn_q4 : exact decode over a q4 cache, arguments, workspace
+ *                        (kq8_decode_workspace_bytes) and status as
+ *                        kq8_decode_attn.  There is no q4 block-sparse call.
+ */
+int kq8_append_kv_q4(const kq8_cache_t* cache, const float* k, const float* v,
+                     const int32_t* slot, int32_t T, uint32_t* status, kq8_stream_t stream);
+int kq8_decode_attn_q4(float* out, const float* q, const kq8_cache_t* cache,
+                       const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                       int32_t max_seq_len, int32_t B, int32_t nq, float scale, void* workspace,
+                       size_t workspace_bytes, kq8_stream_t stream);
+
+/*
  * Copies the status word of `workspace` (or of a kq8_append_kv status word) to
  * *status (host), then clears it; synchronises `stream`.
  */

@@ -242,6 +242,33 @@ int kq8_append_kv(const kq8_cache_t* cache, const float* k, const float* v, cons
     return launch_append(*cache, k, v, slot, T, status, (cudaStream_t)stream);
 }
 
+int kq8_append_kv_q4(const kq8_cache_t* cache, const float* k, const float* v,
+                     const int32_t* slot, int32_t T, uint32_t* status, kq8_stream_t stream) {
+    int rc = check_cache_args(cache);
+    if (rc) return rc;
+    if (T < 0) return KQ8_ERR_INVALID_ARG;
+    if (T == 0) return KQ8_OK;
+    if (!k || !v || !slot || !aligned(k, 16) || !aligned(v, 16)) return KQ8_ERR_INVALID_ARG;
+    if (status && !aligned(status, 4)) return KQ8_ERR_INVALID_ARG;
+    return launch_append_q4(*cache, k, v, slot, T, status, (cudaStream_t)stream);
+}
+
+int kq8_decode_attn_q4(float* out, const float* q, const kq8_cache_t* cache,
+                       const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                       int32_t max_seq_len, int32_t B, int32_t nq, float scale, void* workspace,
+                       size_t workspace_bytes, kq8_stream_t stream) {
+    int rc = check_decode(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq);
+    if (rc) return rc;
+    const int nkv = cache->num_kv_heads;
+    const Plan plan = plan_exact(B, nq, nkv, max_seq_len);
+    rc = check_ws(workspace, workspace_bytes, plan.total);
+    if (rc) return rc;
+    if (B == 0) return KQ8_OK;
+    AttnParams p = attn_params(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq,
+                               scale, plan, workspace);
+    return launch_attn_q4(p, nq / nkv, B, nkv, (cudaStream_t)stream);
+}
+
 size_t kq8_decode_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len) {
     if (B < 0 || nq < 1 || nkv < 1 || max_seq_len < 0) return 0;
     return plan_exact(B, nq, nkv, max_seq_len).total;

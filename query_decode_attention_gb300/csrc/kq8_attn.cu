@@ -4,9 +4,9 @@
 
 namespace kq8 {
 
-template <int G, bool SPARSE>
+template <int G, bool SPARSE, bool Q4>
 static int launch_attn_g(const AttnParams& p, int B, int nkv, cudaStream_t s) {
-    auto kern = kq8_attn_kernel<G, SPARSE>;
+    auto kern = kq8_attn_kernel<G, SPARSE, Q4>;
     const size_t smem = sizeof(AttnSmem<G>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -21,24 +21,30 @@ static int launch_attn_g(const AttnParams& p, int B, int nkv, cudaStream_t s) {
     return KQ8_OK;
 }
 
-template <bool SPARSE>
+template <bool SPARSE, bool Q4>
 static int launch_attn_s(const AttnParams& p, int G, int B, int nkv, cudaStream_t s) {
     switch (G) {
-        case 1: return launch_attn_g<1, SPARSE>(p, B, nkv, s);
-        case 2: return launch_attn_g<2, SPARSE>(p, B, nkv, s);
-        case 3: return launch_attn_g<3, SPARSE>(p, B, nkv, s);
-        case 4: return launch_attn_g<4, SPARSE>(p, B, nkv, s);
-        case 5: return launch_attn_g<5, SPARSE>(p, B, nkv, s);
-        case 6: return launch_attn_g<6, SPARSE>(p, B, nkv, s);
-        case 7: return launch_attn_g<7, SPARSE>(p, B, nkv, s);
-        case 8: return launch_attn_g<8, SPARSE>(p, B, nkv, s);
+        case 1: return launch_attn_g<1, SPARSE, Q4>(p, B, nkv, s);
+        case 2: return launch_attn_g<2, SPARSE, Q4>(p, B, nkv, s);
+        case 3: return launch_attn_g<3, SPARSE, Q4>(p, B, nkv, s);
+        case 4: return launch_attn_g<4, SPARSE, Q4>(p, B, nkv, s);
+        case 5: return launch_attn_g<5, SPARSE, Q4>(p, B, nkv, s);
+        case 6: return launch_attn_g<6, SPARSE, Q4>(p, B, nkv, s);
+        case 7: return launch_attn_g<7, SPARSE, Q4>(p, B, nkv, s);
+        case 8: return launch_attn_g<8, SPARSE, Q4>(p, B, nkv, s);
         default: return KQ8_ERR_UNSUPPORTED;
     }
 }
 
 int launch_attn(const AttnParams& p, int G, bool sparse, int B, int nkv, cudaStream_t s) {
     if (B == 0) return KQ8_OK;
-    return sparse ? launch_attn_s<true>(p, G, B, nkv, s) : launch_attn_s<false>(p, G, B, nkv, s);
+    return sparse ? launch_attn_s<true, false>(p, G, B, nkv, s)
+                  : launch_attn_s<false, false>(p, G, B, nkv, s);
+}
+
+int launch_attn_q4(const AttnParams& p, int G, int B, int nkv, cudaStream_t s) {
+    if (B == 0) return KQ8_OK;
+    return launch_attn_s<false, true>(p, G, B, nkv, s);
 }
 
 // Running states: reset to empty (max -1e9, sum 0, acc 0) and finalise to

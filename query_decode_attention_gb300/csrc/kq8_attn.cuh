@@ -87,6 +87,7 @@ struct AttnSmem {
     alignas(16) float4 p[ATTN_WARPS][TILE][AttnShape<G>::GP];
     alignas(16) int8_t qi[G][HD];
     alignas(16) float qsc[G][NB];
+    int qsum[G][NB];  // sum of each 32-element block's Q codes (q4 cache only)
     alignas(8) uint64_t bar[ATTN_WARPS][ATTN_STAGES];
     int last;  // this CTA drew the last ticket of its (sequence, KV head)
 };
@@ -109,6 +110,33 @@ __device__ __forceinline__ void i8x4_to_f2(uint32_t w, float2& a, float2& b) {
     b = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
                                __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543))),
                    bias);
+}
+
+// q4 word (8 offset-binary nibbles, elements 0-3 low, 4-7 high) -> four
+// float pairs, exactly: each nibble u = c + 8 into the mantissa of 2^23, one
+// packed subtract of 2^23 + 8 per pair.
+__device__ __forceinline__ void u4x8_to_f2(uint32_t w, float2& a, float2& b, float2& c,
+                                           float2& d) {
+    const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+    const float2 bias = make_float2(-8388616.0f, -8388616.0f);
+    a = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7540)),
+                               __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7541))),
+                   bias);
+    b = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7542)),
+                               __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7543))),
+                   bias);
+    c = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7540)),
+                               __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7541))),
+                   bias);
+    d = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7542)),
+                               __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7543))),
+                   bias);
+}
+// Unsigned bytes of a times signed bytes of b, summed into c.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
 // Two int32 dots (|d| < 2^22) -> a float pair, exactly.
@@ -163,7 +191,7 @@ __device__ __forceinline__ void fold_state(float mo, float so, float m, float s,
     S = so * fo + s * fn;
 }
 
-template <int G, bool SPARSE>
+template <int G, bool SPARSE, bool Q4 = false>
 __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     kq8_attn_kernel(const AttnParams P) {
     using Sh = AttnShape<G>;
@@ -196,6 +224,13 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
         const uint32_t codes = quantize_q_lane(x, qs);
         reinterpret_cast<uint32_t*>(S.qi[g])[lane] = codes;
         if ((lane & 7) == 0) S.qsc[g][lane >> 3] = qs;
+        if (Q4) {  // q4: dot = sum q * (u - 8) = dp4a(u, q) - 8 * sum q per block
+            int qs4 = __dp4a((int)codes, 0x01010101, 0);
+            qs4 += __shfl_xor_sync(0xffffffffu, qs4, 1);
+            qs4 += __shfl_xor_sync(0xffffffffu, qs4, 2);
+            qs4 += __shfl_xor_sync(0xffffffffu, qs4, 4);
+            if ((lane & 7) == 0) S.qsum[g][lane >> 3] = qs4;
+        }
     }
     // ---- this warp's tiles, one per lane: tile index, head mask, page (-1 if bad)
     int my_tile = 0;
@@ -236,11 +271,18 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             } else {
                 const int sub = tile % subs;
                 uint8_t* st = S.stage[warp][i % NS];
-                const size_t kvo = kv_sub_off(pg, h, nkv, kv_bs, sub);
                 const size_t so = scale_sub_off(pg, h, nkv, kv_bs, sub);
-                mbar_arrive_expect_tx(bar, STAGE_BYTES);
-                bulk_g2s(st, P.cache.k + kvo, SUB_K_BYTES, bar, pol);
-                bulk_g2s(st + SUB_K_BYTES, P.cache.v + kvo, SUB_V_BYTES, bar, pol);
+                if (Q4) {  // half-size codes at the q8 stage offsets
+                    const size_t kvo = kv4_sub_off(pg, h, nkv, kv_bs, sub);
+                    mbar_arrive_expect_tx(bar, SUB_K4_BYTES + SUB_V4_BYTES + 2 * SUB_S_BYTES);
+                    bulk_g2s(st, P.cache.k + kvo, SUB_K4_BYTES, bar, pol);
+                    bulk_g2s(st + SUB_K_BYTES, P.cache.v + kvo, SUB_V4_BYTES, bar, pol);
+                } else {
+                    const size_t kvo = kv_sub_off(pg, h, nkv, kv_bs, sub);
+                    mbar_arrive_expect_tx(bar, STAGE_BYTES);
+                    bulk_g2s(st, P.cache.k + kvo, SUB_K_BYTES, bar, pol);
+                    bulk_g2s(st + SUB_K_BYTES, P.cache.v + kvo, SUB_V_BYTES, bar, pol);
+                }
                 bulk_g2s(st + SUB_K_BYTES + SUB_V_BYTES, P.cache.kscale + so, SUB_S_BYTES, bar,
                          pol);
                 bulk_g2s(st + SUB_K_BYTES + SUB_V_BYTES + SUB_S_BYTES, P.cache.vscale + so,
@@ -266,7 +308,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
         for (int bb = 0; bb < NB; bb++)
             qsc2[gp][bb] = make_float2(S.qsc[2 * gp][bb], S.qsc[min(2 * gp + 1, G - 1)][bb]);
     // stored K max -> step (1/127), softmax scale and the move to base 2
-    const float kscale_mul = inv127() * P.scale * LOG2E;
+    const float kscale_mul = (Q4 ? inv7() : inv127()) * P.scale * LOG2E;
     float Mhi[G];  // rescale threshold: running max + RESCALE_SLACK
 #pragma unroll
     for (int g = 0; g < G; g++) Mhi[g] = M_INIT + RESCALE_SLACK;
@@ -294,33 +336,53 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             const int t = krow(q);
             const bool live = tile * TILE + t < n && tile * TILE + t >= begin;
             int dot[G][NB];
-            const int hs = (q >> 2) & 1;  // half order that keeps the loads conflict-free
+            const int hs = Q4 ? 0 : (q >> 2) & 1;  // half order: conflict-free loads
 #pragma unroll
             for (int bb = 0; bb < NB; bb++) {
-                const uint4 kA =
-                    *reinterpret_cast<const uint4*>(kst + bb * 1024 + q * 32 + hs * 16);
-                const uint4 kB =
-                    *reinterpret_cast<const uint4*>(kst + bb * 1024 + q * 32 + (hs ^ 1) * 16);
+                uint4 kA, kB;
+                if (Q4) {  // 16 B = 32 nibbles -> offset-binary bytes in element order
+                    const uint4 kp = *reinterpret_cast<const uint4*>(kst + bb * 512 + q * 16);
+                    kA = make_uint4(kp.x & 0x0F0F0F0Fu, (kp.x >> 4) & 0x0F0F0F0Fu,
+                                    kp.y & 0x0F0F0F0Fu, (kp.y >> 4) & 0x0F0F0F0Fu);
+                    kB = make_uint4(kp.z & 0x0F0F0F0Fu, (kp.z >> 4) & 0x0F0F0F0Fu,
+                                    kp.w & 0x0F0F0F0Fu, (kp.w >> 4) & 0x0F0F0F0Fu);
+                } else {
+                    kA = *reinterpret_cast<const uint4*>(kst + bb * 1024 + q * 32 + hs * 16);
+                    kB = *reinterpret_cast<const uint4*>(kst + bb * 1024 + q * 32 +
+                                                         (hs ^ 1) * 16);
+                }
 #pragma unroll
                 for (int g = 0; g < G; g++) {
                     const uint4 qA =
                         *reinterpret_cast<const uint4*>(S.qi[g] + bb * 32 + hs * 16);
                     const uint4 qB =
                         *reinterpret_cast<const uint4*>(S.qi[g] + bb * 32 + (hs ^ 1) * 16);
-                    int d = __dp4a((int)kA.x, (int)qA.x, 0);
-                    d = __dp4a((int)kA.y, (int)qA.y, d);
-                    d = __dp4a((int)kA.z, (int)qA.z, d);
-                    d = __dp4a((int)kA.w, (int)qA.w, d);
-                    d = __dp4a((int)kB.x, (int)qB.x, d);
-                    d = __dp4a((int)kB.y, (int)qB.y, d);
-                    d = __dp4a((int)kB.z, (int)qB.z, d);
-                    d = __dp4a((int)kB.w, (int)qB.w, d);
+                    int d;
+                    if (Q4) {
+                        d = dp4a_us(kA.x, qA.x, -8 * S.qsum[g][bb]);
+                        d = dp4a_us(kA.y, qA.y, d);
+                        d = dp4a_us(kA.z, qA.z, d);
+                        d = dp4a_us(kA.w, qA.w, d);
+                        d = dp4a_us(kB.x, qB.x, d);
+                        d = dp4a_us(kB.y, qB.y, d);
+                        d = dp4a_us(kB.z, qB.z, d);
+                        d = dp4a_us(kB.w, qB.w, d);
+                    } else {
+                        d = __dp4a((int)kA.x, (int)qA.x, 0);
+                        d = __dp4a((int)kA.y, (int)qA.y, d);
+                        d = __dp4a((int)kA.z, (int)qA.z, d);
+                        d = __dp4a((int)kA.w, (int)qA.w, d);
+                        d = __dp4a((int)kB.x, (int)qB.x, d);
+                        d = __dp4a((int)kB.y, (int)qB.y, d);
+                        d = __dp4a((int)kB.z, (int)qB.z, d);
+                        d = __dp4a((int)kB.w, (int)qB.w, d);
+                    }
                     dot[g][bb] = d;
                 }
             }
             // (s * ks) * scale * log2(e) with ks = kscale / 127: one multiplier per token
             const float kmul = __fmul_rn(kss[t], kscale_mul);
-            const float vstep = __fmul_rn(vss[t], inv127());
+            const float vstep = __fmul_rn(vss[t], Q4 ? inv7() : inv127());
             float sv[2 * GP];
 #pragma unroll
             for (int gp = 0; gp < GP; gp++) {
@@ -385,7 +447,16 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
 #pragma unroll
             for (int r = tg; r < TILE; r += TG) {
                 float2 f[EP];
-                if (E == 16) {
+                if (Q4) {
+                    if (E == 16) {
+                        const uint2 vv = *reinterpret_cast<const uint2*>(vst + r * (HD / 2) + c * 8);
+                        u4x8_to_f2(vv.x, f[0], f[1], f[2], f[3]);
+                        u4x8_to_f2(vv.y, f[4], f[5], f[6], f[7]);
+                    } else {
+                        const uint32_t vv = *reinterpret_cast<const uint32_t*>(vst + r * (HD / 2) + c * 4);
+                        u4x8_to_f2(vv, f[0], f[1], f[2], f[3]);
+                    }
+                } else if (E == 16) {
                     const uint4 vv = *reinterpret_cast<const uint4*>(vst + r * HD + c * 16);
                     i8x4_to_f2(vv.x, f[0], f[1]);
                     i8x4_to_f2(vv.y, f[2], f[3]);

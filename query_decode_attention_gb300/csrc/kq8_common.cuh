@@ -33,6 +33,9 @@ constexpr int MAX_G = 8;             // query heads per KV head handled
 // The inverse of 127 as a float: the per-row step is max|x| * (1/127) and the
 // readers multiply stored maxima by it (article 9-2 §2, article 9-3 §2).
 __host__ __device__ constexpr float inv127() { return 1.0f / 127.0f; }
+// q4 cache (the --kv-q4 switch of article 10-1 §2; no page gives the format):
+// the same rule with 7 levels a side -- step max|x| * (1/7), codes in [-7, 7].
+__host__ __device__ constexpr float inv7() { return 1.0f / 7.0f; }
 
 // ---------------------------------------------------------------------------
 // Cache addressing
@@ -43,6 +46,18 @@ __host__ __device__ __forceinline__ int krow(int q) { return (q & 7) * 4 + (q >>
 __device__ __forceinline__ size_t page_head(int32_t page, int h, int nkv) {
     return (size_t)page * (size_t)nkv + (size_t)h;
 }
+// q4 cache layout, per (page p, KV head h): codes as 4-bit offset binary
+// (nibble = code + 8); within every 4-byte word of a row, byte i holds
+// element i in its low nibble and element i + 4 in its high nibble, so a
+// word covers 8 consecutive elements.
+//   K: kv_bs/32 sub-tiles of 2 KB = 4 blocks x 32 row positions (kpos) x 16 B
+//   V: kv_bs rows of 64 B;  kscale, vscale as for q8
+constexpr int SUB_K4_BYTES = TILE * HD / 2;
+constexpr int SUB_V4_BYTES = TILE * HD / 2;
+__device__ __forceinline__ size_t kv4_sub_off(int32_t page, int h, int nkv, int kv_bs, int sub) {
+    return page_head(page, h, nkv) * (size_t)kv_bs * (HD / 2) + (size_t)sub * SUB_K4_BYTES;
+}
+
 // Byte offset of sub-tile `sub` of (page, head) in the K or V array.
 __device__ __forceinline__ size_t kv_sub_off(int32_t page, int h, int nkv, int kv_bs, int sub) {
     return page_head(page, h, nkv) * (size_t)kv_bs * HD + (size_t)sub * (TILE * HD);

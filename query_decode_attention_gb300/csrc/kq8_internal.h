@@ -17,6 +17,8 @@ int check_cache_args(const kq8_cache_t* c);
 
 int launch_append(const kq8_cache_t& c, const float* k, const float* v, const int32_t* slot,
                   int32_t T, uint32_t* status, cudaStream_t stream);
+int launch_append_q4(const kq8_cache_t& c, const float* k, const float* v, const int32_t* slot,
+                     int32_t T, uint32_t* status, cudaStream_t stream);
 int launch_debug_quantize(int8_t* qi, float* qsc, const float* q, int32_t rows, cudaStream_t s);
 int launch_debug_dots(int32_t* dots, const float* q, const kq8_cache_t& c,
                       const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
@@ -24,6 +26,7 @@ int launch_debug_dots(int32_t* dots, const float* q, const kq8_cache_t& c,
 
 // Attention over KV chunks (+ the merge when any sequence spans > 1 chunk).
 int launch_attn(const AttnParams& p, int G, bool sparse, int B, int nkv, cudaStream_t s);
+int launch_attn_q4(const AttnParams& p, int G, int B, int nkv, cudaStream_t s);
 int launch_probe(const SparseParams& p, int G, int B, int nkv, cudaStream_t s);
 int launch_state_reset(float* acc, float2* ms, int rows, cudaStream_t s);
 int launch_state_finalize(float* out, const float* acc, const float2* ms, int rows, cudaStream_t s);

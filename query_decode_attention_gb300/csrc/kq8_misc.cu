@@ -63,6 +63,79 @@ __global__ void __launch_bounds__(APPEND_WARPS * 32)
     }
 }
 
+// q4 write path (the q8 rule with 7 for 127): lane l holds elements 4l..4l+3
+// and returns their codes as offset-binary nibbles (code + 8) in the low
+// nibble of each byte.
+__device__ __forceinline__ uint32_t kv_quantize_lane_q4(const float4 x, float& m_out) {
+    float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+    m = warp_max(m);
+    m_out = m;
+    if (m == 0.0f) return 0x08080808u;
+    const float d = __fmul_rn(m, inv7());
+    auto code = [&](float v) -> uint32_t {
+        float r = roundf(__fdiv_rn(v, d));
+        r = fminf(fmaxf(r, -7.0f), 7.0f);
+        return (uint32_t)((int)r + 8);
+    };
+    return code(x.x) | (code(x.y) << 8) | (code(x.z) << 16) | (code(x.w) << 24);
+}
+
+// One warp per (token, head) as above; lanes 2w and 2w+1 hold the 8 elements of
+// packed word w (byte i = element i | element i + 4 << 4), which the even lane
+// writes: K at sub-tile r/32, block w/4, position kpos(r%32), bytes 4*(w%4);
+// V at row r, bytes 4w.
+__global__ void __launch_bounds__(APPEND_WARPS * 32)
+    kq8_append_q4_kernel(const kq8_cache_t c, const float* __restrict__ k,
+                         const float* __restrict__ v, const int32_t* __restrict__ slot, int32_t T,
+                         uint32_t* status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t item = (int64_t)blockIdx.x * APPEND_WARPS + (threadIdx.x >> 5);
+    const int nkv = c.num_kv_heads, kv_bs = c.kv_bs;
+    if (item >= (int64_t)T * nkv) return;
+    const int64_t t = item / nkv;
+    const int h = (int)(item % nkv);
+    const int32_t sl = slot[t];
+    if (sl < 0) return;
+    if ((int64_t)sl >= (int64_t)c.num_pages * kv_bs) {
+        if (lane == 0 && status) atomicOr(status, KQ8_STATUS_BAD_SLOT);
+        return;
+    }
+    const int32_t page = sl / kv_bs;
+    const int r = sl % kv_bs;
+    const size_t row = (size_t)item * HD;
+    const float4 xk = __ldcs(reinterpret_cast<const float4*>(k + row) + lane);
+    const float4 xv = __ldcs(reinterpret_cast<const float4*>(v + row) + lane);
+    float mk, mv;
+    const uint32_t ck = kv_quantize_lane_q4(xk, mk);
+    const uint32_t cv = kv_quantize_lane_q4(xv, mv);
+    const uint32_t ck_hi = __shfl_down_sync(0xffffffffu, ck, 1);
+    const uint32_t cv_hi = __shfl_down_sync(0xffffffffu, cv, 1);
+    if ((lane & 1) == 0) {
+        const int w = lane >> 1;  // packed word: elements 8w .. 8w+7
+        const size_t ko = kv4_sub_off(page, h, nkv, kv_bs, r / TILE) + (size_t)(w >> 2) * 512 +
+                          (size_t)kpos(r % TILE) * 16 + (size_t)(w & 3) * 4;
+        *reinterpret_cast<uint32_t*>(c.k + ko) = ck | (ck_hi << 4);
+        const size_t vo = page_head(page, h, nkv) * (size_t)kv_bs * (HD / 2) + (size_t)r * (HD / 2) +
+                          (size_t)w * 4;
+        *reinterpret_cast<uint32_t*>(c.v + vo) = cv | (cv_hi << 4);
+    }
+    if (lane == 0) {
+        const size_t so = page_head(page, h, nkv) * (size_t)kv_bs + r;
+        c.kscale[so] = mk;
+        c.vscale[so] = mv;
+    }
+}
+
+int launch_append_q4(const kq8_cache_t& c, const float* k, const float* v, const int32_t* slot,
+                     int32_t T, uint32_t* status, cudaStream_t stream) {
+    const int64_t items = (int64_t)T * c.num_kv_heads;
+    if (items == 0) return KQ8_OK;
+    const int64_t blocks = (items + APPEND_WARPS - 1) / APPEND_WARPS;
+    kq8_append_q4_kernel<<<(unsigned)blocks, APPEND_WARPS * 32, 0, stream>>>(c, k, v, slot, T,
+                                                                            status);
+    return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+}
+
 int launch_append(const kq8_cache_t& c, const float* k, const float* v, const int32_t* slot,
                   int32_t T, uint32_t* status, cudaStream_t stream) {
     const int64_t items = (int64_t)T * c.num_kv_heads;

@@ -80,6 +80,9 @@ _lib.kq8_sparse_prefill_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32
 _lib.kq8_sparse_prefill_workspace_bytes.restype = _SZ
 _lib.kq8_sparse_prefill_attn.argtypes = [_P, _P, _I32, _CP, _P, _I32, _P, _P, _I32, _I32, _I32,
                                          _I32, ctypes.c_float, _I32, _I32, _I32, _P, _P, _SZ, _P]
+_lib.kq8_append_kv_q4.argtypes = [_CP, _P, _P, _P, _I32, _P, _P]
+_lib.kq8_decode_attn_q4.argtypes = [_P, _P, _CP, _P, _I32, _P, _I32, _I32, _I32, ctypes.c_float,
+                                    _P, _SZ, _P]
 _lib.kq8_read_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), _P]
 _lib.kq8_strerror.argtypes = [ctypes.c_int]
 _lib.kq8_strerror.restype = ctypes.c_char_p
@@ -133,18 +136,24 @@ def kq8_version() -> int:
 class PagedKVCache:
     """Device pool of one layer in the kq8_cache_t layout (torch-allocated).
 
-    k: int8 [num_pages, nkv, kv_bs/32, 4, 32, 32]; v: int8 [num_pages, nkv,
-    kv_bs, 128]; kscale/vscale: float32 [num_pages, nkv, kv_bs]."""
+    bits=8: k int8 [num_pages, nkv, kv_bs/32, 4, 32, 32], v int8 [num_pages,
+    nkv, kv_bs, 128]; bits=4 (q4 cache, packed nibbles): k [.., 4, 32, 16],
+    v [num_pages, nkv, kv_bs, 64]; kscale/vscale: float32 [num_pages, nkv,
+    kv_bs]."""
 
     def __init__(self, num_pages: int, num_kv_heads: int, kv_bs: int = 32, device="cuda",
-                 k=None, v=None, kscale=None, vscale=None):
+                 k=None, v=None, kscale=None, vscale=None, bits: int = 8):
+        if bits not in (8, 4):
+            raise ValueError("bits must be 8 or 4")
         self.num_pages, self.num_kv_heads, self.kv_bs = int(num_pages), int(num_kv_heads), int(kv_bs)
         self.head_dim = HEAD_DIM
+        self.bits = bits
         sub = kv_bs // 32
+        row = HEAD_DIM if bits == 8 else HEAD_DIM // 2
         self.k = k if k is not None else torch.zeros(
-            (num_pages, num_kv_heads, sub, 4, 32, 32), dtype=torch.int8, device=device)
+            (num_pages, num_kv_heads, sub, 4, 32, row // 4), dtype=torch.int8, device=device)
         self.v = v if v is not None else torch.zeros(
-            (num_pages, num_kv_heads, kv_bs, HEAD_DIM), dtype=torch.int8, device=device)
+            (num_pages, num_kv_heads, kv_bs, row), dtype=torch.int8, device=device)
         self.kscale = kscale if kscale is not None else torch.zeros(
             (num_pages, num_kv_heads, kv_bs), dtype=torch.float32, device=device)
         self.vscale = vscale if vscale is not None else torch.zeros(
@@ -161,9 +170,9 @@ class PagedKVCache:
         return sum(t.numel() * t.element_size() for t in (self.k, self.v, self.kscale, self.vscale))
 
 
-def kq8_append_kv(cache: PagedKVCache, k: torch.Tensor, v: torch.Tensor, slot: torch.Tensor,
-                  status: Optional[torch.Tensor] = None, stream=None) -> None:
-    """Write path: k, v float32 [T, nkv, 128]; slot int32 [T]."""
+def _append_args(cache, k, v, slot, status, bits):
+    if cache.bits != bits:
+        raise ValueError(f"this call writes a q{bits} cache, got q{cache.bits}")
     _dtype(k, torch.float32, "k")
     _dtype(v, torch.float32, "v")
     _dtype(slot, torch.int32, "slot")
@@ -172,8 +181,23 @@ def kq8_append_kv(cache: PagedKVCache, k: torch.Tensor, v: torch.Tensor, slot: t
         raise ValueError("k/v must be [T, nkv, 128] with T = len(slot)")
     if status is not None:
         _dtype(status, torch.int32, "status")
+    return T
+
+
+def kq8_append_kv(cache: PagedKVCache, k: torch.Tensor, v: torch.Tensor, slot: torch.Tensor,
+                  status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Write path: k, v float32 [T, nkv, 128]; slot int32 [T]."""
+    T = _append_args(cache, k, v, slot, status, 8)
     _check(_lib.kq8_append_kv(ctypes.byref(cache.struct), _ptr(k), _ptr(v), _ptr(slot), T,
                               _ptr(status), _stream(stream)), "kq8_append_kv")
+
+
+def kq8_append_kv_q4(cache: PagedKVCache, k: torch.Tensor, v: torch.Tensor, slot: torch.Tensor,
+                     status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """q4 write path (include/kq8.h) into a PagedKVCache(bits=4)."""
+    T = _append_args(cache, k, v, slot, status, 4)
+    _check(_lib.kq8_append_kv_q4(ctypes.byref(cache.struct), _ptr(k), _ptr(v), _ptr(slot), T,
+                                 _ptr(status), _stream(stream)), "kq8_append_kv_q4")
 
 
 def kq8_decode_workspace_bytes(B: int, nq: int, nkv: int, max_seq_len: int) -> int:
@@ -213,7 +237,9 @@ def new_workspace(nbytes: int, device="cuda", stream=None) -> torch.Tensor:
     return ws
 
 
-def _decode_args(out, q, cache, page_table, seq_lens):
+def _decode_args(out, q, cache, page_table, seq_lens, bits=8):
+    if cache.bits != bits:
+        raise ValueError(f"this call reads a q{bits} cache, got q{cache.bits}")
     _dtype(out, torch.float32, "out")
     _dtype(q, torch.float32, "q")
     _dtype(page_table, torch.int32, "page_table")
@@ -235,6 +261,18 @@ def kq8_decode_attn(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
                                 max_pages, _ptr(seq_lens), int(max_seq_len), B, nq, float(scale),
                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 _stream(stream)), "kq8_decode_attn")
+
+
+def kq8_decode_attn_q4(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
+                       page_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                       scale: float, workspace: torch.Tensor, stream=None) -> None:
+    """Exact decode over a q4 cache (include/kq8.h)."""
+    B, nq, max_pages = _decode_args(out, q, cache, page_table, seq_lens, bits=4)
+    _check(_lib.kq8_decode_attn_q4(_ptr(out), _ptr(q), ctypes.byref(cache.struct),
+                                   _ptr(page_table), max_pages, _ptr(seq_lens), int(max_seq_len),
+                                   B, nq, float(scale), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+           "kq8_decode_attn_q4")
 
 
 def kq8_decode_attn_noalloc(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
@@ -324,6 +362,8 @@ def kq8_prefill_attn(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
     """Batched causal prefill attention (include/kq8.h): q and out are
     [total_q, nq, 128], packed by sequence per q_offsets [B+1]; seq_lens
     counts each sequence's cached tokens including its new ones."""
+    if cache.bits != 8:
+        raise ValueError("prefill reads a q8 cache")
     _dtype(out, torch.float32, "out")
     _dtype(q, torch.float32, "q")
     _dtype(page_table, torch.int32, "page_table")
@@ -355,6 +395,8 @@ def kq8_sparse_prefill_attn(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCa
                             stream=None) -> None:
     """Block-sparse batched prefill (include/kq8.h); arguments as
     kq8_prefill_attn plus the block-sparse knobs of kq8_sparse_decode_attn."""
+    if cache.bits != 8:
+        raise ValueError("sparse prefill reads a q8 cache")
     _dtype(out, torch.float32, "out")
     _dtype(q, torch.float32, "q")
     _dtype(page_table, torch.int32, "page_table")

@@ -153,3 +153,17 @@ def test_sparse_prefill_argument_validation_without_device(lib):
     assert call(ws=None) == lib.KQ8_ERR_WORKSPACE
     assert call(ws_bytes=1024) == lib.KQ8_ERR_WORKSPACE
     assert call(total_q=0) == lib.KQ8_OK
+
+
+def test_q4_argument_validation_without_device(lib):
+    ok = _cache_struct(lib)
+    so = lib._lib
+    assert so.kq8_append_kv_q4(ctypes.byref(ok), 256, 256, 256, -1, None, None) == lib.KQ8_ERR_INVALID_ARG
+    assert so.kq8_append_kv_q4(ctypes.byref(ok), 256, 256, 256, 0, None, None) == lib.KQ8_OK
+    assert so.kq8_append_kv_q4(ctypes.byref(ok), 260, 256, 256, 1, None, None) == lib.KQ8_ERR_INVALID_ARG
+    dec = so.kq8_decode_attn_q4
+    args = (256, 256, ctypes.byref(ok), 256, 2, 256)
+    assert dec(*args, 64, 1, 12, ctypes.c_float(0.1), 512, 1 << 20, None) == lib.KQ8_ERR_UNSUPPORTED
+    assert dec(*args, 100, 1, 16, ctypes.c_float(0.1), 512, 1 << 20, None) == lib.KQ8_ERR_INVALID_ARG
+    assert dec(*args, 64, 1, 16, ctypes.c_float(0.1), None, 1 << 20, None) == lib.KQ8_ERR_WORKSPACE
+    assert dec(*args, 64, 0, 16, ctypes.c_float(0.1), 512, 1 << 20, None) == lib.KQ8_OK
