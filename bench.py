@@ -86,6 +86,22 @@ def measured_bf16_peak():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def max_over_ranks(ms: float, pg, device) -> float:
+    """The slowest rank's elapsed time, on every rank (a no-op for one rank)."""
+    if not pg:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate_gbs(bytes_per_step: float, steps: int, world: int, ms: float) -> float:
+    """Whole-job GB/s: each of the `world` replicas processed bytes_per_step in
+    each of `steps` steps within the slowest rank's `ms` (weak scaling)."""
+    return bytes_per_step * steps * world / (ms * 1e-3) / 1e9
+
+
 def kernel_source_hash(sources) -> str:
     """Hash of the csrc files a kernel and its launch plan are built from."""
     h = hashlib.sha256()
@@ -242,6 +258,9 @@ def run_reference(args, rank, world):
     the same workload per step (value: the same exact-equivalent KV GB/s)."""
     if rank != 0:
         return
+    if args.workload == "prefill":
+        run_reference_prefill(args)
+        return
     wl, sparse = make_workload(args, 0)
     threads = oracle_threads()
     nseq = {"serving": 4, "long": 1, "sparse": 2, "qwen2b": 1}[args.workload]
@@ -262,6 +281,40 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def run_reference_prefill(args):
+    """Reference arm of --workload prefill: the oracle's batched prefill of the
+    last 16 tokens of the first prompt (each sees ~n tokens) per step."""
+    import oracle
+    from query_decode_attention_gb300 import workloads as W
+    name, nq, nkv, n = PREFILL_CASES[0]
+    wl = W.Workload(name, 1, nq, nkv, np.array([n], np.int32), kind="sigma", seed=2100 + n)
+    K, V = W.host_kv(wl, 0)
+    k8, ks = oracle.kv_quantize_rows(K)
+    v8, vs = oracle.kv_quantize_rows(V)
+    nb = 16
+    q = np.random.default_rng(7).standard_normal((nb, nq, wl.hd)).astype(np.float32)
+    run = lambda: oracle.prefill_batch(q, [nb], [k8], [ks], [v8], [vs], wl.scale,
+                                       nthreads=oracle_threads())
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    secs = time.perf_counter() - t0
+    v = prefill_flops(nq, n, nb) * args.steps / secs / 1e12
+    sample = (f"oracle prefill of the last {nb} tokens of the {n}-token {name} prompt "
+              f"(all {nq} query heads, one layer), OpenMP over (token, head), one call per step")
+    cores = oracle_threads() if oracle.openmp_threads() else 1
+    print(json.dumps({"impl": "reference", "metric": "q8-KV causal prefill attention TFLOP/s",
+                      "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+                      "warmup": args.warmup, "higher_is_better": True, "data": "synthetic",
+                      "config": {"workload": name},
+                      "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": cores,
+                                       "kind": "oracle", "sample": sample},
+                      "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                              "d2h_bytes_per_step": 0}}))
 
 
 def make_workload(args, rank):
@@ -462,13 +515,9 @@ def main():
         torch.cuda.synchronize()
     clk.__exit__(None, None, None)
     clocks = clk.summary()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    if pg:
-        t = torch.tensor([elapsed_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), pg, dev)
     ms_per_step = elapsed_ms / args.steps
-    value = bytes_per_step * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+    value = job_rate_gbs(bytes_per_step, args.steps, world, elapsed_ms)
     decode_ms = [timers[s][l][0].elapsed_time(timers[s][l][1])
                  for s in range(args.steps) for l in range(L)]
     dec_avg_ms = sum(decode_ms) / len(decode_ms)
@@ -563,14 +612,10 @@ def e2e_measure(args, sc, stream, bytes_per_step, world, pg):
         step()
     ev1.record(stream)
     torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1)
-    if pg:
-        t = torch.tensor([ms], device=sc.dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), pg, sc.dev)
     h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_slots))
     d2h = h_out.numel() * h_out.element_size()
-    return {"value": round(bytes_per_step * steps * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+    return {"value": round(job_rate_gbs(bytes_per_step, steps, world, ms), 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(ms / steps, 4)}
 
