@@ -98,6 +98,12 @@ def lib():
             L.kq8o_decode_batch_q4.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                                _I, _F, _I]
             L.kq8o_decode_batch_q4.restype = _I
+            L.kq8o_sparse_attn_group.argtypes = [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                                 _I, _F, _I, _I, _I, _P]
+            L.kq8o_sparse_attn_group.restype = _I
+            L.kq8o_decode_batch_shared.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I,
+                                                   _I, _I, _F, _I, _I, _I, _P, _I]
+            L.kq8o_decode_batch_shared.restype = _I
             L.kq8o_has_openmp.restype = _I
             _lib = L
     return _lib
@@ -402,6 +408,42 @@ def decode_batch(q, k8_list, ks_list, v8_list, vs_list, scale, kv_bs=32, sparse=
     if rc != 0:
         raise ValueError("oracle: unsupported shape")
     return (out, sel[:, :, :topk]) if sparse else out
+
+
+def sparse_attn_group(q, cache: SeqCache, kh, scale, block, topk, probe):
+    """One selection for the G query heads q [G, hd] of KV head kh (the max
+    of their block scores); returns (out [G, hd], sel [topk], used)."""
+    q, pq = _c(q, np.float32)
+    G = q.shape[0]
+    out = np.empty((G, cache.hd), np.float32)
+    sel = np.full(max(1, topk), -1, np.int32)
+    kp, vp = cache.scale_ptrs(kh)
+    used = lib().kq8o_sparse_attn_group(out.ctypes.data_as(_P), pq, G, cache.k_ptrs, cache.v_ptrs,
+                                        kp, vp, cache.n, cache.kv_dim, cache.kv_bs, cache.nkv,
+                                        kh * cache.hd, cache.hd, float(np.float32(scale)), block,
+                                        topk, probe, sel.ctypes.data_as(_P))
+    return out, sel[:topk], bool(used)
+
+
+def decode_batch_shared(q, k8_list, ks_list, v8_list, vs_list, scale, kv_bs=32, block=32,
+                        topk=32, probe=8, nthreads=0):
+    """Block-sparse decode with one selection per KV head; returns (out
+    [B, nq, hd], sel [B, nq, topk])."""
+    q = np.ascontiguousarray(q, np.float32)
+    B, nq, hd = q.shape
+    k_rows, v_rows, ks, vs, offs, lens, nkv = _pack_layer(k8_list, ks_list, v8_list, vs_list, hd,
+                                                          kv_bs)
+    out = np.empty((B, nq, hd), np.float32)
+    sel = np.full((B, nq, max(1, topk)), -1, np.int32)
+    rc = lib().kq8o_decode_batch_shared(out.ctypes.data_as(_P), q.ctypes.data_as(_P),
+                                        k_rows.ctypes.data_as(_P), v_rows.ctypes.data_as(_P),
+                                        ks.ctypes.data_as(_P), vs.ctypes.data_as(_P),
+                                        offs.ctypes.data_as(_P), lens.ctypes.data_as(_P), B, nq,
+                                        nkv, hd, kv_bs, float(np.float32(scale)), block, topk,
+                                        probe, sel.ctypes.data_as(_P), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle: unsupported shape")
+    return out, sel[:, :, :topk]
 
 
 def decode_batch_q4(q, k4_list, ks_list, v4_list, vs_list, scale, kv_bs=32, nthreads=0):

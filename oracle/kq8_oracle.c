@@ -502,6 +502,55 @@ int kq8o_sparse_attn_head(float* out, const float* q,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Shared selection per KV head (not on the pages: the variant that lets the */
+/* G query heads of a KV head read the same blocks once).  READING: the      */
+/* group's score of block j is the max over its G query heads of their       */
+/* [10-1] block scores; one top-k on that (ties to the lower block); every   */
+/* head then runs the one pass over the same kept blocks in ascending order. */
+/* The gate is the same.  q, out: [G][hd]; sel_out (optional): [topk].       */
+/* ------------------------------------------------------------------------ */
+int kq8o_sparse_attn_group(float* out, const float* q, int G, int8_t* const* k_blocks,
+                           int8_t* const* v_blocks, const float* kscale, const float* vscale,
+                           int seq_len, int kv_dim, int kv_bs, int nkv, int kh_off, int hd,
+                           float scale, int block, int topk, int probe, int32_t* sel_out) {
+    if (sel_out)
+        for (int i = 0; i < topk; i++) sel_out[i] = -1;
+    if (seq_len <= 2 * block) {
+        for (int g = 0; g < G; g++)
+            kq8o_attn_single_q(out + (size_t)g * hd, q + (size_t)g * hd, k_blocks, v_blocks,
+                               kscale, vscale, seq_len, kv_dim, kv_bs, nkv, kh_off, hd, scale,
+                               NULL, 0, NULL, NULL);
+        return 0;
+    }
+    int nb = (seq_len + block - 1) / block;
+    float* best = (float*)malloc(sizeof(float) * (size_t)nb);
+    float* bs = (float*)malloc(sizeof(float) * (size_t)nb);
+    for (int g = 0; g < G; g++) {
+        kq8o_probe_block_scores(bs, q + (size_t)g * hd, k_blocks, kscale, seq_len, kv_dim, kv_bs,
+                                nkv, kh_off, hd, scale, block, probe);
+        for (int j = 0; j < nb; j++) best[j] = (g == 0 || bs[j] > best[j]) ? bs[j] : best[j];
+    }
+    int32_t* sel = (int32_t*)malloc(sizeof(int32_t) * (size_t)(topk < nb ? topk : nb));
+    int m = kq8o_topk_blocks(sel, best, nb, topk);
+    int32_t* toks = (int32_t*)malloc(sizeof(int32_t) * (size_t)m * (size_t)block);
+    int nt = 0;
+    for (int i = 0; i < m; i++) {
+        int j = sel[i];
+        for (int t = j * block; t < (j + 1) * block && t < seq_len; t++) toks[nt++] = t;
+        if (sel_out) sel_out[i] = j;
+    }
+    for (int g = 0; g < G; g++)
+        kq8o_attn_single_q(out + (size_t)g * hd, q + (size_t)g * hd, k_blocks, v_blocks, kscale,
+                           vscale, seq_len, kv_dim, kv_bs, nkv, kh_off, hd, scale, toks, nt, NULL,
+                           NULL);
+    free(toks);
+    free(sel);
+    free(bs);
+    free(best);
+    return 1;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Batch drivers over the pages' layout.  All B sequences of one layer live  */
 /* in one token-major array rows[total_tokens][nkv*hd] (int8) with           */
 /* row_offset[b] the first row of sequence b, and scales[total_tokens][nkv]; */
@@ -623,7 +672,43 @@ void kq8o_kv_quantize_rows(const float* x, int64_t T, int nkv, int hd, int8_t* c
         }
 }
 
-/* q4 write path over a batch of rows (reading above). */
+/* Block-sparse decode with one selection per KV head (kq8o_sparse_attn_group)
+ * over the batch layout of kq8o_decode_batch; sel_out: [B][nq][topk], the
+ * group's selection repeated for each of its query heads. */
+int kq8o_decode_batch_shared(float* out, const float* q, int8_t* k_rows, int8_t* v_rows,
+                             const float* kscale, const float* vscale, const int64_t* row_offset,
+                             const int32_t* seq_lens, int B, int nq, int nkv, int hd, int kv_bs,
+                             float scale, int block, int topk, int probe, int32_t* sel_out,
+                             int nthreads) {
+    if (hd > KQ8O_MAX_HD || hd % 32 != 0 || nkv <= 0 || nq % nkv != 0) return -1;
+    int G = nq / nkv;
+    int kv_dim = nkv * hd;
+    int64_t units = (int64_t)B * nkv;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t u = 0; u < units; u++) {
+        int b = (int)(u / nkv), kh = (int)(u % nkv);
+        int8_t** kb = make_block_ptrs(k_rows, row_offset[b], seq_lens[b], kv_bs, kv_dim);
+        int8_t** vb = make_block_ptrs(v_rows, row_offset[b], seq_lens[b], kv_bs, kv_dim);
+        size_t row0 = (size_t)b * nq + (size_t)kh * G;
+        int32_t* sel = sel_out ? sel_out + row0 * topk : NULL;
+        kq8o_sparse_attn_group(out + row0 * hd, q + row0 * hd, G, kb, vb,
+                               kscale + (size_t)row_offset[b] * nkv + kh,
+                               vscale + (size_t)row_offset[b] * nkv + kh, seq_lens[b], kv_dim,
+                               kv_bs, nkv, kh * hd, hd, scale, block, topk, probe, sel);
+        if (sel)
+            for (int g = 1; g < G; g++) memcpy(sel + (size_t)g * topk, sel, sizeof(int32_t) * topk);
+        free(kb);
+        free(vb);
+    }
+    return 0;
+}
+
+/* q4 write path over a batch of rows (reading above). *//* q4 write path over a batch of rows (reading above). */
 void kq8o_kv_quantize_rows_q4(const float* x, int64_t T, int nkv, int hd, int8_t* codes,
                               float* maxima) {
     for (int64_t t = 0; t < T; t++)

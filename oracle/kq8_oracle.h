@@ -67,6 +67,15 @@ int kq8o_decode_batch_q4(float* out, const float* q, int8_t* k_rows, int8_t* v_r
                          const float* kscale, const float* vscale, const int64_t* row_offset,
                          const int32_t* seq_lens, int B, int nq, int nkv, int hd, int kv_bs,
                          float scale, int nthreads);
+int kq8o_sparse_attn_group(float* out, const float* q, int G, int8_t* const* k_blocks,
+                           int8_t* const* v_blocks, const float* kscale, const float* vscale,
+                           int seq_len, int kv_dim, int kv_bs, int nkv, int kh_off, int hd,
+                           float scale, int block, int topk, int probe, int32_t* sel_out);
+int kq8o_decode_batch_shared(float* out, const float* q, int8_t* k_rows, int8_t* v_rows,
+                             const float* kscale, const float* vscale, const int64_t* row_offset,
+                             const int32_t* seq_lens, int B, int nq, int nkv, int hd, int kv_bs,
+                             float scale, int block, int topk, int probe, int32_t* sel_out,
+                             int nthreads);
 int kq8o_has_openmp(void);
 
 #endif

@@ -548,3 +548,55 @@ def test_streaming_empty_state_and_empty_pieces():
     assert not st.output().any()
     oracle.attn_stream(st, q, cache, 0, 0.1, 5, 5)  # empty piece changes nothing
     assert st.S[0] == 0 and st.M[0] == np.float32(-1e9)
+
+
+# ---------------------------------------------------------------------------
+# Shared selection per KV head (the variant that lets a KV head's G query heads
+# read the same blocks; its reading is the oracle's: max of their block scores)
+# ---------------------------------------------------------------------------
+
+def test_shared_selection_is_topk_of_the_heads_max_and_one_pass_each():
+    n, block, topk, probe = 700, 32, 5, 8
+    cache, _ = _cache(n, nkv=1, seed=80)
+    q = np.random.default_rng(81).standard_normal((4, 128)).astype(np.float32)
+    out, sel, used = oracle.sparse_attn_group(q, cache, 0, 0.1, block, topk, probe)
+    assert used
+    scores = np.max([oracle.probe_block_scores(q[g], cache, 0, 0.1, block, probe)
+                     for g in range(4)], axis=0)
+    want = sorted(sorted(range(len(scores)), key=lambda j: (-scores[j], j))[:topk])
+    assert list(sel) == want
+    toks = np.concatenate([np.arange(j * block, min((j + 1) * block, n)) for j in want])
+    for g in range(4):
+        assert np.array_equal(out[g], oracle.attn_single_q(q[g], cache, 0, 0.1, tokens=toks))
+
+
+def test_shared_selection_one_head_equals_per_head_and_gate():
+    cache, _ = _cache(500, nkv=1, seed=82)
+    q = np.random.default_rng(83).standard_normal((1, 128)).astype(np.float32)
+    o1, s1, _ = oracle.sparse_attn_group(q, cache, 0, 0.1, 32, 4, 8)
+    o2, s2, _ = oracle.sparse_attn_head(q[0], cache, 0, 0.1, 32, 4, 8)
+    assert np.array_equal(o1[0], o2) and np.array_equal(s1, s2)
+    small, _ = _cache(64, nkv=1, seed=84)
+    q2 = np.random.default_rng(85).standard_normal((2, 128)).astype(np.float32)
+    o3, s3, used = oracle.sparse_attn_group(q2, small, 0, 0.1, 32, 4, 8)
+    assert not used and np.all(s3 == -1)
+    assert np.array_equal(o3[1], oracle.attn_single_q(q2[1], small, 0, 0.1))
+
+
+def test_shared_selection_batch_driver_matches_group_calls():
+    lens = [400, 50]
+    rng = np.random.default_rng(86)
+    caches, raw = [], []
+    for b, n in enumerate(lens):
+        c, r = _cache(n, nkv=2, seed=87 + b)
+        caches.append(c)
+        raw.append(r)
+    q = rng.standard_normal((2, 4, 128)).astype(np.float32)
+    out, sel = oracle.decode_batch_shared(q, [r[0] for r in raw], [r[1] for r in raw],
+                                          [r[2] for r in raw], [r[3] for r in raw], 0.1,
+                                          block=32, topk=3, probe=8)
+    for b in range(2):
+        for kh in range(2):
+            o, s, _ = oracle.sparse_attn_group(q[b, 2 * kh:2 * kh + 2], caches[b], kh, 0.1, 32, 3, 8)
+            assert np.array_equal(out[b, 2 * kh:2 * kh + 2], o)
+            assert np.array_equal(sel[b, 2 * kh], s) and np.array_equal(sel[b, 2 * kh + 1], s)
