@@ -793,11 +793,15 @@ def extras(dev, kq8, paged, W, peak):
     ms_ex = _time_calls(lambda: kq8.kq8_decode_attn(out, case.q, case.cache, case.page_table,
                                                     case.seq_lens, wl.max_seq_len, wl.scale, wsx,
                                                     stream=stream), 10, stream)
+    ms_sh = _time_calls(lambda: kq8.kq8_sparse_decode_attn_shared(
+        out, case.q, case.cache, case.page_table, case.seq_lens, wl.max_seq_len, wl.scale,
+        wl.block, wl.topk, wl.probe, ws, stream=stream), 10, stream)
     nblk = -(-65536 // wl.block)
     probe_bytes = wl.B * wl.nkv * nblk * wl.probe * (wl.hd + 4)
     sel_bytes = wl.B * wl.nq * wl.topk * wl.block * (2 * wl.hd + 8)
     res["sparse_n65536"] = {"workload": wl.name, "ms": round(ms, 4), "exact_ms": round(ms_ex, 4),
                             "speedup_vs_exact": round(ms_ex / ms, 2),
+                            "shared_selection_ms": round(ms_sh, 4),
                             "probe_plus_selected_bytes": probe_bytes + sel_bytes,
                             "exact_GB/s": round(wl.kv_bytes_per_layer() / (ms_ex * 1e-3) / 1e9, 1)}
     del case, out, ws, wsx

@@ -241,6 +241,24 @@ int kq8_state_finalize(float* out, const float* state_acc, const float* state_ms
                        kq8_stream_t stream);
 
 /*
+ * Block-sparse decode with one selection per KV head: the G query heads of a
+ * KV head keep the same top-k blocks, so the bounded attention reads each kept
+ * block once for all of them.  Not on the pages (their selection is per query
+ * head, kq8_sparse_decode_attn); this library's reading: the group's score of a
+ * block is the max over its G query heads of their block scores, one top-k on
+ * that (ties to the lower block), then each head runs the one pass over those
+ * blocks.  Arguments, gate, workspace (kq8_sparse_decode_workspace_bytes) and
+ * status as kq8_sparse_decode_attn; sel_blocks repeats the group's selection
+ * for each of its query heads.
+ */
+int kq8_sparse_decode_attn_shared(float* out, const float* q, const kq8_cache_t* cache,
+                                  const int32_t* page_table, int32_t max_pages,
+                                  const int32_t* seq_lens, int32_t max_seq_len, int32_t B,
+                                  int32_t nq, float scale, int32_t block, int32_t topk,
+                                  int32_t probe, int32_t* sel_blocks, void* workspace,
+                                  size_t workspace_bytes, kq8_stream_t stream);
+
+/*
  * Batched causal prefill attention over the q8 cache ([10-1] §1: a batch of nb
  * new tokens scores against the whole history, O(nb*n); §2: the exact batched
  * kernel of the prefill gate).  Reading (the page gives no formula for the

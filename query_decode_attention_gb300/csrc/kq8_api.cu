@@ -157,7 +157,7 @@ int run_sparse(float* out, const float* q, const kq8_cache_t* cache, const int32
                int32_t max_pages, const int32_t* row_len, const int32_t* row_seq,
                int32_t max_seq_len, int32_t rows, int32_t nq, float scale, int32_t block,
                int32_t topk, int32_t probe, int32_t* sel_blocks, const Plan& plan,
-               void* workspace, cudaStream_t s) {
+               void* workspace, cudaStream_t s, bool shared_sel = false) {
     const int nkv = cache->num_kv_heads;
     const int G = nq / nkv;
     char* ws = static_cast<char*>(workspace);
@@ -185,6 +185,7 @@ int run_sparse(float* out, const float* q, const kq8_cache_t* cache, const int32
     sp.sel_blocks = sel_blocks;
     sp.status = reinterpret_cast<uint32_t*>(ws);
     sp.row_seq = row_seq;
+    sp.shared_sel = shared_sel ? 1 : 0;
     int rc = launch_probe(sp, G, rows, nkv, s);
     if (rc) return rc;
     rc = launch_topk(sp, G, rows, nkv, s);
@@ -342,6 +343,26 @@ int kq8_sparse_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
     if (B == 0) return KQ8_OK;
     return run_sparse(out, q, cache, page_table, max_pages, seq_lens, nullptr, max_seq_len, B, nq,
                       scale, block, topk, probe, sel_blocks, plan, workspace, (cudaStream_t)stream);
+}
+
+int kq8_sparse_decode_attn_shared(float* out, const float* q, const kq8_cache_t* cache,
+                                  const int32_t* page_table, int32_t max_pages,
+                                  const int32_t* seq_lens, int32_t max_seq_len, int32_t B,
+                                  int32_t nq, float scale, int32_t block, int32_t topk,
+                                  int32_t probe, int32_t* sel_blocks, void* workspace,
+                                  size_t workspace_bytes, kq8_stream_t stream) {
+    int rc = check_decode(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq);
+    if (rc) return rc;
+    if (block < TILE || block % TILE != 0 || topk < 1 || probe < 1 || probe > block)
+        return KQ8_ERR_UNSUPPORTED;
+    if (sel_blocks && !aligned(sel_blocks, 4)) return KQ8_ERR_INVALID_ARG;
+    const Plan plan = plan_sparse(B, nq, cache->num_kv_heads, max_seq_len, block, topk);
+    rc = check_ws(workspace, workspace_bytes, plan.total);
+    if (rc) return rc;
+    if (B == 0) return KQ8_OK;
+    return run_sparse(out, q, cache, page_table, max_pages, seq_lens, nullptr, max_seq_len, B, nq,
+                      scale, block, topk, probe, sel_blocks, plan, workspace, (cudaStream_t)stream,
+                      true);
 }
 
 size_t kq8_sparse_prefill_workspace_bytes(int32_t total_q, int32_t nq, int32_t nkv,

@@ -34,6 +34,7 @@ struct SparseParams {
     int32_t* sel_blocks;     // optional [B][nq][topk]
     uint32_t* status;
     const int32_t* row_seq;  // optional [B]: page-table row of row b (null = b)
+    int32_t shared_sel;      // 1: one selection per KV head (max of its heads' block scores)
 };
 
 __device__ __forceinline__ int sparse_seq_len(const SparseParams& P, int b) {
@@ -264,9 +265,25 @@ __global__ void __launch_bounds__(TOPK_THREADS) kq8_topk_kernel(const SparsePara
     const int nblk = (n + P.block - 1) / P.block;
     uint8_t* masks = P.masks + (size_t)(b * nkv + h) * P.max_nblk;
     for (int j = tid; j < nblk; j += TOPK_THREADS) masks[j] = 0;
+    if (P.shared_sel) {
+        // one selection for the group: head 0's row becomes the max over the G
+        // heads of their block scores (in place; the scores are this call's)
+        float* sc0 = P.scores + ((size_t)b * P.nq + (size_t)h * G) * P.max_nblk;
+        for (int j = tid; j < nblk; j += TOPK_THREADS) {
+            float m = sc0[j];
+#pragma unroll
+            for (int g = 1; g < G; g++) {
+                const float v = P.scores[((size_t)b * P.nq + (size_t)h * G + g) * P.max_nblk + j];
+                m = v > m ? v : m;
+            }
+            sc0[j] = m;
+        }
+    }
     __syncthreads();
 
-    for (int g = 0; g < G; g++) {
+    const int nsel = P.shared_sel ? 1 : G;
+    const uint8_t group_mask = (uint8_t)((1u << G) - 1u);
+    for (int g = 0; g < nsel; g++) {
         const float* sc = P.scores + ((size_t)b * P.nq + (size_t)h * G + g) * P.max_nblk;
         int32_t* sel = P.sel_blocks ? P.sel_blocks + ((size_t)b * P.nq + (size_t)h * G + g) * P.topk
                                     : nullptr;
@@ -320,8 +337,14 @@ __global__ void __launch_bounds__(TOPK_THREADS) kq8_topk_kernel(const SparsePara
             int keep_tot;
             const int pos = block_excl_scan(keep ? 1 : 0, scan_tmp, keep_tot) + kept_before;
             if (keep) {
-                masks[j] |= (uint8_t)(1u << g);
-                if (sel) sel[pos] = j;
+                masks[j] |= P.shared_sel ? group_mask : (uint8_t)(1u << g);
+                if (sel) {
+                    if (P.shared_sel) {
+                        for (int gg = 0; gg < G; gg++) sel[(size_t)gg * P.topk + pos] = j;
+                    } else {
+                        sel[pos] = j;
+                    }
+                }
             }
             ties_before += tie_tot;
             kept_before += keep_tot;

@@ -83,6 +83,8 @@ _lib.kq8_sparse_prefill_attn.argtypes = [_P, _P, _I32, _CP, _P, _I32, _P, _P, _I
 _lib.kq8_append_kv_q4.argtypes = [_CP, _P, _P, _P, _I32, _P, _P]
 _lib.kq8_decode_attn_q4.argtypes = [_P, _P, _CP, _P, _I32, _P, _I32, _I32, _I32, ctypes.c_float,
                                     _P, _SZ, _P]
+_lib.kq8_sparse_decode_attn_shared.argtypes = [_P, _P, _CP, _P, _I32, _P, _I32, _I32, _I32,
+                                               ctypes.c_float, _I32, _I32, _I32, _P, _P, _SZ, _P]
 _lib.kq8_read_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), _P]
 _lib.kq8_strerror.argtypes = [ctypes.c_int]
 _lib.kq8_strerror.restype = ctypes.c_char_p
@@ -380,6 +382,26 @@ def kq8_prefill_attn(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
                                  float(scale), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream)),
            "kq8_prefill_attn")
+
+
+def kq8_sparse_decode_attn_shared(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
+                                  page_table: torch.Tensor, seq_lens: torch.Tensor,
+                                  max_seq_len: int, scale: float, block: int, topk: int,
+                                  probe: int, workspace: torch.Tensor,
+                                  sel_blocks: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Block-sparse decode with one selection per KV head (include/kq8.h)."""
+    B, nq, max_pages = _decode_args(out, q, cache, page_table, seq_lens)
+    if sel_blocks is not None:
+        _dtype(sel_blocks, torch.int32, "sel_blocks")
+        if sel_blocks.numel() != B * nq * topk:
+            raise ValueError("sel_blocks must be [B, nq, topk]")
+    _check(_lib.kq8_sparse_decode_attn_shared(_ptr(out), _ptr(q), ctypes.byref(cache.struct),
+                                              _ptr(page_table), max_pages, _ptr(seq_lens),
+                                              int(max_seq_len), B, nq, float(scale), int(block),
+                                              int(topk), int(probe), _ptr(sel_blocks),
+                                              _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(),
+                                              _stream(stream)), "kq8_sparse_decode_attn_shared")
 
 
 def kq8_sparse_prefill_workspace_bytes(total_q: int, nq: int, nkv: int, max_seq_len: int,

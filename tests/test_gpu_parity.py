@@ -274,6 +274,55 @@ def test_sparse_planted_full_size():
                 assert set(sel[b, h].tolist()) == set(W.planted_blocks(wl, b, h // wl.G).tolist())
 
 
+def _decode_shared(case):
+    wl = case.wl
+    out = torch.empty((wl.B, wl.nq, wl.hd), dtype=torch.float32, device=DEV)
+    nb = kq8.kq8_sparse_decode_workspace_bytes(wl.B, wl.nq, wl.nkv, wl.max_seq_len, wl.block,
+                                               wl.topk)
+    ws = kq8.new_workspace(nb, DEV)
+    sb = torch.full((wl.B, wl.nq, wl.topk), -7, dtype=torch.int32, device=DEV)
+    kq8.kq8_sparse_decode_attn_shared(out, case.q, case.cache, case.page_table, case.seq_lens,
+                                      wl.max_seq_len, wl.scale, wl.block, wl.topk, wl.probe, ws,
+                                      sel_blocks=sb)
+    assert kq8.kq8_read_status(ws) == 0
+    return out.cpu().numpy(), sb.cpu().numpy()
+
+
+@pytest.mark.parametrize("nq,nkv,lens,block,topk,probe", [
+    (16, 8, [3000, 65, 800], 32, 4, 8),      # G = 2, one sequence at the gate
+    (32, 8, [5000, 2000], 32, 8, 8),         # G = 4
+    (64, 8, [1500], 64, 3, 16),              # G = 8, block 64
+])
+def test_shared_selection_matches_oracle(nq, nkv, lens, block, topk, probe):
+    # one selection per KV head (max of its query heads' block scores)
+    wl = W.custom(len(lens), nq, nkv, lens, seed=sum(lens) + nq, block=block, topk=topk,
+                  probe=probe)
+    case, q, Ks, Vs = _host_case(wl)
+    got, sel = _decode_shared(case)
+    k8s, kss, v8s, vss = oracle_quantized(Ks, Vs)
+    ref, rsel = oracle.decode_batch_shared(q, k8s, kss, v8s, vss, wl.scale, kv_bs=wl.kv_bs,
+                                           block=block, topk=topk, probe=probe)
+    assert np.array_equal(sel, rsel)
+    assert_out_close(got, ref, f"shared selection G={wl.G}")
+    for b in range(wl.B):                    # the group's heads share their blocks
+        for h in range(0, wl.nq, wl.G):
+            assert all(np.array_equal(sel[b, h], sel[b, h + g]) for g in range(wl.G))
+
+
+def test_shared_selection_planted_recall():
+    wl = W.sparse_planted(16384, B=4)
+    case, q, Ks, Vs = _host_case(wl)
+    got, sel = _decode_shared(case)
+    k8s, kss, v8s, vss = oracle_quantized(Ks, Vs)
+    ref, rsel = oracle.decode_batch_shared(q, k8s, kss, v8s, vss, wl.scale, block=wl.block,
+                                           topk=wl.topk, probe=wl.probe)
+    assert np.array_equal(sel, rsel)
+    assert_out_close(got, ref, "shared selection, planted")
+    for b in range(wl.B):
+        for h in range(wl.nq):
+            assert set(sel[b, h].tolist()) == set(W.planted_blocks(wl, b, h // wl.G).tolist())
+
+
 # ---------------------------------------------------------------------------
 # device-side checks of untrusted metadata
 # ---------------------------------------------------------------------------
