@@ -1,8 +1,8 @@
 // kq8_tc.cuh -- 5th-generation tensor core (tcgen05) helpers for sm_103a:
 // tensor-memory allocation, shared-memory matrix descriptors, MMA issue and
 // commit, tensor-memory loads and stores, and the ordering fences between
-// them.  Inline PTX only; one elected thread issues MMAs, all four warps of a
-// 128-thread CTA read and write their own 32-lane slice of tensor memory.
+// them.  Inline PTX only; one thread issues MMAs, and warp w reads and writes
+// the 32-lane slice 32*(w % 4) .. 32*(w % 4) + 31 of tensor memory.
 #pragma once
 
 #include <cstdint>
