@@ -822,8 +822,14 @@ def cpu_baseline(wl, sparse=False, seconds=10.0):
     while secs < seconds and passes < 1000:
         secs += smp.run(threads)
         passes += 1
-    return {"value": round(smp.nbytes * passes / secs / 1e9, 4), "unit": UNIT, "cores": threads,
-            "kind": "oracle", "sample": smp.describe() + f", {passes} passes in {secs:.1f} s"}
+    res = {"value": round(smp.nbytes * passes / secs / 1e9, 4), "unit": UNIT, "cores": threads,
+           "kind": "oracle", "sample": smp.describe() + f", {passes} passes in {secs:.1f} s"}
+    # the same oracle on one core: one pass over the first sequence of the sample
+    one = OracleSample(wl, range(1), sparse=sparse)
+    t1 = one.run(1)
+    res["single_core"] = {"value": round(one.nbytes / t1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                          "sample": one.describe() + f", one pass in {t1:.2f} s"}
+    return res
 
 
 if __name__ == "__main__":
