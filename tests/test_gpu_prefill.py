@@ -63,6 +63,14 @@ def test_prefill_sigma_kv_and_kv_bs_64():
     assert_out_close(got, ref, "sigma, kv_bs 64")
 
 
+@pytest.mark.parametrize("kv_bs", [128, 256])
+def test_prefill_large_pages(kv_bs):
+    wl = W.custom(2, 32, 8, [1100, 300], seed=kv_bs, kv_bs=kv_bs)
+    got, ref, status = _run(wl, [333, 300], seed=kv_bs + 1, pt_seed=5)
+    assert status == 0
+    assert_out_close(got, ref, f"kv_bs {kv_bs}")
+
+
 def test_prefill_outlier_keys_force_rescales():
     # Student-t keys with x20 channels: the running max jumps often, so the
     # lazy O rescale in tensor memory runs on many rows

@@ -53,6 +53,8 @@ def test_q4_append_bit_exact(kv_bs):
     (8, 8, [300], 64),                # G = 1, kv_bs 64
     (64, 8, [1000, 64], 32),          # G = 8
     (6, 2, [129], 32),                # G = 3
+    (16, 8, [1500, 257], 128),        # large pages
+    (16, 8, [700], 256),
 ])
 def test_q4_decode_matches_oracle(nq, nkv, lens, kv_bs):
     wl = W.custom(len(lens), nq, nkv, lens, kind="sigma", seed=sum(lens) + nq, kv_bs=kv_bs)
