@@ -739,7 +739,8 @@ def extras(dev, kq8, paged, W, peak):
         kq8.kq8_state_reset(state, stream=stream)
         for k in range(pieces):
             kq8.kq8_decode_attn_update(state, case.q, case.cache, case.page_table, bounds[k],
-                                       bounds[k + 1], wl.max_seq_len, wl.scale, ws, stream=stream)
+                                       bounds[k + 1], wl.max_seq_len, wl.scale, ws, stream=stream,
+                                       max_range_len=-(-wl.max_seq_len // pieces))
         kq8.kq8_state_finalize(out, state, stream=stream)
     ms_s = _time_calls(stream_all, 10, stream)
     gbs_s = wl.kv_bytes_per_layer() / (ms_s * 1e-3) / 1e9

@@ -229,14 +229,19 @@ int kq8_sparse_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
  *                            kq8_decode_attn (workspace from
  *                            kq8_decode_workspace_bytes).  Feeding a sequence in
  *                            pieces gives the one-call result up to rounding.
+ *                            max_range_len (host): an upper bound on
+ *                            seq_end[b] - seq_begin[b], used to split the ranges
+ *                            over enough CTAs; 0 = max_seq_len.  A range longer
+ *                            than the bound sets KQ8_STATUS_BAD_SEQLEN and that
+ *                            sequence is skipped.
  *   kq8_state_finalize     : out = acc / sum per row (0 for an empty row).
  */
 int kq8_state_reset(float* state_acc, float* state_ms, int32_t rows, kq8_stream_t stream);
 int kq8_decode_attn_update(float* state_acc, float* state_ms, const float* q,
                            const kq8_cache_t* cache, const int32_t* page_table, int32_t max_pages,
                            const int32_t* seq_begin, const int32_t* seq_end, int32_t max_seq_len,
-                           int32_t B, int32_t nq, float scale, void* workspace,
-                           size_t workspace_bytes, kq8_stream_t stream);
+                           int32_t max_range_len, int32_t B, int32_t nq, float scale,
+                           void* workspace, size_t workspace_bytes, kq8_stream_t stream);
 int kq8_state_finalize(float* out, const float* state_acc, const float* state_ms, int32_t rows,
                        kq8_stream_t stream);
 

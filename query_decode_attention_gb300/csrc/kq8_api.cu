@@ -71,6 +71,26 @@ Plan plan_exact(int B, int nq, int nkv, int max_seq_len) {
     return p;
 }
 
+// The exact plan's workspace layout with chunks sized for token ranges of at
+// most max_range tokens (streaming updates): more, shorter chunks per range, but
+// never more chunks than the full plan, so its workspace still suffices.
+Plan plan_exact_range(int B, int nq, int nkv, int max_seq_len, int max_range) {
+    Plan p = plan_exact(B, nq, nkv, max_seq_len);
+    if (max_range <= 0 || max_range >= max_seq_len) return p;
+    // a range not starting on a tile boundary touches one tile more
+    const int64_t tiles = ((int64_t)max_range + TILE - 1) / TILE + 1;
+    int ct, nch;
+    chunking(B, nkv, tiles, device_sms(), ct, nch);
+    if (nch > p.num_chunks) {
+        ct = (int)((tiles + p.num_chunks - 1) / p.num_chunks);
+        ct = (ct + ATTN_WARPS - 1) / ATTN_WARPS * ATTN_WARPS;
+        nch = (int)((tiles + ct - 1) / ct);
+    }
+    p.chunk_tiles = ct;
+    p.num_chunks = nch;
+    return p;
+}
+
 Plan plan_sparse(int B, int nq, int nkv, int max_seq_len, int block, int topk) {
     Plan p;
     const int G = nq / nkv;
@@ -413,13 +433,14 @@ int kq8_state_reset(float* state_acc, float* state_ms, int32_t rows, kq8_stream_
 int kq8_decode_attn_update(float* state_acc, float* state_ms, const float* q,
                            const kq8_cache_t* cache, const int32_t* page_table, int32_t max_pages,
                            const int32_t* seq_begin, const int32_t* seq_end, int32_t max_seq_len,
-                           int32_t B, int32_t nq, float scale, void* workspace,
-                           size_t workspace_bytes, kq8_stream_t stream) {
+                           int32_t max_range_len, int32_t B, int32_t nq, float scale,
+                           void* workspace, size_t workspace_bytes, kq8_stream_t stream) {
     int rc = check_decode(state_acc, q, cache, page_table, max_pages, seq_end, max_seq_len, B, nq);
     if (rc) return rc;
     if (B > 0 && (!state_ms || !aligned(state_ms, 8))) return KQ8_ERR_INVALID_ARG;
+    if (max_range_len < 0) return KQ8_ERR_INVALID_ARG;
     const int nkv = cache->num_kv_heads;
-    const Plan plan = plan_exact(B, nq, nkv, max_seq_len);
+    const Plan plan = plan_exact_range(B, nq, nkv, max_seq_len, max_range_len);
     rc = check_ws(workspace, workspace_bytes, plan.total);
     if (rc) return rc;
     if (B == 0) return KQ8_OK;

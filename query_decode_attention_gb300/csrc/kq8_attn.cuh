@@ -178,6 +178,10 @@ __device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h)
         r.entries = P.list_len[b * P.cache.num_kv_heads + h];
     else
         r.entries = (r.n + TILE - 1) / TILE - r.first_tile;
+    if (r.entries > P.num_chunks * P.chunk_tiles) {  // longer than the plan's grid covers
+        r.bad = true;
+        r.entries = 0;
+    }
     return r;
 }
 

@@ -70,7 +70,7 @@ _lib.kq8_decode_attn_noalloc.argtypes = [_P, _P, _CP, _P, _I32, _P, _I32, _I32, 
                                          ctypes.c_float, _P]
 _lib.kq8_state_reset.argtypes = [_P, _P, _I32, _P]
 _lib.kq8_decode_attn_update.argtypes = [_P, _P, _P, _CP, _P, _I32, _P, _P, _I32, _I32, _I32,
-                                        ctypes.c_float, _P, _SZ, _P]
+                                        _I32, ctypes.c_float, _P, _SZ, _P]
 _lib.kq8_state_finalize.argtypes = [_P, _P, _P, _I32, _P]
 _lib.kq8_prefill_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32]
 _lib.kq8_prefill_workspace_bytes.restype = _SZ
@@ -328,8 +328,9 @@ def kq8_state_reset(state: AttnState, stream=None) -> None:
 def kq8_decode_attn_update(state: AttnState, q: torch.Tensor, cache: PagedKVCache,
                            page_table: torch.Tensor, seq_begin: Optional[torch.Tensor],
                            seq_end: torch.Tensor, max_seq_len: int, scale: float,
-                           workspace: torch.Tensor, stream=None) -> None:
-    """Fold tokens [seq_begin, seq_end) of each sequence into `state`."""
+                           workspace: torch.Tensor, stream=None, max_range_len: int = 0) -> None:
+    """Fold tokens [seq_begin, seq_end) of each sequence into `state`;
+    max_range_len bounds seq_end - seq_begin (0: max_seq_len)."""
     B, nq, max_pages = _decode_args(state.acc, q, cache, page_table, seq_end)
     if seq_begin is not None:
         _dtype(seq_begin, torch.int32, "seq_begin")
@@ -337,7 +338,8 @@ def kq8_decode_attn_update(state: AttnState, q: torch.Tensor, cache: PagedKVCach
             raise ValueError("seq_begin must be [B]")
     _check(_lib.kq8_decode_attn_update(_ptr(state.acc), _ptr(state.ms), _ptr(q),
                                        ctypes.byref(cache.struct), _ptr(page_table), max_pages,
-                                       _ptr(seq_begin), _ptr(seq_end), int(max_seq_len), B, nq,
+                                       _ptr(seq_begin), _ptr(seq_end), int(max_seq_len),
+                                       int(max_range_len), B, nq,
                                        float(scale), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(),
                                        _stream(stream)), "kq8_decode_attn_update")

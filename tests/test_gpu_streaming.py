@@ -49,7 +49,8 @@ def test_pieces_match_one_pass(nq, nkv, lens, pieces):
         b0 = torch.tensor(cuts[:, k], dtype=torch.int32, device=DEV)
         b1 = torch.tensor(cuts[:, k + 1], dtype=torch.int32, device=DEV)
         kq8.kq8_decode_attn_update(state, case.q, case.cache, case.page_table, b0, b1,
-                                   wl.max_seq_len, wl.scale, ws)
+                                   wl.max_seq_len, wl.scale, ws,
+                                   max_range_len=int((cuts[:, k + 1] - cuts[:, k]).max()))
     assert kq8.kq8_read_status(ws) == 0
     assert_out_close(_finalize(state, wl), oracle_decode(wl, q, Ks, Vs), f"{pieces} pieces")
 
@@ -112,3 +113,18 @@ def test_empty_pieces_and_bad_start():
     c = oracle.SeqCache(k8, ks, v8, vs)
     for h in range(wl.nq):
         assert_out_close(got[0, h], oracle.attn_single_q(q[0, h], c, h // wl.G, wl.scale), "seq 0")
+
+
+def test_range_longer_than_the_hint_is_reported_and_skipped():
+    wl = W.custom(2, 16, 8, [3000, 500], seed=61)
+    q, Ks, Vs = host_inputs(wl)
+    case = paged.fill_from_host(wl, Ks, Vs, DEV, q_host=q)
+    state = kq8.AttnState(wl.B, wl.nq, DEV)
+    ws = _ws(wl)
+    # hint 500 tokens: sequence 0's 3000-token range exceeds what the grid covers
+    kq8.kq8_decode_attn_update(state, case.q, case.cache, case.page_table, None, case.seq_lens,
+                               wl.max_seq_len, wl.scale, ws, max_range_len=500)
+    assert kq8.kq8_read_status(ws) == kq8.KQ8_STATUS_BAD_SEQLEN
+    got = _finalize(state, wl)
+    ref = oracle_decode(wl, q, Ks, Vs)
+    assert_out_close(got[1], ref[1], "the in-bound sequence")
