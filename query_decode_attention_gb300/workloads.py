@@ -170,7 +170,7 @@ def host_kv(wl: Workload, b: int, layer: int = 0, q: Optional[np.ndarray] = None
         chi2 = (r.standard_normal((3,) + shape, dtype=np.float32) ** 2).sum(0)
         K = (z / np.sqrt(chi2 / 3.0)).astype(np.float32)
         ch = _outlier_channels(wl)
-        K.reshape(n, -1)[:, ch] *= np.float32(20.0)
+        K.reshape(n, wl.nkv * wl.hd)[:, ch] *= np.float32(20.0)
         V = r.standard_normal(shape, dtype=np.float32)
     else:
         raise ValueError(wl.kind)
