@@ -13,20 +13,23 @@
 // GB300 mapping.  A CTA (one per SM: all 512 TMEM columns) takes two query
 // tiles A and B of 128 (token, query head) rows each -- 128/G consecutive new
 // tokens x the G query heads of one KV head -- and walks the KV history in
-// 32-token cache sub-tiles.  Warps have fixed roles and meet only on mbarriers:
-//   warp 13     copies raw sub-tiles (codes + scales as stored) into a
+// 64-token steps, each filled from two 32-token cache sub-tiles.  Warps have
+// fixed roles and meet only on mbarriers:
+//   warp 11     copies raw sub-tiles (codes + scales as stored) into a
 //               three-stage ring with bulk-async copies;
-//   warps 8-11  widen them exactly to tensor-core operands: K to fp16, V to
-//               bf16 (every int8 is exact in both), double-buffered;
-//   warp 12     one thread issues every MMA: S_t = Q_t K^T as four per-block
-//               MMA pairs into four TMEM accumulators (each holds the exact
-//               integer block dot), and O_t += W_hi V + W_lo V;
+//   warps 8-9   widen them exactly to tensor-core operands: K to fp16, V to
+//               bf16 (every int8 is exact in both), double-buffered by step;
+//   warp 10     one thread issues every MMA: S_t = Q_t K^T as four per-block
+//               MMA pairs (N = 64) into four TMEM accumulators (each holds the
+//               exact integer block dot), and O_t += W_hi V + W_lo V (N = 128);
 //   warps 0-7   softmax of tile A (0-3) and B (4-7), one thread per row (TMEM
 //               lane): the scores from the block dots in the method's order,
 //               the online softmax with a lazy rescale of the TMEM O row, and
 //               the weights w = p * vscale / 127 as bf16 hi + lo (2^-16).
-// While the softmax warps of one tile work, the tensor core runs the other
-// tile's MMAs: the two tiles alternate (ping-pong).
+// The two tiles take the block-dot accumulators in turn: while one tile's
+// softmax works, the tensor core scores the other (ping-pong).  An M = 128,
+// K = 16 MMA costs the same issue time for N = 32, 64 or 128, so the 64-token
+// step halves the S instructions per token against 32-token steps.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -38,51 +41,56 @@ namespace kq8 {
 namespace {
 
 constexpr int PF_ROWS = 128;            // rows per query tile (MMA M, TMEM lanes)
-constexpr int PF_NT = TILE;             // KV tokens per step: one cache sub-tile
+constexpr int PF_NT = TILE;             // tokens per cache sub-tile (copy and widening unit)
+constexpr int PF_STEP = 2 * TILE;       // tokens per pipeline step (S and PV unit)
 constexpr int PF_RAW = 3;               // raw sub-tile ring stages
-constexpr int PF_CV_WARP = 8;           // warps 8-11 widen K/V
-constexpr int PF_MMA_WARP = 12;
-constexpr int PF_LOAD_WARP = 13;
-constexpr int PF_THREADS = 14 * 32;
-constexpr uint32_t PF_TMEM_COLS = 512;  // tile t: O at 256 t, block dots at 256 t + 128
-constexpr uint32_t PF_COL_D = 128;
+constexpr int PF_CV_WARP = 8;           // warps 8-9 widen K/V
+constexpr int PF_CV_WARPS = 2;
+constexpr int PF_MMA_WARP = 10;
+constexpr int PF_LOAD_WARP = 11;
+constexpr int PF_THREADS = 12 * 32;
+// TMEM columns: O of tile t at 128 t; the block dots of the tile being scored
+// (the two tiles take it in turn) at 256 + 64 b for block b.
+constexpr uint32_t PF_TMEM_COLS = 512;
+constexpr uint32_t PF_COL_D = 256;
 
 // Shared memory map (bytes).  Tensor-core operands are K-major without
-// swizzle: 8-row x 16-byte core matrices, 128 B each.
+// swizzle: 8-row x 16-byte core matrices, 128 B each.  A 64-token step's K and
+// V buffers are filled one 32-token cache sub-tile (one half) at a time.
 constexpr uint32_t SM_Q = 0;            // 2 tiles x fp16 Q codes, 128 rows x 128 dims (32 KB)
-constexpr uint32_t SM_K = 65536;        // 2 buffers x fp16 K codes, 32 tokens x 128 dims (8 KB)
-constexpr uint32_t SM_V = 81920;        // 2 buffers x bf16 V codes, 128 dims x 32 tokens (8 KB)
-constexpr uint32_t SM_W = 98304;        // [tile][buffer] bf16 weights hi, lo: 128 x 32 (16 KB)
-constexpr uint32_t SM_RAW = 163840;     // 3 stages x raw sub-tile (8448 B)
-constexpr uint32_t SM_SC = 189184;      // 2 buffers x (32 score multipliers, 32 value steps)
-constexpr uint32_t SM_OK = 189696;      // int: page valid, 2 buffers then 3 raw stages
-constexpr uint32_t SM_BAR = 189728;     // mbarriers (below)
-constexpr uint32_t SM_TMEM = 189888;    // TMEM base address written by the allocator
-constexpr uint32_t SM_ABORT = 189892;   // set when a bounded wait ran out
-constexpr uint32_t PF_SMEM = 189952;
+constexpr uint32_t SM_K = 65536;        // 2 buffers x fp16 K codes, 64 tokens x 128 dims (16 KB)
+constexpr uint32_t SM_V = 98304;        // 2 buffers x bf16 V codes, 128 dims x 64 tokens (16 KB)
+constexpr uint32_t SM_W = 131072;       // 2 tiles x bf16 weights hi, lo: 128 x 64 (32 KB)
+constexpr uint32_t SM_RAW = 196608;     // 3 stages x raw sub-tile (8448 B)
+constexpr uint32_t SM_SC = 221952;      // 2 buffers x (64 score multipliers, 64 value steps)
+constexpr uint32_t SM_OK = 222976;      // int: page valid per (buffer, half), then per raw stage
+constexpr uint32_t SM_BAR = 223008;     // mbarriers (below)
+constexpr uint32_t SM_TMEM = 223152;    // TMEM base address written by the allocator
+constexpr uint32_t SM_ABORT = 223156;   // set when a bounded wait ran out
+constexpr uint32_t PF_SMEM = 223232;
 
 // mbarriers: index, arrivals per phase
 constexpr int B_RAW_FULL = 0;   // [3] producer's expect-tx arrive + the copied bytes
-constexpr int B_RAW_EMPTY = 3;  // [3] 4 widening warps
-constexpr int B_KV_FULL = 6;    // [2] 4 widening warps
+constexpr int B_RAW_EMPTY = 3;  // [3] 2 widening warps
+constexpr int B_KV_FULL = 6;    // [2] 2 widening warps x the step's 2 sub-tiles
 constexpr int B_KV_EMPTY = 8;   // [2] commit after the last MMA reading the buffer
 constexpr int B_S_FULL = 10;    // [tile] commit after S_t
-constexpr int B_D_FREE = 12;    // [tile] 4 softmax warps have read S_t
+constexpr int B_D_FREE = 12;    // [tile] 4 softmax warps have read S_t: the block dots are free
 constexpr int B_W_FULL = 14;    // [tile] 4 softmax warps wrote W_t (and rescaled O_t)
-constexpr int B_PV_DONE = 16;   // [tile][buffer] commit after PV_t
-constexpr int B_COUNT = 20;
+constexpr int B_PV_DONE = 16;   // [tile] commit after PV_t
+constexpr int B_COUNT = 18;
 
 constexpr size_t PF_STATUS_BYTES = 256;  // workspace: the status word (256-byte slot)
 
 constexpr float PF_LOG2E = 1.4426950408889634f;
 constexpr float PF_RESCALE_SLACK = 8.0f;  // log2 units: rescale O when the max grows > 2^8
 
-__device__ __forceinline__ uint32_t sm_k(int p) { return SM_K + 8192u * p; }
-__device__ __forceinline__ uint32_t sm_v(int p) { return SM_V + 8192u * p; }
-__device__ __forceinline__ uint32_t sm_whi(int t, int p) { return SM_W + 32768u * t + 16384u * p; }
+__device__ __forceinline__ uint32_t sm_k(int p) { return SM_K + 16384u * p; }
+__device__ __forceinline__ uint32_t sm_v(int p) { return SM_V + 16384u * p; }
+__device__ __forceinline__ uint32_t sm_whi(int t) { return SM_W + 32768u * t; }
 __device__ __forceinline__ uint32_t sm_raw(int s) { return SM_RAW + (uint32_t)STAGE_BYTES * s; }
-__device__ __forceinline__ uint32_t sm_km(int p) { return SM_SC + 256u * p; }
-__device__ __forceinline__ uint32_t sm_vs(int p) { return SM_SC + 256u * p + 128u; }
+__device__ __forceinline__ uint32_t sm_km(int p) { return SM_SC + 512u * p; }
+__device__ __forceinline__ uint32_t sm_vs(int p) { return SM_SC + 512u * p + 256u; }
 
 // Byte offset of the 16-byte chunk holding elements 8*kc .. 8*kc+7 of row r in
 // a K-major operand of R rows: core matrices adjacent along K are R*16 B apart
@@ -160,21 +168,26 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
     const int i0 = qt * 2 * TQ;  // first new token of tile A; tile B follows
     if (i0 >= nb) return;
     const int ntok = min(2 * TQ, nb - i0);
-    const int ntiles = (n - nb + i0 + ntok - 1) / PF_NT + 1;
+    const int nsub = (n - nb + i0 + ntok - 1) / PF_NT + 1;  // cache sub-tiles the CTA reads
+    const int nsteps = (nsub + 1) / 2;                       // 64-token steps
     const int pos_first = n - nb + i0;  // position of the CTA's first new token
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SM_BAR);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SM_TMEM);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM_ABORT);
-    volatile int* okv = reinterpret_cast<volatile int*>(sm + SM_OK);  // [0..1] buffers, [2..4] raw
+    // page-valid flags: [0..3] per (buffer, half), [4..6] per raw stage
+    volatile int* okv = reinterpret_cast<volatile int*>(sm + SM_OK);
     if (warp == 0) {
         __syncwarp();
         tc::tmem_alloc(tslot, PF_TMEM_COLS);
     }
     if (tid == 0) {
         for (int i = 0; i < B_COUNT; i++) {
-            const bool four = (i >= B_RAW_EMPTY && i < B_KV_EMPTY) || (i >= B_D_FREE && i < B_PV_DONE);
-            mbar_init(bars + i, four ? 4 : 1);
+            uint32_t cnt = 1;
+            if (i >= B_D_FREE && i < B_PV_DONE) cnt = 4;
+            if (i >= B_RAW_EMPTY && i < B_KV_FULL) cnt = PF_CV_WARPS;
+            if (i >= B_KV_FULL && i < B_KV_EMPTY) cnt = 2 * PF_CV_WARPS;
+            mbar_init(bars + i, cnt);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -241,17 +254,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
 
     if (warp == PF_LOAD_WARP) {
         // ---- producer: raw sub-tile t into ring stage t % 3 (page ids one per
-        // lane for a 32-sub-tile window, fetched a window ahead)
+        // lane for a 32-sub-tile window, fetched a window ahead).  A step's
+        // second half past the last sub-tile is an empty sub-tile (no copy).
         auto load_window = [&](int w) -> int32_t {
             const int t = 32 * w + lane;
-            if (t >= ntiles) return -1;
+            if (t >= nsub) return -1;
             const int32_t pg = P.page_table[(size_t)b * P.max_pages + (t * PF_NT) / kv_bs];
-            return (pg >= 0 && pg < P.cache.num_pages) ? pg : -1;
+            return (pg >= 0 && pg < P.cache.num_pages) ? pg : -2;
         };
         int32_t pw_cur = load_window(0), pw_nxt = load_window(1);
         uint64_t pol;
         asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-        for (int t = 0; t < ntiles; t++) {
+        for (int t = 0; t < 2 * nsteps; t++) {
             const int s = t % PF_RAW;
             if (t >= PF_RAW &&
                 !__all_sync(0xffffffffu, wait(B_RAW_EMPTY + s, ((t - PF_RAW) / PF_RAW) & 1)))
@@ -260,13 +274,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
                 pw_cur = pw_nxt;
                 pw_nxt = load_window((t >> 5) + 1);
             }
-            const int32_t pg = __shfl_sync(0xffffffffu, pw_cur, t & 31);
+            const int32_t pg = __shfl_sync(0xffffffffu, pw_cur, t & 31);  // -1: none, -2: bad
             if (lane == 0) {
                 uint64_t* bar = bars + B_RAW_FULL + s;
                 uint8_t* st = sm + sm_raw(s);
-                okv[2 + s] = pg >= 0;
+                okv[4 + s] = pg >= 0;
                 if (pg < 0) {
-                    atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
+                    if (pg == -2) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
                     mbar_arrive_expect_tx(bar, 0);  // completes the phase with no data
                 } else {
                     const int sub = ((t * PF_NT) % kv_bs) / PF_NT;
@@ -282,62 +296,69 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
                 }
             }
         }
-    } else if (warp >= PF_CV_WARP && warp < PF_CV_WARP + 4) {
-        // ---- widening: raw sub-tile j -> fp16 K, bf16 V and scales of buffer j & 1
-        const int cw = warp - PF_CV_WARP;
+    } else if (warp >= PF_CV_WARP && warp < PF_CV_WARP + PF_CV_WARPS) {
+        // ---- widening: raw sub-tile t -> half t & 1 of the fp16 K, bf16 V and
+        // scales of buffer (t >> 1) & 1
         const float kmul = inv127() * P.scale * PF_LOG2E;  // score multiplier per kscale
-        for (int j = 0; j < ntiles; j++) {
-            const int s = j % PF_RAW, p = j & 1;
-            bool ok = __all_sync(0xffffffffu, wait(B_RAW_FULL + s, (j / PF_RAW) & 1));
-            if (ok && j >= 2) ok = __all_sync(0xffffffffu, wait(B_KV_EMPTY + p, ((j - 2) >> 1) & 1));
+        for (int t = 0; t < 2 * nsteps; t++) {
+            const int s = t % PF_RAW, j = t >> 1, half = t & 1, p = j & 1;
+            bool ok = __all_sync(0xffffffffu, wait(B_RAW_FULL + s, (t / PF_RAW) & 1));
+            if (ok && j >= 2)
+                ok = __all_sync(0xffffffffu, wait(B_KV_EMPTY + p, ((j - 2) >> 1) & 1));
             if (!ok) break;
             const uint8_t* st = sm + sm_raw(s);
-            const bool tok = okv[2 + s] != 0;
-            // K: warp = 32-element block, lane = token row (stored at position kpos)
-            const uint4* kr = reinterpret_cast<const uint4*>(st + cw * 1024 + kpos(lane) * 32);
-            const uint4 ka = kr[0], kb = kr[1];
-            const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-            uint8_t* Ks = sm + sm_k(p);
+            const bool tok = okv[4 + s] != 0;
+            // warp w widens K block / V token group cw = w and w + 2
+#pragma unroll 1
+            for (int cw = warp - PF_CV_WARP; cw < 4; cw += PF_CV_WARPS) {
+                // K: warp = 32-element block, lane = token row (stored at position kpos)
+                const uint4* kr = reinterpret_cast<const uint4*>(st + cw * 1024 + kpos(lane) * 32);
+                const uint4 ka = kr[0], kb = kr[1];
+                const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+                uint8_t* Ks = sm + sm_k(p);
 #pragma unroll
-            for (int c = 0; c < 4; c++)
-                *reinterpret_cast<uint4*>(Ks + cm_off(lane, cw * 4 + c, PF_NT)) =
-                    make_uint4(i8x2_to_h2(kw[2 * c], 0), i8x2_to_h2(kw[2 * c], 1),
-                               i8x2_to_h2(kw[2 * c + 1], 0), i8x2_to_h2(kw[2 * c + 1], 1));
-            // V transposed (dims as rows, tokens along K): tokens 8*cw .. +7, dims
-            // 4*lane .. +3; the dim order rotates per lane pair so that the eight
-            // lanes of each 16-byte store phase hit eight bank groups
-            const uint32_t* vr =
-                reinterpret_cast<const uint32_t*>(st + SUB_K_BYTES + cw * 8 * HD) + lane;
-            uint32_t u[8];
+                for (int c = 0; c < 4; c++)
+                    *reinterpret_cast<uint4*>(Ks + cm_off(32 * half + lane, cw * 4 + c, PF_STEP)) =
+                        make_uint4(i8x2_to_h2(kw[2 * c], 0), i8x2_to_h2(kw[2 * c], 1),
+                                   i8x2_to_h2(kw[2 * c + 1], 0), i8x2_to_h2(kw[2 * c + 1], 1));
+                // V transposed (dims as rows, tokens along K): tokens 8*cw .. +7 of
+                // this half, dims 4*lane .. +3; the dim order rotates per lane pair so
+                // that the eight lanes of each 16-byte store phase hit eight bank groups
+                const uint32_t* vr =
+                    reinterpret_cast<const uint32_t*>(st + SUB_K_BYTES + cw * 8 * HD) + lane;
+                uint32_t u[8];
 #pragma unroll
-            for (int tt = 0; tt < 8; tt++) u[tt] = vr[tt * (HD / 4)] ^ 0x80808080u;
-            uint8_t* Vs = sm + sm_v(p);
-            const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+                for (int tt = 0; tt < 8; tt++) u[tt] = vr[tt * (HD / 4)] ^ 0x80808080u;
+                uint8_t* Vs = sm + sm_v(p);
+                const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
 #pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const int ee = (e + (lane >> 1)) & 3;
-                const uint32_t sel = 0x7540u | (uint32_t)ee;
-                float2 f[4];
+                for (int e = 0; e < 4; e++) {
+                    const int ee = (e + (lane >> 1)) & 3;
+                    const uint32_t sel = 0x7540u | (uint32_t)ee;
+                    float2 f[4];
 #pragma unroll
-                for (int q2 = 0; q2 < 4; q2++)
-                    f[q2] = __fadd2_rn(
-                        make_float2(__uint_as_float(__byte_perm(u[2 * q2], 0x4B000000u, sel)),
-                                    __uint_as_float(__byte_perm(u[2 * q2 + 1], 0x4B000000u, sel))),
-                        bias);
-                *reinterpret_cast<uint4*>(Vs + cm_off(4 * lane + ee, cw, PF_ROWS)) =
-                    make_uint4(bf2_bits(f[0].x, f[0].y), bf2_bits(f[1].x, f[1].y),
-                               bf2_bits(f[2].x, f[2].y), bf2_bits(f[3].x, f[3].y));
+                    for (int q2 = 0; q2 < 4; q2++)
+                        f[q2] = __fadd2_rn(
+                            make_float2(
+                                __uint_as_float(__byte_perm(u[2 * q2], 0x4B000000u, sel)),
+                                __uint_as_float(__byte_perm(u[2 * q2 + 1], 0x4B000000u, sel))),
+                            bias);
+                    *reinterpret_cast<uint4*>(Vs + cm_off(4 * lane + ee, 4 * half + cw, PF_ROWS)) =
+                        make_uint4(bf2_bits(f[0].x, f[0].y), bf2_bits(f[1].x, f[1].y),
+                                   bf2_bits(f[2].x, f[2].y), bf2_bits(f[3].x, f[3].y));
+                }
+                // scales: 0 for a missing page, an empty half and past the sequence
+                // end (masked tokens must carry finite weights)
+                if (cw < 2) {
+                    const float* rs =
+                        reinterpret_cast<const float*>(st + SUB_K_BYTES + SUB_V_BYTES) + 32 * cw;
+                    const bool live = tok && t * PF_NT + lane < n;
+                    float* dst = reinterpret_cast<float*>(sm + (cw == 0 ? sm_km(p) : sm_vs(p)));
+                    dst[32 * half + lane] =
+                        live ? __fmul_rn(rs[lane], cw == 0 ? kmul : inv127()) : 0.0f;
+                }
             }
-            // scales: 0 for a missing page and past the sequence end (masked
-            // tokens must carry finite weights)
-            if (cw < 2) {
-                const float* rs = reinterpret_cast<const float*>(st + SUB_K_BYTES + SUB_V_BYTES) +
-                                  32 * cw;
-                const bool live = tok && j * PF_NT + lane < n;
-                reinterpret_cast<float*>(sm + (cw == 0 ? sm_km(p) : sm_vs(p)))[lane] =
-                    live ? __fmul_rn(rs[lane], cw == 0 ? kmul : inv127()) : 0.0f;
-            }
-            if (cw == 0 && lane == 0) okv[p] = tok;
+            if (warp == PF_CV_WARP && lane == 0) okv[2 * p + half] = tok;
             tc::fence_smem_to_async();
             __syncwarp();
             if (lane == 0) {
@@ -350,51 +371,55 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
         // MMA at K chunk kc adds kc * leading-byte-offset / 16 to the address
         if (lane == 0) {
             const uint64_t d_q = tc::sdesc(smem_u32(sm + SM_Q), PF_ROWS * 16, 128);
-            const uint64_t d_k = tc::sdesc(smem_u32(sm + SM_K), PF_NT * 16, 128);
+            const uint64_t d_k = tc::sdesc(smem_u32(sm + SM_K), PF_STEP * 16, 128);
             const uint64_t d_v = tc::sdesc(smem_u32(sm + SM_V), PF_ROWS * 16, 128);
             const uint64_t d_w = tc::sdesc(smem_u32(sm + SM_W), PF_ROWS * 16, 128);
-            auto issue_s = [&](int t, int p) {  // D_blk = Q_blk K_blk^T, blk = 0..3
+            auto issue_s = [&](int t, int p) {  // D_blk = Q_blk K_blk^T, blk = 0..3, 64 tokens
                 const uint64_t dq = d_q + (uint64_t)t * (32768u >> 4);
-                const uint64_t dk = d_k + (uint64_t)p * (8192u >> 4);
-                constexpr uint32_t ID = tc::IDesc<128, PF_NT, false>::value;
+                const uint64_t dk = d_k + (uint64_t)p * (16384u >> 4);
+                constexpr uint32_t ID = tc::IDesc<128, PF_STEP, false>::value;
 #pragma unroll
                 for (int blk = 0; blk < NB; blk++)
 #pragma unroll
                     for (int kk = 0; kk < 2; kk++) {
                         const int kc = blk * 4 + kk * 2;
-                        tc::mma_f16(tbase + 256 * t + PF_COL_D + 32 * blk,
-                                    dq + (uint64_t)(kc * PF_ROWS), dk + (uint64_t)(kc * PF_NT), ID,
-                                    kk > 0);
+                        tc::mma_f16(tbase + PF_COL_D + 64 * blk, dq + (uint64_t)(kc * PF_ROWS),
+                                    dk + (uint64_t)(kc * PF_STEP), ID, kk > 0);
                     }
                 tc::mma_commit(bars + B_S_FULL + t);
             };
             auto issue_pv = [&](int t, int p, bool accumulate) {  // O_t (+)= W_hi V + W_lo V
-                const uint64_t dv = d_v + (uint64_t)p * (8192u >> 4);
-                const uint64_t dh = d_w + (uint64_t)(sm_whi(t, p) - SM_W) / 16, dl = dh + (8192u >> 4);
+                const uint64_t dv = d_v + (uint64_t)p * (16384u >> 4);
+                const uint64_t dh = d_w + (uint64_t)(sm_whi(t) - SM_W) / 16;
+                const uint64_t dl = dh + (16384u >> 4);
                 constexpr uint32_t ID = tc::IDesc<128, HD, true>::value;
 #pragma unroll
-                for (int kk = 0; kk < PF_NT / 16; kk++) {
+                for (int kk = 0; kk < PF_STEP / 16; kk++) {
                     const uint64_t off = (uint64_t)(kk * 2 * PF_ROWS);
-                    tc::mma_f16(tbase + 256 * t, dh + off, dv + off, ID, accumulate || kk > 0);
-                    tc::mma_f16(tbase + 256 * t, dl + off, dv + off, ID, true);
+                    tc::mma_f16(tbase + 128 * t, dh + off, dv + off, ID, accumulate || kk > 0);
+                    tc::mma_f16(tbase + 128 * t, dl + off, dv + off, ID, true);
                 }
-                tc::mma_commit(bars + B_PV_DONE + 2 * t + p);
+                tc::mma_commit(bars + B_PV_DONE + t);
             };
+            // The tiles take the block dots in turn: S_A(j), (A has read them)
+            // S_B(j), (B has read them) S_A(j+1), ...
             bool ok = wait(B_KV_FULL, 0);
             if (ok) {
                 tc::fence_after_sync();
                 issue_s(0, 0);
-                issue_s(1, 0);
             }
-            for (int j = 0; ok && j < ntiles; j++) {
+            for (int j = 0; ok && j < nsteps; j++) {
                 const int p = j & 1;
-                const bool more = j + 1 < ntiles;
+                const bool more = j + 1 < nsteps;
+                if (!(ok = wait(B_D_FREE + 0, j & 1))) break;
+                tc::fence_after_sync();
+                issue_s(1, p);
                 if (!(ok = wait(B_W_FULL + 0, j & 1))) break;
                 tc::fence_after_sync();
                 issue_pv(0, p, j > 0);
                 if (more) {
                     if (!(ok = wait(B_KV_FULL + (p ^ 1), ((j + 1) >> 1) & 1) &&
-                               wait(B_D_FREE + 0, j & 1)))
+                               wait(B_D_FREE + 1, j & 1)))
                         break;
                     tc::fence_after_sync();
                     issue_s(0, p ^ 1);
@@ -403,72 +428,66 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
                 tc::fence_after_sync();
                 issue_pv(1, p, j > 0);
                 // buffer p is free once these MMAs land; signalled only when a
-                // later sub-tile reuses it (every commit must be waited on
-                // before the CTA exits)
-                if (j + 2 < ntiles) tc::mma_commit(bars + B_KV_EMPTY + p);
-                if (more) {
-                    if (!(ok = wait(B_D_FREE + 1, j & 1))) break;
-                    tc::fence_after_sync();
-                    issue_s(1, p ^ 1);
-                }
+                // later step reuses it (every commit must be waited on before
+                // the CTA exits)
+                if (j + 2 < nsteps) tc::mma_commit(bars + B_KV_EMPTY + p);
             }
         }
     } else if (warp < 8) {
-        // ---- softmax of this row over every sub-tile
+        // ---- softmax of this row over every 64-token step
         const uint32_t t_row = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
-        const uint32_t tO = tbase + 256 * qtile + t_row, tD = tO + PF_COL_D;
+        const uint32_t tO = tbase + 128 * qtile + t_row, tD = tbase + PF_COL_D + t_row;
         float M2 = M_INIT, Mhi = M_INIT + PF_RESCALE_SLACK;
         float2 S2 = make_float2(0.0f, 0.0f);  // running sum, even and odd tokens
         bool ok = true;
-        for (int j = 0; j < ntiles; j++) {
+        for (int j = 0; j < nsteps; j++) {
             const int p = j & 1;
             ok = __all_sync(0xffffffffu, wait(B_S_FULL + qtile, j & 1));
-            // the widening warps' scales and page flag of buffer p (long complete)
+            // the widening warps' scales and page flags of buffer p (long complete)
             if (ok) ok = __all_sync(0xffffffffu, wait(B_KV_FULL + p, (j >> 1) & 1));
             if (!ok) break;
             tc::fence_after_sync();
-            // scores against the sub-tile (article 9-2 §2 seg. 2): s = sum_b
-            // dot_b * qsc_b, times the token's kscale / 127 * scale, base 2
-            float2 x[PF_NT / 2];
-            {
-                float d[PF_NT];
-                tc::tmem_ld32(tD, d);
-                const float2 c0 = make_float2(qsc[0], qsc[0]);
+            // scores against the step's 64 tokens (article 9-2 §2 seg. 2): s =
+            // sum_b dot_b * qsc_b, times the token's kscale / 127 * scale, base 2
+            float2 x[PF_STEP / 2];
 #pragma unroll
-                for (int i = 0; i < PF_NT / 2; i++)
-                    x[i] = __fmul2_rn(make_float2(d[2 * i], d[2 * i + 1]), c0);
+            for (int blk = 0; blk < NB; blk++) {
+                const float2 cb = make_float2(qsc[blk], qsc[blk]);
 #pragma unroll
-                for (int blk = 1; blk < NB; blk++) {
-                    tc::tmem_ld32(tD + 32 * blk, d);
-                    const float2 cb = make_float2(qsc[blk], qsc[blk]);
+                for (int q16 = 0; q16 < PF_STEP / 16; q16++) {
+                    float d[16];
+                    tc::tmem_ld16(tD + 64 * blk + 16 * q16, d);
 #pragma unroll
-                    for (int i = 0; i < PF_NT / 2; i++)
-                        x[i] = __ffma2_rn(make_float2(d[2 * i], d[2 * i + 1]), cb, x[i]);
+                    for (int i = 0; i < 8; i++) {
+                        const float2 dv = make_float2(d[2 * i], d[2 * i + 1]);
+                        x[8 * q16 + i] =
+                            blk == 0 ? __fmul2_rn(dv, cb) : __ffma2_rn(dv, cb, x[8 * q16 + i]);
+                    }
                 }
             }
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) pf_arrive(bars + B_D_FREE + qtile);  // S_t may be overwritten
+            if (lane == 0) pf_arrive(bars + B_D_FREE + qtile);  // the block dots may be overwritten
             const float2* km2 = reinterpret_cast<const float2*>(sm + sm_km(p));
 #pragma unroll
-            for (int i = 0; i < PF_NT / 2; i++) x[i] = __fmul2_rn(x[i], km2[i]);
-            const int t0 = j * PF_NT;
-            const bool tok = okv[p] != 0;
-            // every row of the CTA sees every token of this sub-tile: no masking
-            const bool full = tok && t0 + PF_NT - 1 <= pos_first;
+            for (int i = 0; i < PF_STEP / 2; i++) x[i] = __fmul2_rn(x[i], km2[i]);
+            const int t0 = j * PF_STEP;
+            const bool ok0 = okv[2 * p] != 0, ok1 = okv[2 * p + 1] != 0;
+            // every row of the CTA sees every token of this step: no masking
+            const bool full = ok0 && ok1 && t0 + PF_STEP - 1 <= pos_first;
             if (!full) {
-                const int nvis = tok ? max(0, min(PF_NT, pos - t0 + 1)) : 0;
+                const int nvis = max(0, min(PF_STEP, pos - t0 + 1));
 #pragma unroll
-                for (int i = 0; i < PF_NT / 2; i++) {
-                    if (2 * i >= nvis) x[i].x = -INFINITY;
-                    if (2 * i + 1 >= nvis) x[i].y = -INFINITY;
+                for (int i = 0; i < PF_STEP / 2; i++) {
+                    const bool hok = (2 * i < PF_NT) ? ok0 : ok1;
+                    if (!hok || 2 * i >= nvis) x[i].x = -INFINITY;
+                    if (!hok || 2 * i + 1 >= nvis) x[i].y = -INFINITY;
                 }
             }
             float mt = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < PF_NT / 2; i++) mt = fmaxf(mt, fmaxf(x[i].x, x[i].y));
-            // lazy rescale of S and of this row of O (online-softmax max), once
-            // PV_t of the previous sub-tile has landed
+            for (int i = 0; i < PF_STEP / 2; i++) mt = fmaxf(mt, fmaxf(x[i].x, x[i].y));
+            // lazy rescale of S and of this row of O (online-softmax max)
             const bool need = mt > Mhi;
             float cf = 1.0f;
             if (need) {
@@ -477,10 +496,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
                 M2 = mt;
                 Mhi = mt + PF_RESCALE_SLACK;
             }
+            // PV_t of the previous step has read W_t and written O_t
+            if (j > 0 && !(ok = __all_sync(0xffffffffu, wait(B_PV_DONE + qtile, (j - 1) & 1))))
+                break;
             if (j > 0 && __any_sync(0xffffffffu, need)) {
-                if (!(ok = __all_sync(0xffffffffu,
-                                      wait(B_PV_DONE + 2 * qtile + (p ^ 1), ((j - 1) >> 1) & 1))))
-                    break;
                 tc::fence_after_sync();
 #pragma unroll 1
                 for (int c = 0; c < HD / 32; c++) {
@@ -491,18 +510,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
                     tc::tmem_st32(tO + 32 * c, o);
                 }
             }
-            // W_t buffer p was last read by PV_t two sub-tiles ago
-            if (j >= 2 &&
-                !(ok = __all_sync(0xffffffffu, wait(B_PV_DONE + 2 * qtile + p, ((j - 2) >> 1) & 1))))
-                break;
             // weights w = p * vscale / 127 = hi + lo: hi is w cut to bf16 (its
             // top 16 bits), lo = w - hi (exact) rounded to bf16
-            uint8_t* Wh = sm + sm_whi(qtile, p);
-            uint8_t* Wl = Wh + 8192;
+            uint8_t* Wh = sm + sm_whi(qtile);
+            uint8_t* Wl = Wh + 16384;
             const float2* vs2 = reinterpret_cast<const float2*>(sm + sm_vs(p));
             const float2 negm = make_float2(-M2, -M2);
 #pragma unroll
-            for (int c = 0; c < PF_NT / 8; c++) {
+            for (int c = 0; c < PF_STEP / 8; c++) {
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int u2 = 0; u2 < 4; u2++) {
@@ -528,9 +543,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
             if (lane == 0) pf_arrive(bars + B_W_FULL + qtile);
         }
         // ---- output: acc / S after the last PV_t
-        if (ok)
-            ok = __all_sync(0xffffffffu, wait(B_PV_DONE + 2 * qtile + ((ntiles - 1) & 1),
-                                              ((ntiles - 1) >> 1) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, wait(B_PV_DONE + qtile, (nsteps - 1) & 1));
         if (ok) {
             tc::fence_after_sync();
             const float S = S2.x + S2.y;
@@ -558,8 +571,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
     tc::fence_before_sync();
     __syncthreads();
     if (*abort_flag && tid == 0) {
-        for (int t = 0; t < 2; t++)
-            mbar_wait_bounded(bars + B_PV_DONE + 2 * t + ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1);
+        for (int t = 0; t < 2; t++) mbar_wait_bounded(bars + B_PV_DONE + t, (nsteps - 1) & 1);
     }
     __syncthreads();
     if (warp == 0) {
