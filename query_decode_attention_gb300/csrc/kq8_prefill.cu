@@ -18,7 +18,8 @@
 //   warp 11     copies raw sub-tiles (codes + scales as stored) into a
 //               three-stage ring with bulk-async copies;
 //   warps 8-9   widen them exactly to tensor-core operands: K to fp16, V to
-//               bf16 (every int8 is exact in both), double-buffered by step;
+//               bf16 (every int8 is exact in both), double-buffered by step,
+//               K of a step before its V;
 //   warp 10     one thread issues every MMA: S_t = Q_t K^T as four per-block
 //               MMA pairs (N = 64) into four TMEM accumulators (each holds the
 //               exact integer block dot), and O_t += W_hi V + W_lo V (N = 128);
@@ -26,10 +27,13 @@
 //               lane): the scores from the block dots in the method's order,
 //               the online softmax with a lazy rescale of the TMEM O row, and
 //               the weights w = p * vscale / 127 as bf16 hi + lo (2^-16).
-// The two tiles take the block-dot accumulators in turn: while one tile's
-// softmax works, the tensor core scores the other (ping-pong).  An M = 128,
-// K = 16 MMA costs the same issue time for N = 32, 64 or 128, so the 64-token
-// step halves the S instructions per token against 32-token steps.
+// The two tiles take the block-dot accumulators in turn, and each PV is
+// followed by the other tile's next S: the tiles run half a step apart, one
+// scoring while the other computes.  An M = 128, K = 16 MMA costs the same
+// issue time for N = 32, 64 or 128, so the 64-token step halves the S
+// instructions per token against 32-token steps.  K and V buffers are
+// released separately (K once both tiles have read the step's scores, V after
+// the second PV), so the widening of the next step's K never waits for a PV.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -65,20 +69,23 @@ constexpr uint32_t SM_RAW = 196608;     // 3 stages x raw sub-tile (8448 B)
 constexpr uint32_t SM_SC = 221952;      // 2 buffers x (64 score multipliers, 64 value steps)
 constexpr uint32_t SM_OK = 222976;      // int: page valid per (buffer, half), then per raw stage
 constexpr uint32_t SM_BAR = 223008;     // mbarriers (below)
-constexpr uint32_t SM_TMEM = 223152;    // TMEM base address written by the allocator
-constexpr uint32_t SM_ABORT = 223156;   // set when a bounded wait ran out
+constexpr uint32_t SM_TMEM = 223200;    // TMEM base address written by the allocator
+constexpr uint32_t SM_ABORT = 223204;   // set when a bounded wait ran out
 constexpr uint32_t PF_SMEM = 223232;
 
 // mbarriers: index, arrivals per phase
 constexpr int B_RAW_FULL = 0;   // [3] producer's expect-tx arrive + the copied bytes
 constexpr int B_RAW_EMPTY = 3;  // [3] 2 widening warps
-constexpr int B_KV_FULL = 6;    // [2] 2 widening warps x the step's 2 sub-tiles
-constexpr int B_KV_EMPTY = 8;   // [2] commit after the last MMA reading the buffer
-constexpr int B_S_FULL = 10;    // [tile] commit after S_t
-constexpr int B_D_FREE = 12;    // [tile] 4 softmax warps have read S_t: the block dots are free
-constexpr int B_W_FULL = 14;    // [tile] 4 softmax warps wrote W_t (and rescaled O_t)
-constexpr int B_PV_DONE = 16;   // [tile] commit after PV_t
-constexpr int B_COUNT = 18;
+constexpr int B_K_FULL = 6;     // [2] 2 widening warps x the step's 2 sub-tiles (K, scales)
+constexpr int B_V_FULL = 8;     // [2] the same for V and its scales
+constexpr int B_K_EMPTY = 10;   // [2] commit once both tiles have read S of the step
+constexpr int B_V_EMPTY = 12;   // [2] commit after the second tile's PV of the step
+constexpr int B_S_FULL = 14;    // [tile] commit after S_t
+constexpr int B_D_FREE = 16;    // [tile] 4 softmax warps have read S_t (and its multipliers)
+constexpr int B_W_FULL = 18;    // [tile] 4 softmax warps wrote W_t (and rescaled O_t)
+constexpr int B_PV_DONE = 20;   // [tile] commit after PV_t
+constexpr int B_FINAL = 22;     // last commit of the MMA thread, waited on before TMEM is freed
+constexpr int B_COUNT = 23;
 
 constexpr size_t PF_STATUS_BYTES = 256;  // workspace: the status word (256-byte slot)
 
@@ -185,8 +192,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
         for (int i = 0; i < B_COUNT; i++) {
             uint32_t cnt = 1;
             if (i >= B_D_FREE && i < B_PV_DONE) cnt = 4;
-            if (i >= B_RAW_EMPTY && i < B_KV_FULL) cnt = PF_CV_WARPS;
-            if (i >= B_KV_FULL && i < B_KV_EMPTY) cnt = 2 * PF_CV_WARPS;
+            if (i >= B_RAW_EMPTY && i < B_K_FULL) cnt = PF_CV_WARPS;
+            if (i >= B_K_FULL && i < B_K_EMPTY) cnt = 2 * PF_CV_WARPS;
             mbar_init(bars + i, cnt);
         }
         *abort_flag = 0;
@@ -297,74 +304,104 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
             }
         }
     } else if (warp >= PF_CV_WARP && warp < PF_CV_WARP + PF_CV_WARPS) {
-        // ---- widening: raw sub-tile t -> half t & 1 of the fp16 K, bf16 V and
-        // scales of buffer (t >> 1) & 1
+        // ---- widening, one step at a time: K of both raw sub-tiles (halves)
+        // of step j into buffer j & 1, then V of both.  K and V are released
+        // separately -- K once both tiles have scored the step, V after the
+        // second tile's PV -- and the K of a step never waits behind the V of
+        // an earlier one, so scoring runs a step ahead of PV.
         const float kmul = inv127() * P.scale * PF_LOG2E;  // score multiplier per kscale
-        for (int t = 0; t < 2 * nsteps; t++) {
-            const int s = t % PF_RAW, j = t >> 1, half = t & 1, p = j & 1;
-            bool ok = __all_sync(0xffffffffu, wait(B_RAW_FULL + s, (t / PF_RAW) & 1));
-            if (ok && j >= 2)
-                ok = __all_sync(0xffffffffu, wait(B_KV_EMPTY + p, ((j - 2) >> 1) & 1));
-            if (!ok) break;
-            const uint8_t* st = sm + sm_raw(s);
-            const bool tok = okv[4 + s] != 0;
-            // warp w widens K block / V token group cw = w and w + 2
+        for (int j = 0; j < nsteps; j++) {
+            const int p = j & 1;
+            const uint32_t reuse = ((j - 2) >> 1) & 1;  // phase of the step that used buffer p
+            bool ok = j < 2 || __all_sync(0xffffffffu, wait(B_K_EMPTY + p, reuse));
 #pragma unroll 1
-            for (int cw = warp - PF_CV_WARP; cw < 4; cw += PF_CV_WARPS) {
-                // K: warp = 32-element block, lane = token row (stored at position kpos)
-                const uint4* kr = reinterpret_cast<const uint4*>(st + cw * 1024 + kpos(lane) * 32);
-                const uint4 ka = kr[0], kb = kr[1];
-                const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+            for (int half = 0; ok && half < 2; half++) {
+                const int t = 2 * j + half, s = t % PF_RAW;
+                if (!(ok = __all_sync(0xffffffffu, wait(B_RAW_FULL + s, (t / PF_RAW) & 1)))) break;
+                const uint8_t* st = sm + sm_raw(s);
+                const bool tok = okv[4 + s] != 0;
+                // K: cw = 32-element block (warp w takes w and w + 2), lane =
+                // token row (stored at position kpos)
                 uint8_t* Ks = sm + sm_k(p);
+#pragma unroll 1
+                for (int cw = warp - PF_CV_WARP; cw < 4; cw += PF_CV_WARPS) {
+                    const uint4* kr =
+                        reinterpret_cast<const uint4*>(st + cw * 1024 + kpos(lane) * 32);
+                    const uint4 ka = kr[0], kb = kr[1];
+                    const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
-                for (int c = 0; c < 4; c++)
-                    *reinterpret_cast<uint4*>(Ks + cm_off(32 * half + lane, cw * 4 + c, PF_STEP)) =
-                        make_uint4(i8x2_to_h2(kw[2 * c], 0), i8x2_to_h2(kw[2 * c], 1),
-                                   i8x2_to_h2(kw[2 * c + 1], 0), i8x2_to_h2(kw[2 * c + 1], 1));
-                // V transposed (dims as rows, tokens along K): tokens 8*cw .. +7 of
-                // this half, dims 4*lane .. +3; the dim order rotates per lane pair so
-                // that the eight lanes of each 16-byte store phase hit eight bank groups
-                const uint32_t* vr =
-                    reinterpret_cast<const uint32_t*>(st + SUB_K_BYTES + cw * 8 * HD) + lane;
-                uint32_t u[8];
-#pragma unroll
-                for (int tt = 0; tt < 8; tt++) u[tt] = vr[tt * (HD / 4)] ^ 0x80808080u;
-                uint8_t* Vs = sm + sm_v(p);
-                const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const int ee = (e + (lane >> 1)) & 3;
-                    const uint32_t sel = 0x7540u | (uint32_t)ee;
-                    float2 f[4];
-#pragma unroll
-                    for (int q2 = 0; q2 < 4; q2++)
-                        f[q2] = __fadd2_rn(
-                            make_float2(
-                                __uint_as_float(__byte_perm(u[2 * q2], 0x4B000000u, sel)),
-                                __uint_as_float(__byte_perm(u[2 * q2 + 1], 0x4B000000u, sel))),
-                            bias);
-                    *reinterpret_cast<uint4*>(Vs + cm_off(4 * lane + ee, 4 * half + cw, PF_ROWS)) =
-                        make_uint4(bf2_bits(f[0].x, f[0].y), bf2_bits(f[1].x, f[1].y),
-                                   bf2_bits(f[2].x, f[2].y), bf2_bits(f[3].x, f[3].y));
+                    for (int c = 0; c < 4; c++)
+                        *reinterpret_cast<uint4*>(
+                            Ks + cm_off(32 * half + lane, cw * 4 + c, PF_STEP)) =
+                            make_uint4(i8x2_to_h2(kw[2 * c], 0), i8x2_to_h2(kw[2 * c], 1),
+                                       i8x2_to_h2(kw[2 * c + 1], 0), i8x2_to_h2(kw[2 * c + 1], 1));
                 }
-                // scales: 0 for a missing page, an empty half and past the sequence
-                // end (masked tokens must carry finite weights)
-                if (cw < 2) {
+                // score multipliers: 0 for a missing page, an empty half and past
+                // the sequence end (masked tokens must carry finite values)
+                if (warp == PF_CV_WARP) {
                     const float* rs =
-                        reinterpret_cast<const float*>(st + SUB_K_BYTES + SUB_V_BYTES) + 32 * cw;
+                        reinterpret_cast<const float*>(st + SUB_K_BYTES + SUB_V_BYTES);
                     const bool live = tok && t * PF_NT + lane < n;
-                    float* dst = reinterpret_cast<float*>(sm + (cw == 0 ? sm_km(p) : sm_vs(p)));
-                    dst[32 * half + lane] =
-                        live ? __fmul_rn(rs[lane], cw == 0 ? kmul : inv127()) : 0.0f;
+                    reinterpret_cast<float*>(sm + sm_km(p))[32 * half + lane] =
+                        live ? __fmul_rn(rs[lane], kmul) : 0.0f;
+                    if (lane == 0) okv[2 * p + half] = tok;
+                }
+                tc::fence_smem_to_async();
+                __syncwarp();
+                if (lane == 0) pf_arrive(bars + B_K_FULL + p);
+            }
+            if (ok && j >= 2) ok = __all_sync(0xffffffffu, wait(B_V_EMPTY + p, reuse));
+#pragma unroll 1
+            for (int half = 0; ok && half < 2; half++) {
+                const int t = 2 * j + half, s = t % PF_RAW;
+                const uint8_t* st = sm + sm_raw(s);
+                const bool tok = okv[4 + s] != 0;
+                // V transposed (dims as rows, tokens along K): tokens 8*cw .. +7
+                // of this half, dims 4*lane .. +3; the dim order rotates per lane
+                // pair so that the eight lanes of each 16-byte store phase hit
+                // eight bank groups
+                uint8_t* Vs = sm + sm_v(p);
+#pragma unroll 1
+                for (int cw = warp - PF_CV_WARP; cw < 4; cw += PF_CV_WARPS) {
+                    const uint32_t* vr =
+                        reinterpret_cast<const uint32_t*>(st + SUB_K_BYTES + cw * 8 * HD) + lane;
+                    uint32_t u[8];
+#pragma unroll
+                    for (int tt = 0; tt < 8; tt++) u[tt] = vr[tt * (HD / 4)] ^ 0x80808080u;
+                    const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int ee = (e + (lane >> 1)) & 3;
+                        const uint32_t sel = 0x7540u | (uint32_t)ee;
+                        float2 f[4];
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; q2++)
+                            f[q2] = __fadd2_rn(
+                                make_float2(
+                                    __uint_as_float(__byte_perm(u[2 * q2], 0x4B000000u, sel)),
+                                    __uint_as_float(__byte_perm(u[2 * q2 + 1], 0x4B000000u, sel))),
+                                bias);
+                        *reinterpret_cast<uint4*>(
+                            Vs + cm_off(4 * lane + ee, 4 * half + cw, PF_ROWS)) =
+                            make_uint4(bf2_bits(f[0].x, f[0].y), bf2_bits(f[1].x, f[1].y),
+                                       bf2_bits(f[2].x, f[2].y), bf2_bits(f[3].x, f[3].y));
+                    }
+                }
+                if (warp == PF_CV_WARP + PF_CV_WARPS - 1) {
+                    const float* rs =
+                        reinterpret_cast<const float*>(st + SUB_K_BYTES + SUB_V_BYTES) + 32;
+                    const bool live = tok && t * PF_NT + lane < n;
+                    reinterpret_cast<float*>(sm + sm_vs(p))[32 * half + lane] =
+                        live ? __fmul_rn(rs[lane], inv127()) : 0.0f;
+                }
+                tc::fence_smem_to_async();
+                __syncwarp();
+                if (lane == 0) {
+                    pf_arrive(bars + B_RAW_EMPTY + s);
+                    pf_arrive(bars + B_V_FULL + p);
                 }
             }
-            if (warp == PF_CV_WARP && lane == 0) okv[2 * p + half] = tok;
-            tc::fence_smem_to_async();
-            __syncwarp();
-            if (lane == 0) {
-                pf_arrive(bars + B_RAW_EMPTY + s);
-                pf_arrive(bars + B_KV_FULL + p);
-            }
+            if (!ok) break;
         }
     } else if (warp == PF_MMA_WARP) {
         // ---- one thread issues every MMA; descriptors are built once and an
@@ -402,36 +439,58 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
                 tc::mma_commit(bars + B_PV_DONE + t);
             };
             // The tiles take the block dots in turn: S_A(j), (A has read them)
-            // S_B(j), (B has read them) S_A(j+1), ...
-            bool ok = wait(B_KV_FULL, 0);
+            // S_B(j), (B has read them) S_A(j+1), ...  Each PV is followed by
+            // the other tile's next S, so a tile's next S waits for the other
+            // tile, not for its own PV; the tiles settle half a step apart.
+            // K buffer p is released once B has read S(j) and its multipliers,
+            // V buffer p after PV_B(j); a release (a commit) is issued only
+            // when a later step reuses the buffer (every commit must be waited
+            // on before the CTA exits).
+            bool ok = wait(B_K_FULL, 0);
             if (ok) {
                 tc::fence_after_sync();
                 issue_s(0, 0);
+                ok = wait(B_D_FREE + 0, 0);
+            }
+            if (ok) {
+                tc::fence_after_sync();
+                issue_s(1, 0);
+                ok = wait(B_D_FREE + 1, 0);
+            }
+            if (ok) {
+                if (2 < nsteps) tc::mma_commit(bars + B_K_EMPTY + 0);
+                if (nsteps > 1 && (ok = wait(B_K_FULL + 1, 0))) {
+                    tc::fence_after_sync();
+                    issue_s(0, 1);
+                }
             }
             for (int j = 0; ok && j < nsteps; j++) {
                 const int p = j & 1;
-                const bool more = j + 1 < nsteps;
-                if (!(ok = wait(B_D_FREE + 0, j & 1))) break;
-                tc::fence_after_sync();
-                issue_s(1, p);
-                if (!(ok = wait(B_W_FULL + 0, j & 1))) break;
+                if (!(ok = wait(B_W_FULL + 0, j & 1) && wait(B_V_FULL + p, (j >> 1) & 1))) break;
                 tc::fence_after_sync();
                 issue_pv(0, p, j > 0);
-                if (more) {
-                    if (!(ok = wait(B_KV_FULL + (p ^ 1), ((j + 1) >> 1) & 1) &&
-                               wait(B_D_FREE + 1, j & 1)))
-                        break;
+                if (j + 1 < nsteps) {
+                    if (!(ok = wait(B_D_FREE + 0, (j + 1) & 1))) break;
                     tc::fence_after_sync();
-                    issue_s(0, p ^ 1);
+                    issue_s(1, p ^ 1);
                 }
                 if (!(ok = wait(B_W_FULL + 1, j & 1))) break;
                 tc::fence_after_sync();
                 issue_pv(1, p, j > 0);
-                // buffer p is free once these MMAs land; signalled only when a
-                // later step reuses it (every commit must be waited on before
-                // the CTA exits)
-                if (j + 2 < nsteps) tc::mma_commit(bars + B_KV_EMPTY + p);
+                if (j + 2 < nsteps) tc::mma_commit(bars + B_V_EMPTY + p);
+                if (j + 1 < nsteps) {
+                    if (!(ok = wait(B_D_FREE + 1, (j + 1) & 1))) break;
+                    if (j + 3 < nsteps) tc::mma_commit(bars + B_K_EMPTY + (p ^ 1));
+                    if (j + 2 < nsteps) {
+                        if (!(ok = wait(B_K_FULL + p, ((j + 2) >> 1) & 1))) break;
+                        tc::fence_after_sync();
+                        issue_s(0, p);
+                    }
+                }
             }
+            // completes once every MMA issued above has (bounded wait)
+            tc::mma_commit(bars + B_FINAL);
+            mbar_wait_bounded(bars + B_FINAL, 0);
         }
     } else if (warp < 8) {
         // ---- softmax of this row over every 64-token step
@@ -444,7 +503,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
             const int p = j & 1;
             ok = __all_sync(0xffffffffu, wait(B_S_FULL + qtile, j & 1));
             // the widening warps' scales and page flags of buffer p (long complete)
-            if (ok) ok = __all_sync(0xffffffffu, wait(B_KV_FULL + p, (j >> 1) & 1));
+            if (ok) ok = __all_sync(0xffffffffu, wait(B_K_FULL + p, (j >> 1) & 1));
             if (!ok) break;
             tc::fence_after_sync();
             // scores against the step's 64 tokens (article 9-2 §2 seg. 2): s =
@@ -465,14 +524,16 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
                     }
                 }
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) pf_arrive(bars + B_D_FREE + qtile);  // the block dots may be overwritten
             const float2* km2 = reinterpret_cast<const float2*>(sm + sm_km(p));
 #pragma unroll
             for (int i = 0; i < PF_STEP / 2; i++) x[i] = __fmul2_rn(x[i], km2[i]);
-            const int t0 = j * PF_STEP;
             const bool ok0 = okv[2 * p] != 0, ok1 = okv[2 * p + 1] != 0;
+            // the block dots may be overwritten, and (once both tiles are here)
+            // K buffer p with its multipliers and page flags
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) pf_arrive(bars + B_D_FREE + qtile);
+            const int t0 = j * PF_STEP;
             // every row of the CTA sees every token of this step: no masking
             const bool full = ok0 && ok1 && t0 + PF_STEP - 1 <= pos_first;
             if (!full) {
@@ -510,6 +571,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
                     tc::tmem_st32(tO + 32 * c, o);
                 }
             }
+            if (!(ok = __all_sync(0xffffffffu, wait(B_V_FULL + p, (j >> 1) & 1)))) break;
             // weights w = p * vscale / 127 = hi + lo: hi is w cut to bf16 (its
             // top 16 bits), lo = w - hi (exact) rounded to bf16
             uint8_t* Wh = sm + sm_whi(qtile);
@@ -566,13 +628,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
             }
         }
     }
-    // ---- teardown: every role has left its loop; an aborted CTA gives the
-    // tensor core one more bounded wait on its last commits before TMEM goes
+    // ---- teardown: every role has left its loop and the MMA thread has seen
+    // its last commit complete (bounded) before TMEM goes
     tc::fence_before_sync();
-    __syncthreads();
-    if (*abort_flag && tid == 0) {
-        for (int t = 0; t < 2; t++) mbar_wait_bounded(bars + B_PV_DONE + t, (nsteps - 1) & 1);
-    }
     __syncthreads();
     if (warp == 0) {
         __syncwarp();
