@@ -378,6 +378,21 @@ int kq8_debug_probe_scores(float* scores, const float* q, const kq8_cache_t* cac
                            int32_t max_seq_len, int32_t B, int32_t nq, float scale, int32_t block,
                            int32_t probe, kq8_stream_t stream);
 
+/* Failure-detection hook: kq8_prefill_attn with the bulk copy of raw
+ * 32-token sub-tile `withhold_sub` (>= 0, counted from position 0 of each
+ * CTA's walk) never issued, so the bounded wait on it runs out (2^28 SM clocks)
+ * in every CTA that reaches it.  Such a CTA sets KQ8_STATUS_TIMEOUT, lets its
+ * other copies and MMAs finish (bounded), frees its tensor memory and leaves
+ * its rows unwritten; the context stays usable.  Returns as kq8_prefill_attn;
+ * KQ8_ERR_INVALID_ARG for withhold_sub < 0. */
+int kq8_debug_prefill_withhold(float* out, const float* q, int32_t total_q,
+                               const kq8_cache_t* cache, const int32_t* page_table,
+                               int32_t max_pages, const int32_t* seq_lens,
+                               const int32_t* q_offsets, int32_t max_seq_len, int32_t max_q_len,
+                               int32_t B, int32_t nq, float scale, void* workspace,
+                               size_t workspace_bytes, int32_t withhold_sub,
+                               kq8_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -153,6 +153,7 @@ struct PrefillParams {
     int32_t nq;
     float scale;
     uint32_t* status;
+    int32_t withhold_sub;  // test hook: this raw sub-tile is never copied (-1: none)
 };
 
 template <int G>
@@ -270,6 +271,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
             return (pg >= 0 && pg < P.cache.num_pages) ? pg : -2;
         };
         int32_t pw_cur = load_window(0), pw_nxt = load_window(1);
+        int armed[PF_RAW] = {-1, -1, -1};  // last sub-tile whose copies went into each stage
         uint64_t pol;
         asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
         for (int t = 0; t < 2 * nsteps; t++) {
@@ -282,7 +284,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
                 pw_nxt = load_window((t >> 5) + 1);
             }
             const int32_t pg = __shfl_sync(0xffffffffu, pw_cur, t & 31);  // -1: none, -2: bad
-            if (lane == 0) {
+            if (lane == 0 && t != P.withhold_sub) {
+                armed[s] = t;
                 uint64_t* bar = bars + B_RAW_FULL + s;
                 uint8_t* st = sm + sm_raw(s);
                 okv[4 + s] = pg >= 0;
@@ -302,6 +305,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
                              SUB_S_BYTES, bar, pol);
                 }
             }
+        }
+        // an aborted CTA lets the copies it started land before shared memory
+        // is given up (each stage's last armed phase, bounded)
+        if (*abort_flag && lane == 0) {
+            for (int s = 0; s < PF_RAW; s++)
+                if (armed[s] >= 0)
+                    mbar_wait_bounded(bars + B_RAW_FULL + s, (armed[s] / PF_RAW) & 1);
         }
     } else if (warp >= PF_CV_WARP && warp < PF_CV_WARP + PF_CV_WARPS) {
         // ---- widening, one step at a time: K of both raw sub-tiles (halves)
@@ -676,11 +686,15 @@ size_t kq8_prefill_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int32_t m
     return PF_STATUS_BYTES;
 }
 
-int kq8_prefill_attn(float* out, const float* q, int32_t total_q, const kq8_cache_t* cache,
-                     const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
-                     const int32_t* q_offsets, int32_t max_seq_len, int32_t max_q_len, int32_t B,
-                     int32_t nq, float scale, void* workspace, size_t workspace_bytes,
-                     kq8_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int prefill_impl(float* out, const float* q, int32_t total_q, const kq8_cache_t* cache,
+                 const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                 const int32_t* q_offsets, int32_t max_seq_len, int32_t max_q_len, int32_t B,
+                 int32_t nq, float scale, void* workspace, size_t workspace_bytes,
+                 kq8_stream_t stream, int32_t withhold_sub) {
     int rc = check_cache_args(cache);
     if (rc) return rc;
     if (B < 0 || nq < 1 || total_q < 0 || max_seq_len < 0 || max_q_len < 0 || max_pages < 0)
@@ -711,7 +725,35 @@ int kq8_prefill_attn(float* out, const float* q, int32_t total_q, const kq8_cach
     p.nq = nq;
     p.scale = scale;
     p.status = static_cast<uint32_t*>(workspace);
+    p.withhold_sub = withhold_sub;
     return launch_prefill(p, nq / nkv, nkv, (cudaStream_t)stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int kq8_prefill_attn(float* out, const float* q, int32_t total_q, const kq8_cache_t* cache,
+                     const int32_t* page_table, int32_t max_pages, const int32_t* seq_lens,
+                     const int32_t* q_offsets, int32_t max_seq_len, int32_t max_q_len, int32_t B,
+                     int32_t nq, float scale, void* workspace, size_t workspace_bytes,
+                     kq8_stream_t stream) {
+    return prefill_impl(out, q, total_q, cache, page_table, max_pages, seq_lens, q_offsets,
+                        max_seq_len, max_q_len, B, nq, scale, workspace, workspace_bytes, stream,
+                        -1);
+}
+
+int kq8_debug_prefill_withhold(float* out, const float* q, int32_t total_q,
+                               const kq8_cache_t* cache, const int32_t* page_table,
+                               int32_t max_pages, const int32_t* seq_lens,
+                               const int32_t* q_offsets, int32_t max_seq_len, int32_t max_q_len,
+                               int32_t B, int32_t nq, float scale, void* workspace,
+                               size_t workspace_bytes, int32_t withhold_sub,
+                               kq8_stream_t stream) {
+    if (withhold_sub < 0) return KQ8_ERR_INVALID_ARG;
+    return prefill_impl(out, q, total_q, cache, page_table, max_pages, seq_lens, q_offsets,
+                        max_seq_len, max_q_len, B, nq, scale, workspace, workspace_bytes, stream,
+                        withhold_sub);
 }
 
 }  // extern "C"

@@ -76,6 +76,8 @@ _lib.kq8_prefill_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32]
 _lib.kq8_prefill_workspace_bytes.restype = _SZ
 _lib.kq8_prefill_attn.argtypes = [_P, _P, _I32, _CP, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
                                   ctypes.c_float, _P, _SZ, _P]
+_lib.kq8_debug_prefill_withhold.argtypes = [_P, _P, _I32, _CP, _P, _I32, _P, _P, _I32, _I32,
+                                            _I32, _I32, ctypes.c_float, _P, _SZ, _I32, _P]
 _lib.kq8_sparse_prefill_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32]
 _lib.kq8_sparse_prefill_workspace_bytes.restype = _SZ
 _lib.kq8_sparse_prefill_attn.argtypes = [_P, _P, _I32, _CP, _P, _I32, _P, _P, _I32, _I32, _I32,
@@ -384,6 +386,26 @@ def kq8_prefill_attn(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
                                  float(scale), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream)),
            "kq8_prefill_attn")
+
+
+def kq8_debug_prefill_withhold(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
+                               page_table: torch.Tensor, seq_lens: torch.Tensor,
+                               q_offsets: torch.Tensor, max_seq_len: int, max_q_len: int,
+                               scale: float, workspace: torch.Tensor, withhold_sub: int,
+                               stream=None) -> None:
+    """Failure-detection hook (include/kq8.h): the prefill with one raw
+    sub-tile's copy never issued, so its bounded wait runs out."""
+    if cache.bits != 8:
+        raise ValueError("prefill reads a q8 cache")
+    B = seq_lens.numel()
+    _check(_lib.kq8_debug_prefill_withhold(_ptr(out), _ptr(q), q.shape[0],
+                                           ctypes.byref(cache.struct), _ptr(page_table),
+                                           page_table.shape[1], _ptr(seq_lens), _ptr(q_offsets),
+                                           int(max_seq_len), int(max_q_len), B, q.shape[1],
+                                           float(scale), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(),
+                                           int(withhold_sub), _stream(stream)),
+           "kq8_debug_prefill_withhold")
 
 
 def kq8_sparse_decode_attn_shared(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
