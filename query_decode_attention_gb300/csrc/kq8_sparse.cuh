@@ -46,28 +46,27 @@ __device__ __forceinline__ int sparse_seq_len(const SparseParams& P, int b) {
 // ---------------------------------------------------------------------------
 // Probe: grid (ceil(max_nblk / probe_bpc), nkv, B), 8 warps.  The CTA's page
 // ids are read once into shared memory (no K load waits on a page-table load).
-// Warp w owns blocks j0 + w + 8i; it walks units = (pass of 8 probe rows,
-// group of PROBE_UNROLL of its blocks) and issues the next unit's loads
-// before computing the current one, so loads stay in flight.  Lane (row
-// pr = lane/4, 32-element block bb = lane%4) loads the 32 bytes of block bb
-// of probe row pr, forms G int32 dots, and the 4 lanes of a row combine them
-// in the method's order (bb = 0, 1, 2, 3) into the exact score; block maxima
-// collect in shared memory across passes.
+// The CTA's blocks form groups of 4; warp w owns groups w, w + 8, ... and walks
+// units = (pass of 8 probe rows, group), loading the next unit before computing
+// the current one so that loads stay in flight.  Lane (block gb = lane / 8 of
+// the group, probe row pr = lane % 8 of the pass) loads its whole K row (the
+// four 32-byte blocks of a row sit 1 KB apart in the sub-tile), forms the
+// exact score in its own registers in the method's order, and the 8 lanes of a
+// block take the maximum with three shuffles; block maxima collect in shared
+// memory across passes.
 // ---------------------------------------------------------------------------
 constexpr int PROBE_WARPS = 8;
 constexpr int PROBE_MAX_BPC = 128;     // blocks per CTA
 constexpr int PROBE_MAX_PAGES = 256;   // page ids a CTA stages
-constexpr int PROBE_UNROLL = 4;
 
-struct ProbeUnit {
-    uint4 ka[PROBE_UNROLL], kb[PROBE_UNROLL];
-    float kst[PROBE_UNROLL];
-    bool valid[PROBE_UNROLL];
+struct ProbeRow {
+    uint4 k[2 * NB];  // the row's 128 int8 codes, block by block
+    float kst;        // its stored K maximum
+    bool valid;
 };
 
 template <int G>
 __global__ void __launch_bounds__(PROBE_WARPS * 32) kq8_probe_kernel(const SparseParams P) {
-    constexpr int U = PROBE_UNROLL;
     __shared__ __align__(16) int8_t qi[G][HD];
     __shared__ float qsc[G][NB];
     __shared__ int32_t pages[PROBE_MAX_PAGES];
@@ -103,83 +102,75 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32) kq8_probe_kernel(const Spars
     }
     __syncthreads();
 
-    const int pr = lane >> 2, bb = lane & 3;
+    const int gb = lane >> 3, pr = lane & 7;
     const int stride = P.block / P.probe;
-    uint4 qa[G], qb[G];
-    float qs[G];
+    float qs[G][NB];
 #pragma unroll
-    for (int g = 0; g < G; g++) {
-        qa[g] = *reinterpret_cast<const uint4*>(qi[g] + bb * 32);
-        qb[g] = *reinterpret_cast<const uint4*>(qi[g] + bb * 32 + 16);
-        qs[g] = qsc[g][bb];
-    }
+    for (int g = 0; g < G; g++)
+#pragma unroll
+        for (int bb = 0; bb < NB; bb++) qs[g][bb] = qsc[g][bb];
     const float scale = P.scale;
 
-    // this warp's units: (pass, group of U of its blocks)
-    const int my_blocks = (j1 - j0 > warp) ? (j1 - j0 - warp + PROBE_WARPS - 1) / PROBE_WARPS : 0;
-    const int ngroups = (my_blocks + U - 1) / U;
+    // this warp's units: (pass, group of 4 blocks)
+    const int ngroups_cta = (j1 - j0 + 3) / 4;
+    const int my_groups =
+        (ngroups_cta > warp) ? (ngroups_cta - warp + PROBE_WARPS - 1) / PROBE_WARPS : 0;
     const int npass = (P.probe + 7) / 8;
-    const int nunits = ngroups * npass;
-    auto block_of = [&](int group, int u) { return j0 + warp + PROBE_WARPS * (group * U + u); };
-    auto load = [&](ProbeUnit& L, int k) {
-        const int group = k % ngroups, p = (k / ngroups) * 8 + pr;
+    const int nunits = my_groups * npass;
+    auto block_of = [&](int k) { return j0 + 4 * (warp + PROBE_WARPS * (k % my_groups)) + gb; };
+    auto load = [&](ProbeRow& R, int k) {
+        const int jj = block_of(k), p = (k / my_groups) * 8 + pr;
+        const int t = jj * P.block + p * stride;
+        R.valid = (jj < j1) && (p < P.probe) && (t < n);
 #pragma unroll
-        for (int u = 0; u < U; u++) {
-            const int jj = block_of(group, u);
-            const int t = jj * P.block + p * stride;
-            L.valid[u] = (jj < j1) && (p < P.probe) && (t < n);
-            L.ka[u] = make_uint4(0, 0, 0, 0);
-            L.kb[u] = L.ka[u];
-            L.kst[u] = 0.0f;
-            if (L.valid[u]) {
-                const int32_t pg = pages[t / kv_bs - pg0];
-                if (pg >= 0) {
-                    const int r = t % kv_bs;
-                    const int8_t* src = P.cache.k + kv_sub_off(pg, h, nkv, kv_bs, r / TILE) +
-                                        bb * 1024 + kpos(r % TILE) * 32;
-                    L.ka[u] = __ldg(reinterpret_cast<const uint4*>(src));
-                    L.kb[u] = __ldg(reinterpret_cast<const uint4*>(src + 16));
-                    L.kst[u] = __ldg(P.cache.kscale + scale_sub_off(pg, h, nkv, kv_bs, r / TILE) +
-                                     r % TILE);
-                } else {
-                    L.valid[u] = false;
+        for (int i = 0; i < 2 * NB; i++) R.k[i] = make_uint4(0, 0, 0, 0);
+        R.kst = 0.0f;
+        if (R.valid) {
+            const int32_t pg = pages[t / kv_bs - pg0];
+            if (pg >= 0) {
+                const int r = t % kv_bs;
+                const int8_t* src =
+                    P.cache.k + kv_sub_off(pg, h, nkv, kv_bs, r / TILE) + kpos(r % TILE) * 32;
+#pragma unroll
+                for (int bb = 0; bb < NB; bb++) {
+                    R.k[2 * bb] = __ldg(reinterpret_cast<const uint4*>(src + bb * 1024));
+                    R.k[2 * bb + 1] = __ldg(reinterpret_cast<const uint4*>(src + bb * 1024 + 16));
                 }
+                R.kst = __ldg(P.cache.kscale + scale_sub_off(pg, h, nkv, kv_bs, r / TILE) +
+                              r % TILE);
+            } else {
+                R.valid = false;
             }
         }
     };
-    auto compute = [&](const ProbeUnit& L, int k) {
-        const int group = k % ngroups;
+    auto compute = [&](const ProbeRow& R, int k) {
+        const int jj = block_of(k);
 #pragma unroll
-        for (int u = 0; u < U; u++) {
+        for (int g = 0; g < G; g++) {
+            int d[NB];
 #pragma unroll
-            for (int g = 0; g < G; g++) {
-                int d = __dp4a((int)L.ka[u].x, (int)qa[g].x, 0);
-                d = __dp4a((int)L.ka[u].y, (int)qa[g].y, d);
-                d = __dp4a((int)L.ka[u].z, (int)qa[g].z, d);
-                d = __dp4a((int)L.ka[u].w, (int)qa[g].w, d);
-                d = __dp4a((int)L.kb[u].x, (int)qb[g].x, d);
-                d = __dp4a((int)L.kb[u].y, (int)qb[g].y, d);
-                d = __dp4a((int)L.kb[u].z, (int)qb[g].z, d);
-                d = __dp4a((int)L.kb[u].w, (int)qb[g].w, d);
-                const float x = __fmul_rn(i2f_exact(d), qs[g]);
-                // lanes 4pr+1..3 hand their block terms to lane 4pr, summed in order
-                const float x1 = __shfl_down_sync(0xffffffffu, x, 1);
-                const float x2 = __shfl_down_sync(0xffffffffu, x, 2);
-                const float x3 = __shfl_down_sync(0xffffffffu, x, 3);
-                float s = __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(0.0f, x), x1), x2), x3);
-                s = __fmul_rn(__fmul_rn(s, __fmul_rn(L.kst[u], inv127())), scale);
-                if (!L.valid[u]) s = -INFINITY;
-                // max over the 8 rows held by lanes 0, 4, ..., 28
-                s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 4));
-                s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 8));
-                s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 16));
-                const int jj = block_of(group, u);
-                // lanes with bb != 0 carried partial terms; lane 0 holds the rows' max
-                if (lane == 0 && jj < j1) best[jj - j0][g] = fmaxf(best[jj - j0][g], s);
+            for (int bb = 0; bb < NB; bb++) {
+                const uint4 qa = *reinterpret_cast<const uint4*>(qi[g] + bb * 32);
+                const uint4 qb = *reinterpret_cast<const uint4*>(qi[g] + bb * 32 + 16);
+                const uint4 ka = R.k[2 * bb], kb = R.k[2 * bb + 1];
+                int x = __dp4a((int)ka.x, (int)qa.x, 0);
+                x = __dp4a((int)ka.y, (int)qa.y, x);
+                x = __dp4a((int)ka.z, (int)qa.z, x);
+                x = __dp4a((int)ka.w, (int)qa.w, x);
+                x = __dp4a((int)kb.x, (int)qb.x, x);
+                x = __dp4a((int)kb.y, (int)qb.y, x);
+                x = __dp4a((int)kb.z, (int)qb.z, x);
+                d[bb] = __dp4a((int)kb.w, (int)qb.w, x);
             }
+            float s = R.valid ? score_exact(d, qs[g], R.kst, scale) : -INFINITY;
+            // max over the 8 probe rows of the block (lanes 8gb .. 8gb+7)
+            s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 1));
+            s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 2));
+            s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 4));
+            if (pr == 0 && jj < j1) best[jj - j0][g] = fmaxf(best[jj - j0][g], s);
         }
     };
-    ProbeUnit A, Bu;
+    ProbeRow A, Bu;
     if (nunits > 0) load(A, 0);
     for (int k = 0; k < nunits; k += 2) {
         if (k + 1 < nunits) load(Bu, k + 1);
