@@ -107,7 +107,7 @@ Plan plan_sparse(int B, int nq, int nkv, int max_seq_len, int block, int topk) {
     p.off_scores = o;
     o = align_up(o + (size_t)B * nq * p.max_nblk * sizeof(float), WS_ALIGN);
     p.off_masks = o;
-    o = align_up(o + (size_t)B * nkv * p.max_nblk, WS_ALIGN);
+    o = align_up(o + (size_t)B * nkv * p.max_nblk * sizeof(uint32_t), WS_ALIGN);
     p.off_list = o;
     o = align_up(o + (size_t)B * nkv * p.list_cap * sizeof(int32_t), WS_ALIGN);
     p.off_len = o;
@@ -198,7 +198,7 @@ int run_sparse(float* out, const float* q, const kq8_cache_t* cache, const int32
     sp.max_nblk = plan.max_nblk;
     sp.probe_bpc = probe_blocks_per_cta(block, cache->kv_bs);
     sp.scores = reinterpret_cast<float*>(ws + plan.off_scores);
-    sp.masks = reinterpret_cast<uint8_t*>(ws + plan.off_masks);
+    sp.masks = reinterpret_cast<uint32_t*>(ws + plan.off_masks);
     sp.tile_list = reinterpret_cast<int32_t*>(ws + plan.off_list);
     sp.list_len = reinterpret_cast<int32_t*>(ws + plan.off_len);
     sp.list_cap = plan.list_cap;
@@ -206,6 +206,11 @@ int run_sparse(float* out, const float* q, const kq8_cache_t* cache, const int32
     sp.status = reinterpret_cast<uint32_t*>(ws);
     sp.row_seq = row_seq;
     sp.shared_sel = shared_sel ? 1 : 0;
+    // the top-k tickets share the header's per-(sequence, KV head) counters
+    // with the attention kernel's chunk merge: both leave them at zero
+    sp.tickets = ((size_t)rows * (size_t)nkv <= MAX_COUNTERS)
+                     ? reinterpret_cast<uint32_t*>(ws + STATUS_BYTES)
+                     : nullptr;
     int rc = launch_probe(sp, G, rows, nkv, s);
     if (rc) return rc;
     rc = launch_topk(sp, G, rows, nkv, s);

@@ -13,7 +13,9 @@ static int launch_probe_g(const SparseParams& p, int B, int nkv, cudaStream_t s)
 
 template <int G>
 static int launch_topk_g(const SparseParams& p, int B, int nkv, cudaStream_t s) {
-    dim3 grid(nkv, B);
+    // one CTA per query head when the union can be left to the last of them
+    const bool per_head = p.tickets && !p.shared_sel && G > 1;
+    dim3 grid(nkv, B, per_head ? G : 1);
     kq8_topk_kernel<G><<<grid, TOPK_THREADS, 0, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
 }

@@ -27,7 +27,7 @@ struct SparseParams {
     int32_t max_nblk;        // ceil(max_seq_len / block)
     int32_t probe_bpc;       // probe blocks per CTA (its pages fit PROBE_MAX_PAGES)
     float* scores;           // [B][nq][max_nblk]
-    uint8_t* masks;          // [B][nkv][max_nblk]
+    uint32_t* masks;         // [B][nkv][max_nblk]: bit g = head g kept the block
     int32_t* tile_list;      // [B][nkv][list_cap]
     int32_t* list_len;       // [B][nkv]
     int32_t list_cap;
@@ -35,6 +35,7 @@ struct SparseParams {
     uint32_t* status;
     const int32_t* row_seq;  // optional [B]: page-table row of row b (null = b)
     int32_t shared_sel;      // 1: one selection per KV head (max of its heads' block scores)
+    uint32_t* tickets;       // [B][nkv], zero between calls; null: one top-k CTA per KV head
 };
 
 __device__ __forceinline__ int sparse_seq_len(const SparseParams& P, int b) {
@@ -92,6 +93,11 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32) kq8_probe_kernel(const Spars
     }
     for (int i = threadIdx.x; i < (j1 - j0) * G; i += PROBE_WARPS * 32)
         best[i / G][i % G] = -INFINITY;
+    // the top-k kernel ORs its heads' choices into these blocks' masks (a
+    // probe-only call passes none)
+    if (P.masks)
+        for (int i = threadIdx.x; i < j1 - j0; i += PROBE_WARPS * 32)
+            P.masks[(size_t)(b * nkv + h) * P.max_nblk + j0 + i] = 0u;
     for (int g = warp; g < G; g += PROBE_WARPS) {
         const float4 x =
             reinterpret_cast<const float4*>(P.q + ((size_t)b * P.nq + (size_t)h * G + g) * HD)[lane];
@@ -187,7 +193,11 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32) kq8_probe_kernel(const Spars
 }
 
 // ---------------------------------------------------------------------------
-// Top-k + union: one CTA of 256 threads per (KV head, sequence).
+// Top-k + union: grid (KV head, sequence, head g) with one CTA of 256
+// threads per query head when tickets are available (a CTA selects head g's
+// blocks and ORs bit g into the block masks, which the probe kernel cleared;
+// the last of the G CTAs to finish builds the union), else one CTA per KV
+// head that selects its G heads in turn.
 // ---------------------------------------------------------------------------
 constexpr int TOPK_THREADS = 256;
 
@@ -228,6 +238,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) kq8_topk_kernel(const SparsePara
     __shared__ int scan_tmp[TOPK_THREADS / 32];
     __shared__ uint32_t s_prefix;
     __shared__ int s_kk;
+    __shared__ int s_last;
     const int h = blockIdx.x, b = blockIdx.y;
     const int nkv = P.cache.num_kv_heads;
     const int tid = threadIdx.x;
@@ -241,21 +252,24 @@ __global__ void __launch_bounds__(TOPK_THREADS) kq8_topk_kernel(const SparsePara
     int32_t* list = P.tile_list + (size_t)(b * nkv + h) * P.list_cap;
     const bool gated = n <= 2 * P.block;
 
+    const bool per_head = gridDim.z > 1;
+    const int g_first = per_head ? (int)blockIdx.z : 0;
+    const int g_end = per_head ? g_first + 1 : G;
     if (P.sel_blocks) {
-        for (int g = 0; g < G; g++) {
+        for (int g = g_first; g < g_end; g++) {
             int32_t* sel = P.sel_blocks + ((size_t)b * P.nq + (size_t)h * G + g) * P.topk;
             for (int i = tid; i < P.topk; i += TOPK_THREADS) sel[i] = -1;
         }
     }
     if (gated) {  // exact path: every tile, every head
+        if (g_first != 0) return;
         const int32_t all = (int32_t)(((1u << G) - 1u) << 24);
         for (int i = tid; i < ntiles; i += TOPK_THREADS) list[i] = i | all;
         if (tid == 0) P.list_len[b * nkv + h] = ntiles;
         return;
     }
     const int nblk = (n + P.block - 1) / P.block;
-    uint8_t* masks = P.masks + (size_t)(b * nkv + h) * P.max_nblk;
-    for (int j = tid; j < nblk; j += TOPK_THREADS) masks[j] = 0;
+    uint32_t* masks = P.masks + (size_t)(b * nkv + h) * P.max_nblk;
     if (P.shared_sel) {
         // one selection for the group: head 0's row becomes the max over the G
         // heads of their block scores (in place; the scores are this call's)
@@ -272,9 +286,9 @@ __global__ void __launch_bounds__(TOPK_THREADS) kq8_topk_kernel(const SparsePara
     }
     __syncthreads();
 
-    const int nsel = P.shared_sel ? 1 : G;
-    const uint8_t group_mask = (uint8_t)((1u << G) - 1u);
-    for (int g = 0; g < nsel; g++) {
+    const int nsel = P.shared_sel ? 1 : g_end;
+    const uint32_t group_mask = (1u << G) - 1u;
+    for (int g = g_first; g < nsel; g++) {
         const float* sc = P.scores + ((size_t)b * P.nq + (size_t)h * G + g) * P.max_nblk;
         int32_t* sel = P.sel_blocks ? P.sel_blocks + ((size_t)b * P.nq + (size_t)h * G + g) * P.topk
                                     : nullptr;
@@ -328,7 +342,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) kq8_topk_kernel(const SparsePara
             int keep_tot;
             const int pos = block_excl_scan(keep ? 1 : 0, scan_tmp, keep_tot) + kept_before;
             if (keep) {
-                masks[j] |= P.shared_sel ? group_mask : (uint8_t)(1u << g);
+                atomicOr(masks + j, P.shared_sel ? group_mask : (1u << g));
                 if (sel) {
                     if (P.shared_sel) {
                         for (int gg = 0; gg < G; gg++) sel[(size_t)gg * P.topk + pos] = j;
@@ -343,18 +357,30 @@ __global__ void __launch_bounds__(TOPK_THREADS) kq8_topk_kernel(const SparsePara
         __syncthreads();
     }
 
+    if (per_head) {
+        // the last of the G CTAs of this (sequence, KV head) builds the union
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_last = atomicAdd(P.tickets + b * nkv + h, 1u) == (uint32_t)(G - 1);
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+    }
     // union over the G heads -> ascending tile list with per-entry head masks
     int written = 0;
     for (int base = 0; base < nblk; base += TOPK_THREADS) {
         const int j = base + tid;
-        const uint32_t mk = (j < nblk) ? masks[j] : 0u;
+        const uint32_t mk = (j < nblk) ? __ldcg(masks + j) : 0u;
         const int cnt = mk ? min(m, ntiles - j * m) : 0;
         int tot;
         const int pos = block_excl_scan(cnt, scan_tmp, tot) + written;
         for (int s = 0; s < cnt; s++) list[pos + s] = (j * m + s) | (int32_t)(mk << 24);
         written += tot;
     }
-    if (tid == 0) P.list_len[b * nkv + h] = written;
+    if (tid == 0) {
+        P.list_len[b * nkv + h] = written;
+        if (per_head) P.tickets[b * nkv + h] = 0u;  // ready for the next call
+    }
 }
 
 }  // namespace kq8
