@@ -232,6 +232,20 @@ def test_sparse_matches_oracle(n):
     assert_out_close(got, ref, f"sparse n={n}")
 
 
+def test_sparse_many_sequences_one_topk_cta_per_kv_head():
+    # more (sequence, KV head) pairs than the workspace header has counters
+    # (16384): the top-k runs one CTA per KV head selecting its G heads in
+    # turn instead of one CTA per query head; selections and outputs as before
+    B = 2050
+    lens = np.random.default_rng(77).integers(65, 200, B)
+    wl = W.custom(B, 16, 8, [int(x) for x in lens], seed=78, block=32, topk=3, probe=4)
+    case, q, Ks, Vs = _host_case(wl)
+    got, sel = _decode(case, sparse=True, sel=True)
+    ref, rsel = oracle_decode(wl, q, Ks, Vs, sparse=True)
+    assert np.array_equal(sel, rsel)
+    assert_out_close(got, ref, "sparse, 2050 sequences")
+
+
 @pytest.mark.parametrize("block,topk,probe", [(32, 4, 8), (64, 3, 5), (32, 7, 32), (96, 2, 1)])
 def test_sparse_knobs(block, topk, probe):
     wl = W.custom(3, 16, 4, [2000, 700, 3001], seed=block + topk + probe, block=block, topk=topk,
