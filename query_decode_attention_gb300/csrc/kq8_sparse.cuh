@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) kq8_topk_kernel(const SparsePara
     __shared__ int hist[256];
     __shared__ int scan_tmp[TOPK_THREADS / 32];
     __shared__ uint32_t s_prefix;
-    __shared__ int s_kk;
+    __shared__ int s_kk, s_cnt;
     __shared__ int s_last;
     const int h = blockIdx.x, b = blockIdx.y;
     const int nkv = P.cache.num_kv_heads;
@@ -293,13 +293,17 @@ __global__ void __launch_bounds__(TOPK_THREADS) kq8_topk_kernel(const SparsePara
         int32_t* sel = P.sel_blocks ? P.sel_blocks + ((size_t)b * P.nq + (size_t)h * G + g) * P.topk
                                     : nullptr;
         const int k = min(P.topk, nblk);
-        uint32_t thr = 0;  // keys > thr are kept, plus the first kk keys == thr
+        // keys whose top bits (tmask) exceed thr are kept, plus the first kk
+        // whose top bits equal thr
+        uint32_t thr = 0, tmask = 0xFFFFFFFFu;
         int kk = 0;
         if (k == nblk) {
             thr = 0;
             kk = nblk;  // every key >= 0: take all ties at key 0 too
         } else {
-            // radix select of the k-th largest key, 8 bits at a time from the top
+            // radix select of the k-th largest key, 8 bits at a time from the top;
+            // it stops early once every key of the chosen bucket is kept (the
+            // lower bits can then change nothing)
             uint32_t prefix = 0, pmask = 0;
             int rem = k;
             for (int pass = 0; pass < 4; pass++) {
@@ -318,21 +322,25 @@ __global__ void __launch_bounds__(TOPK_THREADS) kq8_topk_kernel(const SparsePara
                 if (excl < rem && excl + cnt >= rem) {
                     s_prefix = prefix | ((uint32_t)(255 - tid) << shift);
                     s_kk = rem - excl;
+                    s_cnt = cnt;
                 }
                 __syncthreads();
                 prefix = s_prefix;
                 rem = s_kk;
                 pmask |= 0xFFu << shift;
+                const bool all_kept = s_cnt == rem;
                 __syncthreads();
+                if (all_kept) break;
             }
             thr = prefix;
+            tmask = pmask;
             kk = rem;
         }
-        // mark: key > thr, or key == thr among the first kk such keys by index
+        // mark: top bits > thr, or == thr among the first kk such keys by index
         int ties_before = 0, kept_before = 0;
         for (int base = 0; base < nblk; base += TOPK_THREADS) {
             const int j = base + tid;
-            const uint32_t u = (j < nblk) ? order_key(sc[j]) : 0u;
+            const uint32_t u = (j < nblk) ? (order_key(sc[j]) & tmask) : 0u;
             const bool in = j < nblk;
             const bool gt = in && (k == nblk || u > thr);
             const bool eq = in && !gt && u == thr;
