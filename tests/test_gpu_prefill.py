@@ -147,6 +147,32 @@ def test_prefill_qwen2b_prompt_sampled_rows():
         assert_out_close(got[i:i + 1], ref, f"token {i}")
 
 
+def test_prefill_qwen8b_prompt_sampled_rows():
+    # a whole 8192-token Qwen3-VL-8B prompt (32 query heads on 8 KV heads, G = 4)
+    # in one call, the other prefill bench line; 40 sampled tokens, every head
+    n = 8192
+    wl = W.Workload("qwen3vl8b_prompt_n8192", 1, 32, 8, np.array([n], np.int32), kind="sigma",
+                    seed=2100 + n)
+    _, Ks, Vs = host_inputs(wl)
+    qp = np.random.default_rng(21).standard_normal((n, wl.nq, wl.hd)).astype(np.float32)
+    case = paged.fill_from_host(wl, Ks, Vs, DEV)
+    out = torch.empty((n, wl.nq, wl.hd), device=DEV)
+    ws = kq8.new_workspace(4096, DEV)
+    kq8.kq8_prefill_attn(out, torch.tensor(qp, device=DEV), case.cache, case.page_table,
+                         case.seq_lens, torch.tensor([0, n], dtype=torch.int32, device=DEV), n, n,
+                         wl.scale, ws)
+    assert kq8.kq8_read_status(ws) == 0
+    got = out.cpu().numpy()
+    rows = np.unique(np.concatenate([[0, 31, 32, 63, 64, 4095, n - 1],
+                                     np.random.default_rng(22).integers(0, n, 33)]))
+    k8s, kss, v8s, vss = oracle_quantized(Ks, Vs)
+    for i in rows:
+        p = int(i) + 1
+        ref = oracle.prefill_batch(qp[i:i + 1], [1], [k8s[0][:p]], [kss[0][:p]], [v8s[0][:p]],
+                                   [vss[0][:p]], wl.scale)
+        assert_out_close(got[i:i + 1], ref, f"token {i}")
+
+
 # ---------------------------------------------------------------------------
 # Block-sparse prefill (article 10-1 §1-§2): per token, the block-sparse decode
 # query over its own prefix; selections bit-exact, outputs within tolerance.
