@@ -102,3 +102,28 @@ def test_q4_bad_page_sets_status_and_caches_are_not_mixed():
     with pytest.raises(ValueError):
         kq8.kq8_decode_attn(out, case.q, case.cache, pt, case.seq_lens, wl.max_seq_len, wl.scale,
                             ws)
+
+
+def test_q4_serving_full_size_sampled():
+    # the bench's q4 line: the whole batch-64 serving layer in a q4 cache, in
+    # its launch configuration; sampled (sequence, head) pairs against the
+    # oracle's q4 write path and decode
+    wl = W.serving_8b(layers=1)
+    case = paged.fill_cache(wl, 0, DEV, bits=4)
+    out = torch.empty((wl.B, wl.nq, wl.hd), device=DEV)
+    ws = kq8.new_workspace(kq8.kq8_decode_workspace_bytes(wl.B, wl.nq, wl.nkv, wl.max_seq_len), DEV)
+    kq8.kq8_decode_attn_q4(out, case.q, case.cache, case.page_table, case.seq_lens, wl.max_seq_len,
+                           wl.scale, ws)
+    assert kq8.kq8_read_status(ws) == 0
+    got = out.cpu().numpy()
+    qh = case.q.cpu().numpy()
+    hi, lo = int(np.argmax(wl.seq_lens)), int(np.argmin(wl.seq_lens))
+    for b, h in [(hi, 0), (hi, 30), (lo, 6), (21, 13), (63, 27)]:
+        n = int(wl.seq_lens[b])
+        K, V = case.device_kv(b, 0, n)
+        kh = h // wl.G
+        k4, ks = oracle.kv_quantize_rows_q4(K[:, kh:kh + 1].cpu().numpy())
+        v4, vs = oracle.kv_quantize_rows_q4(V[:, kh:kh + 1].cpu().numpy())
+        c = oracle.SeqCache(k4, ks, v4, vs, kv_bs=wl.kv_bs)
+        ref = oracle.attn_single_q_q4(qh[b, h], c, 0, np.float32(wl.scale))
+        assert_out_close(got[b, h], ref, f"q4 full size b={b} h={h}")

@@ -128,3 +128,40 @@ def test_range_longer_than_the_hint_is_reported_and_skipped():
     got = _finalize(state, wl)
     ref = oracle_decode(wl, q, Ks, Vs)
     assert_out_close(got[1], ref[1], "the in-bound sequence")
+
+
+def test_long_context_full_size_eight_pieces_sampled():
+    # the bench's streaming line: 8 sequences of 131072 tokens (Student-t keys
+    # with outlier channels) folded in 8 equal pieces, in its launch
+    # configuration; sampled (sequence, head) pairs against the oracle's one
+    # pass, every output against the one-call decode
+    wl = W.long_context()
+    case = paged.fill_cache(wl, 0, DEV)
+    ws = _ws(wl)
+    pieces = 8
+    state = kq8.AttnState(wl.B, wl.nq, DEV)
+    kq8.kq8_state_reset(state)
+    for k in range(pieces):
+        b0 = torch.full((wl.B,), (wl.max_seq_len * k) // pieces, dtype=torch.int32, device=DEV)
+        b1 = torch.full((wl.B,), (wl.max_seq_len * (k + 1)) // pieces, dtype=torch.int32,
+                        device=DEV)
+        kq8.kq8_decode_attn_update(state, case.q, case.cache, case.page_table, b0, b1,
+                                   wl.max_seq_len, wl.scale, ws,
+                                   max_range_len=-(-wl.max_seq_len // pieces))
+    assert kq8.kq8_read_status(ws) == 0
+    got = _finalize(state, wl)
+    one = torch.empty((wl.B, wl.nq, wl.hd), device=DEV)
+    kq8.kq8_decode_attn(one, case.q, case.cache, case.page_table, case.seq_lens,
+                        wl.max_seq_len, wl.scale, ws)
+    assert kq8.kq8_read_status(ws) == 0
+    assert_out_close(got, one.cpu().numpy(), "8 pieces vs one call")
+    qh = case.q.cpu().numpy()
+    for b, h in [(0, 0), (2, 9), (7, 15)]:
+        n = int(wl.seq_lens[b])
+        K, V = case.device_kv(b, 0, n)
+        kh = h // wl.G
+        k8, ks = oracle.kv_quantize_rows(K[:, kh:kh + 1].cpu().numpy())
+        v8, vs = oracle.kv_quantize_rows(V[:, kh:kh + 1].cpu().numpy())
+        c = oracle.SeqCache(k8, ks, v8, vs, kv_bs=wl.kv_bs)
+        ref = oracle.attn_single_q(qh[b, h], c, 0, np.float32(wl.scale))
+        assert_out_close(got[b, h], ref, f"streamed b={b} h={h}")
