@@ -221,3 +221,35 @@ def test_sparse_prefill_full_cover_equals_exact_prefill():
     assert status == 0 and status2 == 0
     assert_out_close(got, exact, "sparse (all blocks kept) vs exact prefill")
     assert_out_close(got, ref, "sparse vs oracle")
+
+
+@pytest.mark.parametrize("nq,nkv,n", [(16, 8, 4059), (32, 8, 8192)])
+def test_sparse_prefill_bench_prompts_sampled_rows(nq, nkv, n):
+    # the bench's block-sparse prefill lines (block 32, k 32, probe 8) on the
+    # whole prompt in its launch configuration; the 8192-token prompt has more
+    # (row, KV head) pairs than ticket counters, so its top-k runs one CTA per
+    # KV head.  Sampled tokens: selections bit-exact, outputs within tolerance
+    wl = W.Workload(f"prompt_n{n}", 1, nq, nkv, np.array([n], np.int32), kind="sigma",
+                    seed=2100 + n)
+    case = paged.fill_cache(wl, 0, DEV)
+    g = W.device_generator(DEV, 7 + n)
+    q = torch.randn((n, nq, wl.hd), generator=g, device=DEV)
+    out = torch.empty_like(q)
+    sel = torch.full((n, nq, 32), -7, dtype=torch.int32, device=DEV)
+    q_off = torch.tensor([0, n], dtype=torch.int32, device=DEV)
+    ws = kq8.new_workspace(kq8.kq8_sparse_prefill_workspace_bytes(n, nq, nkv, n, 32, 32), DEV)
+    kq8.kq8_sparse_prefill_attn(out, q, case.cache, case.page_table, case.seq_lens, q_off, n, n,
+                                wl.scale, 32, 32, 8, ws, sel_blocks=sel)
+    assert kq8.kq8_read_status(ws) == 0
+    got, gsel, qh = out.cpu().numpy(), sel.cpu().numpy(), q.cpu().numpy()
+    K, V = case.device_kv(0, 0, n)
+    k8, ks = oracle.kv_quantize_rows(K.cpu().numpy())
+    v8, vs = oracle.kv_quantize_rows(V.cpu().numpy())
+    rows = np.unique(np.concatenate([[0, 63, 64, 65, 1024, n - 1],
+                                     np.random.default_rng(n).integers(0, n, 18)]))
+    for i in rows:
+        p = int(i) + 1
+        ref, rsel = oracle.prefill_batch(qh[i:i + 1], [1], [k8[:p]], [ks[:p]], [v8[:p]], [vs[:p]],
+                                         wl.scale, sparse=True, block=32, topk=32, probe=8)
+        assert np.array_equal(gsel[i:i + 1], rsel), f"selection of token {i}"
+        assert_out_close(got[i:i + 1], ref, f"sparse token {i}")
