@@ -71,6 +71,30 @@ def test_append_bit_exact(kind, kv_bs):
         assert np.array_equal(vs.view(np.uint32), ovs.view(np.uint32))
 
 
+def test_append_8x4096_full_size_sampled():
+    # the bench's write-path line: 8 x 4096 new tokens x 8 KV heads in one call
+    # (its launch configuration); sampled token rows bit-exact against the oracle
+    T, nkv = 8 * 4096, 8
+    wl = W.custom(8, 16, nkv, [4096] * 8, seed=99)
+    cache, pt = paged.new_cache(wl, device=DEV)
+    case = paged.DeviceCase(wl, cache, pt, DEV, 0)
+    g = W.device_generator(DEV, 99)
+    kn = torch.randn((T, nkv, 128), generator=g, device=DEV)
+    vn = torch.randn((T, nkv, 128), generator=g, device=DEV)
+    sl = np.concatenate([case.slots(b, 0, 4096) for b in range(8)]).astype(np.int32)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kq8.kq8_append_kv(cache, kn, vn, torch.tensor(sl, device=DEV), status=st)
+    assert kq8.kq8_read_status(st) == 0
+    rows = np.unique(np.concatenate([[0, 31, 32, 4095, 4096, T - 1],
+                                     np.random.default_rng(99).integers(0, T, 250)]))
+    k8, ks, v8, vs = paged.unpack(cache, sl[rows])
+    ok8, oks = oracle.kv_quantize_rows(kn[rows].cpu().numpy())
+    ov8, ovs = oracle.kv_quantize_rows(vn[rows].cpu().numpy())
+    assert np.array_equal(k8, ok8) and np.array_equal(v8, ov8)
+    assert np.array_equal(ks.view(np.uint32), oks.view(np.uint32))
+    assert np.array_equal(vs.view(np.uint32), ovs.view(np.uint32))
+
+
 def test_append_edge_rows_and_skipped_slots():
     nkv, T = 2, 6
     K = np.random.default_rng(1).standard_normal((T, nkv, 128)).astype(np.float32)
