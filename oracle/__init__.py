@@ -79,6 +79,7 @@ def lib():
             L.kq8o_attn_two_pass_f64.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                                  _F, _P, _I]
             L.kq8o_attn_ref_f64.argtypes = [_P, _P, _P, _P, _I, _I, _D]
+            L.kq8o_attn_exact_sum.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F]
             L.kq8o_probe_block_scores.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _I,
                                                   _I]
             L.kq8o_topk_blocks.argtypes = [_P, _P, _I, _I]
@@ -303,6 +304,21 @@ def attn_two_pass_f64(q, cache: SeqCache, kh, scale, tokens=None):
     lib().kq8o_attn_two_pass_f64(out.ctypes.data_as(_P), pq, cache.k_ptrs, cache.v_ptrs, kp, vp,
                                  cache.n, cache.kv_dim, cache.kv_bs, cache.nkv, kh * cache.hd,
                                  cache.hd, float(np.float32(scale)), pt, nt)
+    return out
+
+
+def attn_exact_sum(q, cache: SeqCache, kh, scale):
+    """The method's result with exact sums (article 9-2 §3: one pass and two
+    passes are the same computation): the method's fp32 scores and V steps,
+    then the softmax and the weighted V sum in fp64, two passes.  The value the
+    fp32 one-pass loop (attn_single_q) approximates; over very long sequences
+    that loop's own rounding can exceed the output tolerance."""
+    q, pq = _c(q, np.float32)
+    out = np.empty(cache.hd, np.float64)
+    kp, vp = cache.scale_ptrs(kh)
+    lib().kq8o_attn_exact_sum(out.ctypes.data_as(_P), pq, cache.k_ptrs, cache.v_ptrs, kp, vp,
+                              cache.n, cache.kv_dim, cache.kv_bs, cache.nkv, kh * cache.hd,
+                              cache.hd, float(np.float32(scale)))
     return out
 
 

@@ -361,6 +361,50 @@ void kq8o_attn_two_pass_f64(double* out, const float* q,
 }
 
 /* ------------------------------------------------------------------------ */
+/* The method's result with exact sums ([9-2] §3: the one pass and the two    */
+/* passes are the same computation, so they differ only by rounding).  The    */
+/* scores are the method's fp32 scores, formed exactly as segment 2 writes    */
+/* them (kq8o_score), and the V steps are its fp32 vscale * KVQ_INV; the      */
+/* softmax and the weighted sum of the dequantised V rows then run in fp64, in */
+/* two passes.  This is the value the fp32 one-pass loop approximates: its    */
+/* own rounding grows with the sequence (many small weights added to a large  */
+/* running sum lose their low bits), and over ~10^5 tokens it can exceed      */
+/* 1e-4 on an output.                                                          */
+/* ------------------------------------------------------------------------ */
+void kq8o_attn_exact_sum(double* out, const float* q, int8_t* const* k_blocks,
+                         int8_t* const* v_blocks, const float* kscale, const float* vscale,
+                         int seq_len, int kv_dim, int kv_bs, int nkv, int kh_off, int hd,
+                         float scale) {
+    int nblk = hd / 32;
+    int8_t qi[KQ8O_MAX_HD];
+    float qsc[KQ8O_MAX_HD / 32];
+    int32_t dots[KQ8O_MAX_HD / 32];
+    kq8o_quantize_q(q, hd, qi, qsc);
+    for (int i = 0; i < hd; i++) out[i] = 0.0;
+    if (seq_len <= 0) return;
+    double* w = (double*)malloc(sizeof(double) * (size_t)seq_len);
+    double mx = -INFINITY;
+    for (int t = 0; t < seq_len; t++) {
+        const int8_t* kt = row_ptr(k_blocks, t, kv_bs, kv_dim, kh_off);
+        kq8o_block_dots(qi, kt, hd, dots);
+        w[t] = (double)kq8o_score(dots, qsc, nblk, kscale[(size_t)t * nkv], scale);
+        if (w[t] > mx) mx = w[t];
+    }
+    double den = 0.0;
+    for (int t = 0; t < seq_len; t++) {
+        w[t] = exp(w[t] - mx);
+        den += w[t];
+    }
+    for (int t = 0; t < seq_len; t++) {
+        const int8_t* vt = row_ptr(v_blocks, t, kv_bs, kv_dim, kh_off);
+        const double step = (double)(vscale[(size_t)t * nkv] * KVQ_INV);
+        const double p = w[t] / den;
+        for (int i = 0; i < hd; i++) out[i] += p * ((double)vt[i] * step);
+    }
+    free(w);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Standard attention on float K/V, fp64 inside ([9-3] §1 baseline arm:      */
 /* score = Q.K^T * scale, max-subtracted softmax, weighted V).  K and V are   */
 /* dense [n][hd].  Used for both arms of the [9-3] experiment (raw fp32 K/V   */

@@ -36,6 +36,10 @@ void kq8o_attn_two_pass_f64(double* out, const float* q, int8_t* const* k_blocks
                             float scale, const int32_t* tokens, int n_tokens);
 void kq8o_attn_ref_f64(double* out, const float* q, const float* K, const float* V, int n, int hd,
                        double scale);
+void kq8o_attn_exact_sum(double* out, const float* q, int8_t* const* k_blocks,
+                         int8_t* const* v_blocks, const float* kscale, const float* vscale,
+                         int seq_len, int kv_dim, int kv_bs, int nkv, int kh_off, int hd,
+                         float scale);
 
 void kq8o_probe_block_scores(float* block_scores, const float* q, int8_t* const* k_blocks,
                              const float* kscale, int seq_len, int kv_dim, int kv_bs, int nkv,

@@ -156,7 +156,7 @@ def host_kv(wl: Workload, b: int, layer: int = 0, q: Optional[np.ndarray] = None
     n = int(wl.seq_lens[b])
     r = _rng(_layer_seed(wl, layer, 1, b))
     shape = (n, wl.nkv, wl.hd)
-    if wl.kind in ("normal", "planted"):
+    if wl.kind in ("normal", "planted", "ties"):
         K = r.standard_normal(shape, dtype=np.float32)
         V = r.standard_normal(shape, dtype=np.float32)
     elif wl.kind == "sigma":
@@ -178,7 +178,63 @@ def host_kv(wl: Workload, b: int, layer: int = 0, q: Optional[np.ndarray] = None
         if q is None:
             q = host_q(wl, layer)
         _plant(wl, b, K, q[b], n)
+    if wl.kind == "ties":
+        if q is None:
+            q = host_q(wl, layer)
+        _plant_ties(wl, b, K, q[b], n)
     return K.astype(np.float32), V.astype(np.float32)
+
+
+def _aligned_rows(rr, u: np.ndarray, rows: int, hd: int, cos: float) -> np.ndarray:
+    """`rows` vectors sqrt(hd) * (cos u + sin x_perp), x_perp random unit
+    vectors orthogonal to the unit vector u."""
+    x = rr.standard_normal((rows, hd))
+    x -= (x @ u)[:, None] * u[None, :]
+    x /= np.linalg.norm(x, axis=1, keepdims=True)
+    return math.sqrt(hd) * (cos * u[None, :] + math.sqrt(1.0 - cos * cos) * x)
+
+
+def tie_mode(b: int) -> int:
+    """How sequence b of a "ties" workload is built: 0 all-zero K, 1 every
+    block a copy of block 0, 2 a few strong blocks plus more copies of one
+    block than the top-k has places left."""
+    return b % 3
+
+
+def tie_counts(wl: Workload, n: int):
+    """(strong blocks, copied blocks) of a mode-2 sequence of length n: only
+    whole blocks are used, and the copies outnumber the places the strong
+    blocks leave in the top-k, so equal block scores straddle the k-th place."""
+    full = n // wl.block
+    strong = min(10, full // 4, wl.topk // 2)
+    copies = min(full - strong, wl.topk - strong + 8)
+    return strong, copies
+
+
+def _plant_ties(wl: Workload, b: int, K: np.ndarray, qb: np.ndarray, n: int) -> None:
+    """K of a "ties" sequence (tie_mode): equal K rows give equal int8 codes
+    and stored maxima, so their block scores are equal on any implementation
+    of the method."""
+    mode = tie_mode(b)
+    if mode == 0:
+        K[:] = 0.0
+        return
+    if mode == 1:
+        for t0 in range(wl.block, n, wl.block):
+            K[t0:min(n, t0 + wl.block)] = K[:min(n, t0 + wl.block) - t0]
+        return
+    G = wl.G
+    strong, copies = tie_counts(wl, n)
+    for kh in range(wl.nkv):
+        u = qb[kh * G:(kh + 1) * G].astype(np.float64).sum(0)
+        u /= np.linalg.norm(u)
+        rr = _rng(_layer_seed(wl, 0, 13, b * 64 + kh))
+        chosen = rr.choice(n // wl.block, size=strong + copies, replace=False)
+        for j in chosen[:strong]:
+            K[j * wl.block:(j + 1) * wl.block, kh] = _aligned_rows(rr, u, wl.block, wl.hd, 0.9)
+        src = _aligned_rows(rr, u, wl.block, wl.hd, 0.8).astype(np.float32)
+        for j in chosen[strong:]:
+            K[j * wl.block:(j + 1) * wl.block, kh] = src
 
 
 def _plant(wl: Workload, b: int, K: np.ndarray, qb: np.ndarray, n: int) -> None:

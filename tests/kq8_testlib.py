@@ -12,13 +12,31 @@ def out_tolerance(ref: np.ndarray) -> float:
     return min(1e-4, 1e-3 * m)
 
 
-def assert_out_close(got: np.ndarray, ref: np.ndarray, what: str = "") -> float:
+def assert_out_close(got: np.ndarray, ref: np.ndarray, what: str = "", exact=None) -> float:
+    """got within the tolerance of the oracle's fp32 one-pass result `ref`.
+
+    `exact` (optional): the oracle's exact-sum result for the same rows
+    (oracle.attn_exact_sum: the method's fp32 scores, fp64 sums).  The fp32
+    one-pass loop and the kernels' tile-wise loop are two roundings of the same
+    computation (article 9-2 §3); over very long sequences the loop's own
+    rounding can exceed the tolerance.  Only where it measurably does (ref more
+    than half the tolerance from `exact`) is got held to `exact` instead."""
     assert got.shape == ref.shape, (got.shape, ref.shape)
     assert np.all(np.isfinite(got)), what
-    err = float(np.abs(got.astype(np.float64) - ref.astype(np.float64)).max()) if got.size else 0.0
+    got64 = got.astype(np.float64)
+    err = float(np.abs(got64 - ref.astype(np.float64)).max()) if got.size else 0.0
     tol = out_tolerance(ref)
-    assert err <= tol, f"{what}: max abs err {err:.3e} > tol {tol:.3e}"
-    return err
+    if err <= tol or exact is None:
+        assert err <= tol, f"{what}: max abs err {err:.3e} > tol {tol:.3e}"
+        return err
+    own = float(np.abs(ref.astype(np.float64) - exact).max())
+    err_exact = float(np.abs(got64 - exact).max())
+    tol_exact = out_tolerance(exact)
+    assert own > tol / 2 and err_exact <= tol_exact, (
+        f"{what}: max abs err {err:.3e} > tol {tol:.3e} against the fp32 one pass; "
+        f"{err_exact:.3e} against the exact sums (tol {tol_exact:.3e}); the one pass "
+        f"itself is {own:.3e} from them")
+    return err_exact
 
 
 def host_inputs(wl: W.Workload, layer: int = 0):

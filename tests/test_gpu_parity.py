@@ -200,6 +200,17 @@ def test_decode_tiny_config_and_precision():
     assert d <= 0.02
 
 
+@pytest.mark.parametrize("k_factor", [8.0, 64.0])
+def test_decode_large_scores(k_factor):
+    # Student-t keys with x20 outlier channels, scaled once more by a power of
+    # two (every score scales exactly): scores in the hundreds and thousands
+    wl = W.custom(3, 32, 8, [6000, 2500, 700], kind="student_t", seed=19)
+    q, Ks, Vs = host_inputs(wl)
+    Ks = [(K * np.float32(k_factor)).astype(np.float32) for K in Ks]
+    case = paged.fill_from_host(wl, Ks, Vs, DEV, q_host=q)
+    assert_out_close(_decode(case), oracle_decode(wl, q, Ks, Vs), f"keys x{k_factor}")
+
+
 @pytest.mark.parametrize("n", [506, 2046, 4059])
 def test_decode_qwen3vl_2b_all_layers(n):
     wl = W.qwen3vl_2b(n)
@@ -213,33 +224,47 @@ def test_decode_qwen3vl_2b_all_layers(n):
 
 
 def _sampled_full_size(wl, samples, layer=0):
-    """Full-size cache on the device; the oracle checks a sample of (b, h)."""
+    """Full-size cache on the device; the oracle checks a sample of (b, h),
+    regenerating each sampled sequence's fp32 K/V once."""
     case = paged.fill_cache(wl, layer, DEV)
     got = _decode(case)
     qh = case.q.cpu().numpy()
+    by_seq = {}
     for b, h in samples:
+        by_seq.setdefault(b, []).append(h)
+    for b, heads in by_seq.items():
         n = int(wl.seq_lens[b])
         K, V = case.device_kv(b, 0, n)
-        kh = h // wl.G
-        k8, ks = oracle.kv_quantize_rows(K[:, kh:kh + 1].cpu().numpy())
-        v8, vs = oracle.kv_quantize_rows(V[:, kh:kh + 1].cpu().numpy())
-        c = oracle.SeqCache(k8, ks, v8, vs, kv_bs=wl.kv_bs)
-        ref = oracle.attn_single_q(qh[b, h], c, 0, np.float32(wl.scale))
-        assert_out_close(got[b, h], ref, f"{wl.name} b={b} h={h}")
+        caches = {}
+        for kh in sorted({h // wl.G for h in heads}):
+            k8, ks = oracle.kv_quantize_rows(K[:, kh:kh + 1].cpu().numpy())
+            v8, vs = oracle.kv_quantize_rows(V[:, kh:kh + 1].cpu().numpy())
+            caches[kh] = oracle.SeqCache(k8, ks, v8, vs, kv_bs=wl.kv_bs)
+        for h in heads:
+            c = caches[h // wl.G]
+            ref = oracle.attn_single_q(qh[b, h], c, 0, np.float32(wl.scale))
+            exact = oracle.attn_exact_sum(qh[b, h], c, 0, np.float32(wl.scale))
+            assert_out_close(got[b, h], ref, f"{wl.name} b={b} h={h}", exact=exact)
+        del K, V
     return case, got
 
 
 def test_decode_serving_full_size_sampled():
+    # every query head of the longest and the shortest sequence (all four heads
+    # of each KV group, so a slip confined to some heads of a group shows), and
+    # a spread of (sequence, head) pairs elsewhere
     wl = W.serving_8b()
     hi = int(np.argmax(wl.seq_lens))
     lo = int(np.argmin(wl.seq_lens))
-    samples = [(hi, 0), (hi, 31), (lo, 5), (lo, 17), (7, 9), (33, 22), (63, 12)]
+    samples = [(hi, h) for h in range(wl.nq)] + [(lo, h) for h in range(wl.nq)]
+    samples += [(7, 9), (33, 22), (63, 12), (20, 3), (50, 30)]
     _sampled_full_size(wl, samples)
 
 
 def test_decode_long_context_full_size_sampled():
+    # all 16 query heads of one 131072-token sequence, and heads of two others
     wl = W.long_context()
-    _sampled_full_size(wl, [(0, 0), (3, 7), (7, 15)])
+    _sampled_full_size(wl, [(3, h) for h in range(wl.nq)] + [(0, 0), (7, 15)])
 
 
 # ---------------------------------------------------------------------------

@@ -156,7 +156,9 @@ def test_long_context_full_size_eight_pieces_sampled():
     assert kq8.kq8_read_status(ws) == 0
     assert_out_close(got, one.cpu().numpy(), "8 pieces vs one call")
     qh = case.q.cpu().numpy()
-    for b, h in [(0, 0), (2, 9), (7, 15)]:
+    # (3, 14): a head whose fp32 one-pass oracle is itself ~9e-4 from the exact
+    # sums (long tail of small weights); there the exact-sum reference decides
+    for b, h in [(0, 0), (2, 9), (3, 14), (7, 15)]:
         n = int(wl.seq_lens[b])
         K, V = case.device_kv(b, 0, n)
         kh = h // wl.G
@@ -164,4 +166,5 @@ def test_long_context_full_size_eight_pieces_sampled():
         v8, vs = oracle.kv_quantize_rows(V[:, kh:kh + 1].cpu().numpy())
         c = oracle.SeqCache(k8, ks, v8, vs, kv_bs=wl.kv_bs)
         ref = oracle.attn_single_q(qh[b, h], c, 0, np.float32(wl.scale))
-        assert_out_close(got[b, h], ref, f"streamed b={b} h={h}")
+        exact = oracle.attn_exact_sum(qh[b, h], c, 0, np.float32(wl.scale))
+        assert_out_close(got[b, h], ref, f"streamed b={b} h={h}", exact=exact)

@@ -600,3 +600,78 @@ def test_shared_selection_batch_driver_matches_group_calls():
             o, s, _ = oracle.sparse_attn_group(q[b, 2 * kh:2 * kh + 2], caches[b], kh, 0.1, 32, 3, 8)
             assert np.array_equal(out[b, 2 * kh:2 * kh + 2], o)
             assert np.array_equal(sel[b, 2 * kh], s) and np.array_equal(sel[b, 2 * kh + 1], s)
+
+
+# ---------------------------------------------------------------------------
+# exact-sum reference (article 9-2 §3: the one pass and the two passes are the
+# same computation, differing only by rounding)
+# ---------------------------------------------------------------------------
+
+def _integer_case(n, seed):
+    """q, K, V whose quantisation is the identity: every 32-element block of q
+    and every K/V row holds a +-127 (so qsc = stored max * (1/127) = 1 and the
+    codes are the integers themselves); the other entries are small integers."""
+    rng = np.random.default_rng(seed)
+    q = rng.integers(-2, 3, 128).astype(np.float32)
+    q[0::32] = 127.0
+    K = rng.integers(-2, 3, (n, 1, 128)).astype(np.float32)
+    K[:, 0, 1::32] = 127.0                      # a +-127 where q is small
+    K[:, 0, 1] *= np.where(rng.random(n) < 0.5, -1, 1).astype(np.float32)
+    V = rng.integers(-127, 128, (n, 1, 128)).astype(np.float32)
+    V[:, 0, 5] = 127.0
+    return q, K, V
+
+
+def test_exact_sum_is_the_textbook_softmax_when_scores_are_exact():
+    n = 777
+    q, K, V = _integer_case(n, 3)
+    k8, ks = oracle.kv_quantize_rows(K)
+    v8, vs = oracle.kv_quantize_rows(V)
+    assert np.array_equal(k8[:, 0].astype(np.float32), K[:, 0])   # identity quantisation
+    qi, qsc = oracle.quantize_q(q)
+    assert np.array_equal(qsc, np.ones(4, np.float32)) and np.array_equal(qi.astype(np.float32), q)
+    scale = 2.0 ** -6                           # every score is exact in fp32
+    s = (K[:, 0].astype(np.float64) @ q.astype(np.float64)) * scale
+    want = scipy.special.softmax(s) @ V[:, 0].astype(np.float64)
+    got = oracle.attn_exact_sum(q, oracle.SeqCache(k8, ks, v8, vs), 0, np.float32(scale))
+    assert np.abs(got - want).max() <= 1e-11 * np.abs(want).max()
+
+
+@pytest.mark.parametrize("n", [1, 33, 1000])
+def test_exact_sum_agrees_with_one_pass_on_short_sequences(n):
+    cache, _ = _cache(n, seed=n)
+    q = np.random.default_rng(n).standard_normal(128).astype(np.float32)
+    for kh in range(2):
+        a = oracle.attn_exact_sum(q, cache, kh, np.float32(0.088))
+        b = oracle.attn_single_q(q, cache, kh, np.float32(0.088))
+        # the fp32 loop's rounding: ~1e-6 of the output at these lengths
+        assert np.abs(a - b).max() <= 1e-5 * max(1.0, np.abs(a).max())
+
+
+def test_one_pass_rounding_grows_on_long_sequences_and_exact_sum_does_not():
+    # token 0 scores highest (weight 1); n - 1 equal tokens each weigh ~1.5e-6.
+    # The fp32 loop adds each small weight to a running sum near 1, whose unit
+    # in the last place is 1.2e-7: every add rounds, the same way, so the sum
+    # drifts.  The exact sum matches the closed form.
+    n = 200000
+    q = np.zeros(128, np.float32)
+    q[0::32] = 127.0
+    K = np.zeros((n, 1, 128), np.float32)
+    K[0, 0, 0::32] = 127.0                      # dot 127 * 508
+    K[1:, 0, 0::32] = 100.0                     # dot 127 * 400
+    K[1:, 0, 2] = 127.0                         # stored max 127 (q is 0 there)
+    V = np.zeros((n, 1, 128), np.float32)
+    V[0, 0, 0] = 127.0
+    V[1:, 0, 1] = 127.0
+    k8, ks = oracle.kv_quantize_rows(K)
+    v8, vs = oracle.kv_quantize_rows(V)
+    scale = 2.0 ** -10
+    cache = oracle.SeqCache(k8, ks, v8, vs)
+    w = math.exp((127 * 400 - 127 * 508) * scale)
+    den = 1.0 + (n - 1) * w
+    want = np.zeros(128)
+    want[0], want[1] = 127.0 / den, 127.0 * (n - 1) * w / den
+    exact = oracle.attn_exact_sum(q, cache, 0, np.float32(scale))
+    assert np.abs(exact - want).max() <= 1e-9 * 127
+    one_pass = oracle.attn_single_q(q, cache, 0, np.float32(scale))
+    assert np.abs(one_pass - want).max() > 1e-4

@@ -4,16 +4,18 @@ It exists for callers that may not allocate device memory -- code running
 inside another runtime's allocator or launch path, or serving loops that forbid
 device allocation after start-up -- and replaces the caller's workspace with a
 fixed scratch array inside the library.  These checks call it through the C ABI
-and compare it with kq8_decode_attn (which takes a caller-allocated workspace)
-on two calls in a row with different shapes, so that the second call also shows
-that nothing left in the shared array from the first call leaks into a result.
+on two calls in a row with different shapes.  Both entry points run the same
+kernel with the same split and the same merge order, so each result must equal
+kq8_decode_attn's (which takes a caller-allocated workspace) bit for bit -- a
+partial left in the shared array by the first call would show in the second --
+and match the CPU oracle within the usual tolerance.
 
 The file is named so that pytest collects it last.
 """
 import numpy as np
 import pytest
 
-from kq8_testlib import assert_out_close, host_inputs
+from kq8_testlib import assert_out_close, host_inputs, oracle_decode
 from query_decode_attention_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -31,6 +33,7 @@ DEV = "cuda:0"
 
 
 def _both(wl):
+    """(no-alloc result, workspace result, oracle result) on the same inputs."""
     q, Ks, Vs = host_inputs(wl)
     case = paged.fill_from_host(wl, Ks, Vs, DEV, q_host=q)
     shape = (wl.B, wl.nq, wl.hd)
@@ -43,19 +46,21 @@ def _both(wl):
     kq8.kq8_decode_attn_noalloc(got, case.q, case.cache, case.page_table, case.seq_lens,
                                 wl.max_seq_len, wl.scale)
     torch.cuda.synchronize()
-    return got.cpu().numpy(), ref.cpu().numpy()
+    assert kq8.kq8_read_status(ws) == 0
+    return got.cpu().numpy(), ref.cpu().numpy(), oracle_decode(wl, q, Ks, Vs)
 
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
     # first call: several chunks per sequence (the merge path uses the scratch)
     wl1 = W.custom(3, 32, 8, [5000, 17, 2100], seed=21)
-    got1, ref1 = _both(wl1)
-    assert_out_close(got1, ref1, "noalloc, first call")
+    got1, ref1, orc1 = _both(wl1)
+    assert np.array_equal(got1, ref1), "noalloc, first call: not bit-identical"
+    assert_out_close(got1, orc1, "noalloc vs oracle, first call")
     # second call, other shapes: a stale partial from call one would show here
     wl2 = W.custom(2, 16, 4, [300, 4096], seed=22)
-    got2, ref2 = _both(wl2)
-    assert_out_close(got2, ref2, "noalloc, second call")
-    assert np.all(np.isfinite(got1)) and np.all(np.isfinite(got2))
+    got2, ref2, orc2 = _both(wl2)
+    assert np.array_equal(got2, ref2), "noalloc, second call: not bit-identical"
+    assert_out_close(got2, orc2, "noalloc vs oracle, second call")
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
