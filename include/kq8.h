@@ -160,14 +160,22 @@ int kq8_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
  * deployment convenience.
  * Same arguments and result as kq8_decode_attn, without the workspace: the
  * partials go to a scratch array of KQ8_NOALLOC_SCRATCH_BYTES compiled into the
- * library, which every GPU that loads the library holds until the process exits.
- * Returns KQ8_ERR_WORKSPACE when these sizes need more scratch than that (see
- * kq8_decode_workspace_bytes).  Calls no allocating routine.
- * The first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream capture.
+ * library, which every GPU that loads the library's code holds until the
+ * process exits.  Returns KQ8_ERR_WORKSPACE when these sizes need more scratch
+ * than that (see kq8_decode_workspace_bytes).  Calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ * First call on a device: under CUDA's default lazy module loading
+ * (CUDA_MODULE_LOADING=LAZY) the array is reserved only when the library's
+ * code is first used on a device, which for a caller of this entry point alone
+ * is this first call; it also looks up the array's device address (with that
+ * device current) and caches it.  So the first call on each device may take
+ * the 32 MiB of device memory and synchronise: make it at start-up, before any
+ * stream capture.  Later calls only enqueue the kernel.
  * Every call uses the same array: calls that overlap on the GPU (other streams,
  * other threads, the same device) race and corrupt each other's results.
- * Device-side status bits are not reported by this entry point.
+ * Outputs are unchecked: device-side checks (bad page ids or lengths, a timed
+ * out copy wait) leave their status bits in the array where nobody reads them.
+ * A caller that needs them uses kq8_decode_attn and kq8_read_status.
  */
 #define KQ8_NOALLOC_SCRATCH_BYTES (32u << 20)
 int kq8_decode_attn_noalloc(float* out, const float* q, const kq8_cache_t* cache,
@@ -218,7 +226,7 @@ int kq8_sparse_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
  * caller memory between calls: state_acc float [rows][hd] (16-byte aligned)
  * and state_ms float [rows][2] (8-byte aligned), rows = B * nq in the layout
  * of `out`.  Its contents are this library's unnormalised online-softmax state
- * (running max in base-2 units of the scaled score, running sum, accumulator);
+ * (running max of the scores, running sum, accumulator);
  * treat them as opaque.
  *   kq8_state_reset        : makes every row empty.
  *   kq8_decode_attn_update : attends tokens [seq_begin[b], seq_end[b]) of each
@@ -244,6 +252,25 @@ int kq8_decode_attn_update(float* state_acc, float* state_ms, const float* q,
                            void* workspace, size_t workspace_bytes, kq8_stream_t stream);
 int kq8_state_finalize(float* out, const float* state_acc, const float* state_ms, int32_t rows,
                        kq8_stream_t stream);
+
+/*
+ * Merge of running states computed elsewhere ([9-2] §3: the one pass lets KV
+ * arrive piece by piece; the pieces may as well be attended by different
+ * devices or processes, each holding a range of one sequence's tokens).
+ * Folds `parts` partial states into the running state (state_acc, state_ms,
+ * as above), in order, by their log-sum-exp: with M the larger of the two
+ * running maxima, both sums and accumulators are scaled by e^(their max - M)
+ * and added.  Each partial is a state in this library's format, e.g. made by
+ * kq8_state_reset + kq8_decode_attn_update over one token range and copied
+ * from another device; an empty partial changes nothing.
+ *   part_acc : float [parts][rows][hd] (device).
+ *   part_ms  : float [parts][rows][2] (device, 8-byte aligned).
+ * Merging the states of a split of a sequence's tokens gives the state of the
+ * whole range up to rounding (the result does not depend on the split, as
+ * for kq8_decode_attn_update pieces).  One block of hd threads per row.
+ */
+int kq8_state_merge(float* state_acc, float* state_ms, const float* part_acc,
+                    const float* part_ms, int32_t parts, int32_t rows, kq8_stream_t stream);
 
 /*
  * Block-sparse decode with one selection per KV head: the G query heads of a
@@ -392,6 +419,21 @@ int kq8_debug_prefill_withhold(float* out, const float* q, int32_t total_q,
                                int32_t B, int32_t nq, float scale, void* workspace,
                                size_t workspace_bytes, int32_t withhold_sub,
                                kq8_stream_t stream);
+
+/* Failure-detection hook: kq8_decode_attn with the bulk copy of the tile at
+ * index `withhold_tile` (>= 0) of every warp's walk never issued (each warp of
+ * a CTA walks every fourth 32-token tile of its chunk; index 0 is its first).
+ * The bounded wait on it runs out (2^28 SM clocks) in every warp whose walk is
+ * that long; the warp lets its other copies land (bounded) and its CTA sets
+ * KQ8_STATUS_TIMEOUT and writes no result, so the rows of every (sequence, KV
+ * head) that had such a CTA are left as they were; the other rows are exact
+ * and the context stays usable.  Arguments and workspace as kq8_decode_attn
+ * (G = nq / nkv in {1, 2, 4, 8}); KQ8_ERR_INVALID_ARG for withhold_tile < 0. */
+int kq8_debug_decode_withhold(float* out, const float* q, const kq8_cache_t* cache,
+                              const int32_t* page_table, int32_t max_pages,
+                              const int32_t* seq_lens, int32_t max_seq_len, int32_t B, int32_t nq,
+                              float scale, void* workspace, size_t workspace_bytes,
+                              int32_t withhold_tile, kq8_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -34,17 +34,23 @@ int device_sms() {
     return sms;
 }
 
+#ifndef KQ8_MAX_CHUNK
+#define KQ8_MAX_CHUNK 128
+#endif
 // Split of each (sequence, KV head) list of `tiles_max` 32-token tiles into
 // chunks of `chunk_tiles` tiles (a multiple of the CTA's 4 warps).  The chunk
 // is sized so that B * nkv * (chunks) CTAs give about four waves of three CTAs
-// per SM, between 4 and 64 tiles (128 to 2048 tokens).
+// per SM, between 4 and KQ8_MAX_CHUNK tiles (128 to 4096 tokens): each CTA has
+// a prologue and a merge tail in which it streams nothing, so large problems
+// take long chunks.
 void chunking(int64_t B, int64_t nkv, int64_t tiles_max, int sms, int& ct, int& nch) {
+    static_assert(KQ8_MAX_CHUNK % ATTN_WARPS == 0 && KQ8_MAX_CHUNK <= MAX_CHUNK_TILES, "chunk");
     const int64_t total = B * nkv * tiles_max;
     const int64_t target = (int64_t)sms * 3 * 4;
     int64_t c = (total + target - 1) / (target > 0 ? target : 1);
     c = (c + ATTN_WARPS - 1) / ATTN_WARPS * ATTN_WARPS;
     if (c < ATTN_WARPS) c = ATTN_WARPS;
-    if (c > 64) c = 64;
+    if (c > KQ8_MAX_CHUNK) c = KQ8_MAX_CHUNK;
     ct = (int)c;
     nch = (int)((tiles_max + c - 1) / c);
     if (nch < 1) nch = 1;
@@ -168,6 +174,7 @@ AttnParams attn_params(float* out, const float* q, const kq8_cache_t* c, const i
     p.counters = ((size_t)B * (size_t)c->num_kv_heads <= MAX_COUNTERS)
                      ? reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + STATUS_BYTES)
                      : nullptr;
+    p.withhold = -1;
     return p;
 }
 
@@ -206,8 +213,10 @@ int run_sparse(float* out, const float* q, const kq8_cache_t* cache, const int32
     sp.status = reinterpret_cast<uint32_t*>(ws);
     sp.row_seq = row_seq;
     sp.shared_sel = shared_sel ? 1 : 0;
-    // the top-k tickets share the header's per-(sequence, KV head) counters
-    // with the attention kernel's chunk merge: both leave them at zero
+    // the selection tickets (the probe kernel's last CTA of a (sequence, KV
+    // head) selects) share the header's per-(sequence, KV head) counters with
+    // the attention kernel's chunk merge: both leave them at zero; without
+    // them a separate top-k kernel selects
     sp.tickets = ((size_t)rows * (size_t)nkv <= MAX_COUNTERS)
                      ? reinterpret_cast<uint32_t*>(ws + STATUS_BYTES)
                      : nullptr;
@@ -465,6 +474,18 @@ int kq8_state_finalize(float* out, const float* state_acc, const float* state_ms
                                  (cudaStream_t)stream);
 }
 
+int kq8_state_merge(float* state_acc, float* state_ms, const float* part_acc,
+                    const float* part_ms, int32_t parts, int32_t rows, kq8_stream_t stream) {
+    if (rows < 0 || parts < 0) return KQ8_ERR_INVALID_ARG;
+    if (rows == 0 || parts == 0) return KQ8_OK;
+    if (!state_acc || !state_ms || !part_acc || !part_ms || !aligned(state_ms, 8) ||
+        !aligned(part_ms, 8))
+        return KQ8_ERR_INVALID_ARG;
+    return launch_state_merge(state_acc, reinterpret_cast<float2*>(state_ms), part_acc,
+                              reinterpret_cast<const float2*>(part_ms), parts, rows,
+                              (cudaStream_t)stream);
+}
+
 int kq8_read_status(void* status_word, uint32_t* status, kq8_stream_t stream) {
     if (!status_word || !status || !aligned(status_word, 4)) return KQ8_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
@@ -491,6 +512,25 @@ int kq8_debug_block_dots(int32_t* dots, const float* q, const kq8_cache_t* cache
     if (rc) return rc;
     return launch_debug_dots(dots, q, *cache, page_table, max_pages, seq_lens, max_seq_len, B, nq,
                              (cudaStream_t)stream);
+}
+
+int kq8_debug_decode_withhold(float* out, const float* q, const kq8_cache_t* cache,
+                              const int32_t* page_table, int32_t max_pages,
+                              const int32_t* seq_lens, int32_t max_seq_len, int32_t B, int32_t nq,
+                              float scale, void* workspace, size_t workspace_bytes,
+                              int32_t withhold_tile, kq8_stream_t stream) {
+    if (withhold_tile < 0) return KQ8_ERR_INVALID_ARG;
+    int rc = check_decode(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq);
+    if (rc) return rc;
+    const int nkv = cache->num_kv_heads;
+    const Plan plan = plan_exact(B, nq, nkv, max_seq_len);
+    rc = check_ws(workspace, workspace_bytes, plan.total);
+    if (rc) return rc;
+    if (B == 0) return KQ8_OK;
+    AttnParams p = attn_params(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq,
+                               scale, plan, workspace);
+    p.withhold = withhold_tile;
+    return launch_attn_withhold(p, nq / nkv, B, nkv, (cudaStream_t)stream);
 }
 
 int kq8_debug_probe_scores(float* scores, const float* q, const kq8_cache_t* cache,
@@ -530,8 +570,10 @@ int kq8_debug_probe_scores(float* scores, const float* q, const kq8_cache_t* cac
 // device, stalling every other stream), and serving loops that forbid device
 // allocation once they have started.  For them, kq8_decode_attn_noalloc uses a
 // fixed scratch array compiled into this library instead of a caller-provided
-// workspace.  The array lives in every device's global memory from the moment
-// the library is loaded until the process exits.
+// workspace.  The array lives in a device's global memory from the moment this
+// file's module is loaded on it -- with CUDA's default lazy loading, at the
+// first use of the array there, i.e. the first call's cudaGetSymbolAddress --
+// until the process exits.
 // ---------------------------------------------------------------------------
 #include <mutex>
 

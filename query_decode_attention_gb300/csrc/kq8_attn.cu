@@ -4,9 +4,9 @@
 
 namespace kq8 {
 
-template <int G, bool SPARSE, bool Q4>
+template <int G, bool SPARSE, bool Q4, bool WITHHOLD = false>
 static int launch_attn_g(const AttnParams& p, int B, int nkv, cudaStream_t s) {
-    auto kern = kq8_attn_kernel<G, SPARSE, Q4>;
+    auto kern = kq8_attn_kernel<G, SPARSE, Q4, WITHHOLD>;
     const size_t smem = sizeof(AttnSmem<G>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
@@ -47,6 +47,18 @@ int launch_attn_q4(const AttnParams& p, int G, int B, int nkv, cudaStream_t s) {
     return launch_attn_s<false, true>(p, G, B, nkv, s);
 }
 
+// The exact decode with the failure-detection hook compiled in (p.withhold).
+int launch_attn_withhold(const AttnParams& p, int G, int B, int nkv, cudaStream_t s) {
+    if (B == 0) return KQ8_OK;
+    switch (G) {
+        case 1: return launch_attn_g<1, false, false, true>(p, B, nkv, s);
+        case 2: return launch_attn_g<2, false, false, true>(p, B, nkv, s);
+        case 4: return launch_attn_g<4, false, false, true>(p, B, nkv, s);
+        case 8: return launch_attn_g<8, false, false, true>(p, B, nkv, s);
+        default: return KQ8_ERR_UNSUPPORTED;
+    }
+}
+
 // Running states: reset to empty (max -1e9, sum 0, acc 0) and finalise to
 // out = acc / S (0 for an empty state), one block of HD threads per row.
 __global__ void __launch_bounds__(HD) kq8_state_reset_kernel(float* acc, float2* ms) {
@@ -58,6 +70,34 @@ __global__ void __launch_bounds__(HD) kq8_state_finalize_kernel(float* out, cons
     const float s = ms[blockIdx.x].y;
     const size_t i = (size_t)blockIdx.x * HD + threadIdx.x;
     out[i] = (s > 0.0f) ? acc[i] / s : 0.0f;
+}
+
+// Folds `parts` partial states (each [rows][HD] + [rows] (max, sum), the
+// running-state format) into the running state in order, by their
+// log-sum-exp: M = max, both sides scaled by 2^(their max - M) and added.
+__global__ void __launch_bounds__(HD) kq8_state_merge_kernel(float* acc, float2* ms,
+                                                             const float* pacc, const float2* pms,
+                                                             int parts, int rows) {
+    const int row = blockIdx.x, d = threadIdx.x;
+    float2 cur = ms[row];
+    float a = acc[(size_t)row * HD + d];
+    for (int r = 0; r < parts; r++) {
+        const size_t pr = (size_t)r * rows + row;
+        const float2 p = pms[pr];
+        float M, S, fo, fn;
+        fold_state(cur.x, cur.y, p.x, p.y, M, S, fo, fn);
+        a = a * fo + pacc[pr * HD + d] * fn;
+        cur = make_float2(M, S);
+    }
+    acc[(size_t)row * HD + d] = a;
+    if (d == 0) ms[row] = cur;
+}
+
+int launch_state_merge(float* acc, float2* ms, const float* pacc, const float2* pms, int parts,
+                       int rows, cudaStream_t s) {
+    if (rows == 0 || parts == 0) return KQ8_OK;
+    kq8_state_merge_kernel<<<rows, HD, 0, s>>>(acc, ms, pacc, pms, parts, rows);
+    return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
 }
 
 int launch_state_reset(float* acc, float2* ms, int rows, cudaStream_t s) {

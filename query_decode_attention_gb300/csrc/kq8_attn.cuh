@@ -12,12 +12,13 @@
 // tile:
 //   score phase (lane = token): int32 block dots of the token's K row with
 //     the G int8 query rows (dp4a), the fp32 score in the method's order on
-//     pairs of heads (packed fp32 ops, each lane still rounded separately),
-//     moved to base 2; a warp vote checks whether any score exceeds the
-//     running max by more than RESCALE_SLACK and only then reduces the tile
-//     max and rescales the warp's state (the online-softmax rescale of
-//     article 9-2 §1, done lazily: between rescales the weights may exceed 1
-//     by at most 2^RESCALE_SLACK, which fp32 absorbs); w = 2^(s - M);
+//     pairs of heads (packed fp32 ops, each lane still rounded separately, so
+//     every score is the method's fp32 score bit for bit); a warp vote checks
+//     whether any weight e^(s - M) would exceed 2^RESCALE_SLACK and only then
+//     reduces the tile max and rescales the warp's state (the online-softmax
+//     rescale of article 9-2 §1, done lazily: between rescales the weights may
+//     exceed 1 by at most 2^8, which fp32 absorbs); w = e^(s - M), the
+//     difference taken before the move to base 2;
 //   value phase (lane = 16 bytes of a V row, 4 rows per instruction): int8 ->
 //     fp32 by byte permutes and a packed subtract, acc += v * (w * vs) with
 //     packed FMAs.
@@ -27,6 +28,11 @@
 // finish (an atomic ticket per (sequence, KV head)) combines them by their
 // log-sum-exp -- the same algebra as the online rescale.  Without ticket
 // counters (very large batches) kq8_merge_kernel does that step instead.
+//
+// Every wait on a copy is bounded and decided for the whole warp at once.  A
+// CTA in which a wait ran out sets KQ8_STATUS_TIMEOUT and writes no result:
+// a single-chunk row is left as it was, and a partial is marked failed
+// (S = -1) so that the merge leaves the row as it was too.
 #pragma once
 
 #include "kq8_common.cuh"
@@ -39,7 +45,8 @@ constexpr int ATTN_STAGES = 2;
 constexpr int MAX_WARP_TILES = 32;     // tiles per warp per chunk, one per lane
 constexpr int MAX_CHUNK_TILES = ATTN_WARPS * MAX_WARP_TILES;
 constexpr float LOG2E = 1.4426950408889634f;
-constexpr float RESCALE_SLACK = 8.0f;  // base-2 units
+// Lazy rescale: between rescales a weight stays below 2^RESCALE_SLACK.
+constexpr float RESCALE_SLACK = 8.0f;
 
 struct AttnParams {
     float* out;
@@ -54,14 +61,14 @@ struct AttnParams {
     int32_t chunk_tiles;   // multiple of ATTN_WARPS, <= MAX_CHUNK_TILES
     int32_t num_chunks;    // grid.x
     float* part_acc;       // [B][nq][num_chunks][HD]
-    float2* part_ms;       // [B][nq][num_chunks] (M in base 2, S)
+    float2* part_ms;       // [B][nq][num_chunks] (M in score units, S)
     uint32_t* status;
     uint32_t* counters;    // [B][nkv] chunk tickets, zero between calls; null: merge kernel
     // streaming form (exact mode only): attend tokens [seq_begin[b], seq_lens[b])
     // and fold the result into a caller-held running state instead of `out`
     const int32_t* seq_begin;  // optional [B]
     float* state_acc;          // optional [B][nq][HD] unnormalised accumulator
-    float2* state_ms;          // optional [B][nq] (running max in base 2, running sum)
+    float2* state_ms;          // optional [B][nq] (running max, running sum)
     // block-sparse tile lists (SPARSE only): entry = tile | head_mask << 24
     const int32_t* tile_list;  // [B][nkv][list_cap]
     const int32_t* list_len;   // [B][nkv]
@@ -69,6 +76,9 @@ struct AttnParams {
     // optional [B]: the page-table row of each row b (prefill: the query
     // token's sequence); null = row b
     const int32_t* row_seq;
+    // failure-detection hook (WITHHOLD kernels only): the copy of the tile at
+    // this index of every warp's walk is never issued, so its wait runs out
+    int32_t withhold;
 };
 
 template <int G>
@@ -97,6 +107,10 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// e^(a - b) for two scores: the difference is taken first (exact whenever a and
+// b are close, else rounded relative to it), and only then moved to base 2, so
+// the result does not depend on how large the scores themselves are.
+__device__ __forceinline__ float exp_diff(float a, float b) { return ex2((a - b) * LOG2E); }
 
 // Four int8 codes in one word -> two float pairs, exactly: flip the sign bits
 // (offset binary u = c + 128), drop each byte into the mantissa of 2^23 with a
@@ -185,17 +199,19 @@ __device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h)
     return r;
 }
 
-// Folds a result (m, s, a) into a running state (mo, so, ao), base-2 maxima:
-// M = max, then both sides are scaled by 2^(their max - M) and added.
+// Folds a result (m, s, a) into a running state (mo, so, ao), maxima in score
+// units: M = max, then both sides are scaled by e^(their max - M) and added.
 __device__ __forceinline__ void fold_state(float mo, float so, float m, float s, float& M,
                                            float& S, float& fo, float& fn) {
     M = fmaxf(mo, m);
-    fo = ex2(mo - M);
-    fn = ex2(m - M);
+    fo = exp_diff(mo, M);
+    fn = exp_diff(m, M);
     S = so * fo + s * fn;
 }
 
-template <int G, bool SPARSE, bool Q4 = false>
+// WITHHOLD: the failure-detection test build (P.withhold honoured); the
+// production instantiations compile the check out.
+template <int G, bool SPARSE, bool Q4 = false, bool WITHHOLD = false>
 __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     kq8_attn_kernel(const AttnParams P) {
     using Sh = AttnShape<G>;
@@ -268,6 +284,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     auto issue = [&](int i) {
         const int tile = __shfl_sync(0xffffffffu, my_tile, i);
         const int32_t pg = __shfl_sync(0xffffffffu, my_page, i);
+        if (WITHHOLD && i == P.withhold) return;  // test hook: the phase never completes
         if (lane == 0) {
             uint64_t* bar = &S.bar[warp][i % NS];
             if (pg < 0) {
@@ -311,11 +328,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
 #pragma unroll
         for (int bb = 0; bb < NB; bb++)
             qsc2[gp][bb] = make_float2(S.qsc[2 * gp][bb], S.qsc[min(2 * gp + 1, G - 1)][bb]);
-    // stored K max -> step (1/127), softmax scale and the move to base 2
-    const float kscale_mul = (Q4 ? inv7() : inv127()) * P.scale * LOG2E;
-    float Mhi[G];  // rescale threshold: running max + RESCALE_SLACK
-#pragma unroll
-    for (int g = 0; g < G; g++) Mhi[g] = M_INIT + RESCALE_SLACK;
+    // stored K max -> step (1/127); the softmax scale is applied after it
+    const float kstep = Q4 ? inv7() : inv127();
+    const float2 scale2 = make_float2(P.scale, P.scale);
 
     bool failed = false;
     int i = 0;
@@ -323,7 +338,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
         const int tile = __shfl_sync(0xffffffffu, my_tile, i);
         const uint32_t mask = __shfl_sync(0xffffffffu, my_mask, i);
         const int32_t pg = __shfl_sync(0xffffffffu, my_page, i);
-        if (!mbar_wait_bounded(&S.bar[warp][i % NS], (i / NS) & 1)) {
+        // every lane waits (each needs the barrier's acquire of the copied
+        // bytes); the warp gives up only together, so no lane is left behind
+        // in a shuffle
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&S.bar[warp][i % NS], (i / NS) & 1))) {
             failed = true;
             break;
         }
@@ -384,8 +402,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                     dot[g][bb] = d;
                 }
             }
-            // (s * ks) * scale * log2(e) with ks = kscale / 127: one multiplier per token
-            const float kmul = __fmul_rn(kss[t], kscale_mul);
+            // s = (s * ks) * scale with ks = kscale / 127, each product rounded
+            // as the method writes it, so every score equals the oracle's
+            const float ks = __fmul_rn(kss[t], kstep);
             const float vstep = __fmul_rn(vss[t], Q4 ? inv7() : inv127());
             float sv[2 * GP];
 #pragma unroll
@@ -401,16 +420,27 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                     s = __fadd2_rn(s, __fmul2_rn(make_float2(__int2float_rn(dot[2 * gp][bb]),
                                                              __int2float_rn(dot[g1][bb])),
                                                  qsc2[gp][bb]));
-                s = __fmul2_rn(s, make_float2(kmul, kmul));
+                s = __fmul2_rn(__fmul2_rn(s, make_float2(ks, ks)), scale2);
                 sv[2 * gp] = s.x;
                 sv[2 * gp + 1] = s.y;
             }
-            bool grow = false;
 #pragma unroll
             for (int g = 0; g < G; g++) {
                 const bool on = live && ((mask >> g) & 1u);
                 sv[g] = on ? sv[g] : -INFINITY;
-                grow |= sv[g] > Mhi[g];
+            }
+            // (s - M) * log2(e): the difference first, then base 2 (masked: -inf)
+            float dd[2 * GP];
+            bool grow = false;
+#pragma unroll
+            for (int gp = 0; gp < GP; gp++) {
+                const int g1 = min(2 * gp + 1, G - 1);
+                const float2 x = __fmul2_rn(
+                    __fadd2_rn(make_float2(sv[2 * gp], sv[g1]), make_float2(-M2[2 * gp], -M2[g1])),
+                    make_float2(LOG2E, LOG2E));
+                dd[2 * gp] = x.x;
+                dd[2 * gp + 1] = x.y;
+                grow |= x.x > RESCALE_SLACK || x.y > RESCALE_SLACK;
             }
             if (__any_sync(0xffffffffu, grow)) {
                 // rare: some head's maximum grew by a wide margin -> rescale its state
@@ -418,20 +448,20 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                 for (int g = 0; g < G; g++) {
                     const float mn = fmaxf(M2[g], warp_max(sv[g]));
                     if (mn > M2[g]) {
-                        const float c = ex2(M2[g] - mn);
+                        const float c = exp_diff(M2[g], mn);
                         Sl[g] *= c;
 #pragma unroll
                         for (int e = 0; e < EP; e++)
                             acc[g][e] = __fmul2_rn(acc[g][e], make_float2(c, c));
                         M2[g] = mn;
-                        Mhi[g] = mn + RESCALE_SLACK;
+                        dd[g] = (sv[g] - mn) * LOG2E;
                     }
                 }
             }
             float w[2 * GP];
 #pragma unroll
             for (int g = 0; g < G; g++) {
-                w[g] = ex2(sv[g] - M2[g]);  // masked: ex2(-inf) = 0
+                w[g] = ex2(dd[g]);  // masked: ex2(-inf) = 0
                 Sl[g] += w[g];
             }
             if constexpr ((G & 1) != 0) w[G] = 0.0f;
@@ -492,11 +522,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
         if (lane == 0) atomicOr(P.status, KQ8_STATUS_TIMEOUT);
         // let the copies this warp still has in flight land before leaving
         for (int j = i; j < mine && j < i + NS; j++)
-            mbar_wait_bounded(&S.bar[warp][j % NS], (j / NS) & 1);
+            __all_sync(0xffffffffu, mbar_wait_bounded(&S.bar[warp][j % NS], (j / NS) & 1));
 #pragma unroll
         for (int g = 0; g < G; g++) {
             M2[g] = M_INIT;
-            Mhi[g] = M_INIT + RESCALE_SLACK;
             Sl[g] = 0.0f;
 #pragma unroll
             for (int e = 0; e < EP; e++) acc[g][e] = make_float2(0.0f, 0.0f);
@@ -517,7 +546,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     }
 
     // ---- merge the 4 warps in shared memory (reuses the stage buffers)
-    __syncthreads();
+    const bool cta_failed = __syncthreads_or(failed ? 1 : 0) != 0;
     float* macc = reinterpret_cast<float*>(S.stage);                      // [W][G][HD]
     float2* mms = reinterpret_cast<float2*>(macc + ATTN_WARPS * G * HD);  // [W][G]
     if (lane < NC) {
@@ -542,12 +571,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
 #pragma unroll
         for (int w = 0; w < ATTN_WARPS; w++) {
             const float2 ms = mms[w * G + g];
-            const float f = ex2(ms.x - mx);
+            const float f = exp_diff(ms.x, mx);
             ssum += ms.y * f;
             a += macc[(w * G + g) * HD + d] * f;
         }
         const size_t row = (size_t)b * P.nq + (size_t)h * G + g;
-        if (nch == 1 && P.state_acc) {
+        if (nch == 1 && cta_failed) {
+            // a timed-out walk: the row (or its running state) stays as it was
+        } else if (nch == 1 && P.state_acc) {
             const float2 old = P.state_ms[row];
             float M, Sn, fo, fn;
             fold_state(old.x, old.y, mx, ssum, M, Sn, fo, fn);
@@ -560,16 +591,18 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
         } else {
             const size_t pr = row * P.num_chunks + chunk;
             P.part_acc[pr * HD + d] = a;
-            if (d == 0) P.part_ms[pr] = make_float2(mx, ssum);
+            if (d == 0) P.part_ms[pr] = make_float2(mx, cta_failed ? -1.0f : ssum);
         }
     }
     if (nch == 1 || P.counters == nullptr) return;
 
     // ---- the last CTA of this (sequence, KV head) to finish merges the chunks
-    //   M = max_c m_c, out = sum_c acc_c 2^(m_c - M) / sum_c S_c 2^(m_c - M)
-    __threadfence();  // this thread's partials are visible before the ticket
-    __syncthreads();
+    //   M = max_c m_c, out = sum_c acc_c e^(m_c - M) / sum_c S_c e^(m_c - M)
+    __syncthreads();  // every partial of this CTA is written
     if (threadIdx.x == 0) {
+        // one fence after the CTA barrier orders all of them before the ticket
+        // (a fence is cumulative over the writes that happen before it)
+        __threadfence();
         const unsigned ticket = atomicAdd(&P.counters[b * nkv + h], 1u);
         S.last = (ticket == (unsigned)(nch - 1));
     }
@@ -582,12 +615,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
         const size_t base = ((size_t)b * P.nq + (size_t)h * G + g) * P.num_chunks;
         float mx = M_INIT, ssum = 0.0f;
         float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        bool chunk_failed = false;
 #pragma unroll 8
         for (int c = 0; c < nch; c++) {
             const float2 ms = __ldcg(&P.part_ms[base + c]);
+            chunk_failed |= ms.y < 0.0f;
             const float4 x = __ldcg(reinterpret_cast<const float4*>(P.part_acc + (base + c) * HD) + lane);
             const float mn = fmaxf(mx, ms.x);
-            const float fo = ex2(mx - mn), fn = ex2(ms.x - mn);
+            const float fo = exp_diff(mx, mn), fn = exp_diff(ms.x, mn);
             ssum = ssum * fo + ms.y * fn;
             a.x = a.x * fo + x.x * fn;
             a.y = a.y * fo + x.y * fn;
@@ -596,7 +631,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             mx = mn;
         }
         const size_t row = (size_t)b * P.nq + (size_t)h * G + g;
-        if (P.state_acc) {  // fold into the caller's running state (this warp owns the row)
+        if (chunk_failed) {
+            // some chunk's walk timed out: the row (or its state) stays as it was
+        } else if (P.state_acc) {  // fold into the caller's running state (this warp owns the row)
             const float2 old = P.state_ms[row];
             float M, Sn, fo, fn;
             fold_state(old.x, old.y, mx, ssum, M, Sn, fo, fn);
@@ -615,8 +652,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     if (threadIdx.x == 0) P.counters[b * nkv + h] = 0;  // ready for the next call
 }
 
-// Combine the partials of sequences split over several chunks (base-2 maxima):
-//   M = max_c m_c, out = sum_c acc_c 2^(m_c - M) / sum_c S_c 2^(m_c - M).
+// Combine the partials of sequences split over several chunks:
+//   M = max_c m_c, out = sum_c acc_c e^(m_c - M) / sum_c S_c e^(m_c - M).
 template <bool SPARSE>
 __global__ void __launch_bounds__(HD) kq8_merge_kernel(const AttnParams P) {
     const int row = blockIdx.x;  // b * nq + hq
@@ -628,11 +665,14 @@ __global__ void __launch_bounds__(HD) kq8_merge_kernel(const AttnParams P) {
     if (nch <= 1) return;
     const size_t base = (size_t)row * P.num_chunks;
     float mx = M_INIT;
-    for (int c = 0; c < nch; c++) mx = fmaxf(mx, P.part_ms[base + c].x);
+    for (int c = 0; c < nch; c++) {
+        if (P.part_ms[base + c].y < 0.0f) return;  // a timed-out chunk: row left as it was
+        mx = fmaxf(mx, P.part_ms[base + c].x);
+    }
     float ssum = 0.0f, a = 0.0f;
     for (int c = 0; c < nch; c++) {
         const float2 ms = P.part_ms[base + c];
-        const float f = ex2(ms.x - mx);
+        const float f = exp_diff(ms.x, mx);
         ssum += ms.y * f;
         a += P.part_acc[(base + c) * HD + threadIdx.x] * f;
     }

@@ -27,9 +27,12 @@ int launch_debug_dots(int32_t* dots, const float* q, const kq8_cache_t& c,
 // Attention over KV chunks (+ the merge when any sequence spans > 1 chunk).
 int launch_attn(const AttnParams& p, int G, bool sparse, int B, int nkv, cudaStream_t s);
 int launch_attn_q4(const AttnParams& p, int G, int B, int nkv, cudaStream_t s);
+int launch_attn_withhold(const AttnParams& p, int G, int B, int nkv, cudaStream_t s);
 int launch_probe(const SparseParams& p, int G, int B, int nkv, cudaStream_t s);
 int launch_state_reset(float* acc, float2* ms, int rows, cudaStream_t s);
 int launch_state_finalize(float* out, const float* acc, const float2* ms, int rows, cudaStream_t s);
+int launch_state_merge(float* acc, float2* ms, const float* pacc, const float2* pms, int parts,
+                       int rows, cudaStream_t s);
 int probe_blocks_per_cta(int block, int kv_bs);
 int launch_prefill(const PrefillParams& p, int G, int nkv, cudaStream_t s);
 int launch_prefill_rows(int32_t* row_seq, int32_t* row_len, const int32_t* q_off,

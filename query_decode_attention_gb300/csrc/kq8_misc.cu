@@ -5,61 +5,107 @@
 
 namespace kq8 {
 
+// roundf(x / d) for the elements of a row whose step is d, |x / d| < 128, with
+// r = RN(1 / d).  r and the product q = RN(x * r) each round once (relative
+// 2^-24), so |q - x / d| <= 128 * 2^-23 and |fl(x / d) - x / d| <= 2^-18:
+// q is within 2^-15.5 of the IEEE quotient fl(x / d).  Unless q lies within
+// 2^-14 of a half-integer both therefore round to the same integer, and rint(q)
+// (no tie possible) is roundf(fl(x / d)).  The rare near-half case (about 1 in
+// 8000 elements), and a non-finite q (d subnormal or 0), take the IEEE quotient
+// itself, so the result always equals the method's roundf(x / d) bit for bit.
+// The lane's four quotients roundf(x_i / d), computed as described above;
+// one (rarely taken) branch for the lane's four elements together.
+__device__ __forceinline__ float4 round_quotients(const float4 x, float d, float lo, float hi) {
+    const float r = __frcp_rn(d);
+    const float q0 = __fmul_rn(x.x, r), q1 = __fmul_rn(x.y, r);
+    const float q2 = __fmul_rn(x.z, r), q3 = __fmul_rn(x.w, r);
+    float4 n = make_float4(rintf(q0), rintf(q1), rintf(q2), rintf(q3));
+    const float far = 0.5f - 0x1p-14f;  // NaN / inf compare false
+    const bool ok = fabsf(q0 - n.x) < far && fabsf(q1 - n.y) < far && fabsf(q2 - n.z) < far &&
+                    fabsf(q3 - n.w) < far;
+    if (!ok)
+        n = make_float4(roundf(__fdiv_rn(x.x, d)), roundf(__fdiv_rn(x.y, d)),
+                        roundf(__fdiv_rn(x.z, d)), roundf(__fdiv_rn(x.w, d)));
+    return make_float4(fminf(fmaxf(n.x, lo), hi), fminf(fmaxf(n.y, lo), hi),
+                       fminf(fmaxf(n.z, lo), hi), fminf(fmaxf(n.w, lo), hi));
+}
+
 // One (token, KV head) row of K or V, one warp: lane l holds elements
 // 4l..4l+3.  m = max |x| (exact, order-free), stored as the scale; codes are
-// roundf(x / (m * (1/127))) clamped to [-127, 127] with an IEEE divide, as the
-// oracle does; an all-zero row gives zero codes.  Returns the lane's 4 codes.
+// roundf(x / (m * (1/127))) clamped to [-127, 127], as the oracle computes
+// them (IEEE quotient, see round_quotients); an all-zero row gives zero codes.
+// Returns the lane's 4 codes.
 __device__ __forceinline__ uint32_t kv_quantize_lane(const float4 x, float& m_out) {
     float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
     m = warp_max(m);
     m_out = m;
     if (m == 0.0f) return 0u;
-    const float d = __fmul_rn(m, inv127());
-    auto code = [&](float v) -> uint32_t {
-        float r = roundf(__fdiv_rn(v, d));
-        r = fminf(fmaxf(r, -127.0f), 127.0f);
-        return (uint32_t)((int)r & 0xff);
-    };
-    return code(x.x) | (code(x.y) << 8) | (code(x.z) << 16) | (code(x.w) << 24);
+    const float4 n = round_quotients(x, __fmul_rn(m, inv127()), -127.0f, 127.0f);
+    return ((uint32_t)(int)n.x & 0xffu) | (((uint32_t)(int)n.y & 0xffu) << 8) |
+           (((uint32_t)(int)n.z & 0xffu) << 16) | ((uint32_t)(int)n.w << 24);
 }
 
 constexpr int APPEND_WARPS = 8;
+constexpr int APPEND_ITEMS = 4;  // (token, head) rows per warp, all loaded up front
 
-// grid: ceil(T * nkv / APPEND_WARPS) blocks of APPEND_WARPS warps; warp = one
-// (token, head) item, quantising its K and its V row.
+// grid: ceil(T * nkv / (APPEND_WARPS * APPEND_ITEMS)) blocks of APPEND_WARPS
+// warps; warp = APPEND_ITEMS consecutive (token, head) items (consecutive
+// heads of a token: their fp32 rows are contiguous), each quantising its K and
+// its V row.  Every item's loads are issued before the first is used.
 __global__ void __launch_bounds__(APPEND_WARPS * 32)
     kq8_append_kernel(const kq8_cache_t c, const float* __restrict__ k, const float* __restrict__ v,
                       const int32_t* __restrict__ slot, int32_t T, uint32_t* status) {
     const int lane = threadIdx.x & 31;
-    const int64_t item = (int64_t)blockIdx.x * APPEND_WARPS + (threadIdx.x >> 5);
+    const int64_t item0 =
+        ((int64_t)blockIdx.x * APPEND_WARPS + (threadIdx.x >> 5)) * APPEND_ITEMS;
     const int nkv = c.num_kv_heads, kv_bs = c.kv_bs;
-    if (item >= (int64_t)T * nkv) return;
-    const int64_t t = item / nkv;
-    const int h = (int)(item % nkv);
-    const int32_t sl = slot[t];
-    if (sl < 0) return;
-    if ((int64_t)sl >= (int64_t)c.num_pages * kv_bs) {
-        if (lane == 0 && status) atomicOr(status, KQ8_STATUS_BAD_SLOT);
-        return;
+    const int64_t items = (int64_t)T * nkv;
+    if (item0 >= items) return;
+    float4 xk[APPEND_ITEMS], xv[APPEND_ITEMS];
+    int32_t sl[APPEND_ITEMS], hh[APPEND_ITEMS];
+    int64_t t = item0 / nkv;  // the only division: later items step through the heads
+    int h = (int)(item0 - t * nkv);
+#pragma unroll
+    for (int i = 0; i < APPEND_ITEMS; i++) {
+        const int64_t item = item0 + i;
+        sl[i] = -1;
+        hh[i] = h;
+        if (item < items) {
+            sl[i] = __ldg(slot + t);
+            const size_t row = (size_t)item * HD;
+            xk[i] = __ldcs(reinterpret_cast<const float4*>(k + row) + lane);
+            xv[i] = __ldcs(reinterpret_cast<const float4*>(v + row) + lane);
+        }
+        if (++h == nkv) {
+            h = 0;
+            t++;
+        }
     }
-    const int32_t page = sl / kv_bs;
-    const int r = sl % kv_bs;
-    const size_t row = (size_t)item * HD;
-    const float4 xk = __ldcs(reinterpret_cast<const float4*>(k + row) + lane);
-    const float4 xv = __ldcs(reinterpret_cast<const float4*>(v + row) + lane);
-    float mk, mv;
-    const uint32_t ck = kv_quantize_lane(xk, mk);
-    const uint32_t cv = kv_quantize_lane(xv, mv);
-    // K: element i of row r at sub-tile r/32, block i/32, position kpos(r%32), byte i%32
-    const size_t ko = kv_sub_off(page, h, nkv, kv_bs, r / TILE) + (size_t)(lane >> 3) * 1024 +
-                      (size_t)kpos(r % TILE) * 32 + (size_t)(lane & 7) * 4;
-    *reinterpret_cast<uint32_t*>(c.k + ko) = ck;
-    const size_t vo = page_head(page, h, nkv) * (size_t)kv_bs * HD + (size_t)r * HD + lane * 4;
-    *reinterpret_cast<uint32_t*>(c.v + vo) = cv;
-    if (lane == 0) {
-        const size_t so = page_head(page, h, nkv) * (size_t)kv_bs + r;
-        c.kscale[so] = mk;
-        c.vscale[so] = mv;
+    const int64_t pool_slots = (int64_t)c.num_pages * kv_bs;
+#pragma unroll
+    for (int i = 0; i < APPEND_ITEMS; i++) {
+        if (sl[i] < 0) continue;  // past the end, or a skipped token
+        if ((int64_t)sl[i] >= pool_slots) {
+            if (lane == 0 && status) atomicOr(status, KQ8_STATUS_BAD_SLOT);
+            continue;
+        }
+        const int h = hh[i];
+        const int32_t page = sl[i] / kv_bs;
+        const int r = sl[i] % kv_bs;
+        float mk, mv;
+        const uint32_t ck = kv_quantize_lane(xk[i], mk);
+        const uint32_t cv = kv_quantize_lane(xv[i], mv);
+        // K: element e of row r at sub-tile r/32, block e/32, position kpos(r%32), byte e%32
+        const size_t ko = kv_sub_off(page, h, nkv, kv_bs, r / TILE) + (size_t)(lane >> 3) * 1024 +
+                          (size_t)kpos(r % TILE) * 32 + (size_t)(lane & 7) * 4;
+        *reinterpret_cast<uint32_t*>(c.k + ko) = ck;
+        const size_t vo = page_head(page, h, nkv) * (size_t)kv_bs * HD + (size_t)r * HD + lane * 4;
+        *reinterpret_cast<uint32_t*>(c.v + vo) = cv;
+        if (lane == 0) {
+            const size_t so = page_head(page, h, nkv) * (size_t)kv_bs + r;
+            c.kscale[so] = mk;
+            c.vscale[so] = mv;
+        }
     }
 }
 
@@ -71,13 +117,9 @@ __device__ __forceinline__ uint32_t kv_quantize_lane_q4(const float4 x, float& m
     m = warp_max(m);
     m_out = m;
     if (m == 0.0f) return 0x08080808u;
-    const float d = __fmul_rn(m, inv7());
-    auto code = [&](float v) -> uint32_t {
-        float r = roundf(__fdiv_rn(v, d));
-        r = fminf(fmaxf(r, -7.0f), 7.0f);
-        return (uint32_t)((int)r + 8);
-    };
-    return code(x.x) | (code(x.y) << 8) | (code(x.z) << 16) | (code(x.w) << 24);
+    const float4 n = round_quotients(x, __fmul_rn(m, inv7()), -7.0f, 7.0f);
+    return (uint32_t)((int)n.x + 8) | ((uint32_t)((int)n.y + 8) << 8) |
+           ((uint32_t)((int)n.z + 8) << 16) | ((uint32_t)((int)n.w + 8) << 24);
 }
 
 // One warp per (token, head) as above; lanes 2w and 2w+1 hold the 8 elements of
@@ -140,7 +182,7 @@ int launch_append(const kq8_cache_t& c, const float* k, const float* v, const in
                   int32_t T, uint32_t* status, cudaStream_t stream) {
     const int64_t items = (int64_t)T * c.num_kv_heads;
     if (items == 0) return KQ8_OK;
-    const int64_t blocks = (items + APPEND_WARPS - 1) / APPEND_WARPS;
+    const int64_t blocks = (items + APPEND_WARPS * APPEND_ITEMS - 1) / (APPEND_WARPS * APPEND_ITEMS);
     kq8_append_kernel<<<(unsigned)blocks, APPEND_WARPS * 32, 0, stream>>>(c, k, v, slot, T, status);
     return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
 }

@@ -13,9 +13,7 @@ static int launch_probe_g(const SparseParams& p, int B, int nkv, cudaStream_t s)
 
 template <int G>
 static int launch_topk_g(const SparseParams& p, int B, int nkv, cudaStream_t s) {
-    // one CTA per query head when the union can be left to the last of them
-    const bool per_head = p.tickets && !p.shared_sel && G > 1;
-    dim3 grid(nkv, B, per_head ? G : 1);
+    dim3 grid(nkv, B);
     kq8_topk_kernel<G><<<grid, TOPK_THREADS, 0, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
 }
@@ -41,14 +39,24 @@ int probe_blocks_per_cta(int block, int kv_bs) {
 }
 
 int launch_probe(const SparseParams& p, int G, int B, int nkv, cudaStream_t s) {
-    if (B == 0 || p.max_nblk == 0) return KQ8_OK;
+    if (B == 0) return KQ8_OK;
+    if (p.max_nblk == 0) {
+        if (!p.tickets) return KQ8_OK;
+        // every sequence is empty: CTA 0 of each (sequence, KV head) still
+        // writes its (empty) list and clears its selection
+        SparseParams q = p;
+        q.max_nblk = 1;
+        KQ8_SWITCH_G(launch_probe_g, q, B, nkv, s)
+    }
     if (p.probe_bpc < 1 || (long long)p.probe_bpc * p.block / p.cache.kv_bs + 1 > PROBE_MAX_PAGES)
         return KQ8_ERR_INVALID_ARG;
     KQ8_SWITCH_G(launch_probe_g, p, B, nkv, s)
 }
 
+// Only needed without tickets: otherwise the probe kernel's last CTA of each
+// (sequence, KV head) has already selected.
 int launch_topk(const SparseParams& p, int G, int B, int nkv, cudaStream_t s) {
-    if (B == 0) return KQ8_OK;
+    if (B == 0 || p.tickets) return KQ8_OK;
     KQ8_SWITCH_G(launch_topk_g, p, B, nkv, s)
 }
 

@@ -72,12 +72,15 @@ _lib.kq8_state_reset.argtypes = [_P, _P, _I32, _P]
 _lib.kq8_decode_attn_update.argtypes = [_P, _P, _P, _CP, _P, _I32, _P, _P, _I32, _I32, _I32,
                                         _I32, ctypes.c_float, _P, _SZ, _P]
 _lib.kq8_state_finalize.argtypes = [_P, _P, _P, _I32, _P]
+_lib.kq8_state_merge.argtypes = [_P, _P, _P, _P, _I32, _I32, _P]
 _lib.kq8_prefill_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32]
 _lib.kq8_prefill_workspace_bytes.restype = _SZ
 _lib.kq8_prefill_attn.argtypes = [_P, _P, _I32, _CP, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
                                   ctypes.c_float, _P, _SZ, _P]
 _lib.kq8_debug_prefill_withhold.argtypes = [_P, _P, _I32, _CP, _P, _I32, _P, _P, _I32, _I32,
                                             _I32, _I32, ctypes.c_float, _P, _SZ, _I32, _P]
+_lib.kq8_debug_decode_withhold.argtypes = [_P, _P, _CP, _P, _I32, _P, _I32, _I32, _I32,
+                                           ctypes.c_float, _P, _SZ, _I32, _P]
 _lib.kq8_sparse_prefill_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32]
 _lib.kq8_sparse_prefill_workspace_bytes.restype = _SZ
 _lib.kq8_sparse_prefill_attn.argtypes = [_P, _P, _I32, _CP, _P, _I32, _P, _P, _I32, _I32, _I32,
@@ -292,6 +295,21 @@ def kq8_decode_attn_noalloc(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCa
            "kq8_decode_attn_noalloc")
 
 
+def kq8_debug_decode_withhold(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
+                              page_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                              scale: float, workspace: torch.Tensor, withhold_tile: int,
+                              stream=None) -> None:
+    """Failure-detection hook (include/kq8.h): the exact decode with one tile
+    copy of every warp's walk never issued, so its bounded wait runs out."""
+    B, nq, max_pages = _decode_args(out, q, cache, page_table, seq_lens)
+    _check(_lib.kq8_debug_decode_withhold(_ptr(out), _ptr(q), ctypes.byref(cache.struct),
+                                          _ptr(page_table), max_pages, _ptr(seq_lens),
+                                          int(max_seq_len), B, nq, float(scale), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(),
+                                          int(withhold_tile), _stream(stream)),
+           "kq8_debug_decode_withhold")
+
+
 def kq8_sparse_decode_attn(out: torch.Tensor, q: torch.Tensor, cache: PagedKVCache,
                            page_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
                            scale: float, block: int, topk: int, probe: int,
@@ -354,6 +372,22 @@ def kq8_state_finalize(out: torch.Tensor, state: AttnState, stream=None) -> None
     rows = state.acc.numel() // HEAD_DIM
     _check(_lib.kq8_state_finalize(_ptr(out), _ptr(state.acc), _ptr(state.ms), rows,
                                    _stream(stream)), "kq8_state_finalize")
+
+
+def kq8_state_merge(state: AttnState, part_acc: torch.Tensor, part_ms: torch.Tensor,
+                    stream=None) -> None:
+    """Fold partial states part_acc [parts, B, nq, 128] / part_ms [parts, B, nq, 2]
+    (this library's state format, e.g. other ranks' states) into `state`."""
+    _dtype(part_acc, torch.float32, "part_acc")
+    _dtype(part_ms, torch.float32, "part_ms")
+    if (part_acc.dim() != 4 or part_acc.shape[1:] != state.acc.shape
+            or part_ms.shape != (part_acc.shape[0],) + tuple(state.ms.shape)):
+        raise ValueError("part_acc must be [parts, B, nq, 128] and part_ms [parts, B, nq, 2]")
+    if not (part_acc.is_contiguous() and part_ms.is_contiguous()):
+        raise ValueError("partial states must be contiguous")
+    rows = state.acc.numel() // HEAD_DIM
+    _check(_lib.kq8_state_merge(_ptr(state.acc), _ptr(state.ms), _ptr(part_acc), _ptr(part_ms),
+                                part_acc.shape[0], rows, _stream(stream)), "kq8_state_merge")
 
 
 def kq8_prefill_workspace_bytes(B: int, nq: int, nkv: int, max_seq_len: int,

@@ -20,11 +20,13 @@ from query_decode_attention_gb300 import kq8, paged  # noqa: E402
 DEV = "cuda:0"
 
 
-def _run(wl, q_lens, seed=0, kind="normal", pt_seed=None):
+def _run(wl, q_lens, seed=0, kind="normal", pt_seed=None, k_factor=1.0):
     """Cache of wl (its seq_lens include the new tokens), packed queries for
-    q_lens new tokens per sequence; returns (gpu out, oracle out, status)."""
+    q_lens new tokens per sequence; returns (gpu out, oracle out, status).
+    k_factor scales every key (a power of two scales every score exactly)."""
     q_lens = np.asarray(q_lens, np.int32)
     _, Ks, Vs = host_inputs(wl)
+    Ks = [(K * np.float32(k_factor)).astype(np.float32) for K in Ks]
     T = int(q_lens.sum())
     qp = np.random.default_rng(seed).standard_normal((T, wl.nq, wl.hd)).astype(np.float32)
     case = paged.fill_from_host(wl, Ks, Vs, DEV, pt_seed=pt_seed)
