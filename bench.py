@@ -36,7 +36,7 @@ METRIC = "q8-KV decode attention: effective KV GB/s and % of GB300 HBM peak"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-WORKLOADS = ("serving", "long", "sparse", "qwen2b", "prefill")
+WORKLOADS = ("serving", "long", "sparse", "qwen2b", "prefill", "append")
 
 
 def parse():
@@ -48,7 +48,8 @@ def parse():
     ap.add_argument("--workload", default="serving", choices=WORKLOADS,
                     help="serving: B=64 ragged 1K-32K, 36 layers (default); long: B=8 n=131072; "
                          "sparse: block-sparse B=16 n=65536; qwen2b: B=1 n=4059, 28 layers; "
-                         "prefill: the causal prefill kernel alone (Qwen3-VL prompts, TFLOP/s)")
+                         "prefill: the causal prefill kernel alone (Qwen3-VL prompts, TFLOP/s); "
+                         "append: the write path alone (8 x 4096 new tokens, GB/s)")
     ap.add_argument("--layers", type=int, default=36)
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],
@@ -329,6 +330,26 @@ def make_workload(args, rank):
     return W.qwen3vl_2b(4059, seed=2000 + rank), False
 
 
+def sparse_call_bytes(wl, sel):
+    """Bytes one block-sparse call must read: probe rows (K row + scale) of
+    every probed block plus whole 32-token tiles (K, V, scales) of the
+    per-KV-head union of kept blocks; gated sequences read all of their KV."""
+    total = 0
+    for b in range(wl.B):
+        n = int(wl.seq_lens[b])
+        if n <= 2 * wl.block:
+            total += -(-n // 32) * wl.nkv * 8448
+            continue
+        nblk = -(-n // wl.block)
+        rows = sum(len(range(j * wl.block, min((j + 1) * wl.block, n), wl.block // wl.probe)[:wl.probe])
+                   for j in range(nblk))
+        total += rows * wl.nkv * (wl.hd + 4)
+        for h in range(wl.nkv):
+            blocks = set(sel[b, h * wl.G:(h + 1) * wl.G].ravel().tolist()) - {-1}
+            total += sum(min(wl.block, n - j * wl.block) + 31 >> 5 for j in blocks) * 8448
+    return total
+
+
 class Scenario:
     """A workload resident on the device: one paged q8 pool per layer (round
     robin over fewer pools when memory is short), per-step inputs and the
@@ -423,25 +444,7 @@ class Scenario:
         return self.wl.kv_bytes_per_layer()
 
     def sparse_bytes_per_layer(self):
-        """Bytes the sparse call must read per layer: probe rows (K row +
-        scale) of every probed block plus whole 32-token tiles (K, V, scales)
-        of the per-KV-head union of kept blocks; gated sequences read all."""
-        wl = self.wl
-        sel = self.sel.cpu().numpy()
-        total = 0
-        for b in range(wl.B):
-            n = int(wl.seq_lens[b])
-            if n <= 2 * wl.block:
-                total += -(-n // 32) * wl.nkv * 8448
-                continue
-            nblk = -(-n // wl.block)
-            rows = sum(len(range(j * wl.block, min((j + 1) * wl.block, n), wl.block // wl.probe)[:wl.probe])
-                       for j in range(nblk))
-            total += rows * wl.nkv * (wl.hd + 4)
-            for h in range(wl.nkv):
-                blocks = set(sel[b, h * wl.G:(h + 1) * wl.G].ravel().tolist()) - {-1}
-                total += len(blocks) * (wl.block // 32) * 8448
-        return total
+        return sparse_call_bytes(self.wl, self.sel.cpu().numpy())
 
 
 def main():
@@ -452,6 +455,9 @@ def main():
         return
     if args.workload == "prefill":
         run_prefill_bench(args)
+        return
+    if args.workload == "append":
+        run_append_bench(args)
         return
 
     import torch
@@ -710,6 +716,229 @@ def run_prefill_bench(args):
                       "cases": res}))
 
 
+def _graph_step_ms(fn, dev, reps=20):
+    """Capture fn() (enqueueing on the current stream) as one CUDA graph and
+    time its replays: median ms per replay over reps, after 3 warm-ups."""
+    import torch
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        fn()  # eager warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    torch.cuda.synchronize()
+    return _time_calls(g.replay, reps, torch.cuda.current_stream(dev))
+
+
+def qwen2b_decode_steps(dev, kq8, paged, W, reps=20):
+    """The pages' own decode configuration (article 10-1 Table B): Qwen3-VL-2B,
+    batch 1, 28 layers, contexts 506 / 2046 / 4059; one step = per layer the
+    new token's append and exact or block-sparse (block 32, k 32, probe 8)
+    decode attention, replayed as one CUDA graph (its per-layer GPU work is
+    shorter than the host launch path).  28 distinct layer pools (> L2 at
+    n = 4059: 240 MB)."""
+    import torch
+    res = {}
+    for n in (506, 2046, 4059):
+        wl = W.qwen3vl_2b(n)
+        cases = [paged.fill_cache(wl, layer, dev) for layer in range(wl.layers)]
+        L, B, nq, nkv, hd = wl.layers, wl.B, wl.nq, wl.nkv, wl.hd
+        g = W.device_generator(dev, 11 + n)
+        kn = torch.randn((L, B, nkv, hd), generator=g, device=dev)
+        vn = torch.randn((L, B, nkv, hd), generator=g, device=dev)
+        slot = torch.tensor(cases[0].slots(0, n - 1, n), dtype=torch.int32, device=dev)
+        out = torch.empty((L, B, nq, hd), device=dev)
+        wse = kq8.new_workspace(kq8.kq8_decode_workspace_bytes(B, nq, nkv, n), dev)
+        wss = kq8.new_workspace(kq8.kq8_sparse_decode_workspace_bytes(B, nq, nkv, n, 32, 32), dev)
+
+        def step(sparse):
+            st = torch.cuda.current_stream(dev)
+            for layer, c in enumerate(cases):
+                kq8.kq8_append_kv(c.cache, kn[layer], vn[layer], slot, stream=st)
+                if sparse:
+                    kq8.kq8_sparse_decode_attn(out[layer], c.q, c.cache, c.page_table, c.seq_lens,
+                                               n, wl.scale, 32, 32, 8, wss, stream=st)
+                else:
+                    kq8.kq8_decode_attn(out[layer], c.q, c.cache, c.page_table, c.seq_lens, n,
+                                        wl.scale, wse, stream=st)
+        ms_ex = _graph_step_ms(lambda: step(False), dev, reps)
+        ms_sp = _graph_step_ms(lambda: step(True), dev, reps)
+        kv = wl.kv_bytes_per_layer() * L
+        res[f"n{n}"] = {"exact_ms_per_token": round(ms_ex, 4),
+                        "sparse_k32_ms_per_token": round(ms_sp, 4),
+                        "sparse_speedup_vs_exact": round(ms_ex / ms_sp, 3),
+                        "exact_us_per_layer": round(1e3 * ms_ex / L, 2),
+                        "exact_kv_GB/s": round(kv / (ms_ex * 1e-3) / 1e9, 1),
+                        "kv_bytes_per_token": kv,
+                        "status_words": [kq8.kq8_read_status(wse), kq8.kq8_read_status(wss)]}
+        del cases, kn, vn, out, wse, wss
+        torch.cuda.empty_cache()
+    res["step"] = ("28 layers x (append 1 token + decode attention), one CUDA graph; "
+                   "the pages' RK3588 figures for the same step: exact 9.7 / 48.9 / 110.7 ms, "
+                   "sparse 13.4 / 39.1 / 55.4 ms (context, not a target)")
+    return res
+
+
+def sparse_sweep(dev, kq8, paged, W, peak, reps=10):
+    """The block-sparse configuration over its context lengths (B = 16, 16/8
+    heads, block 32, k 32, probe 8, 32 planted blocks per (sequence, KV head)):
+    exact vs block-sparse vs shared-selection decode, one call each, timed
+    alone (median of reps).  n = 64 is at the gate (the exact kernel runs).
+    frac_of_peak: the union of kept tiles plus the probe rows read, per call
+    time, against the measured HBM peak.  Returns the results and, for the CPU
+    baseline, the host inputs of the n = 4059 case."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    res, keep = {}, None
+    for n in (64, 506, 4059, 16384, 65536):
+        wl = W.sparse_planted(n, B=16)
+        q = W.host_q(wl)
+        Ks, Vs = zip(*[W.host_kv(wl, b, q=q) for b in range(wl.B)])
+        case = paged.fill_from_host(wl, list(Ks), list(Vs), dev, q_host=q)
+        if n == 4059:
+            keep = (wl, q, list(Ks), list(Vs))
+        del Ks, Vs
+        out = torch.empty((wl.B, wl.nq, wl.hd), device=dev)
+        ws = kq8.new_workspace(kq8.kq8_sparse_decode_workspace_bytes(
+            wl.B, wl.nq, wl.nkv, wl.max_seq_len, wl.block, wl.topk), dev)
+        sel = torch.empty((wl.B, wl.nq, wl.topk), dtype=torch.int32, device=dev)
+        wsx = kq8.new_workspace(kq8.kq8_decode_workspace_bytes(wl.B, wl.nq, wl.nkv,
+                                                               wl.max_seq_len), dev)
+        args = (case.q, case.cache, case.page_table, case.seq_lens, wl.max_seq_len, wl.scale)
+        ms = _time_calls(lambda: kq8.kq8_sparse_decode_attn(
+            out, *args, wl.block, wl.topk, wl.probe, ws, sel_blocks=sel, stream=stream),
+            reps, stream)
+        ms_ex = _time_calls(lambda: kq8.kq8_decode_attn(out, *args, wsx, stream=stream), reps,
+                            stream)
+        ms_sh = _time_calls(lambda: kq8.kq8_sparse_decode_attn_shared(
+            out, *args, wl.block, wl.topk, wl.probe, ws, stream=stream), reps, stream)
+        nbytes = sparse_call_bytes(wl, sel.cpu().numpy())
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[f"n{n}"] = {"sparse_ms": round(ms, 4), "exact_ms": round(ms_ex, 4),
+                        "shared_selection_ms": round(ms_sh, 4),
+                        "speedup_vs_exact": round(ms_ex / ms, 3),
+                        "sparse_bytes_read": nbytes, "sparse_GB/s": round(gbs, 1),
+                        "frac_of_peak": round(gbs / peak, 4),
+                        "exact_GB/s": round(wl.kv_bytes_per_layer() / (ms_ex * 1e-3) / 1e9, 1),
+                        "status_words": [kq8.kq8_read_status(ws), kq8.kq8_read_status(wsx)]}
+        del case, out, ws, wsx, sel
+        torch.cuda.empty_cache()
+    return res, keep
+
+
+def oracle_config_baselines(keep, W, seconds=4.0):
+    """The CPU oracle on the pages' configurations' full inputs: the
+    Qwen3-VL-2B decode step (28 layers, n = 4059, exact) and one block-sparse
+    layer (B = 16, n = 4059, block 32, k 32, probe 8), OpenMP over
+    (sequence, head)."""
+    import oracle
+    oracle.build()
+    threads = oracle_threads()
+    cores = threads if oracle.openmp_threads() else 1
+    res = {}
+    wl = W.qwen3vl_2b(4059)
+    layers = []
+    for layer in range(wl.layers):
+        K, V = W.host_kv(wl, 0, layer)
+        k8, ks = oracle.kv_quantize_rows(K)
+        v8, vs = oracle.kv_quantize_rows(V)
+        layers.append((W.host_q(wl, layer), k8, ks, v8, vs))
+
+    def step():
+        for q, k8, ks, v8, vs in layers:
+            oracle.decode_batch(q, [k8], [ks], [v8], [vs], wl.scale, nthreads=threads)
+    step()
+    passes, t = 0, 0.0
+    while t < seconds:
+        t0 = time.perf_counter()
+        step()
+        t += time.perf_counter() - t0
+        passes += 1
+    ms = 1e3 * t / passes
+    res["qwen3vl2b_n4059_28_layers"] = {
+        "ms_per_token": round(ms, 3), "cores": cores,
+        "GB/s": round(wl.kv_bytes_per_layer() * wl.layers / (ms * 1e-3) / 1e9, 4),
+        "sample": f"the full 28-layer step, exact decode, {passes} passes"}
+    if keep is not None:
+        wl, q, Ks, Vs = keep
+        k8s, kss, v8s, vss = [], [], [], []
+        for K, V in zip(Ks, Vs):
+            k8, ks = oracle.kv_quantize_rows(K)
+            v8, vs = oracle.kv_quantize_rows(V)
+            k8s.append(k8), kss.append(ks), v8s.append(v8), vss.append(vs)
+        for sparse in (True, False):
+            run = lambda: oracle.decode_batch(q, k8s, kss, v8s, vss, wl.scale, sparse=sparse,
+                                              block=wl.block, topk=wl.topk, probe=wl.probe,
+                                              nthreads=threads)
+            run()
+            passes, t = 0, 0.0
+            while t < seconds / 2:
+                t0 = time.perf_counter()
+                run()
+                t += time.perf_counter() - t0
+                passes += 1
+            ms = 1e3 * t / passes
+            res[f"sparse_cfg_B16_n4059_{'sparse' if sparse else 'exact'}"] = {
+                "ms_per_call": round(ms, 3), "cores": cores,
+                "exact_equivalent_GB/s": round(wl.kv_bytes_per_layer() / (ms * 1e-3) / 1e9, 4),
+                "sample": f"all 16 sequences and 16 query heads of one layer, {passes} passes"}
+    return res
+
+
+def append_case(dev, kq8, paged, W, T_per_seq=4096, B=8):
+    """The write path of the long-context configuration: B x T_per_seq new
+    tokens (fp32 K/V, 8 KV heads) quantised into a paged pool of exactly their
+    pages (random page order); inputs 268 MB, far beyond L2."""
+    import torch
+    wl = W.custom(B, 16, 8, [T_per_seq] * B, seed=4000, name="append_8x4096")
+    cache, pt = paged.new_cache(wl, device=dev)
+    T = B * T_per_seq
+    g = W.device_generator(dev, 99)
+    kn = torch.randn((T, wl.nkv, wl.hd), generator=g, device=dev)
+    vn = torch.randn((T, wl.nkv, wl.hd), generator=g, device=dev)
+    sl = torch.tensor(W.all_slots(wl, pt), dtype=torch.int32, device=dev)
+    nbytes = T * wl.nkv * (2 * wl.hd * 4 + 2 * wl.hd + 8)  # fp32 K+V read, codes + maxima written
+    return wl, cache, kn, vn, sl, nbytes
+
+
+def run_append_bench(args):
+    """--workload append: kq8_append_kv alone, one JSON line (GB/s of fp32
+    read plus q8 written, against the measured HBM peak)."""
+    import torch
+    from query_decode_attention_gb300 import build as kbuild
+    kbuild.build()
+    from query_decode_attention_gb300 import kq8, paged
+    from query_decode_attention_gb300 import workloads as W
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    wl, cache, kn, vn, sl, nbytes = append_case(dev, kq8, paged, W)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(max(3, args.warmup)):
+        kq8.kq8_append_kv(cache, kn, vn, sl, status=st, stream=stream)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in evs:
+        a.record(stream)
+        kq8.kq8_append_kv(cache, kn, vn, sl, status=st, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+    peak, kind = measured_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({"metric": "q8 KV append (write path) GB/s", "value": round(gbs, 1),
+                      "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "higher_is_better": True,
+                      "config": {"workload": wl.name, "tokens": int(sl.numel()), "nkv": wl.nkv},
+                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                                   "unit": "GB/s", "frac": round(gbs / peak, 4),
+                                   "peak_kind": f"{kind} hbm_gbs", "bytes_per_launch": nbytes,
+                                   "launch_ms": round(ms, 5)},
+                      "status_word": kq8.kq8_read_status(st)}))
+
+
 def extras(dev, kq8, paged, W, peak):
     """Secondary measurements: long-context exact decode, the streaming form,
     the write path and the block-sparse path (each timed alone with CUDA
@@ -747,18 +976,14 @@ def extras(dev, kq8, paged, W, peak):
     res["long_context_streamed_8_pieces"] = {"ms": round(ms_s, 4), "GB/s": round(gbs_s, 1),
                                              "frac_of_peak": round(gbs_s / peak, 4),
                                              "vs_one_call": round(ms / ms_s, 3)}
-    # write path: 8 x 4096 new tokens into that cache
-    T = 8 * 4096
-    g = W.device_generator(dev, 99)
-    kn = torch.randn((T, wl.nkv, wl.hd), generator=g, device=dev)
-    vn = torch.randn((T, wl.nkv, wl.hd), generator=g, device=dev)
-    sl = torch.tensor(np.concatenate([case.slots(b, 0, 4096) for b in range(8)]), dtype=torch.int32,
-                      device=dev)
-    ms = _time_calls(lambda: kq8.kq8_append_kv(case.cache, kn, vn, sl, stream=stream), 20, stream)
-    ab = T * wl.nkv * (2 * wl.hd * 4 + 2 * wl.hd + 8)
+    del case, out
+    torch.cuda.empty_cache()
+    # write path: 8 x 4096 new tokens
+    _, acache, kn, vn, sl, ab = append_case(dev, kq8, paged, W)
+    ms = _time_calls(lambda: kq8.kq8_append_kv(acache, kn, vn, sl, stream=stream), 20, stream)
     res["append_8x4096"] = {"ms": round(ms, 4), "GB/s": round(ab / (ms * 1e-3) / 1e9, 1),
                             "bytes": ab, "frac_of_peak": round(ab / (ms * 1e-3) / 1e9 / peak, 4)}
-    del case, out, kn, vn
+    del acache, kn, vn
     torch.cuda.empty_cache()
     # q4 cache: the serving shape (B = 64, ragged 1K-32K, one layer) read through
     # kq8_decode_attn_q4; per (token, KV head) 64 + 64 B of codes + 8 B of scales
@@ -776,37 +1001,17 @@ def extras(dev, kq8, paged, W, peak):
                                "bytes": b4, "status_word": kq8.kq8_read_status(ws4)}
     del case4, out4, ws4
     torch.cuda.empty_cache()
-    # block-sparse: B = 16, n = 65536, block 32, k 32, probe 8 (host-drawn planted inputs)
-    wl = W.sparse_planted(65536, B=16)
-    q = W.host_q(wl)
-    Ks, Vs = zip(*[W.host_kv(wl, b, q=q) for b in range(wl.B)])
-    case = paged.fill_from_host(wl, list(Ks), list(Vs), dev, q_host=q)
-    del Ks, Vs
-    out = torch.empty((wl.B, wl.nq, wl.hd), device=dev)
-    nb = kq8.kq8_sparse_decode_workspace_bytes(wl.B, wl.nq, wl.nkv, wl.max_seq_len, wl.block,
-                                               wl.topk)
-    ws = kq8.new_workspace(nb, dev)
-    ms = _time_calls(lambda: kq8.kq8_sparse_decode_attn(out, case.q, case.cache, case.page_table,
-                                                        case.seq_lens, wl.max_seq_len, wl.scale,
-                                                        wl.block, wl.topk, wl.probe, ws,
-                                                        stream=stream), 10, stream)
-    wsx = kq8.new_workspace(kq8.kq8_decode_workspace_bytes(wl.B, wl.nq, wl.nkv, wl.max_seq_len), dev)
-    ms_ex = _time_calls(lambda: kq8.kq8_decode_attn(out, case.q, case.cache, case.page_table,
-                                                    case.seq_lens, wl.max_seq_len, wl.scale, wsx,
-                                                    stream=stream), 10, stream)
-    ms_sh = _time_calls(lambda: kq8.kq8_sparse_decode_attn_shared(
-        out, case.q, case.cache, case.page_table, case.seq_lens, wl.max_seq_len, wl.scale,
-        wl.block, wl.topk, wl.probe, ws, stream=stream), 10, stream)
-    nblk = -(-65536 // wl.block)
-    probe_bytes = wl.B * wl.nkv * nblk * wl.probe * (wl.hd + 4)
-    sel_bytes = wl.B * wl.nq * wl.topk * wl.block * (2 * wl.hd + 8)
-    res["sparse_n65536"] = {"workload": wl.name, "ms": round(ms, 4), "exact_ms": round(ms_ex, 4),
-                            "speedup_vs_exact": round(ms_ex / ms, 2),
-                            "shared_selection_ms": round(ms_sh, 4),
-                            "probe_plus_selected_bytes": probe_bytes + sel_bytes,
-                            "exact_GB/s": round(wl.kv_bytes_per_layer() / (ms_ex * 1e-3) / 1e9, 1)}
-    del case, out, ws, wsx
-    torch.cuda.empty_cache()
+    # block-sparse configuration over its context lengths, then the pages' own
+    # Qwen3-VL-2B decode step, then the CPU oracle on those configurations
+    sweep, keep = sparse_sweep(dev, kq8, paged, W, peak)
+    res["sparse_sweep_B16"] = sweep
+    res["sparse_n65536"] = {"workload": "sparse_n65536", "ms": sweep["n65536"]["sparse_ms"],
+                            "exact_ms": sweep["n65536"]["exact_ms"],
+                            "speedup_vs_exact": sweep["n65536"]["speedup_vs_exact"],
+                            "frac_of_peak": sweep["n65536"]["frac_of_peak"]}
+    res["qwen3vl2b_decode_step_B1_28_layers"] = qwen2b_decode_steps(dev, kq8, paged, W)
+    res["cpu_oracle_pages_configs"] = oracle_config_baselines(keep, W)
+    del keep
     # causal prefill of whole prompts on the tensor cores
     res["prefill"] = prefill_measure(dev, kq8, paged, W, measured_bf16_peak()[0])
     return res
