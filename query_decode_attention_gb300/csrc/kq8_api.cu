@@ -1,8 +1,11 @@
 // kq8_api.cu -- the C ABI of libkq8 (declared in include/kq8.h): argument
 // checks, workspace planning and kernel dispatch.  All compute runs in the
 // CUDA kernels; this file only validates, plans and launches.
+#include <cudaTypedefs.h>
+
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "kq8_attn.cuh"
 #include "kq8_internal.h"
@@ -178,6 +181,41 @@ AttnParams attn_params(float* out, const float* q, const kq8_cache_t* c, const i
     return p;
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link to the
+// driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The q8 V array as the 3-D tensor the attention kernel copies sub-tiles of:
+// {128 bytes, kv_bs rows, num_pages * nkv (page, head) pairs}, boxes of 32 rows,
+// 128-byte swizzle in shared memory.
+int set_vmap(AttnParams& p) {
+    const kq8_cache_t& c = p.cache;
+    const uint64_t pairs = (uint64_t)c.num_pages * (uint64_t)c.num_kv_heads;
+    if (pairs > 0x7FFFFFFFull) return KQ8_ERR_UNSUPPORTED;  // the copy's coordinate is int32
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return KQ8_ERR_CUDA;
+    const cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)c.kv_bs, (cuuint64_t)pairs};
+    const cuuint64_t strides[2] = {(cuuint64_t)HD, (cuuint64_t)c.kv_bs * HD};
+    const cuuint32_t box[3] = {(cuuint32_t)HD, (cuuint32_t)TILE, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = enc(&p.vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.v, dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? KQ8_OK : KQ8_ERR_CUDA;
+}
+
 // Probe, top-k and bounded attention over `rows` decode rows (article 10-1
 // §1-§2); row_seq (optional) maps each row to its page-table row.
 int run_sparse(float* out, const float* q, const kq8_cache_t* cache, const int32_t* page_table,
@@ -230,6 +268,8 @@ int run_sparse(float* out, const float* q, const kq8_cache_t* cache, const int32
     p.list_len = sp.list_len;
     p.list_cap = sp.list_cap;
     p.row_seq = row_seq;
+    rc = set_vmap(p);
+    if (rc) return rc;
     return launch_attn(p, G, true, rows, nkv, s);
 }
 
@@ -358,6 +398,8 @@ int kq8_decode_attn(float* out, const float* q, const kq8_cache_t* cache,
     if (B == 0) return KQ8_OK;
     AttnParams p = attn_params(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq,
                                scale, plan, workspace);
+    rc = set_vmap(p);
+    if (rc) return rc;
     return launch_attn(p, nq / nkv, false, B, nkv, (cudaStream_t)stream);
 }
 
@@ -463,6 +505,8 @@ int kq8_decode_attn_update(float* state_acc, float* state_ms, const float* q,
     p.seq_begin = seq_begin;
     p.state_acc = state_acc;
     p.state_ms = reinterpret_cast<float2*>(state_ms);
+    rc = set_vmap(p);
+    if (rc) return rc;
     return launch_attn(p, nq / nkv, false, B, nkv, (cudaStream_t)stream);
 }
 
@@ -530,6 +574,8 @@ int kq8_debug_decode_withhold(float* out, const float* q, const kq8_cache_t* cac
     AttnParams p = attn_params(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq,
                                scale, plan, workspace);
     p.withhold = withhold_tile;
+    rc = set_vmap(p);
+    if (rc) return rc;
     return launch_attn_withhold(p, nq / nkv, B, nkv, (cudaStream_t)stream);
 }
 
@@ -626,5 +672,7 @@ extern "C" int kq8_decode_attn_noalloc(float* out, const float* q, const kq8_cac
     // collects error bits that this entry point does not report.
     AttnParams p = attn_params(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq,
                                scale, plan, ws);
+    rc = set_vmap(p);
+    if (rc) return rc;
     return launch_attn(p, nq / nkv, false, B, nkv, (cudaStream_t)stream);
 }

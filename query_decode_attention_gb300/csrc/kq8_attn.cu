@@ -4,10 +4,12 @@
 
 namespace kq8 {
 
+size_t attn_smem_bytes(int G);
+
 template <int G, bool SPARSE, bool Q4, bool WITHHOLD = false>
 static int launch_attn_g(const AttnParams& p, int B, int nkv, cudaStream_t s) {
     auto kern = kq8_attn_kernel<G, SPARSE, Q4, WITHHOLD>;
-    const size_t smem = sizeof(AttnSmem<G>);
+    const size_t smem = attn_smem_bytes(G);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return KQ8_ERR_CUDA;
@@ -112,17 +114,21 @@ int launch_state_finalize(float* out, const float* acc, const float2* ms, int ro
     return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
 }
 
+// Dynamic shared memory of the attention kernel: its AttnSmem plus 1 KB of
+// slack to align the V tiles to 1024 bytes.
 size_t attn_smem_bytes(int G) {
+    size_t b;
     switch (G) {
-        case 1: return sizeof(AttnSmem<1>);
-        case 2: return sizeof(AttnSmem<2>);
-        case 3: return sizeof(AttnSmem<3>);
-        case 4: return sizeof(AttnSmem<4>);
-        case 5: return sizeof(AttnSmem<5>);
-        case 6: return sizeof(AttnSmem<6>);
-        case 7: return sizeof(AttnSmem<7>);
-        default: return sizeof(AttnSmem<8>);
+        case 1: b = sizeof(AttnSmem<1>); break;
+        case 2: b = sizeof(AttnSmem<2>); break;
+        case 3: b = sizeof(AttnSmem<3>); break;
+        case 4: b = sizeof(AttnSmem<4>); break;
+        case 5: b = sizeof(AttnSmem<5>); break;
+        case 6: b = sizeof(AttnSmem<6>); break;
+        case 7: b = sizeof(AttnSmem<7>); break;
+        default: b = sizeof(AttnSmem<8>); break;
     }
+    return b + 1024;
 }
 
 }  // namespace kq8

@@ -49,6 +49,10 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_SLACK = 8.0f;
 
 struct AttnParams {
+    // V sub-tiles of a q8 cache as a 3-D tensor {128 B, kv_bs rows, num_pages *
+    // nkv}, copied into shared memory with the 128-byte swizzle (the value
+    // phase reads them with conflict-free ldmatrix); unused for q4 caches
+    CUtensorMap vmap;
     float* out;
     const float* q;
     kq8_cache_t cache;
@@ -92,9 +96,17 @@ struct AttnShape {
 
 template <int G>
 struct AttnSmem {
-    alignas(128) uint8_t stage[ATTN_WARPS][ATTN_STAGES][STAGE_BYTES];
-    // per K position: (p_g, p_g, p_g+1, p_g+1) for each head pair, p = w * vs
-    alignas(16) float4 p[ATTN_WARPS][TILE][AttnShape<G>::GP];
+    // per warp and stage: a V sub-tile (q8: 128-byte swizzled by the tensor
+    // copy, so 1024-byte aligned; q4: 2 KB of rows), a K sub-tile, the scales
+    alignas(1024) uint8_t v[ATTN_WARPS][ATTN_STAGES][SUB_V_BYTES];
+    alignas(128) uint8_t k[ATTN_WARPS][ATTN_STAGES][SUB_K_BYTES];
+    alignas(16) float sc[ATTN_WARPS][ATTN_STAGES][2][TILE];  // kscale, vscale
+    // q8: the weights as fp16 (hi, lo) pairs per (head, token slot sigma(t));
+    // q4: per K position (p_g, p_g, p_g+1, p_g+1) for each head pair
+    union {
+        alignas(16) uint32_t pw[ATTN_WARPS][G][TILE];
+        alignas(16) float4 p[ATTN_WARPS][TILE][AttnShape<G>::GP];
+    };
     alignas(16) int8_t qi[G][HD];
     alignas(16) float qsc[G][NB];
     int qsum[G][NB];  // sum of each 32-element block's Q codes (q4 cache only)
@@ -213,13 +225,16 @@ __device__ __forceinline__ void fold_state(float mo, float so, float m, float s,
 // production instantiations compile the check out.
 template <int G, bool SPARSE, bool Q4 = false, bool WITHHOLD = false>
 __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
-    kq8_attn_kernel(const AttnParams P) {
+    kq8_attn_kernel(const __grid_constant__ AttnParams P) {
     using Sh = AttnShape<G>;
     constexpr int E = Sh::E, NC = Sh::NC, TG = Sh::TG, GP = Sh::GP;
     constexpr int EP = E / 2;  // float2 pairs per head per lane
     constexpr int NS = ATTN_STAGES;
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    AttnSmem<G>& S = *reinterpret_cast<AttnSmem<G>*>(smem_raw);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the swizzled tensor copies want 1024-byte aligned V tiles: the launch
+    // adds 1 KB of slack to round the base up
+    AttnSmem<G>& S = *reinterpret_cast<AttnSmem<G>*>(
+        smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -279,7 +294,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     fence_barrier_init();
     __syncthreads();
 
-    const uint64_t pol = l2_evict_first_policy();
     // all lanes call this (it shuffles); lane 0 issues the stage's copies
     auto issue = [&](int i) {
         const int tile = __shfl_sync(0xffffffffu, my_tile, i);
@@ -287,34 +301,41 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
         if (WITHHOLD && i == P.withhold) return;  // test hook: the phase never completes
         if (lane == 0) {
             uint64_t* bar = &S.bar[warp][i % NS];
+            const uint64_t pol = l2_evict_first_policy();  // every KV byte is read once
             if (pg < 0) {
                 mbar_arrive_expect_tx(bar, 0);  // completes the phase with no data
             } else {
                 const int sub = tile % subs;
-                uint8_t* st = S.stage[warp][i % NS];
+                const int s = i % NS;
                 const size_t so = scale_sub_off(pg, h, nkv, kv_bs, sub);
-                if (Q4) {  // half-size codes at the q8 stage offsets
+                if (Q4) {  // half-size codes
                     const size_t kvo = kv4_sub_off(pg, h, nkv, kv_bs, sub);
                     mbar_arrive_expect_tx(bar, SUB_K4_BYTES + SUB_V4_BYTES + 2 * SUB_S_BYTES);
-                    bulk_g2s(st, P.cache.k + kvo, SUB_K4_BYTES, bar, pol);
-                    bulk_g2s(st + SUB_K_BYTES, P.cache.v + kvo, SUB_V4_BYTES, bar, pol);
+                    bulk_g2s(S.k[warp][s], P.cache.k + kvo, SUB_K4_BYTES, bar, pol);
+                    bulk_g2s(S.v[warp][s], P.cache.v + kvo, SUB_V4_BYTES, bar, pol);
                 } else {
-                    const size_t kvo = kv_sub_off(pg, h, nkv, kv_bs, sub);
                     mbar_arrive_expect_tx(bar, STAGE_BYTES);
-                    bulk_g2s(st, P.cache.k + kvo, SUB_K_BYTES, bar, pol);
-                    bulk_g2s(st + SUB_K_BYTES, P.cache.v + kvo, SUB_V_BYTES, bar, pol);
+                    bulk_g2s(S.k[warp][s], P.cache.k + kv_sub_off(pg, h, nkv, kv_bs, sub),
+                             SUB_K_BYTES, bar, pol);
+                    tma_load_3d(S.v[warp][s], &P.vmap, 0, sub * TILE, (int)page_head(pg, h, nkv),
+                                bar, pol);
                 }
-                bulk_g2s(st + SUB_K_BYTES + SUB_V_BYTES, P.cache.kscale + so, SUB_S_BYTES, bar,
-                         pol);
-                bulk_g2s(st + SUB_K_BYTES + SUB_V_BYTES + SUB_S_BYTES, P.cache.vscale + so,
-                         SUB_S_BYTES, bar, pol);
+                bulk_g2s(S.sc[warp][s][0], P.cache.kscale + so, SUB_S_BYTES, bar, pol);
+                bulk_g2s(S.sc[warp][s][1], P.cache.vscale + so, SUB_S_BYTES, bar, pol);
             }
         }
     };
     for (int i = 0; i < NS && i < mine; i++) issue(i);
 
     float M2[G], Sl[G];
-    float2 acc[G][EP];
+    float2 acc[G][EP];  // q4: lane (tg, c) accumulates elements c*E.. of every head
+    // q8: the value phase runs on the tensor cores.  Per 16-element chunk cg, an
+    // m16n8k16 tile pair D[cg][0..3] (elements 16cg + 2j) and D[cg][4..7]
+    // (16cg + 2j + 1), rows 0..7 = head (weight hi), 8..15 = head (weight lo):
+    // lane (g, c) holds head g's elements 16cg + 4c .. 16cg + 4c + 3
+    float D[HD / 16][2][4];
+    // q8 weights go to the tensor cores as fp16 scaled by 2^-ev (see below)
+    int ev = -149;
 #pragma unroll
     for (int g = 0; g < G; g++) {
         M2[g] = M_INIT;
@@ -322,6 +343,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
 #pragma unroll
         for (int e = 0; e < EP; e++) acc[g][e] = make_float2(0.0f, 0.0f);
     }
+#pragma unroll
+    for (int cg = 0; cg < HD / 16; cg++)
+#pragma unroll
+        for (int j = 0; j < 4; j++) D[cg][0][j] = D[cg][1][j] = 0.0f;
+    const int gq = lane >> 2, c4 = lane & 3;  // mma fragment coordinates
     float2 qsc2[GP][NB];  // block scales of head pairs (2gp, 2gp+1)
 #pragma unroll
     for (int gp = 0; gp < GP; gp++)
@@ -330,7 +356,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             qsc2[gp][bb] = make_float2(S.qsc[2 * gp][bb], S.qsc[min(2 * gp + 1, G - 1)][bb]);
     // stored K max -> step (1/127); the softmax scale is applied after it
     const float kstep = Q4 ? inv7() : inv127();
-    const float2 scale2 = make_float2(P.scale, P.scale);
 
     bool failed = false;
     int i = 0;
@@ -346,11 +371,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             break;
         }
         if (pg >= 0) {
-            const uint8_t* st = S.stage[warp][i % NS];
-            const int8_t* kst = reinterpret_cast<const int8_t*>(st);
-            const int8_t* vst = reinterpret_cast<const int8_t*>(st + SUB_K_BYTES);
-            const float* kss = reinterpret_cast<const float*>(st + SUB_K_BYTES + SUB_V_BYTES);
-            const float* vss = kss + TILE;
+            const int8_t* kst = reinterpret_cast<const int8_t*>(S.k[warp][i % NS]);
+            const int8_t* vst = reinterpret_cast<const int8_t*>(S.v[warp][i % NS]);
+            const float* kss = S.sc[warp][i % NS][0];
+            const float* vss = S.sc[warp][i % NS][1];
 
             // ---- score phase: lane q reads K position q, i.e. token row
             // t = krow(q) of the tile, and scores it for all G heads
@@ -420,7 +444,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                     s = __fadd2_rn(s, __fmul2_rn(make_float2(__int2float_rn(dot[2 * gp][bb]),
                                                              __int2float_rn(dot[g1][bb])),
                                                  qsc2[gp][bb]));
-                s = __fmul2_rn(__fmul2_rn(s, make_float2(ks, ks)), scale2);
+                s = __fmul2_rn(__fmul2_rn(s, make_float2(ks, ks)), make_float2(P.scale, P.scale));
                 sv[2 * gp] = s.x;
                 sv[2 * gp + 1] = s.y;
             }
@@ -444,18 +468,31 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             }
             if (__any_sync(0xffffffffu, grow)) {
                 // rare: some head's maximum grew by a wide margin -> rescale its state
+                float cl = 1.0f;  // q8: the factor of this lane's accumulator head gq
 #pragma unroll
                 for (int g = 0; g < G; g++) {
                     const float mn = fmaxf(M2[g], warp_max(sv[g]));
                     if (mn > M2[g]) {
                         const float c = exp_diff(M2[g], mn);
                         Sl[g] *= c;
+                        if (Q4) {
 #pragma unroll
-                        for (int e = 0; e < EP; e++)
-                            acc[g][e] = __fmul2_rn(acc[g][e], make_float2(c, c));
+                            for (int e = 0; e < EP; e++)
+                                acc[g][e] = __fmul2_rn(acc[g][e], make_float2(c, c));
+                        }
+                        cl = (g == gq) ? c : cl;
                         M2[g] = mn;
                         dd[g] = (sv[g] - mn) * LOG2E;
                     }
+                }
+                if (!Q4) {
+#pragma unroll
+                    for (int cg = 0; cg < HD / 16; cg++)
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            D[cg][0][j] *= cl;
+                            D[cg][1][j] *= cl;
+                        }
                 }
             }
             float w[2 * GP];
@@ -465,18 +502,103 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                 Sl[g] += w[g];
             }
             if constexpr ((G & 1) != 0) w[G] = 0.0f;
+            if (Q4) {
 #pragma unroll
-            for (int gp = 0; gp < GP; gp++) {
-                const float2 pp = __fmul2_rn(make_float2(w[2 * gp], w[2 * gp + 1]),
-                                             make_float2(vstep, vstep));
-                // masked tokens have w = 0; their (possibly stale) scale must not leak in
-                const float p0 = (w[2 * gp] != 0.0f) ? pp.x : 0.0f;
-                const float p1 = (w[2 * gp + 1] != 0.0f) ? pp.y : 0.0f;
-                S.p[warp][q][gp] = make_float4(p0, p0, p1, p1);  // by K position
+                for (int gp = 0; gp < GP; gp++) {
+                    const float2 pp = __fmul2_rn(make_float2(w[2 * gp], w[2 * gp + 1]),
+                                                 make_float2(vstep, vstep));
+                    // masked tokens have w = 0; their (possibly stale) scale must not leak in
+                    const float p0 = (w[2 * gp] != 0.0f) ? pp.x : 0.0f;
+                    const float p1 = (w[2 * gp + 1] != 0.0f) ? pp.y : 0.0f;
+                    S.p[warp][q][gp] = make_float4(p0, p0, p1, p1);  // by K position
+                }
+            } else {
+                // weights for the tensor cores: P' = w * vstep * 2^-ev as fp16 hi + lo
+                // (22 significant bits).  ev keeps the tile's largest live V step
+                // times 2^-ev below 2^7, so with w <= 2^8 (the lazy rescale bound)
+                // P' < 2^15, inside the fp16 range; a tile that needs a larger ev
+                // first scales the accumulators by the exact power of two 2^(old - new)
+                const uint32_t vb = __reduce_max_sync(
+                    0xffffffffu, (live && mask != 0u) ? __float_as_uint(vstep) : 0u);
+                const int ve = (int)(vb >> 23) - 127;
+                if (vb != 0u && ve > ev + 6) {  // warp-uniform, rare
+                    const int en = ve - 6;
+                    const float f = (ev - en >= -126) ? pow2i(ev - en) : 0.0f;
+#pragma unroll
+                    for (int cg = 0; cg < HD / 16; cg++)
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            D[cg][0][j] *= f;
+                            D[cg][1][j] *= f;
+                        }
+                    ev = en;
+                }
+                const int k1 = min(max(-ev, -126), 127);
+                const float vsc = __fmul_rn(__fmul_rn(vstep, pow2i(k1)),
+                                            pow2i(min(max(-ev - k1, -126), 127)));
+                // token t's slot: sigma(t) = 8c + 4ks + 2h + j for t = 16ks + 8h + 2c + j,
+                // so the 8 tokens an mma lane (., c) needs are contiguous
+                const int slot = ((t >> 1) & 3) * 8 + (t >> 4) * 4 + ((t >> 3) & 1) * 2 + (t & 1);
+#pragma unroll
+                for (int gp = 0; gp < GP; gp++) {
+                    float2 pp = __fmul2_rn(make_float2(w[2 * gp], w[2 * gp + 1]),
+                                           make_float2(vsc, vsc));
+                    // masked tokens have w = 0; their (possibly stale) scale must not leak in
+                    pp.x = (w[2 * gp] != 0.0f) ? pp.x : 0.0f;
+                    pp.y = (w[2 * gp + 1] != 0.0f) ? pp.y : 0.0f;
+                    const uint32_t hi = f2_to_h2(pp.x, pp.y);
+                    const float2 hf = h2_to_f2(hi);
+                    const float2 r = __fadd2_rn(pp, make_float2(-hf.x, -hf.y));  // exact
+                    const uint32_t lo = f2_to_h2(r.x, r.y);
+                    S.pw[warp][2 * gp][slot] = __byte_perm(hi, lo, 0x5410);
+                    if (2 * gp + 1 < G) S.pw[warp][2 * gp + 1][slot] = __byte_perm(hi, lo, 0x7632);
+                }
             }
             __syncwarp();
 
-            // ---- value phase: lane (tg, c) covers elements c*E.. of rows tg, tg+TG, ...
+            if (!Q4) {
+                // ---- value phase on the tensor cores: D += P' (rows: heads hi | lo,
+                // k: 32 tokens) x V (k: tokens, n: elements), two m16n8k16 k-steps per
+                // 8-element n-tile.  A (this lane's head gq; zero rows for gq >= G):
+                // tokens 2c, 2c+1, 2c+8, 2c+9 | +16, from slots 8c .. 8c+7.
+                uint32_t a0[4] = {0u, 0u, 0u, 0u}, a1[4] = {0u, 0u, 0u, 0u};
+                if (gq < G) {
+                    const uint4 x0 = *reinterpret_cast<const uint4*>(&S.pw[warp][gq][8 * c4]);
+                    const uint4 x1 = *reinterpret_cast<const uint4*>(&S.pw[warp][gq][8 * c4 + 4]);
+                    a0[0] = __byte_perm(x0.x, x0.y, 0x5410);  // hi of tokens 2c, 2c+1
+                    a0[1] = __byte_perm(x0.x, x0.y, 0x7632);  // lo
+                    a0[2] = __byte_perm(x0.z, x0.w, 0x5410);  // hi of 2c+8, 2c+9
+                    a0[3] = __byte_perm(x0.z, x0.w, 0x7632);
+                    a1[0] = __byte_perm(x1.x, x1.y, 0x5410);  // k-step 1: tokens + 16
+                    a1[1] = __byte_perm(x1.x, x1.y, 0x7632);
+                    a1[2] = __byte_perm(x1.z, x1.w, 0x5410);
+                    a1[3] = __byte_perm(x1.z, x1.w, 0x7632);
+                }
+                // B: per 16-byte chunk cg, one transposed ldmatrix of the four 8-token
+                // blocks as 16-bit element pairs: register i holds, for tokens 8i + 2c
+                // and + 1, elements 16cg + 2g and + 1.  Lane L gives token row L's
+                // chunk, at its 128-byte-swizzled place.
+                const uint32_t vrow = smem_u32(vst) + (uint32_t)lane * HD;
+#pragma unroll
+                for (int cg = 0; cg < HD / 16; cg++) {
+                    uint32_t r[4];
+                    ldsm_x4_trans(vrow + ((uint32_t)(cg ^ (lane & 7)) << 4), r[0], r[1], r[2], r[3]);
+                    // int8 pair -> fp16 pair exactly: offset binary u = c + 128 into the
+                    // mantissa of 1024 (0x64uu), minus 1152
+                    uint32_t be[4], bo[4];
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const uint32_t u = r[j] ^ 0x80808080u;
+                        be[j] = hsub2(__byte_perm(u, 0x64646464u, 0x4240), 0x64806480u);
+                        bo[j] = hsub2(__byte_perm(u, 0x64646464u, 0x4341), 0x64806480u);
+                    }
+                    mma_f16_16816(D[cg][0], a0, be[0], be[1]);
+                    mma_f16_16816(D[cg][0], a1, be[2], be[3]);
+                    mma_f16_16816(D[cg][1], a0, bo[0], bo[1]);
+                    mma_f16_16816(D[cg][1], a1, bo[2], bo[3]);
+                }
+            } else {
+            // ---- value phase (q4): lane (tg, c) covers elements c*E.. of rows tg, tg+TG, ..
             const int tg = lane / NC, c = lane % NC;
 #pragma unroll
             for (int r = tg; r < TILE; r += TG) {
@@ -514,6 +636,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                     }
                 }
             }
+            }
         }
         __syncwarp();
         if (i + NS < mine) issue(i + NS);
@@ -530,32 +653,51 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
 #pragma unroll
             for (int e = 0; e < EP; e++) acc[g][e] = make_float2(0.0f, 0.0f);
         }
+#pragma unroll
+        for (int cg = 0; cg < HD / 16; cg++)
+#pragma unroll
+            for (int j = 0; j < 4; j++) D[cg][0][j] = D[cg][1][j] = 0.0f;
     }
 
-    // ---- reduce the lanes of a warp: V rows were split over TG lane groups
 #pragma unroll
     for (int g = 0; g < G; g++) {
+        if (Q4) {  // V rows were split over TG lane groups
 #pragma unroll
-        for (int o = NC; o < 32; o <<= 1)
+            for (int o = NC; o < 32; o <<= 1)
 #pragma unroll
-            for (int e = 0; e < EP; e++) {
-                acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, o);
-                acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, o);
-            }
+                for (int e = 0; e < EP; e++) {
+                    acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, o);
+                    acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, o);
+                }
+        }
         Sl[g] = warp_sum(Sl[g]);
     }
 
-    // ---- merge the 4 warps in shared memory (reuses the stage buffers)
+    // ---- merge the 4 warps in shared memory (reuses the V buffers)
     const bool cta_failed = __syncthreads_or(failed ? 1 : 0) != 0;
-    float* macc = reinterpret_cast<float*>(S.stage);                      // [W][G][HD]
+    float* macc = reinterpret_cast<float*>(S.v);                          // [W][G][HD]
     float2* mms = reinterpret_cast<float2*>(macc + ATTN_WARPS * G * HD);  // [W][G]
-    if (lane < NC) {
+    if (Q4) {
+        if (lane < NC) {
 #pragma unroll
-        for (int g = 0; g < G; g++)
+            for (int g = 0; g < G; g++)
 #pragma unroll
-            for (int e = 0; e < EP; e++)
-                *reinterpret_cast<float2*>(&macc[(warp * G + g) * HD + lane * E + 2 * e]) =
-                    acc[g][e];
+                for (int e = 0; e < EP; e++)
+                    *reinterpret_cast<float2*>(&macc[(warp * G + g) * HD + lane * E + 2 * e]) =
+                        acc[g][e];
+        }
+    } else if (gq < G) {
+        // head gq's elements 16cg + 4c .. + 3: the hi and lo rows added, and the
+        // weights' 2^-ev scale undone (an exact power of two, in two steps)
+        const int k1 = min(max(ev, -126), 127);
+        const float f1 = pow2i(k1), f2 = pow2i(min(max(ev - k1, -126), 127));
+#pragma unroll
+        for (int cg = 0; cg < HD / 16; cg++) {
+            const float4 o = make_float4(D[cg][0][0] + D[cg][0][2], D[cg][1][0] + D[cg][1][2],
+                                         D[cg][0][1] + D[cg][0][3], D[cg][1][1] + D[cg][1][3]);
+            *reinterpret_cast<float4*>(&macc[(warp * G + gq) * HD + 16 * cg + 4 * c4]) =
+                make_float4(o.x * f1 * f2, o.y * f1 * f2, o.z * f1 * f2, o.w * f1 * f2);
+        }
     }
     if (lane == 0)
 #pragma unroll
