@@ -103,8 +103,9 @@ struct AttnSmem {
     alignas(16) float sc[ATTN_WARPS][ATTN_STAGES][2][TILE];  // kscale, vscale
     // q8: the weights as fp16 (hi, lo) pairs per (head, token slot sigma(t));
     // q4: per K position (p_g, p_g, p_g+1, p_g+1) for each head pair
+    // (pw rows padded to 36 words: the eight heads' fragment loads hit distinct banks)
     union {
-        alignas(16) uint32_t pw[ATTN_WARPS][G][TILE];
+        alignas(16) uint32_t pw[ATTN_WARPS][G][TILE + 4];
         alignas(16) float4 p[ATTN_WARPS][TILE][AttnShape<G>::GP];
     };
     alignas(16) int8_t qi[G][HD];
@@ -240,6 +241,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int nkv = P.cache.num_kv_heads, kv_bs = P.cache.kv_bs;
     const int subs = kv_bs / TILE;
+    // fetch the V tensor map's descriptor while the prologue runs
+    if (!Q4 && threadIdx.x == 0)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.vmap))
+                     : "memory");
 
     const SeqRange rng = seq_range<SPARSE>(P, b, h);
     if (rng.bad && threadIdx.x == 0 && chunk == 0 && h == 0) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);

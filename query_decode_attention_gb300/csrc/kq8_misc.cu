@@ -9,49 +9,59 @@ namespace kq8 {
 // r = RN(1 / d).  r and the product q = RN(x * r) each round once (relative
 // 2^-24), so |q - x / d| <= 128 * 2^-23 and |fl(x / d) - x / d| <= 2^-18:
 // q is within 2^-15.5 of the IEEE quotient fl(x / d).  Unless q lies within
-// 2^-14 of a half-integer both therefore round to the same integer, and rint(q)
-// (no tie possible) is roundf(fl(x / d)).  The rare near-half case (about 1 in
-// 8000 elements), and a non-finite q (d subnormal or 0), take the IEEE quotient
-// itself, so the result always equals the method's roundf(x / d) bit for bit.
-// The lane's four quotients roundf(x_i / d), computed as described above;
-// one (rarely taken) branch for the lane's four elements together.
-__device__ __forceinline__ float4 round_quotients(const float4 x, float d, float lo, float hi) {
+// 2^-14 of a half-integer both therefore round to the same integer, and the
+// nearest integer to q (no tie possible) is roundf(fl(x / d)).  The rare
+// near-half case (about 1 in 8000 elements), and a non-finite q (d subnormal
+// or 0), take the IEEE quotient itself, so the result always equals the
+// method's roundf(x / d) bit for bit.
+// The nearest integer comes from adding 1.5 * 2^23 + off (exact for |q| < 2^22):
+// the sum's low byte is then (n + off) mod 256, the code byte itself.  On the
+// fast path |q| < 127.5 (and < 7.5 for q4), so no clamp is needed there.
+// Returns the lane's four code bytes (element i in byte i); lo / hi clamp the
+// slow path, off is 0 (q8, two's complement) or 8 (q4, offset binary).
+__device__ __forceinline__ uint32_t quantize4(const float4 x, float d, float lo, float hi,
+                                              int off) {
     const float r = __frcp_rn(d);
+    const float magic = 12582912.0f + (float)off;  // 1.5 * 2^23 + off
     const float q0 = __fmul_rn(x.x, r), q1 = __fmul_rn(x.y, r);
     const float q2 = __fmul_rn(x.z, r), q3 = __fmul_rn(x.w, r);
-    float4 n = make_float4(rintf(q0), rintf(q1), rintf(q2), rintf(q3));
+    const float t0 = __fadd_rn(q0, magic), t1 = __fadd_rn(q1, magic);
+    const float t2 = __fadd_rn(q2, magic), t3 = __fadd_rn(q3, magic);
     const float far = 0.5f - 0x1p-14f;  // NaN / inf compare false
-    const bool ok = fabsf(q0 - n.x) < far && fabsf(q1 - n.y) < far && fabsf(q2 - n.z) < far &&
-                    fabsf(q3 - n.w) < far;
-    if (!ok)
-        n = make_float4(roundf(__fdiv_rn(x.x, d)), roundf(__fdiv_rn(x.y, d)),
-                        roundf(__fdiv_rn(x.z, d)), roundf(__fdiv_rn(x.w, d)));
-    return make_float4(fminf(fmaxf(n.x, lo), hi), fminf(fmaxf(n.y, lo), hi),
-                       fminf(fmaxf(n.z, lo), hi), fminf(fmaxf(n.w, lo), hi));
+    const bool ok = fabsf(q0 - (t0 - magic)) < far && fabsf(q1 - (t1 - magic)) < far &&
+                    fabsf(q2 - (t2 - magic)) < far && fabsf(q3 - (t3 - magic)) < far;
+    if (ok)
+        return __byte_perm(__byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x0040),
+                           __byte_perm(__float_as_uint(t2), __float_as_uint(t3), 0x0040), 0x5410);
+    auto slow = [&](float v) -> uint32_t {
+        const float n = fminf(fmaxf(roundf(__fdiv_rn(v, d)), lo), hi);
+        return (uint32_t)((int)n + off) & 0xffu;
+    };
+    return slow(x.x) | (slow(x.y) << 8) | (slow(x.z) << 16) | (slow(x.w) << 24);
 }
 
 // One (token, KV head) row of K or V, one warp: lane l holds elements
 // 4l..4l+3.  m = max |x| (exact, order-free), stored as the scale; codes are
 // roundf(x / (m * (1/127))) clamped to [-127, 127], as the oracle computes
-// them (IEEE quotient, see round_quotients); an all-zero row gives zero codes.
+// them (IEEE quotient, see quantize4); an all-zero row gives zero codes.
 // Returns the lane's 4 codes.
 __device__ __forceinline__ uint32_t kv_quantize_lane(const float4 x, float& m_out) {
     float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
     m = warp_max(m);
     m_out = m;
     if (m == 0.0f) return 0u;
-    const float4 n = round_quotients(x, __fmul_rn(m, inv127()), -127.0f, 127.0f);
-    return ((uint32_t)(int)n.x & 0xffu) | (((uint32_t)(int)n.y & 0xffu) << 8) |
-           (((uint32_t)(int)n.z & 0xffu) << 16) | ((uint32_t)(int)n.w << 24);
+    return quantize4(x, __fmul_rn(m, inv127()), -127.0f, 127.0f, 0);
 }
 
 constexpr int APPEND_WARPS = 8;
-constexpr int APPEND_ITEMS = 4;  // (token, head) rows per warp, all loaded up front
 
 // grid: ceil(T * nkv / (APPEND_WARPS * APPEND_ITEMS)) blocks of APPEND_WARPS
 // warps; warp = APPEND_ITEMS consecutive (token, head) items (consecutive
 // heads of a token: their fp32 rows are contiguous), each quantising its K and
-// its V row.  Every item's loads are issued before the first is used.
+// its V row.  Every item's loads are issued before the first is used: bulk
+// appends take 4 rows per warp (more loads in flight), small ones (a decode
+// step's new tokens) 1 (more warps).
+template <int APPEND_ITEMS>
 __global__ void __launch_bounds__(APPEND_WARPS * 32)
     kq8_append_kernel(const kq8_cache_t c, const float* __restrict__ k, const float* __restrict__ v,
                       const int32_t* __restrict__ slot, int32_t T, uint32_t* status) {
@@ -117,9 +127,7 @@ __device__ __forceinline__ uint32_t kv_quantize_lane_q4(const float4 x, float& m
     m = warp_max(m);
     m_out = m;
     if (m == 0.0f) return 0x08080808u;
-    const float4 n = round_quotients(x, __fmul_rn(m, inv7()), -7.0f, 7.0f);
-    return (uint32_t)((int)n.x + 8) | ((uint32_t)((int)n.y + 8) << 8) |
-           ((uint32_t)((int)n.z + 8) << 16) | ((uint32_t)((int)n.w + 8) << 24);
+    return quantize4(x, __fmul_rn(m, inv7()), -7.0f, 7.0f, 8);
 }
 
 // One warp per (token, head) as above; lanes 2w and 2w+1 hold the 8 elements of
@@ -182,8 +190,15 @@ int launch_append(const kq8_cache_t& c, const float* k, const float* v, const in
                   int32_t T, uint32_t* status, cudaStream_t stream) {
     const int64_t items = (int64_t)T * c.num_kv_heads;
     if (items == 0) return KQ8_OK;
-    const int64_t blocks = (items + APPEND_WARPS * APPEND_ITEMS - 1) / (APPEND_WARPS * APPEND_ITEMS);
-    kq8_append_kernel<<<(unsigned)blocks, APPEND_WARPS * 32, 0, stream>>>(c, k, v, slot, T, status);
+    if (items < 8192) {
+        const int64_t blocks = (items + APPEND_WARPS - 1) / APPEND_WARPS;
+        kq8_append_kernel<1><<<(unsigned)blocks, APPEND_WARPS * 32, 0, stream>>>(c, k, v, slot, T,
+                                                                                status);
+    } else {
+        const int64_t blocks = (items + APPEND_WARPS * 4 - 1) / (APPEND_WARPS * 4);
+        kq8_append_kernel<4><<<(unsigned)blocks, APPEND_WARPS * 32, 0, stream>>>(c, k, v, slot, T,
+                                                                                status);
+    }
     return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
 }
 

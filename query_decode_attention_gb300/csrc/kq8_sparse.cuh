@@ -385,8 +385,11 @@ __device__ __noinline__ void select_all(const SparseParams& P, int b, int h, int
 // ---------------------------------------------------------------------------
 constexpr int PROBE_WARPS = 8;
 static_assert(PROBE_WARPS * 32 == TOPK_THREADS, "the probe CTA runs the selection");
-constexpr int PROBE_MAX_BPC = 128;     // blocks per CTA
-constexpr int PROBE_MAX_PAGES = 256;   // page ids a CTA stages
+// Blocks per CTA: long-lived CTAs (8 units of 4 blocks per warp at block 32)
+// so that the prologue (page ids, Q quantisation, a CTA barrier) and the
+// epilogue weigh little against the streaming.
+constexpr int PROBE_MAX_BPC = 256;
+constexpr int PROBE_MAX_PAGES = 512;   // page ids a CTA stages
 
 struct ProbeRow {
     uint4 k[2 * NB];  // the row's 128 int8 codes, block by block
