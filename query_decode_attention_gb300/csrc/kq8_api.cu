@@ -197,21 +197,24 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// The q8 V array as the 3-D tensor the attention kernel copies sub-tiles of:
-// {128 bytes, kv_bs rows, num_pages * nkv (page, head) pairs}, boxes of 32 rows,
-// 128-byte swizzle in shared memory.
-int set_vmap(AttnParams& p) {
+// The V array as the 3-D tensor the attention kernel copies sub-tiles of:
+// {row bytes, kv_bs rows, num_pages * nkv (page, head) pairs}, boxes of 32 rows.
+// q8 rows are 128 bytes (128-byte swizzle in shared memory), q4 rows 64 bytes
+// (64-byte swizzle).
+int set_vmap(AttnParams& p, bool q4 = false) {
     const kq8_cache_t& c = p.cache;
     const uint64_t pairs = (uint64_t)c.num_pages * (uint64_t)c.num_kv_heads;
     if (pairs > 0x7FFFFFFFull) return KQ8_ERR_UNSUPPORTED;  // the copy's coordinate is int32
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return KQ8_ERR_CUDA;
-    const cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)c.kv_bs, (cuuint64_t)pairs};
-    const cuuint64_t strides[2] = {(cuuint64_t)HD, (cuuint64_t)c.kv_bs * HD};
-    const cuuint32_t box[3] = {(cuuint32_t)HD, (cuuint32_t)TILE, 1u};
+    const cuuint64_t row = q4 ? HD / 2 : HD;
+    const cuuint64_t dims[3] = {row, (cuuint64_t)c.kv_bs, (cuuint64_t)pairs};
+    const cuuint64_t strides[2] = {row, (cuuint64_t)c.kv_bs * row};
+    const cuuint32_t box[3] = {(cuuint32_t)row, (cuuint32_t)TILE, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUresult r = enc(&p.vmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.v, dims, strides, box,
-                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           q4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? KQ8_OK : KQ8_ERR_CUDA;
 }
@@ -341,6 +344,8 @@ int kq8_decode_attn_q4(float* out, const float* q, const kq8_cache_t* cache,
     if (B == 0) return KQ8_OK;
     AttnParams p = attn_params(out, q, cache, page_table, max_pages, seq_lens, max_seq_len, B, nq,
                                scale, plan, workspace);
+    rc = set_vmap(p, true);
+    if (rc) return rc;
     return launch_attn_q4(p, nq / nkv, B, nkv, (cudaStream_t)stream);
 }
 

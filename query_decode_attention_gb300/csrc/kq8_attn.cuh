@@ -19,9 +19,11 @@
 //     rescale of article 9-2 §1, done lazily: between rescales the weights may
 //     exceed 1 by at most 2^8, which fp32 absorbs); w = e^(s - M), the
 //     difference taken before the move to base 2;
-//   value phase (lane = 16 bytes of a V row, 4 rows per instruction): int8 ->
-//     fp32 by byte permutes and a packed subtract, acc += v * (w * vs) with
-//     packed FMAs.
+//   value phase on the tensor cores (mma.sync m16n8k16, fp16 in, fp32
+//     accumulate): the tile's weights times the V step, as fp16 hi + lo rows
+//     of an A operand (one head per row pair), times the V codes, converted
+//     exactly to fp16 after a transposed ldmatrix of the tensor-copied,
+//     swizzled V sub-tile (q8: 128-byte rows; q4: 64-byte rows of nibbles).
 // The 4 warps' (M, S, acc) are merged in shared memory; a chunk that covers
 // the whole sequence writes out = acc / S directly, others write an
 // unnormalised partial (M, S, acc), and the last of a sequence's chunk CTAs to
@@ -49,9 +51,9 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_SLACK = 8.0f;
 
 struct AttnParams {
-    // V sub-tiles of a q8 cache as a 3-D tensor {128 B, kv_bs rows, num_pages *
-    // nkv}, copied into shared memory with the 128-byte swizzle (the value
-    // phase reads them with conflict-free ldmatrix); unused for q4 caches
+    // V sub-tiles as a 3-D tensor {row bytes, kv_bs rows, num_pages * nkv}, copied
+    // into shared memory with the 128-byte (q8: 128-byte rows) or 64-byte (q4:
+    // 64-byte rows) swizzle, so that the value phase's ldmatrix is conflict-free
     CUtensorMap vmap;
     float* out;
     const float* q;
@@ -87,27 +89,20 @@ struct AttnParams {
 
 template <int G>
 struct AttnShape {
-    static constexpr int E = (G <= 4) ? 16 : 8;  // V elements per lane
-    static constexpr int NC = HD / E;            // lanes per V row
-    static constexpr int TG = 32 / NC;           // V rows per instruction
     static constexpr int GP = (G + 1) / 2;       // head pairs
     static constexpr int MIN_CTAS = (G <= 4) ? 3 : 2;
 };
 
 template <int G>
 struct AttnSmem {
-    // per warp and stage: a V sub-tile (q8: 128-byte swizzled by the tensor
-    // copy, so 1024-byte aligned; q4: 2 KB of rows), a K sub-tile, the scales
+    // per warp and stage: a V sub-tile (swizzled by the tensor copy, so
+    // 1024-byte aligned; q4 uses its first 2 KB), a K sub-tile, the scales
     alignas(1024) uint8_t v[ATTN_WARPS][ATTN_STAGES][SUB_V_BYTES];
     alignas(128) uint8_t k[ATTN_WARPS][ATTN_STAGES][SUB_K_BYTES];
     alignas(16) float sc[ATTN_WARPS][ATTN_STAGES][2][TILE];  // kscale, vscale
-    // q8: the weights as fp16 (hi, lo) pairs per (head, token slot sigma(t));
-    // q4: per K position (p_g, p_g, p_g+1, p_g+1) for each head pair
-    // (pw rows padded to 36 words: the eight heads' fragment loads hit distinct banks)
-    union {
-        alignas(16) uint32_t pw[ATTN_WARPS][G][TILE + 4];
-        alignas(16) float4 p[ATTN_WARPS][TILE][AttnShape<G>::GP];
-    };
+    // the tile's weights as fp16 (hi, lo) pairs per (head, token slot sigma(t)),
+    // rows padded to 36 words so the eight heads' fragment loads hit distinct banks
+    alignas(16) uint32_t pw[ATTN_WARPS][G][TILE + 4];
     alignas(16) int8_t qi[G][HD];
     alignas(16) float qsc[G][NB];
     int qsum[G][NB];  // sum of each 32-element block's Q codes (q4 cache only)
@@ -228,8 +223,7 @@ template <int G, bool SPARSE, bool Q4 = false, bool WITHHOLD = false>
 __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     kq8_attn_kernel(const __grid_constant__ AttnParams P) {
     using Sh = AttnShape<G>;
-    constexpr int E = Sh::E, NC = Sh::NC, TG = Sh::TG, GP = Sh::GP;
-    constexpr int EP = E / 2;  // float2 pairs per head per lane
+    constexpr int GP = Sh::GP;
     constexpr int NS = ATTN_STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the swizzled tensor copies want 1024-byte aligned V tiles: the launch
@@ -317,7 +311,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                     const size_t kvo = kv4_sub_off(pg, h, nkv, kv_bs, sub);
                     mbar_arrive_expect_tx(bar, SUB_K4_BYTES + SUB_V4_BYTES + 2 * SUB_S_BYTES);
                     bulk_g2s(S.k[warp][s], P.cache.k + kvo, SUB_K4_BYTES, bar, pol);
-                    bulk_g2s(S.v[warp][s], P.cache.v + kvo, SUB_V4_BYTES, bar, pol);
+                    tma_load_3d(S.v[warp][s], &P.vmap, 0, sub * TILE, (int)page_head(pg, h, nkv),
+                                bar, pol);
                 } else {
                     mbar_arrive_expect_tx(bar, STAGE_BYTES);
                     bulk_g2s(S.k[warp][s], P.cache.k + kv_sub_off(pg, h, nkv, kv_bs, sub),
@@ -333,20 +328,19 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     for (int i = 0; i < NS && i < mine; i++) issue(i);
 
     float M2[G], Sl[G];
-    float2 acc[G][EP];  // q4: lane (tg, c) accumulates elements c*E.. of every head
-    // q8: the value phase runs on the tensor cores.  Per 16-element chunk cg, an
-    // m16n8k16 tile pair D[cg][0..3] (elements 16cg + 2j) and D[cg][4..7]
-    // (16cg + 2j + 1), rows 0..7 = head (weight hi), 8..15 = head (weight lo):
-    // lane (g, c) holds head g's elements 16cg + 4c .. 16cg + 4c + 3
+    // The value phase runs on the tensor cores: 16 m16n8 accumulator tiles D[.][.]
+    // of 4 fp32 per lane, rows 0..7 = head (weight hi), 8..15 = head (weight lo).
+    // q8: D[cg][0] holds elements 16cg + 2j, D[cg][1] 16cg + 2j + 1 (column j);
+    // lane (g, c) then holds head g's elements 16cg + 4c .. + 3.  q4: for the
+    // 32-element chunk q, D[2q + k/2][k%2] holds elements 32q + 8(j/2) + 2(j%2) +
+    // {0, 1, 4, 5}[k]; lane (g, c) holds head g's elements 32q + 8c .. + 7.
     float D[HD / 16][2][4];
-    // q8 weights go to the tensor cores as fp16 scaled by 2^-ev (see below)
+    // the weights go to the tensor cores as fp16 scaled by 2^-ev (see below)
     int ev = -149;
 #pragma unroll
     for (int g = 0; g < G; g++) {
         M2[g] = M_INIT;
         Sl[g] = 0.0f;
-#pragma unroll
-        for (int e = 0; e < EP; e++) acc[g][e] = make_float2(0.0f, 0.0f);
     }
 #pragma unroll
     for (int cg = 0; cg < HD / 16; cg++)
@@ -473,32 +467,25 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             }
             if (__any_sync(0xffffffffu, grow)) {
                 // rare: some head's maximum grew by a wide margin -> rescale its state
-                float cl = 1.0f;  // q8: the factor of this lane's accumulator head gq
+                float cl = 1.0f;  // the factor of this lane's accumulator head gq
 #pragma unroll
                 for (int g = 0; g < G; g++) {
                     const float mn = fmaxf(M2[g], warp_max(sv[g]));
                     if (mn > M2[g]) {
                         const float c = exp_diff(M2[g], mn);
                         Sl[g] *= c;
-                        if (Q4) {
-#pragma unroll
-                            for (int e = 0; e < EP; e++)
-                                acc[g][e] = __fmul2_rn(acc[g][e], make_float2(c, c));
-                        }
                         cl = (g == gq) ? c : cl;
                         M2[g] = mn;
                         dd[g] = (sv[g] - mn) * LOG2E;
                     }
                 }
-                if (!Q4) {
 #pragma unroll
-                    for (int cg = 0; cg < HD / 16; cg++)
+                for (int cg = 0; cg < HD / 16; cg++)
 #pragma unroll
-                        for (int j = 0; j < 4; j++) {
-                            D[cg][0][j] *= cl;
-                            D[cg][1][j] *= cl;
-                        }
-                }
+                    for (int j = 0; j < 4; j++) {
+                        D[cg][0][j] *= cl;
+                        D[cg][1][j] *= cl;
+                    }
             }
             float w[2 * GP];
 #pragma unroll
@@ -507,17 +494,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                 Sl[g] += w[g];
             }
             if constexpr ((G & 1) != 0) w[G] = 0.0f;
-            if (Q4) {
-#pragma unroll
-                for (int gp = 0; gp < GP; gp++) {
-                    const float2 pp = __fmul2_rn(make_float2(w[2 * gp], w[2 * gp + 1]),
-                                                 make_float2(vstep, vstep));
-                    // masked tokens have w = 0; their (possibly stale) scale must not leak in
-                    const float p0 = (w[2 * gp] != 0.0f) ? pp.x : 0.0f;
-                    const float p1 = (w[2 * gp + 1] != 0.0f) ? pp.y : 0.0f;
-                    S.p[warp][q][gp] = make_float4(p0, p0, p1, p1);  // by K position
-                }
-            } else {
+            {
                 // weights for the tensor cores: P' = w * vstep * 2^-ev as fp16 hi + lo
                 // (22 significant bits).  ev keeps the tile's largest live V step
                 // times 2^-ev below 2^7, so with w <= 2^8 (the lazy rescale bound)
@@ -561,7 +538,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             }
             __syncwarp();
 
-            if (!Q4) {
+            {
                 // ---- value phase on the tensor cores: D += P' (rows: heads hi | lo,
                 // k: 32 tokens) x V (k: tokens, n: elements), two m16n8k16 k-steps per
                 // 8-element n-tile.  A (this lane's head gq; zero rows for gq >= G):
@@ -579,68 +556,60 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                     a1[2] = __byte_perm(x1.z, x1.w, 0x5410);
                     a1[3] = __byte_perm(x1.z, x1.w, 0x7632);
                 }
-                // B: per 16-byte chunk cg, one transposed ldmatrix of the four 8-token
-                // blocks as 16-bit element pairs: register i holds, for tokens 8i + 2c
-                // and + 1, elements 16cg + 2g and + 1.  Lane L gives token row L's
-                // chunk, at its 128-byte-swizzled place.
-                const uint32_t vrow = smem_u32(vst) + (uint32_t)lane * HD;
-#pragma unroll
-                for (int cg = 0; cg < HD / 16; cg++) {
-                    uint32_t r[4];
-                    ldsm_x4_trans(vrow + ((uint32_t)(cg ^ (lane & 7)) << 4), r[0], r[1], r[2], r[3]);
-                    // int8 pair -> fp16 pair exactly: offset binary u = c + 128 into the
-                    // mantissa of 1024 (0x64uu), minus 1152
-                    uint32_t be[4], bo[4];
-#pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        const uint32_t u = r[j] ^ 0x80808080u;
-                        be[j] = hsub2(__byte_perm(u, 0x64646464u, 0x4240), 0x64806480u);
-                        bo[j] = hsub2(__byte_perm(u, 0x64646464u, 0x4341), 0x64806480u);
-                    }
-                    mma_f16_16816(D[cg][0], a0, be[0], be[1]);
-                    mma_f16_16816(D[cg][0], a1, be[2], be[3]);
-                    mma_f16_16816(D[cg][1], a0, bo[0], bo[1]);
-                    mma_f16_16816(D[cg][1], a1, bo[2], bo[3]);
-                }
-            } else {
-            // ---- value phase (q4): lane (tg, c) covers elements c*E.. of rows tg, tg+TG, ..
-            const int tg = lane / NC, c = lane % NC;
-#pragma unroll
-            for (int r = tg; r < TILE; r += TG) {
-                float2 f[EP];
                 if (Q4) {
-                    if (E == 16) {
-                        const uint2 vv = *reinterpret_cast<const uint2*>(vst + r * (HD / 2) + c * 8);
-                        u4x8_to_f2(vv.x, f[0], f[1], f[2], f[3]);
-                        u4x8_to_f2(vv.y, f[4], f[5], f[6], f[7]);
-                    } else {
-                        const uint32_t vv = *reinterpret_cast<const uint32_t*>(vst + r * (HD / 2) + c * 4);
-                        u4x8_to_f2(vv, f[0], f[1], f[2], f[3]);
+                    // B (q4): per 16-byte chunk cq of a 64-byte row (32 elements), one
+                    // transposed ldmatrix of the four 8-token blocks as 16-bit words
+                    // (64-byte swizzle: chunk cq of row t at cq ^ ((t / 2) % 4)).
+                    // Register i holds for tokens 8i + 2c and + 1 the bytes 2(g%2),
+                    // 2(g%2) + 1 of word 4cq + g/2: elements e0 = 32cq + 8(g/2) + 2(g%2),
+                    // e0 + 1 (low nibbles) and e0 + 4, e0 + 5 (high nibbles); nibble u
+                    // = code + 8 goes into the mantissa of 1024, minus 1032.
+                    const uint32_t vrow = smem_u32(vst) + (uint32_t)lane * (HD / 2);
+#pragma unroll
+                    for (int cq = 0; cq < HD / 32; cq++) {
+                        uint32_t r[4];
+                        ldsm_x4_trans(vrow + ((uint32_t)(cq ^ ((lane >> 1) & 3)) << 4), r[0],
+                                      r[1], r[2], r[3]);
+                        uint32_t b[4][4];  // [n-tile: +0, +1, +4, +5][register]
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            const uint32_t lo = r[j] & 0x0F0F0F0Fu, hi = (r[j] >> 4) & 0x0F0F0F0Fu;
+                            b[0][j] = hsub2(__byte_perm(lo, 0x64646464u, 0x4240), 0x64086408u);
+                            b[1][j] = hsub2(__byte_perm(lo, 0x64646464u, 0x4341), 0x64086408u);
+                            b[2][j] = hsub2(__byte_perm(hi, 0x64646464u, 0x4240), 0x64086408u);
+                            b[3][j] = hsub2(__byte_perm(hi, 0x64646464u, 0x4341), 0x64086408u);
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; k++) {
+                            mma_f16_16816(D[2 * cq + (k >> 1)][k & 1], a0, b[k][0], b[k][1]);
+                            mma_f16_16816(D[2 * cq + (k >> 1)][k & 1], a1, b[k][2], b[k][3]);
+                        }
                     }
-                } else if (E == 16) {
-                    const uint4 vv = *reinterpret_cast<const uint4*>(vst + r * HD + c * 16);
-                    i8x4_to_f2(vv.x, f[0], f[1]);
-                    i8x4_to_f2(vv.y, f[2], f[3]);
-                    i8x4_to_f2(vv.z, f[4], f[5]);
-                    i8x4_to_f2(vv.w, f[6], f[7]);
                 } else {
-                    const uint2 vv = *reinterpret_cast<const uint2*>(vst + r * HD + c * 8);
-                    i8x4_to_f2(vv.x, f[0], f[1]);
-                    i8x4_to_f2(vv.y, f[2], f[3]);
-                }
+                    // B: per 16-byte chunk cg, one transposed ldmatrix of the four 8-token
+                    // blocks as 16-bit element pairs: register i holds, for tokens 8i + 2c
+                    // and + 1, elements 16cg + 2g and + 1.  Lane L gives token row L's
+                    // chunk, at its 128-byte-swizzled place.
+                    const uint32_t vrow = smem_u32(vst) + (uint32_t)lane * HD;
 #pragma unroll
-                for (int gp = 0; gp < GP; gp++) {
-                    const float4 pp = S.p[warp][kpos(r)][gp];
-                    const float2 pa = make_float2(pp.x, pp.y);
-                    const float2 pb = make_float2(pp.z, pp.w);
+                    for (int cg = 0; cg < HD / 16; cg++) {
+                        uint32_t r[4];
+                        ldsm_x4_trans(vrow + ((uint32_t)(cg ^ (lane & 7)) << 4), r[0], r[1], r[2], r[3]);
+                        // int8 pair -> fp16 pair exactly: offset binary u = c + 128 into the
+                        // mantissa of 1024 (0x64uu), minus 1152
+                        uint32_t be[4], bo[4];
 #pragma unroll
-                    for (int e = 0; e < EP; e++) {
-                        acc[2 * gp][e] = __ffma2_rn(f[e], pa, acc[2 * gp][e]);
-                        if (2 * gp + 1 < G)
-                            acc[2 * gp + 1][e] = __ffma2_rn(f[e], pb, acc[2 * gp + 1][e]);
+                        for (int j = 0; j < 4; j++) {
+                            const uint32_t u = r[j] ^ 0x80808080u;
+                            be[j] = hsub2(__byte_perm(u, 0x64646464u, 0x4240), 0x64806480u);
+                            bo[j] = hsub2(__byte_perm(u, 0x64646464u, 0x4341), 0x64806480u);
+                        }
+                        mma_f16_16816(D[cg][0], a0, be[0], be[1]);
+                        mma_f16_16816(D[cg][0], a1, be[2], be[3]);
+                        mma_f16_16816(D[cg][1], a0, bo[0], bo[1]);
+                        mma_f16_16816(D[cg][1], a1, bo[2], bo[3]);
                     }
                 }
-            }
             }
         }
         __syncwarp();
@@ -655,8 +624,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
         for (int g = 0; g < G; g++) {
             M2[g] = M_INIT;
             Sl[g] = 0.0f;
-#pragma unroll
-            for (int e = 0; e < EP; e++) acc[g][e] = make_float2(0.0f, 0.0f);
         }
 #pragma unroll
         for (int cg = 0; cg < HD / 16; cg++)
@@ -665,43 +632,37 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     }
 
 #pragma unroll
-    for (int g = 0; g < G; g++) {
-        if (Q4) {  // V rows were split over TG lane groups
-#pragma unroll
-            for (int o = NC; o < 32; o <<= 1)
-#pragma unroll
-                for (int e = 0; e < EP; e++) {
-                    acc[g][e].x += __shfl_xor_sync(0xffffffffu, acc[g][e].x, o);
-                    acc[g][e].y += __shfl_xor_sync(0xffffffffu, acc[g][e].y, o);
-                }
-        }
-        Sl[g] = warp_sum(Sl[g]);
-    }
+    for (int g = 0; g < G; g++) Sl[g] = warp_sum(Sl[g]);
 
     // ---- merge the 4 warps in shared memory (reuses the V buffers)
     const bool cta_failed = __syncthreads_or(failed ? 1 : 0) != 0;
     float* macc = reinterpret_cast<float*>(S.v);                          // [W][G][HD]
     float2* mms = reinterpret_cast<float2*>(macc + ATTN_WARPS * G * HD);  // [W][G]
-    if (Q4) {
-        if (lane < NC) {
-#pragma unroll
-            for (int g = 0; g < G; g++)
-#pragma unroll
-                for (int e = 0; e < EP; e++)
-                    *reinterpret_cast<float2*>(&macc[(warp * G + g) * HD + lane * E + 2 * e]) =
-                        acc[g][e];
-        }
-    } else if (gq < G) {
-        // head gq's elements 16cg + 4c .. + 3: the hi and lo rows added, and the
-        // weights' 2^-ev scale undone (an exact power of two, in two steps)
+    if (gq < G) {
+        // head gq's elements: the hi and lo rows added, and the weights' 2^-ev
+        // scale undone (an exact power of two, in two steps)
         const int k1 = min(max(ev, -126), 127);
-        const float f1 = pow2i(k1), f2 = pow2i(min(max(ev - k1, -126), 127));
+        const float f = pow2i(k1), f2 = pow2i(min(max(ev - k1, -126), 127));
+        auto sum = [&](int t, int n, int j) { return (D[t][n][j] + D[t][n][j + 2]) * f * f2; };
+        float* row = &macc[(warp * G + gq) * HD];
 #pragma unroll
-        for (int cg = 0; cg < HD / 16; cg++) {
-            const float4 o = make_float4(D[cg][0][0] + D[cg][0][2], D[cg][1][0] + D[cg][1][2],
-                                         D[cg][0][1] + D[cg][0][3], D[cg][1][1] + D[cg][1][3]);
-            *reinterpret_cast<float4*>(&macc[(warp * G + gq) * HD + 16 * cg + 4 * c4]) =
-                make_float4(o.x * f1 * f2, o.y * f1 * f2, o.z * f1 * f2, o.w * f1 * f2);
+        for (int q = 0; q < HD / 32; q++) {
+            float4 lo, hi;  // elements base .. base + 3 and base + 4 .. base + 7
+            int base;
+            if (Q4) {  // n-tiles +0, +1, +4, +5 of chunk q
+                base = 32 * q + 8 * c4;
+                lo = make_float4(sum(2 * q, 0, 0), sum(2 * q, 1, 0), sum(2 * q, 0, 1),
+                                 sum(2 * q, 1, 1));
+                hi = make_float4(sum(2 * q + 1, 0, 0), sum(2 * q + 1, 1, 0),
+                                 sum(2 * q + 1, 0, 1), sum(2 * q + 1, 1, 1));
+                *reinterpret_cast<float4*>(row + base) = lo;
+                *reinterpret_cast<float4*>(row + base + 4) = hi;
+            } else {  // 16-element chunks 2q and 2q + 1
+#pragma unroll
+                for (int cg = 2 * q; cg < 2 * q + 2; cg++)
+                    *reinterpret_cast<float4*>(row + 16 * cg + 4 * c4) =
+                        make_float4(sum(cg, 0, 0), sum(cg, 1, 0), sum(cg, 0, 1), sum(cg, 1, 1));
+            }
         }
     }
     if (lane == 0)

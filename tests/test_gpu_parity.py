@@ -295,7 +295,8 @@ def test_sparse_many_sequences_one_topk_cta_per_kv_head():
     assert_out_close(got, ref, "sparse, 2050 sequences")
 
 
-@pytest.mark.parametrize("block,topk,probe", [(32, 4, 8), (64, 3, 5), (32, 7, 32), (96, 2, 1)])
+@pytest.mark.parametrize("block,topk,probe", [(32, 4, 8), (64, 3, 5), (32, 7, 32), (96, 2, 1),
+                                               (64, 5, 16), (128, 6, 32)])
 def test_sparse_knobs(block, topk, probe):
     wl = W.custom(3, 16, 4, [2000, 700, 3001], seed=block + topk + probe, block=block, topk=topk,
                   probe=probe)
