@@ -59,6 +59,22 @@ void chunking(int64_t B, int64_t nkv, int64_t tiles_max, int sms, int& ct, int& 
     if (nch < 1) nch = 1;
 }
 
+// The block-sparse lists are short (at most G * k blocks): sized for a single
+// wave of three CTAs per SM instead, as few chunks per list as fill it, so
+// that no CTA is left with a prologue and a merge for a couple of tiles.
+void chunking_one_wave(int64_t B, int64_t nkv, int64_t tiles_max, int sms, int& ct, int& nch) {
+    const int64_t pairs = B * nkv > 0 ? B * nkv : 1;
+    int64_t per = ((int64_t)sms * 3) / pairs;  // chunks per list that still fit one wave
+    if (per < 1) per = 1;
+    int64_t c = (tiles_max + per - 1) / per;
+    c = (c + ATTN_WARPS - 1) / ATTN_WARPS * ATTN_WARPS;
+    if (c < ATTN_WARPS) c = ATTN_WARPS;
+    if (c > KQ8_MAX_CHUNK) c = KQ8_MAX_CHUNK;
+    ct = (int)c;
+    nch = (int)((tiles_max + c - 1) / c);
+    if (nch < 1) nch = 1;
+}
+
 struct Plan {
     int chunk_tiles = ATTN_WARPS, num_chunks = 1;
     size_t off_ms = 0, off_acc = 0;
@@ -111,7 +127,7 @@ Plan plan_sparse(int B, int nq, int nkv, int max_seq_len, int block, int topk) {
     if (cap < 2 * m && cap < tiles) cap = tiles < 2 * m ? tiles : 2 * m;
     if (cap < 1) cap = 1;
     p.list_cap = (int)cap;
-    chunking(B, nkv, p.list_cap, device_sms(), p.chunk_tiles, p.num_chunks);
+    chunking_one_wave(B, nkv, p.list_cap, device_sms(), p.chunk_tiles, p.num_chunks);
     size_t o = HEADER_BYTES;
     p.off_scores = o;
     o = align_up(o + (size_t)B * nq * p.max_nblk * sizeof(float), WS_ALIGN);

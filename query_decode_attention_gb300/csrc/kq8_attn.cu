@@ -14,7 +14,23 @@ static int launch_attn_g(const AttnParams& p, int B, int nkv, cudaStream_t s) {
         cudaSuccess)
         return KQ8_ERR_CUDA;
     dim3 grid(p.num_chunks, nkv, B);
-    kern<<<grid, ATTN_THREADS, smem, s>>>(p);
+    if (SPARSE) {
+        // programmatic launch: the CTAs may start while the selection kernel
+        // before them finishes (they wait for it before reading its lists)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(ATTN_THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return KQ8_ERR_CUDA;
+    } else {
+        kern<<<grid, ATTN_THREADS, smem, s>>>(p);
+    }
     if (cudaGetLastError() != cudaSuccess) return KQ8_ERR_CUDA;
     if (p.num_chunks > 1 && p.counters == nullptr) {
         kq8_merge_kernel<SPARSE><<<B * p.nq, HD, 0, s>>>(p);

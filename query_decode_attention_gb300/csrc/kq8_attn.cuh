@@ -105,7 +105,7 @@ struct AttnSmem {
     alignas(16) uint32_t pw[ATTN_WARPS][G][TILE + 4];
     alignas(16) int8_t qi[G][HD];
     alignas(16) float qsc[G][NB];
-    int qsum[G][NB];  // sum of each 32-element block's Q codes (q4 cache only)
+    int qsum[G][NB];  // -8 x the sum of each 32-element block's Q codes (q4 cache only)
     alignas(8) uint64_t bar[ATTN_WARPS][ATTN_STAGES];
     int last;  // this CTA drew the last ticket of its (sequence, KV head)
 };
@@ -240,17 +240,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.vmap))
                      : "memory");
 
-    const SeqRange rng = seq_range<SPARSE>(P, b, h);
-    if (rng.bad && threadIdx.x == 0 && chunk == 0 && h == 0) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
-    const int n = rng.n, begin = rng.begin;
-    const int entries = rng.entries;
-    const int nch = max(1, (entries + P.chunk_tiles - 1) / P.chunk_tiles);
-    if (chunk >= nch) return;
-    const int e0 = chunk * P.chunk_tiles;
-    const int e1 = min(e0 + P.chunk_tiles, entries);
-    const int mine = (e1 - e0 > warp) ? (e1 - e0 - warp + ATTN_WARPS - 1) / ATTN_WARPS : 0;
-
     // ---- prologue: quantise the G query heads once (article 9-2 §2 seg. 1)
+    auto quantise_q = [&]() {
     for (int g = warp; g < G; g += ATTN_WARPS) {
         const float4 x =
             reinterpret_cast<const float4*>(P.q + ((size_t)b * P.nq + (size_t)h * G + g) * HD)[lane];
@@ -263,9 +254,27 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             qs4 += __shfl_xor_sync(0xffffffffu, qs4, 1);
             qs4 += __shfl_xor_sync(0xffffffffu, qs4, 2);
             qs4 += __shfl_xor_sync(0xffffffffu, qs4, 4);
-            if ((lane & 7) == 0) S.qsum[g][lane >> 3] = qs4;
+            if ((lane & 7) == 0) S.qsum[g][lane >> 3] = -8 * qs4;  // the dots' start value
         }
     }
+    };
+    if (SPARSE) {
+        // the tile lists come from the kernel before this one: with a
+        // programmatic launch this CTA is already resident while that kernel
+        // finishes, quantises Q, and only then waits for its results
+        quantise_q();
+        griddep_wait();
+    }
+    const SeqRange rng = seq_range<SPARSE>(P, b, h);
+    if (rng.bad && threadIdx.x == 0 && chunk == 0 && h == 0) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
+    const int n = rng.n, begin = rng.begin;
+    const int entries = rng.entries;
+    const int nch = max(1, (entries + P.chunk_tiles - 1) / P.chunk_tiles);
+    if (chunk >= nch) return;
+    const int e0 = chunk * P.chunk_tiles;
+    const int e1 = min(e0 + P.chunk_tiles, entries);
+    const int mine = (e1 - e0 > warp) ? (e1 - e0 - warp + ATTN_WARPS - 1) / ATTN_WARPS : 0;
+    if (!SPARSE) quantise_q();
     // ---- this warp's tiles, one per lane: tile index, head mask, page (-1 if bad)
     int my_tile = 0;
     uint32_t my_mask = 0;
@@ -404,7 +413,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                         *reinterpret_cast<const uint4*>(S.qi[g] + bb * 32 + (hs ^ 1) * 16);
                     int d;
                     if (Q4) {
-                        d = dp4a_us(kA.x, qA.x, -8 * S.qsum[g][bb]);
+                        d = dp4a_us(kA.x, qA.x, S.qsum[g][bb]);
                         d = dp4a_us(kA.y, qA.y, d);
                         d = dp4a_us(kA.z, qA.z, d);
                         d = dp4a_us(kA.w, qA.w, d);
@@ -562,8 +571,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                     // (64-byte swizzle: chunk cq of row t at cq ^ ((t / 2) % 4)).
                     // Register i holds for tokens 8i + 2c and + 1 the bytes 2(g%2),
                     // 2(g%2) + 1 of word 4cq + g/2: elements e0 = 32cq + 8(g/2) + 2(g%2),
-                    // e0 + 1 (low nibbles) and e0 + 4, e0 + 5 (high nibbles); nibble u
-                    // = code + 8 goes into the mantissa of 1024, minus 1032.
+                    // e0 + 1 (low nibbles) and e0 + 4, e0 + 5 (high nibbles).  A low
+                    // nibble u = code + 8 masked into the mantissa of 1024 gives 1024 + u,
+                    // minus 1032; a high one gives 1024 + 16u, times 1/16 minus 72 (one
+                    // fma): both exact.
                     const uint32_t vrow = smem_u32(vst) + (uint32_t)lane * (HD / 2);
 #pragma unroll
                     for (int cq = 0; cq < HD / 32; cq++) {
@@ -573,11 +584,13 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                         uint32_t b[4][4];  // [n-tile: +0, +1, +4, +5][register]
 #pragma unroll
                         for (int j = 0; j < 4; j++) {
-                            const uint32_t lo = r[j] & 0x0F0F0F0Fu, hi = (r[j] >> 4) & 0x0F0F0F0Fu;
-                            b[0][j] = hsub2(__byte_perm(lo, 0x64646464u, 0x4240), 0x64086408u);
-                            b[1][j] = hsub2(__byte_perm(lo, 0x64646464u, 0x4341), 0x64086408u);
-                            b[2][j] = hsub2(__byte_perm(hi, 0x64646464u, 0x4240), 0x64086408u);
-                            b[3][j] = hsub2(__byte_perm(hi, 0x64646464u, 0x4341), 0x64086408u);
+                            const uint32_t r8 = r[j] >> 8;  // bytes 1, 3 -> 0, 2
+                            b[0][j] = hsub2(and_or(r[j], 0x000F000Fu, 0x64006400u), 0x64086408u);
+                            b[1][j] = hsub2(and_or(r8, 0x000F000Fu, 0x64006400u), 0x64086408u);
+                            b[2][j] = hfma2(and_or(r[j], 0x00F000F0u, 0x64006400u), 0x2C002C00u,
+                                            0xD480D480u);
+                            b[3][j] = hfma2(and_or(r8, 0x00F000F0u, 0x64006400u), 0x2C002C00u,
+                                            0xD480D480u);
                         }
 #pragma unroll
                         for (int k = 0; k < 4; k++) {

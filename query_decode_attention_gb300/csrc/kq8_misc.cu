@@ -17,11 +17,11 @@ namespace kq8 {
 // The nearest integer comes from adding 1.5 * 2^23 + off (exact for |q| < 2^22):
 // the sum's low byte is then (n + off) mod 256, the code byte itself.  On the
 // fast path |q| < 127.5 (and < 7.5 for q4), so no clamp is needed there.
-// Returns the lane's four code bytes (element i in byte i); lo / hi clamp the
-// slow path, off is 0 (q8, two's complement) or 8 (q4, offset binary).
-__device__ __forceinline__ uint32_t quantize4(const float4 x, float d, float lo, float hi,
+// Returns the lane's four code bytes (element i in byte i); r = RN(1 / d) (the
+// caller computes it once per row), lo / hi clamp the slow path, off is 0 (q8,
+// two's complement) or 8 (q4, offset binary).
+__device__ __forceinline__ uint32_t quantize4(const float4 x, float d, float r, float lo, float hi,
                                               int off) {
-    const float r = __frcp_rn(d);
     const float magic = 12582912.0f + (float)off;  // 1.5 * 2^23 + off
     const float q0 = __fmul_rn(x.x, r), q1 = __fmul_rn(x.y, r);
     const float q2 = __fmul_rn(x.z, r), q3 = __fmul_rn(x.w, r);
@@ -40,84 +40,102 @@ __device__ __forceinline__ uint32_t quantize4(const float4 x, float d, float lo,
     return slow(x.x) | (slow(x.y) << 8) | (slow(x.z) << 16) | (slow(x.w) << 24);
 }
 
-// One (token, KV head) row of K or V, one warp: lane l holds elements
-// 4l..4l+3.  m = max |x| (exact, order-free), stored as the scale; codes are
-// roundf(x / (m * (1/127))) clamped to [-127, 127], as the oracle computes
-// them (IEEE quotient, see quantize4); an all-zero row gives zero codes.
-// Returns the lane's 4 codes.
-__device__ __forceinline__ uint32_t kv_quantize_lane(const float4 x, float& m_out) {
-    float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-    m = warp_max(m);
-    m_out = m;
-    if (m == 0.0f) return 0u;
-    return quantize4(x, __fmul_rn(m, inv127()), -127.0f, 127.0f, 0);
+__device__ __forceinline__ float absmax4(const float4 x) {
+    return fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+}
+
+// The q8 write path: one (token, KV head) row per group of LPR lanes, 32 / LPR
+// rows per warp (consecutive items: the heads of a token, whose fp32 rows are
+// contiguous).  Lane j of a group holds the float4s LPR * i + j (i < 32 / LPR)
+// of its row's K and V, elements 4 (LPR i + j) .. + 3, so every load
+// instruction reads whole 128-byte lines and every store writes whole 32-byte
+// sectors.  Bulk appends take LPR = 8 (16 elements per lane: the row's max
+// reduction, reciprocal and addressing are shared by four rows per warp); a
+// decode step's few new rows take LPR = 32 (a short chain per lane).  The scale
+// m = max |x| (exact, order-free) is stored; codes are roundf(x / (m *
+// (1/127))) clamped to [-127, 127], as the oracle computes them (IEEE quotient,
+// see quantize4); an all-zero row gives zero codes.
+template <int LPR>
+__global__ void __launch_bounds__(256)
+    kq8_append_kernel(const kq8_cache_t c, const float* __restrict__ k, const float* __restrict__ v,
+                      const int32_t* __restrict__ slot, int32_t T, uint32_t* status) {
+    constexpr int RPW = 32 / LPR, NI = HD / 4 / LPR;  // rows per warp, float4s per lane
+    const int lane = threadIdx.x & 31, j = lane % LPR, grp = lane / LPR;
+    const int64_t item0 =
+        ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RPW;
+    const int nkv = c.num_kv_heads, kv_bs = c.kv_bs;
+    const int64_t items = (int64_t)T * nkv;
+    if (item0 >= items) return;  // warp-uniform
+    const int64_t item = item0 + grp;
+    int64_t t = item0 / nkv;  // one division per warp, then the group's offset
+    int h = (int)(item0 - t * nkv) + grp;
+    while (h >= nkv) {
+        h -= nkv;
+        t++;
+    }
+    int32_t sl = -1;
+    float4 xk[NI], xv[NI];
+    if (item < items) {
+        sl = __ldg(slot + t);
+        const float4* kr = reinterpret_cast<const float4*>(k + (size_t)item * HD) + j;
+        const float4* vr = reinterpret_cast<const float4*>(v + (size_t)item * HD) + j;
+#pragma unroll
+        for (int i = 0; i < NI; i++) {
+            xk[i] = __ldcs(kr + LPR * i);
+            xv[i] = __ldcs(vr + LPR * i);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < NI; i++) xk[i] = xv[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    float mk = 0.0f, mv = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NI; i++) {
+        mk = fmaxf(mk, absmax4(xk[i]));
+        mv = fmaxf(mv, absmax4(xv[i]));
+    }
+#pragma unroll
+    for (int o = 1; o < LPR; o <<= 1) {  // within the group
+        mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+        mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+    }
+    if (sl < 0) return;  // past the end, or a skipped token (no collectives follow)
+    if ((int64_t)sl >= (int64_t)c.num_pages * kv_bs) {
+        if (j == 0 && status) atomicOr(status, KQ8_STATUS_BAD_SLOT);
+        return;
+    }
+    uint32_t ck[NI], cv[NI];
+#pragma unroll
+    for (int i = 0; i < NI; i++) ck[i] = cv[i] = 0u;
+    if (mk != 0.0f) {
+        const float d = __fmul_rn(mk, inv127()), r = __frcp_rn(d);
+#pragma unroll
+        for (int i = 0; i < NI; i++) ck[i] = quantize4(xk[i], d, r, -127.0f, 127.0f, 0);
+    }
+    if (mv != 0.0f) {
+        const float d = __fmul_rn(mv, inv127()), r = __frcp_rn(d);
+#pragma unroll
+        for (int i = 0; i < NI; i++) cv[i] = quantize4(xv[i], d, r, -127.0f, 127.0f, 0);
+    }
+    const int32_t page = sl / kv_bs;
+    const int rr = sl - page * kv_bs;
+    // K: element e of row rr at sub-tile rr/32, block e/32, position kpos(rr%32), byte e%32
+    int8_t* ko = c.k + kv_sub_off(page, h, nkv, kv_bs, rr / TILE) + (size_t)kpos(rr % TILE) * 32;
+    int8_t* vo = c.v + (page_head(page, h, nkv) * (size_t)kv_bs + rr) * HD;
+#pragma unroll
+    for (int i = 0; i < NI; i++) {
+        const int e = 4 * (LPR * i + j);
+        *reinterpret_cast<uint32_t*>(ko + (e >> 5) * 1024 + (e & 31)) = ck[i];
+        *reinterpret_cast<uint32_t*>(vo + e) = cv[i];
+    }
+    if (j == 0) {
+        const size_t so = page_head(page, h, nkv) * (size_t)kv_bs + rr;
+        c.kscale[so] = mk;
+        c.vscale[so] = mv;
+    }
 }
 
 constexpr int APPEND_WARPS = 8;
-
-// grid: ceil(T * nkv / (APPEND_WARPS * APPEND_ITEMS)) blocks of APPEND_WARPS
-// warps; warp = APPEND_ITEMS consecutive (token, head) items (consecutive
-// heads of a token: their fp32 rows are contiguous), each quantising its K and
-// its V row.  Every item's loads are issued before the first is used: bulk
-// appends take 4 rows per warp (more loads in flight), small ones (a decode
-// step's new tokens) 1 (more warps).
-template <int APPEND_ITEMS>
-__global__ void __launch_bounds__(APPEND_WARPS * 32)
-    kq8_append_kernel(const kq8_cache_t c, const float* __restrict__ k, const float* __restrict__ v,
-                      const int32_t* __restrict__ slot, int32_t T, uint32_t* status) {
-    const int lane = threadIdx.x & 31;
-    const int64_t item0 =
-        ((int64_t)blockIdx.x * APPEND_WARPS + (threadIdx.x >> 5)) * APPEND_ITEMS;
-    const int nkv = c.num_kv_heads, kv_bs = c.kv_bs;
-    const int64_t items = (int64_t)T * nkv;
-    if (item0 >= items) return;
-    float4 xk[APPEND_ITEMS], xv[APPEND_ITEMS];
-    int32_t sl[APPEND_ITEMS], hh[APPEND_ITEMS];
-    int64_t t = item0 / nkv;  // the only division: later items step through the heads
-    int h = (int)(item0 - t * nkv);
-#pragma unroll
-    for (int i = 0; i < APPEND_ITEMS; i++) {
-        const int64_t item = item0 + i;
-        sl[i] = -1;
-        hh[i] = h;
-        if (item < items) {
-            sl[i] = __ldg(slot + t);
-            const size_t row = (size_t)item * HD;
-            xk[i] = __ldcs(reinterpret_cast<const float4*>(k + row) + lane);
-            xv[i] = __ldcs(reinterpret_cast<const float4*>(v + row) + lane);
-        }
-        if (++h == nkv) {
-            h = 0;
-            t++;
-        }
-    }
-    const int64_t pool_slots = (int64_t)c.num_pages * kv_bs;
-#pragma unroll
-    for (int i = 0; i < APPEND_ITEMS; i++) {
-        if (sl[i] < 0) continue;  // past the end, or a skipped token
-        if ((int64_t)sl[i] >= pool_slots) {
-            if (lane == 0 && status) atomicOr(status, KQ8_STATUS_BAD_SLOT);
-            continue;
-        }
-        const int h = hh[i];
-        const int32_t page = sl[i] / kv_bs;
-        const int r = sl[i] % kv_bs;
-        float mk, mv;
-        const uint32_t ck = kv_quantize_lane(xk[i], mk);
-        const uint32_t cv = kv_quantize_lane(xv[i], mv);
-        // K: element e of row r at sub-tile r/32, block e/32, position kpos(r%32), byte e%32
-        const size_t ko = kv_sub_off(page, h, nkv, kv_bs, r / TILE) + (size_t)(lane >> 3) * 1024 +
-                          (size_t)kpos(r % TILE) * 32 + (size_t)(lane & 7) * 4;
-        *reinterpret_cast<uint32_t*>(c.k + ko) = ck;
-        const size_t vo = page_head(page, h, nkv) * (size_t)kv_bs * HD + (size_t)r * HD + lane * 4;
-        *reinterpret_cast<uint32_t*>(c.v + vo) = cv;
-        if (lane == 0) {
-            const size_t so = page_head(page, h, nkv) * (size_t)kv_bs + r;
-            c.kscale[so] = mk;
-            c.vscale[so] = mv;
-        }
-    }
-}
 
 // q4 write path (the q8 rule with 7 for 127): lane l holds elements 4l..4l+3
 // and returns their codes as offset-binary nibbles (code + 8) in the low
@@ -127,7 +145,8 @@ __device__ __forceinline__ uint32_t kv_quantize_lane_q4(const float4 x, float& m
     m = warp_max(m);
     m_out = m;
     if (m == 0.0f) return 0x08080808u;
-    return quantize4(x, __fmul_rn(m, inv7()), -7.0f, 7.0f, 8);
+    const float d = __fmul_rn(m, inv7());
+    return quantize4(x, d, __frcp_rn(d), -7.0f, 7.0f, 8);
 }
 
 // One warp per (token, head) as above; lanes 2w and 2w+1 hold the 8 elements of
@@ -190,14 +209,14 @@ int launch_append(const kq8_cache_t& c, const float* k, const float* v, const in
                   int32_t T, uint32_t* status, cudaStream_t stream) {
     const int64_t items = (int64_t)T * c.num_kv_heads;
     if (items == 0) return KQ8_OK;
+    // bulk: four rows per warp; a small append (a decode step's new tokens):
+    // one row per warp, so that each lane's chain stays short
     if (items < 8192) {
-        const int64_t blocks = (items + APPEND_WARPS - 1) / APPEND_WARPS;
-        kq8_append_kernel<1><<<(unsigned)blocks, APPEND_WARPS * 32, 0, stream>>>(c, k, v, slot, T,
-                                                                                status);
+        const int64_t blocks = (items + 7) / 8;
+        kq8_append_kernel<32><<<(unsigned)blocks, 256, 0, stream>>>(c, k, v, slot, T, status);
     } else {
-        const int64_t blocks = (items + APPEND_WARPS * 4 - 1) / (APPEND_WARPS * 4);
-        kq8_append_kernel<4><<<(unsigned)blocks, APPEND_WARPS * 32, 0, stream>>>(c, k, v, slot, T,
-                                                                                status);
+        const int64_t blocks = (items + 31) / 32;
+        kq8_append_kernel<8><<<(unsigned)blocks, 256, 0, stream>>>(c, k, v, slot, T, status);
     }
     return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
 }

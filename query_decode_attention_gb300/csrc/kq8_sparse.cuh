@@ -398,7 +398,7 @@ struct ProbeRow {
 };
 
 template <int G>
-__global__ void __launch_bounds__(PROBE_WARPS * 32) kq8_probe_kernel(const SparseParams P) {
+__global__ void __launch_bounds__(PROBE_WARPS * 32, 2) kq8_probe_kernel(const SparseParams P) {
     __shared__ __align__(16) int8_t qi[G][HD];
     __shared__ float qsc[G][NB];
     __shared__ int32_t pages[PROBE_MAX_PAGES];
@@ -407,6 +407,10 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32) kq8_probe_kernel(const Spars
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y, b = blockIdx.z;
     const int nkv = P.cache.num_kv_heads, kv_bs = P.cache.kv_bs;
+    // the attention kernel after this one may become resident as soon as every
+    // probe CTA has started; it waits for this grid's completion before it
+    // reads the tile lists
+    griddep_launch_dependents();
     int n = sparse_seq_len(P, b);
     if (n < 0 || n <= 2 * P.block) {  // gate: the exact path needs no probe
         if (P.tickets && blockIdx.x == 0) {
@@ -555,6 +559,7 @@ template <int G>
 __global__ void __launch_bounds__(TOPK_THREADS) kq8_topk_kernel(const SparseParams P) {
     __shared__ SelectSmem S;
     const int h = blockIdx.x, b = blockIdx.y;
+    griddep_launch_dependents();
     int n = sparse_seq_len(P, b);
     if (n < 0) {
         if (threadIdx.x == 0 && h == 0 && P.status) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
