@@ -235,6 +235,30 @@ int set_vmap(AttnParams& p, bool q4 = false) {
     return r == CUDA_SUCCESS ? KQ8_OK : KQ8_ERR_CUDA;
 }
 
+// The K array as the probe's 3-D tensor {1024 B: 32 positions x 32 B, 4 element
+// blocks, num_pages * nkv * kv_bs / 32 sub-tiles}, boxes of the first 8
+// positions of the 4 blocks (4 x 256 B), unswizzled.  Only for block = 4 *
+// probe, where every probe row sits at positions 0..7 of its sub-tile; the
+// probe keeps its register form otherwise (or when the map cannot be made).
+void set_probe_kmap(SparseParams& sp) {
+    sp.probe_tma = 0;
+    if (sp.block != 4 * sp.probe) return;
+    const kq8_cache_t& c = sp.cache;
+    const uint64_t subtiles =
+        (uint64_t)c.num_pages * (uint64_t)c.num_kv_heads * (uint64_t)(c.kv_bs / TILE);
+    if (subtiles == 0 || subtiles > 0x7FFFFFFFull) return;  // the copy's coordinate is int32
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return;
+    const cuuint64_t dims[3] = {(cuuint64_t)TILE * 32, (cuuint64_t)NB, (cuuint64_t)subtiles};
+    const cuuint64_t strides[2] = {(cuuint64_t)TILE * 32, (cuuint64_t)TILE * HD};
+    const cuuint32_t box[3] = {8u * 32u, (cuuint32_t)NB, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    if (enc(&sp.kmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.k, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+        sp.probe_tma = 1;
+}
+
 // Probe, top-k and bounded attention over `rows` decode rows (article 10-1
 // §1-§2); row_seq (optional) maps each row to its page-table row.
 int run_sparse(float* out, const float* q, const kq8_cache_t* cache, const int32_t* page_table,
@@ -261,6 +285,7 @@ int run_sparse(float* out, const float* q, const kq8_cache_t* cache, const int32
     sp.probe = probe;
     sp.max_nblk = plan.max_nblk;
     sp.probe_bpc = probe_blocks_per_cta(block, cache->kv_bs);
+    set_probe_kmap(sp);
     sp.scores = reinterpret_cast<float*>(ws + plan.off_scores);
     sp.masks = reinterpret_cast<uint32_t*>(ws + plan.off_masks);
     sp.tile_list = reinterpret_cast<int32_t*>(ws + plan.off_list);
@@ -622,6 +647,7 @@ int kq8_debug_probe_scores(float* scores, const float* q, const kq8_cache_t* cac
     sp.probe = probe;
     sp.max_nblk = (int)(((int64_t)max_seq_len + block - 1) / block);
     sp.probe_bpc = probe_blocks_per_cta(block, cache->kv_bs);
+    set_probe_kmap(sp);
     sp.scores = scores;
     sp.status = nullptr;  // bad page ids are skipped without a status word
     return launch_probe(sp, nq / cache->num_kv_heads, B, cache->num_kv_heads,

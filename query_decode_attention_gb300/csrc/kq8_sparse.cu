@@ -7,7 +7,15 @@ namespace kq8 {
 template <int G>
 static int launch_probe_g(const SparseParams& p, int B, int nkv, cudaStream_t s) {
     dim3 grid((p.max_nblk + p.probe_bpc - 1) / p.probe_bpc, nkv, B);
-    kq8_probe_kernel<G><<<grid, PROBE_WARPS * 32, 0, s>>>(p);
+    if (p.probe_tma) {
+        auto kern = kq8_probe_kernel<G, true>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)PROBE_RING_BYTES) != cudaSuccess)
+            return KQ8_ERR_CUDA;
+        kern<<<grid, PROBE_WARPS * 32, PROBE_RING_BYTES, s>>>(p);
+    } else {
+        kq8_probe_kernel<G, false><<<grid, PROBE_WARPS * 32, 0, s>>>(p);
+    }
     return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
 }
 

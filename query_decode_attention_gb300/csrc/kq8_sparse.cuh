@@ -15,6 +15,10 @@
 namespace kq8 {
 
 struct SparseParams {
+    // K sub-tiles as the 3-D tensor {1024 B (32 positions x 32 B), 4 element
+    // blocks, num_pages * nkv * kv_bs / 32 sub-tiles}: the probe's tensor copies
+    // of the first 8 positions of the 4 blocks (set when block = 4 * probe)
+    CUtensorMap kmap;
     const float* q;
     kq8_cache_t cache;
     const int32_t* page_table;
@@ -32,6 +36,7 @@ struct SparseParams {
     int32_t* list_len;       // [B][nkv]
     int32_t list_cap;
     int32_t* sel_blocks;     // optional [B][nq][topk]
+    int32_t probe_tma;       // 1: kmap is set, the probe takes the tensor-copy form
     uint32_t* status;
     const int32_t* row_seq;  // optional [B]: page-table row of row b (null = b)
     int32_t shared_sel;      // 1: one selection per KV head (max of its heads' block scores)
@@ -84,11 +89,16 @@ __device__ __forceinline__ int block_excl_scan(int v, int* tmp, int& total) {
     return base + x - v;
 }
 
+// Rows (query heads) selected together by the in-register selection: they
+// share every CTA barrier and scan.
+constexpr int SEL_HG = 2;
+constexpr int TOPK_KPT = 8;  // consecutive block scores per thread (in-register form)
+
 struct SelectSmem {
-    int hist[256];
-    int scan_tmp[TOPK_THREADS / 32];
-    uint32_t prefix;
-    int kk, cnt;
+    int hist[2][SEL_HG][256];  // double-buffered: a pass clears the next one's
+    int scan_tmp[SEL_HG + 1][TOPK_THREADS / 32];
+    uint32_t prefix[SEL_HG];
+    int kk[SEL_HG], cnt[SEL_HG];
     int last;
 };
 
@@ -154,27 +164,27 @@ __device__ void topk_row_global(const SparseParams& P, int b, int h, int g, int 
         int rem = k;
         for (int pass = 0; pass < 4; pass++) {
             const int shift = 24 - 8 * pass;
-            S.hist[tid] = 0;
+            S.hist[0][0][tid] = 0;
             __syncthreads();
             for (int j = tid; j < nblk; j += TOPK_THREADS) {
                 const uint32_t u = order_key(__ldcg(sc + j));
-                if ((u & pmask) == prefix) atomicAdd(&S.hist[(u >> shift) & 255], 1);
+                if ((u & pmask) == prefix) atomicAdd(&S.hist[0][0][(u >> shift) & 255], 1);
             }
             __syncthreads();
             // inclusive count from digit 255 downwards: thread t holds digit 255 - t
-            const int cnt = S.hist[255 - tid];
+            const int cnt = S.hist[0][0][255 - tid];
             int tot;
-            const int excl = block_excl_scan(cnt, S.scan_tmp, tot);
+            const int excl = block_excl_scan(cnt, S.scan_tmp[0], tot);
             if (excl < rem && excl + cnt >= rem) {
-                S.prefix = prefix | ((uint32_t)(255 - tid) << shift);
-                S.kk = rem - excl;
-                S.cnt = cnt;
+                S.prefix[0] = prefix | ((uint32_t)(255 - tid) << shift);
+                S.kk[0] = rem - excl;
+                S.cnt[0] = cnt;
             }
             __syncthreads();
-            prefix = S.prefix;
-            rem = S.kk;
+            prefix = S.prefix[0];
+            rem = S.kk[0];
             pmask |= 0xFFu << shift;
-            const bool all_kept = S.cnt == rem;
+            const bool all_kept = S.cnt[0] == rem;
             __syncthreads();
             if (all_kept) break;
         }
@@ -191,10 +201,10 @@ __device__ void topk_row_global(const SparseParams& P, int b, int h, int g, int 
         const bool gt = in && u > thr;
         const bool eq = in && !gt && u == thr;
         int tie_tot;
-        const int tie_rank = block_excl_scan(eq ? 1 : 0, S.scan_tmp, tie_tot) + ties_before;
+        const int tie_rank = block_excl_scan(eq ? 1 : 0, S.scan_tmp[0], tie_tot) + ties_before;
         const bool keep = gt || (eq && tie_rank < kk);
         int keep_tot;
-        const int pos = block_excl_scan(keep ? 1 : 0, S.scan_tmp, keep_tot) + kept_before;
+        const int pos = block_excl_scan(keep ? 1 : 0, S.scan_tmp[0], keep_tot) + kept_before;
         if (keep) {
             atomicOr(masks + j, bits);
             if (sel)
@@ -221,151 +231,299 @@ __device__ void build_union_global(const SparseParams& P, int b, int h, int n, i
         const uint32_t mk = (j < nblk) ? __ldcg(masks + j) : 0u;
         const int cnt = mk ? min(m, ntiles - j * m) : 0;
         int tot;
-        const int pos = block_excl_scan(cnt, S.scan_tmp, tot) + written;
+        const int pos = block_excl_scan(cnt, S.scan_tmp[0], tot) + written;
         for (int s = 0; s < cnt; s++) list[pos + s] = (j * m + s) | (int32_t)(mk << 24);
         written += tot;
     }
     if (threadIdx.x == 0) P.list_len[b * nkv + h] = written;
 }
 
-// The same selection with each thread holding TOPK_KPT consecutive block
-// scores in registers (rows of up to TOPK_THREADS * TOPK_KPT blocks): one read
-// of the row, histogram updates aggregated per warp (one shared atomic per
-// distinct digit), and the tie ranks and output positions from one block scan
-// each -- thread t's blocks are t*KPT .. t*KPT+KPT-1, so a scan over threads of
-// per-thread counts orders them by block index.
-constexpr int TOPK_KPT = 8;
-
-template <int G>
-__device__ void topk_row(const SparseParams& P, int b, int h, int g, int nblk, uint32_t* masks,
-                         uint32_t bits, int sel_rows, SelectSmem& S) {
-    if (nblk > TOPK_THREADS * TOPK_KPT) {
-        topk_row_global<G>(P, b, h, g, nblk, masks, bits, sel_rows, S);
-        return;
-    }
-    const int tid = threadIdx.x, lane = tid & 31;
-    const float* sc = P.scores + ((size_t)b * P.nq + (size_t)h * G + g) * P.max_nblk;
-    int32_t* sel = P.sel_blocks ? P.sel_blocks + ((size_t)b * P.nq + (size_t)h * G + g) * P.topk
-                                : nullptr;
-    const int k = min(P.topk, nblk);
-    const int j0 = tid * TOPK_KPT;
-    // keys of real blocks are >= 1 (order_key(-inf) = 0x007FFFFF): 0 marks "no block"
-    uint32_t key[TOPK_KPT];
+// Exclusive block-wide prefix sums of NV values at once (one set of barriers).
+template <int NV>
+__device__ __forceinline__ void block_excl_scan_v(const int (&v)[NV], int (&excl)[NV],
+                                                  int (&total)[NV],
+                                                  int (*tmp)[TOPK_THREADS / 32]) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x[NV];
 #pragma unroll
-    for (int i = 0; i < TOPK_KPT; i++) key[i] = (j0 + i < nblk) ? order_key(__ldcg(sc + j0 + i)) : 0u;
-    uint32_t thr = 0, tmask = 0;  // k == nblk: every block is kept
-    int kk = nblk;
-    if (k < nblk) {
-        uint32_t prefix = 0, pmask = 0;
-        int rem = k;
-        for (int pass = 0; pass < 4; pass++) {
-            const int shift = 24 - 8 * pass;
-            S.hist[tid] = 0;
-            __syncthreads();
+    for (int i = 0; i < NV; i++) x[i] = v[i];
 #pragma unroll
-            for (int i = 0; i < TOPK_KPT; i++) {
-                const bool in = key[i] != 0u && (key[i] & pmask) == prefix;
-                const uint32_t dig = (key[i] >> shift) & 255u;
-                const uint32_t peers = __match_any_sync(0xffffffffu, in ? dig : 0x100u);
-                if (in && (int)(__ffs(peers) - 1) == lane) atomicAdd(&S.hist[dig], __popc(peers));
-            }
-            __syncthreads();
-            // inclusive count from digit 255 downwards: thread t holds digit 255 - t
-            const int cnt = S.hist[255 - tid];
-            int tot;
-            const int excl = block_excl_scan(cnt, S.scan_tmp, tot);
-            if (excl < rem && excl + cnt >= rem) {
-                S.prefix = prefix | ((uint32_t)(255 - tid) << shift);
-                S.kk = rem - excl;
-                S.cnt = cnt;
-            }
-            __syncthreads();
-            prefix = S.prefix;
-            rem = S.kk;
-            pmask |= 0xFFu << shift;
-            const bool all_kept = S.cnt == rem;
-            __syncthreads();
-            if (all_kept) break;
+    for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+            const int y = __shfl_up_sync(0xffffffffu, x[i], o);
+            if (lane >= o) x[i] += y;
         }
-        thr = prefix;
-        tmask = pmask;
-        kk = rem;
-    }
-    // keep: top bits above thr, or equal to it among the first kk such blocks
-    uint32_t gt = 0, eq = 0;
+    if (lane == 31)
 #pragma unroll
-    for (int i = 0; i < TOPK_KPT; i++) {
-        const uint32_t u = key[i] & tmask;
-        const bool valid = key[i] != 0u;
-        gt |= (uint32_t)(valid && u > thr) << i;
-        eq |= (uint32_t)(valid && u == thr && !(u > thr)) << i;
-    }
-    int tie_tot;
-    int rank = block_excl_scan(__popc(eq), S.scan_tmp, tie_tot);
-    uint32_t keep = gt;
+        for (int i = 0; i < NV; i++) tmp[i][warp] = x[i];
+    __syncthreads();
 #pragma unroll
-    for (int i = 0; i < TOPK_KPT; i++)
-        if ((eq >> i) & 1u) keep |= (uint32_t)(rank++ < kk) << i;
-    int keep_tot;
-    int pos = block_excl_scan(__popc(keep), S.scan_tmp, keep_tot);
+    for (int i = 0; i < NV; i++) {
+        int base = 0, tot = 0;
 #pragma unroll
-    for (int i = 0; i < TOPK_KPT; i++) {
-        if (!((keep >> i) & 1u)) continue;
-        atomicOr(masks + j0 + i, bits);
-        if (sel)
-            for (int r = 0; r < sel_rows; r++) sel[(size_t)r * P.topk + pos] = j0 + i;
-        pos++;
+        for (int w = 0; w < TOPK_THREADS / 32; w++) {
+            const int t = tmp[i][w];
+            if (w < warp) base += t;
+            tot += t;
+        }
+        excl[i] = base + x[i] - v[i];
+        total[i] = tot;
     }
     __syncthreads();
 }
 
-// Union tile list from the masks, TOPK_KPT consecutive blocks per thread.
-template <int G>
-__device__ void build_union(const SparseParams& P, int b, int h, int n, int nblk,
-                            const uint32_t* masks, SelectSmem& S) {
-    if (nblk > TOPK_THREADS * TOPK_KPT) {
-        build_union_global<G>(P, b, h, n, nblk, masks, S);
-        return;
-    }
+// The selection and the union list for rows of up to TOPK_THREADS * TOPK_KPT
+// blocks, in registers: thread t holds the order-preserving keys of blocks
+// t*KPT .. t*KPT+KPT-1 of SEL_HG rows at a time (the G heads' rows, or one row
+// of the heads' maxima for a shared selection).  Per row a radix select finds
+// the k-th largest key 8 bits a pass from the top: every thread adds its keys
+// to the row's digit histogram (updates aggregated per warp with
+// __match_any_sync, one shared atomic per distinct digit), then warp r alone
+// scans row r's 256 counts and picks the digit -- two CTA barriers a pass; it
+// stops once every key of the chosen bucket is kept.  Keys above the
+// threshold are kept, plus the first kk equal to it by block index (a scan
+// ranks the ties, only when some are left out); one scan over per-thread
+// counts places the kept ids in ascending order (a thread's blocks are
+// consecutive) and, with the kept head bits held by their threads, the
+// entries of the union tile list.
+template <int G, bool SHARED>
+__device__ __forceinline__ void select_rows_smem(const SparseParams& P, int b, int h, int n,
+                                                 int nblk, SelectSmem& S) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nkv = P.cache.num_kv_heads;
+    const int j0 = tid * TOPK_KPT;
+    constexpr int rows = SHARED ? 1 : G;
+    const int k = min(P.topk, nblk);
     const int ntiles = (n + TILE - 1) / TILE;
     const int m = P.block / TILE;  // tiles per block
+    const float* sc0 = P.scores + ((size_t)b * P.nq + (size_t)h * G) * P.max_nblk;
+    uint8_t kept[TOPK_KPT];  // head bits of this thread's blocks
+#pragma unroll
+    for (int i = 0; i < TOPK_KPT; i++) kept[i] = 0;
+    // entries of the union list this thread writes (blocks are m tiles, the last one shorter)
+    auto list_count = [&]() {
+        int c = 0;
+#pragma unroll
+        for (int i = 0; i < TOPK_KPT; i++) c += kept[i] ? min(m, ntiles - (j0 + i) * m) : 0;
+        return c;
+    };
+    int list_pos = -1, list_tot = 0;
+#pragma unroll 1
+    for (int r0 = 0; r0 < rows; r0 += SEL_HG) {
+        const bool last_group = r0 + SEL_HG >= rows;
+        // keys of real blocks are >= 1 (order_key(-inf) = 0x007FFFFF): 0 marks "no block"
+        uint32_t key[SEL_HG][TOPK_KPT];
+#pragma unroll
+        for (int hh = 0; hh < SEL_HG; hh++)
+#pragma unroll
+            for (int i = 0; i < TOPK_KPT; i++) {
+                const int j = j0 + i;
+                const bool in = j < nblk && r0 + hh < rows;
+                float v = -INFINITY;
+                if (in) {
+                    if (SHARED) {
+                        v = __ldcg(sc0 + j);
+#pragma unroll
+                        for (int g = 1; g < G; g++) {
+                            const float x = __ldcg(sc0 + (size_t)g * P.max_nblk + j);
+                            v = x > v ? x : v;
+                        }
+                    } else {
+                        v = __ldcg(sc0 + (size_t)(r0 + hh) * P.max_nblk + j);
+                    }
+                }
+                key[hh][i] = in ? order_key(v) : 0u;
+            }
+        uint32_t prefix[SEL_HG], pmask[SEL_HG];
+        int rem[SEL_HG];
+        bool done[SEL_HG], exact[SEL_HG];  // exact: every key equal to the threshold is kept
+#pragma unroll
+        for (int hh = 0; hh < SEL_HG; hh++) {
+            prefix[hh] = 0u;
+            pmask[hh] = 0u;  // k == nblk: every block is kept (empty mask, threshold 0)
+            rem[hh] = k;
+            done[hh] = (k >= nblk) || (r0 + hh >= rows);
+            exact[hh] = true;
+            S.hist[0][hh][tid] = 0;
+        }
+        __syncthreads();
+#pragma unroll 1
+        for (int pass = 0; pass < 4; pass++) {
+            bool all = true;
+#pragma unroll
+            for (int hh = 0; hh < SEL_HG; hh++) all = all && done[hh];
+            if (all) break;  // uniform: every thread holds the same flags
+            const int cur = pass & 1, shift = 24 - 8 * pass;
+#pragma unroll
+            for (int hh = 0; hh < SEL_HG; hh++) {
+                S.hist[cur ^ 1][hh][tid] = 0;  // the next pass's buffer (read two barriers ago)
+                if (done[hh]) continue;
+                // pass 0 sees every key (and most share a few exponent digits):
+                // updates aggregated per warp; later passes only the few keys of
+                // the chosen bucket, added one by one
+#pragma unroll
+                for (int i = 0; i < TOPK_KPT; i++) {
+                    const bool in = key[hh][i] != 0u && (key[hh][i] & pmask[hh]) == prefix[hh];
+                    const uint32_t dig = (key[hh][i] >> shift) & 255u;
+                    if (pass == 0) {
+                        const uint32_t peers = __match_any_sync(0xffffffffu, in ? dig : 0x100u);
+                        if (in && (int)(__ffs(peers) - 1) == lane)
+                            atomicAdd(&S.hist[cur][hh][dig], __popc(peers));
+                    } else if (in) {
+                        atomicAdd(&S.hist[cur][hh][dig], 1);
+                    }
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int hh = 0; hh < SEL_HG; hh++) {
+                if (warp != hh || done[hh]) continue;
+                // lane l: digits 255 - 8l .. 248 - 8l, counted from the top
+                int c[8], sum = 0;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    c[i] = S.hist[cur][hh][255 - 8 * lane - i];
+                    sum += c[i];
+                }
+                int incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                int excl = incl - sum;
+                const int r = rem[hh];
+                if (excl < r && incl >= r) {
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        if (excl + c[i] >= r) {
+                            S.prefix[hh] = prefix[hh] | ((uint32_t)(255 - 8 * lane - i) << shift);
+                            S.kk[hh] = r - excl;
+                            S.cnt[hh] = c[i];
+                            break;
+                        }
+                        excl += c[i];
+                    }
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int hh = 0; hh < SEL_HG; hh++) {
+                if (done[hh]) continue;
+                prefix[hh] = S.prefix[hh];
+                rem[hh] = S.kk[hh];
+                pmask[hh] |= 0xFFu << shift;
+                done[hh] = S.cnt[hh] == rem[hh];
+                exact[hh] = done[hh];
+            }
+            // S.prefix / kk / cnt are next written after another barrier
+        }
+        // keep: top bits above the threshold, or equal to it among the first kk
+        uint32_t gt[SEL_HG], eq[SEL_HG];
+        bool ranks = false;
+#pragma unroll
+        for (int hh = 0; hh < SEL_HG; hh++) {
+            gt[hh] = eq[hh] = 0u;
+#pragma unroll
+            for (int i = 0; i < TOPK_KPT; i++) {
+                const uint32_t u = key[hh][i] & pmask[hh];
+                const bool valid = key[hh][i] != 0u;
+                gt[hh] |= (uint32_t)(valid && u > prefix[hh]) << i;
+                eq[hh] |= (uint32_t)(valid && u == prefix[hh]) << i;
+            }
+            ranks = ranks || !exact[hh];
+        }
+        uint32_t keep[SEL_HG];
+        if (ranks) {  // uniform: some row keeps only part of its threshold bucket
+            int ne[SEL_HG], rank[SEL_HG], tie_tot[SEL_HG];
+#pragma unroll
+            for (int hh = 0; hh < SEL_HG; hh++) ne[hh] = __popc(eq[hh]);
+            block_excl_scan_v<SEL_HG>(ne, rank, tie_tot, S.scan_tmp);
+#pragma unroll
+            for (int hh = 0; hh < SEL_HG; hh++) {
+                keep[hh] = gt[hh];
+#pragma unroll
+                for (int i = 0; i < TOPK_KPT; i++)
+                    if ((eq[hh] >> i) & 1u) keep[hh] |= (uint32_t)(rank[hh]++ < rem[hh]) << i;
+            }
+        } else {
+#pragma unroll
+            for (int hh = 0; hh < SEL_HG; hh++) keep[hh] = gt[hh] | eq[hh];
+        }
+#pragma unroll
+        for (int hh = 0; hh < SEL_HG; hh++) {
+            if (r0 + hh >= rows) continue;
+            const uint32_t bits = SHARED ? ((1u << G) - 1u) : (1u << (r0 + hh));
+#pragma unroll
+            for (int i = 0; i < TOPK_KPT; i++)
+                if ((keep[hh] >> i) & 1u) kept[i] |= (uint8_t)bits;
+        }
+        // positions of the kept ids (and, in the last group, of the list entries)
+        int cnt[SEL_HG + 1], pos[SEL_HG + 1], tot[SEL_HG + 1];
+#pragma unroll
+        for (int hh = 0; hh < SEL_HG; hh++) cnt[hh] = __popc(keep[hh]);
+        cnt[SEL_HG] = last_group ? list_count() : 0;
+        block_excl_scan_v<SEL_HG + 1>(cnt, pos, tot, S.scan_tmp);
+        if (last_group) {
+            list_pos = pos[SEL_HG];
+            list_tot = tot[SEL_HG];
+        }
+#pragma unroll
+        for (int hh = 0; hh < SEL_HG; hh++) {
+            if (r0 + hh >= rows || !P.sel_blocks) continue;
+            constexpr int sel_rows = SHARED ? G : 1;
+            int32_t* sel = P.sel_blocks + ((size_t)b * P.nq + (size_t)h * G + r0 + hh) * P.topk;
+            int p = pos[hh];
+            for (uint32_t kb = keep[hh]; kb != 0u; kb &= kb - 1u, p++) {
+                const int j = j0 + __ffs(kb) - 1;
+#pragma unroll
+                for (int r = 0; r < sel_rows; r++) sel[(size_t)r * P.topk + p] = j;
+            }
+            // fewer blocks than topk: the rest of the row is -1
+            if (tid == 0)
+                for (int r = 0; r < sel_rows; r++)
+                    for (int i = k; i < P.topk; i++) sel[(size_t)r * P.topk + i] = -1;
+        }
+    }
+    // the union tile list: ascending blocks, entry = tile | head mask << 24
     int32_t* list = P.tile_list + (size_t)(b * nkv + h) * P.list_cap;
-    const int j0 = threadIdx.x * TOPK_KPT;
-    uint32_t mk[TOPK_KPT];
-    int cnt = 0;
+    uint32_t any = 0;
 #pragma unroll
-    for (int i = 0; i < TOPK_KPT; i++) {
-        mk[i] = (j0 + i < nblk) ? __ldcg(masks + j0 + i) : 0u;
-        cnt += mk[i] ? min(m, ntiles - (j0 + i) * m) : 0;
-    }
-    int tot;
-    int pos = block_excl_scan(cnt, S.scan_tmp, tot);
+    for (int i = 0; i < TOPK_KPT; i++) any |= (uint32_t)(kept[i] != 0) << i;
+    for (; any != 0u; any &= any - 1u) {
+        const int i = __ffs(any) - 1;
+        uint32_t bitsi = 0;
 #pragma unroll
-    for (int i = 0; i < TOPK_KPT; i++) {
-        if (!mk[i]) continue;
-        const int j = j0 + i, c = min(m, ntiles - j * m);
-        for (int s2 = 0; s2 < c; s2++) list[pos + s2] = (j * m + s2) | (int32_t)(mk[i] << 24);
-        pos += c;
+        for (int x = 0; x < TOPK_KPT; x++) bitsi = (x == i) ? kept[x] : bitsi;
+        const int c = min(m, ntiles - (j0 + i) * m);
+        for (int s2 = 0; s2 < c; s2++)
+            list[list_pos++] = ((j0 + i) * m + s2) | (int32_t)(bitsi << 24);
     }
-    if (threadIdx.x == 0) P.list_len[b * nkv + h] = tot;
+    if (tid == 0) P.list_len[b * nkv + h] = list_tot;
 }
 
-// Every head of (b, h), or the group's one shared selection, then the union.
-// Not inlined: its registers stay out of the probe loop's allocation.
 template <int G>
-__device__ __noinline__ void select_all(const SparseParams& P, int b, int h, int n, SelectSmem& S) {
+__device__ __forceinline__ void select_all(const SparseParams& P, int b, int h, int n,
+                                           SelectSmem& S) {
     const int nblk = (n + P.block - 1) / P.block;
+    if (nblk <= TOPK_THREADS * TOPK_KPT) {
+        if (P.shared_sel)
+            select_rows_smem<G, true>(P, b, h, n, nblk, S);
+        else
+            select_rows_smem<G, false>(P, b, h, n, nblk, S);
+        return;
+    }
     uint32_t* masks = P.masks + (size_t)(b * P.cache.num_kv_heads + h) * P.max_nblk;
     clear_selection<G>(P, b, h, 0, G);
     __syncthreads();
     if (P.shared_sel) {
         group_max_scores<G>(P, b, h, nblk);
-        topk_row<G>(P, b, h, 0, nblk, masks, (1u << G) - 1u, G, S);
+        topk_row_global<G>(P, b, h, 0, nblk, masks, (1u << G) - 1u, G, S);
     } else {
-        for (int g = 0; g < G; g++) topk_row<G>(P, b, h, g, nblk, masks, 1u << g, 1, S);
+        for (int g = 0; g < G; g++) topk_row_global<G>(P, b, h, g, nblk, masks, 1u << g, 1, S);
     }
-    build_union<G>(P, b, h, n, nblk, masks, S);
+    build_union_global<G>(P, b, h, n, nblk, masks, S);
 }
 
 // ---------------------------------------------------------------------------
@@ -390,6 +548,11 @@ static_assert(PROBE_WARPS * 32 == TOPK_THREADS, "the probe CTA runs the selectio
 // epilogue weigh little against the streaming.
 constexpr int PROBE_MAX_BPC = 256;
 constexpr int PROBE_MAX_PAGES = 512;   // page ids a CTA stages
+// Tensor-copy form (block = 4 * probe): per warp a ring of PROBE_STAGES units,
+// each the 4 sub-tiles' probe positions (4 x 1 KB), in dynamic shared memory.
+constexpr int PROBE_STAGES = 3;
+constexpr int PROBE_UNIT_BYTES = 4 * 1024;
+constexpr size_t PROBE_RING_BYTES = (size_t)PROBE_WARPS * PROBE_STAGES * PROBE_UNIT_BYTES;
 
 struct ProbeRow {
     uint4 k[2 * NB];  // the row's 128 int8 codes, block by block
@@ -397,13 +560,20 @@ struct ProbeRow {
     bool valid;
 };
 
-template <int G>
-__global__ void __launch_bounds__(PROBE_WARPS * 32, 2) kq8_probe_kernel(const SparseParams P) {
+// TMA: the probe rows come in by tensor copies into a per-warp ring of shared
+// memory (more bytes in flight per SM than registers can hold); valid when
+// block = 4 * probe, where pass q of a block reads positions 0..7 (tokens 0, 4,
+// .., 28) of its sub-tile q -- 4 runs of 256 bytes, 1 KB apart, one box.
+template <int G, bool TMA>
+__global__ void __launch_bounds__(PROBE_WARPS * 32, 2)
+    kq8_probe_kernel(const __grid_constant__ SparseParams P) {
     __shared__ __align__(16) int8_t qi[G][HD];
     __shared__ float qsc[G][NB];
     __shared__ int32_t pages[PROBE_MAX_PAGES];
     __shared__ float best[PROBE_MAX_BPC][G];
     __shared__ SelectSmem sel_smem;
+    __shared__ __align__(8) uint64_t pbar[TMA ? PROBE_WARPS : 1][PROBE_STAGES];
+    extern __shared__ __align__(1024) uint8_t probe_ring[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y, b = blockIdx.z;
     const int nkv = P.cache.num_kv_heads, kv_bs = P.cache.kv_bs;
@@ -451,6 +621,14 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32, 2) kq8_probe_kernel(const Sp
         reinterpret_cast<uint32_t*>(qi[g])[lane] = codes;
         if ((lane & 7) == 0) qsc[g][lane >> 3] = qs;
     }
+    if (TMA) {
+        if (lane == 0)
+            for (int i = 0; i < PROBE_STAGES; i++) mbar_init(&pbar[warp][i], 1);
+        if (threadIdx.x == 0)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.kmap))
+                         : "memory");
+        fence_barrier_init();
+    }
     __syncthreads();
 
     const int gb = lane >> 3, pr = lane & 7;
@@ -494,15 +672,17 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32, 2) kq8_probe_kernel(const Sp
             }
         }
     };
-    auto compute = [&](const ProbeRow& R, int k) {
+    // R.k[2 bb] holds bytes 16 qh .. + 15 of block bb of the row, R.k[2 bb + 1] the
+    // other half (the integer dot does not depend on the order)
+    auto compute = [&](const ProbeRow& R, int k, int qh) {
         const int jj = block_of(k);
 #pragma unroll
         for (int g = 0; g < G; g++) {
             int d[NB];
 #pragma unroll
             for (int bb = 0; bb < NB; bb++) {
-                const uint4 qa = *reinterpret_cast<const uint4*>(qi[g] + bb * 32);
-                const uint4 qb = *reinterpret_cast<const uint4*>(qi[g] + bb * 32 + 16);
+                const uint4 qa = *reinterpret_cast<const uint4*>(qi[g] + bb * 32 + qh * 16);
+                const uint4 qb = *reinterpret_cast<const uint4*>(qi[g] + bb * 32 + (qh ^ 1) * 16);
                 const uint4 ka = R.k[2 * bb], kb = R.k[2 * bb + 1];
                 int x = __dp4a((int)ka.x, (int)qa.x, 0);
                 x = __dp4a((int)ka.y, (int)qa.y, x);
@@ -521,14 +701,90 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32, 2) kq8_probe_kernel(const Sp
             if (pr == 0 && jj < j1) best[jj - j0][g] = fmaxf(best[jj - j0][g], s);
         }
     };
-    ProbeRow A, Bu;
-    if (nunits > 0) load(A, 0);
-    for (int k = 0; k < nunits; k += 2) {
-        if (k + 1 < nunits) load(Bu, k + 1);
-        compute(A, k);
-        if (k + 1 >= nunits) break;
-        if (k + 2 < nunits) load(A, k + 2);
-        compute(Bu, k + 1);
+    if constexpr (TMA) {
+        constexpr int NS = PROBE_STAGES;
+        uint8_t* ring = probe_ring + (size_t)warp * NS * PROBE_UNIT_BYTES;
+        const int subs = kv_bs / TILE;
+        const int hs = (pr >> 2) & 1;  // half order: conflict-free shared loads
+        // this lane's probe row of unit k: token t, page pg; false if none
+        auto row_of = [&](int k, int& t, int& pg) {
+            const int jj = block_of(k), pass = k / my_groups;
+            t = jj * P.block + (8 * pass + pr) * 4;
+            pg = (jj < j1 && t < n) ? pages[t / kv_bs - pg0] : -1;
+            return pg >= 0;
+        };
+        // all lanes: the row's stored maximum (returned); lane 0: the copies of
+        // the unit's sub-tiles (lane 8gb's row is its sub-tile's first)
+        auto issue = [&](int k, int s) -> float {
+            int t, pg;
+            const bool ok = row_of(k, t, pg);
+            float kst = 0.0f;
+            if (ok)
+                kst = __ldg(P.cache.kscale +
+                            scale_sub_off(pg, h, nkv, kv_bs, (t % kv_bs) / TILE) + t % TILE);
+            const uint32_t copy = __ballot_sync(0xffffffffu, ok && pr == 0);
+            int zc[4];
+#pragma unroll
+            for (int g4 = 0; g4 < 4; g4++) {
+                const int tg = __shfl_sync(0xffffffffu, t, 8 * g4);
+                const int pgg = __shfl_sync(0xffffffffu, pg, 8 * g4);
+                zc[g4] = (int)page_head(pgg, h, nkv) * subs + (tg % kv_bs) / TILE;
+            }
+            if (lane == 0) {
+                uint64_t* bar = &pbar[warp][s];
+                mbar_arrive_expect_tx(bar, (uint32_t)__popc(copy) * 1024u);
+                const uint64_t pol = l2_evict_first_policy();  // read once
+#pragma unroll
+                for (int g4 = 0; g4 < 4; g4++)
+                    if (copy & (1u << (8 * g4)))
+                        tma_load_3d(ring + s * PROBE_UNIT_BYTES + g4 * 1024, &P.kmap, 0, 0,
+                                    zc[g4], bar, pol);
+            }
+            return kst;
+        };
+        float scr[NS];  // the rows' stored maxima of the units in flight
+#pragma unroll
+        for (int i = 0; i < NS; i++) scr[i] = (i < nunits) ? issue(i, i) : 0.0f;
+        int k = 0;
+        bool failed = false;
+        for (; k < nunits; k++) {
+            const int s = k % NS;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&pbar[warp][s], (k / NS) & 1))) {
+                failed = true;
+                break;
+            }
+            ProbeRow R;
+            int t, pg;
+            R.valid = row_of(k, t, pg);
+            R.kst = scr[0];
+            const uint8_t* row = ring + s * PROBE_UNIT_BYTES + gb * 1024 + pr * 32;
+#pragma unroll
+            for (int bb = 0; bb < NB; bb++) {
+                R.k[2 * bb] = *reinterpret_cast<const uint4*>(row + bb * 256 + hs * 16);
+                R.k[2 * bb + 1] = *reinterpret_cast<const uint4*>(row + bb * 256 + (hs ^ 1) * 16);
+            }
+            compute(R, k, hs);
+#pragma unroll
+            for (int i = 0; i + 1 < NS; i++) scr[i] = scr[i + 1];
+            __syncwarp();
+            if (k + NS < nunits) scr[NS - 1] = issue(k + NS, s);
+        }
+        if (failed) {
+            if (lane == 0 && P.status) atomicOr(P.status, KQ8_STATUS_TIMEOUT);
+            // let the copies still in flight land before the CTA leaves
+            for (int j = k; j < nunits && j < k + NS; j++)
+                __all_sync(0xffffffffu, mbar_wait_bounded(&pbar[warp][j % NS], (j / NS) & 1));
+        }
+    } else {
+        ProbeRow A, Bu;
+        if (nunits > 0) load(A, 0);
+        for (int k = 0; k < nunits; k += 2) {
+            if (k + 1 < nunits) load(Bu, k + 1);
+            compute(A, k, 0);
+            if (k + 1 >= nunits) break;
+            if (k + 2 < nunits) load(A, k + 2);
+            compute(Bu, k + 1, 0);
+        }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < (j1 - j0) * G; i += PROBE_WARPS * 32) {
@@ -556,7 +812,8 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32, 2) kq8_probe_kernel(const Sp
 // threads per KV head selecting its G heads in turn.
 // ---------------------------------------------------------------------------
 template <int G>
-__global__ void __launch_bounds__(TOPK_THREADS) kq8_topk_kernel(const SparseParams P) {
+__global__ void __launch_bounds__(TOPK_THREADS)
+    kq8_topk_kernel(const __grid_constant__ SparseParams P) {
     __shared__ SelectSmem S;
     const int h = blockIdx.x, b = blockIdx.y;
     griddep_launch_dependents();
