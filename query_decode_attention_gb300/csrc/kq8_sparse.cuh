@@ -359,20 +359,10 @@ __device__ __forceinline__ void select_rows_smem(const SparseParams& P, int b, i
             for (int hh = 0; hh < SEL_HG; hh++) {
                 S.hist[cur ^ 1][hh][tid] = 0;  // the next pass's buffer (read two barriers ago)
                 if (done[hh]) continue;
-                // pass 0 sees every key (and most share a few exponent digits):
-                // updates aggregated per warp; later passes only the few keys of
-                // the chosen bucket, added one by one
 #pragma unroll
                 for (int i = 0; i < TOPK_KPT; i++) {
                     const bool in = key[hh][i] != 0u && (key[hh][i] & pmask[hh]) == prefix[hh];
-                    const uint32_t dig = (key[hh][i] >> shift) & 255u;
-                    if (pass == 0) {
-                        const uint32_t peers = __match_any_sync(0xffffffffu, in ? dig : 0x100u);
-                        if (in && (int)(__ffs(peers) - 1) == lane)
-                            atomicAdd(&S.hist[cur][hh][dig], __popc(peers));
-                    } else if (in) {
-                        atomicAdd(&S.hist[cur][hh][dig], 1);
-                    }
+                    if (in) atomicAdd(&S.hist[cur][hh][(key[hh][i] >> shift) & 255u], 1);
                 }
             }
             __syncthreads();
