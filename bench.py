@@ -400,7 +400,11 @@ class Scenario:
             self.chunk_tiles, self.num_chunks = kq8.kq8_sparse_decode_plan(
                 B, nq, nkv, wl.max_seq_len, wl.block, wl.topk)
             self.sel = torch.empty((B, nq, wl.topk), dtype=torch.int32, device=dev)
-            self.launches_per_layer = 4 + (1 if self._merge_kernel() else 0)
+            # append, probe (its last CTA per (sequence, KV head) selects) and the
+            # bounded attention; past the 16384 counters the selection and the
+            # merge run as kernels of their own
+            many = B * nkv > 16384
+            self.launches_per_layer = 3 + (1 if many else 0) + (1 if self._merge_kernel() else 0)
         else:
             nb = kq8.kq8_decode_workspace_bytes(B, nq, nkv, wl.max_seq_len)
             self.chunk_tiles, self.num_chunks = kq8.kq8_decode_plan(B, nq, nkv, wl.max_seq_len)
