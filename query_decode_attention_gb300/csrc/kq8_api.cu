@@ -285,6 +285,20 @@ int run_sparse(float* out, const float* q, const kq8_cache_t* cache, const int32
     sp.probe = probe;
     sp.max_nblk = plan.max_nblk;
     sp.probe_bpc = probe_blocks_per_cta(block, cache->kv_bs);
+    {
+        // A probe grid that does not fill the SMs once (small batches) is latency,
+        // not bytes: give each (sequence, KV head) more, shorter CTAs, in steps of
+        // 32 blocks (one unit of 4 blocks for each of the 8 warps).
+        const long long pairs = (long long)rows * nkv;
+        const int sms = device_sms();
+        const long long cpp = (plan.max_nblk + sp.probe_bpc - 1) / sp.probe_bpc;
+        if (pairs > 0 && pairs * cpp < sms) {
+            const long long want = sms / pairs > 1 ? sms / pairs : 1;
+            long long bpc = (plan.max_nblk + want - 1) / want;
+            bpc = (bpc + 31) / 32 * 32;
+            if (bpc < sp.probe_bpc) sp.probe_bpc = (int)bpc;
+        }
+    }
     set_probe_kmap(sp);
     sp.scores = reinterpret_cast<float*>(ws + plan.off_scores);
     sp.masks = reinterpret_cast<uint32_t*>(ws + plan.off_masks);

@@ -583,6 +583,21 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32, 2)
         return;
     }
     const int nblk = (n + P.block - 1) / P.block;
+    if (P.tickets && nblk <= P.topk) {
+        // every block is kept whatever its score: the selection is blocks 0 ..
+        // nblk - 1 in order for every head, the union every tile (no scores are
+        // needed; with tickets nothing after this kernel reads them)
+        if (blockIdx.x == 0) {
+            if (P.sel_blocks)
+                for (int g = 0; g < G; g++) {
+                    int32_t* sel = P.sel_blocks + ((size_t)b * P.nq + (size_t)h * G + g) * P.topk;
+                    for (int i = threadIdx.x; i < P.topk; i += PROBE_WARPS * 32)
+                        sel[i] = i < nblk ? i : -1;
+                }
+            gated_list<G>(P, b, h, n);
+        }
+        return;
+    }
     const int j0 = blockIdx.x * P.probe_bpc;
     if (j0 >= nblk) return;
     const int j1 = min(j0 + P.probe_bpc, nblk);

@@ -281,6 +281,19 @@ def test_sparse_matches_oracle(n):
     assert_out_close(got, ref, f"sparse n={n}")
 
 
+def test_sparse_rows_that_keep_every_block_next_to_probed_rows():
+    # rows past the gate (n > 2 * block) but with no more blocks than topk keep
+    # every block, in order, without a probe; they share the batch with rows
+    # that are probed and selected, and with a gated and an empty row
+    wl = W.custom(5, 16, 8, [506, 4059, 100, 64, 0], seed=81, block=32, topk=32, probe=8)
+    case, q, Ks, Vs = _host_case(wl)
+    got, sel = _decode(case, sparse=True, sel=True)
+    ref, rsel = oracle_decode(wl, q, Ks, Vs, sparse=True)
+    assert np.array_equal(sel, rsel)
+    assert (sel[0, :, :16] == np.arange(16)).all() and (sel[0, :, 16:] == -1).all()
+    assert_out_close(got, ref, "sparse, kept-all rows among probed rows")
+
+
 def test_sparse_many_sequences_one_topk_cta_per_kv_head():
     # more (sequence, KV head) pairs than the workspace header has counters
     # (16384): the top-k runs one CTA per KV head selecting its G heads in
