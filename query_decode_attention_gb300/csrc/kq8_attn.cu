@@ -14,9 +14,11 @@ static int launch_attn_g(const AttnParams& p, int B, int nkv, cudaStream_t s) {
         cudaSuccess)
         return KQ8_ERR_CUDA;
     dim3 grid(p.num_chunks, nkv, B);
-    if (SPARSE) {
-        // programmatic launch: the CTAs may start while the selection kernel
-        // before them finishes (they wait for it before reading its lists)
+    {
+        // programmatic launch: the CTAs may start while the kernel before them
+        // (the append of the new tokens, or the selection) finishes; they wait
+        // for it before reading what it writes (the KV, or the tile lists).  A
+        // kernel that does not signal its dependents still completes first.
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
         cfg.blockDim = dim3(ATTN_THREADS);
@@ -28,8 +30,6 @@ static int launch_attn_g(const AttnParams& p, int B, int nkv, cudaStream_t s) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return KQ8_ERR_CUDA;
-    } else {
-        kern<<<grid, ATTN_THREADS, smem, s>>>(p);
     }
     if (cudaGetLastError() != cudaSuccess) return KQ8_ERR_CUDA;
     if (p.num_chunks > 1 && p.counters == nullptr) {

@@ -334,6 +334,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             }
         }
     };
+    // the KV this call reads may have been appended by the kernel just before
+    // (a programmatic launch lets this CTA's prologue overlap it): wait for it
+    // before the first copy
+    if (!SPARSE) griddep_wait();
     for (int i = 0; i < NS && i < mine; i++) issue(i);
 
     float M2[G], Sl[G];

@@ -60,6 +60,9 @@ __global__ void __launch_bounds__(256)
     kq8_append_kernel(const kq8_cache_t c, const float* __restrict__ k, const float* __restrict__ v,
                       const int32_t* __restrict__ slot, int32_t T, uint32_t* status) {
     constexpr int RPW = 32 / LPR, NI = HD / 4 / LPR;  // rows per warp, float4s per lane
+    // the decode attention launched after this kernel may start its prologue
+    // now; it waits for this grid's completion before reading the cache
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31, j = lane % LPR, grp = lane / LPR;
     const int64_t item0 =
         ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RPW;
@@ -157,6 +160,7 @@ __global__ void __launch_bounds__(APPEND_WARPS * 32)
     kq8_append_q4_kernel(const kq8_cache_t c, const float* __restrict__ k,
                          const float* __restrict__ v, const int32_t* __restrict__ slot, int32_t T,
                          uint32_t* status) {
+    griddep_launch_dependents();  // see kq8_append_kernel
     const int lane = threadIdx.x & 31;
     const int64_t item = (int64_t)blockIdx.x * APPEND_WARPS + (threadIdx.x >> 5);
     const int nkv = c.num_kv_heads, kv_bs = c.kv_bs;
