@@ -235,6 +235,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int nkv = P.cache.num_kv_heads, kv_bs = P.cache.kv_bs;
     const int subs = kv_bs / TILE;
+    // a programmatic launch after this one (the next append, update or layer)
+    // may be scheduled now: each of those waits for this grid's completion
+    // before it touches what this kernel reads or writes
+    griddep_launch_dependents();
     // fetch the V tensor map's descriptor while the prologue runs
     if (!Q4 && threadIdx.x == 0)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.vmap))

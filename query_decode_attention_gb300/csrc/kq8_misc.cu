@@ -60,6 +60,9 @@ __global__ void __launch_bounds__(256)
     kq8_append_kernel(const kq8_cache_t c, const float* __restrict__ k, const float* __restrict__ v,
                       const int32_t* __restrict__ slot, int32_t T, uint32_t* status) {
     constexpr int RPW = 32 / LPR, NI = HD / 4 / LPR;  // rows per warp, float4s per lane
+    // launched programmatically: nothing is read or written before the kernel
+    // before this one has completed
+    griddep_wait();
     // the decode attention launched after this kernel may start its prologue
     // now; it waits for this grid's completion before reading the cache
     griddep_launch_dependents();
@@ -160,7 +163,8 @@ __global__ void __launch_bounds__(APPEND_WARPS * 32)
     kq8_append_q4_kernel(const kq8_cache_t c, const float* __restrict__ k,
                          const float* __restrict__ v, const int32_t* __restrict__ slot, int32_t T,
                          uint32_t* status) {
-    griddep_launch_dependents();  // see kq8_append_kernel
+    griddep_wait();  // see kq8_append_kernel
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t item = (int64_t)blockIdx.x * APPEND_WARPS + (threadIdx.x >> 5);
     const int nkv = c.num_kv_heads, kv_bs = c.kv_bs;
@@ -199,14 +203,34 @@ __global__ void __launch_bounds__(APPEND_WARPS * 32)
     }
 }
 
+// The appends are programmatic launches: their CTAs may be scheduled while the
+// kernel before them (typically the previous layer's attention) finishes, and
+// wait for its completion before they read or write anything, so the stream
+// order of the call's effects is unchanged; only the launch latency overlaps.
+template <typename... KArgs, typename... Args>
+static int launch_pdl(void (*kern)(KArgs...), int64_t blocks, int threads, cudaStream_t stream,
+                      Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) return KQ8_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+}
+
 int launch_append_q4(const kq8_cache_t& c, const float* k, const float* v, const int32_t* slot,
                      int32_t T, uint32_t* status, cudaStream_t stream) {
     const int64_t items = (int64_t)T * c.num_kv_heads;
     if (items == 0) return KQ8_OK;
     const int64_t blocks = (items + APPEND_WARPS - 1) / APPEND_WARPS;
-    kq8_append_q4_kernel<<<(unsigned)blocks, APPEND_WARPS * 32, 0, stream>>>(c, k, v, slot, T,
-                                                                            status);
-    return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+    return launch_pdl(kq8_append_q4_kernel, blocks, APPEND_WARPS * 32, stream, c, k, v, slot, T,
+                      status);
 }
 
 int launch_append(const kq8_cache_t& c, const float* k, const float* v, const int32_t* slot,
@@ -215,14 +239,11 @@ int launch_append(const kq8_cache_t& c, const float* k, const float* v, const in
     if (items == 0) return KQ8_OK;
     // bulk: four rows per warp; a small append (a decode step's new tokens):
     // one row per warp, so that each lane's chain stays short
-    if (items < 8192) {
-        const int64_t blocks = (items + 7) / 8;
-        kq8_append_kernel<32><<<(unsigned)blocks, 256, 0, stream>>>(c, k, v, slot, T, status);
-    } else {
-        const int64_t blocks = (items + 31) / 32;
-        kq8_append_kernel<8><<<(unsigned)blocks, 256, 0, stream>>>(c, k, v, slot, T, status);
-    }
-    return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
+    if (items < 8192)
+        return launch_pdl(kq8_append_kernel<32>, (items + 7) / 8, 256, stream, c, k, v, slot, T,
+                          status);
+    return launch_pdl(kq8_append_kernel<8>, (items + 31) / 32, 256, stream, c, k, v, slot, T,
+                      status);
 }
 
 // ---------------------------------------------------------------------------
