@@ -41,16 +41,26 @@ int device_sms() {
 #define KQ8_MAX_CHUNK 128
 #endif
 // Split of each (sequence, KV head) list of `tiles_max` 32-token tiles into
-// chunks of `chunk_tiles` tiles (a multiple of the CTA's 4 warps).  The chunk
-// is sized so that B * nkv * (chunks) CTAs give about four waves of three CTAs
-// per SM, between 4 and KQ8_MAX_CHUNK tiles (128 to 4096 tokens): each CTA has
-// a prologue and a merge tail in which it streams nothing, so large problems
-// take long chunks.
-void chunking(int64_t B, int64_t nkv, int64_t tiles_max, int sms, int& ct, int& nch) {
+// chunks of `chunk_tiles` tiles (a multiple of the CTA's 4 warps), for
+// `per_sm` resident attention CTAs per SM.  If every list fits one wave of CTAs
+// with chunks of at most KQ8_MAX_CHUNK tiles, the chunks are sized for exactly
+// one wave (no tail of a few long CTAs that cannot keep HBM busy).  Otherwise
+// they are sized for about four waves, between 4 and KQ8_MAX_CHUNK tiles (128 to
+// 4096 tokens): each CTA has a prologue and a merge tail in which it streams
+// nothing, so large problems take long chunks.
+void chunking(int64_t B, int64_t nkv, int64_t tiles_max, int sms, int per_sm, int& ct, int& nch) {
     static_assert(KQ8_MAX_CHUNK % ATTN_WARPS == 0 && KQ8_MAX_CHUNK <= MAX_CHUNK_TILES, "chunk");
-    const int64_t total = B * nkv * tiles_max;
-    const int64_t target = (int64_t)sms * 3 * 4;
-    int64_t c = (total + target - 1) / (target > 0 ? target : 1);
+    const int64_t pairs = B * nkv > 0 ? B * nkv : 1;
+    const int64_t slots = (int64_t)sms * per_sm;
+    const int64_t per = slots / pairs;  // chunks per list that one wave holds
+    int64_t c;
+    if (per >= 1 && (tiles_max + per - 1) / per <= KQ8_MAX_CHUNK) {
+        c = (tiles_max + per - 1) / per;
+    } else {
+        const int64_t total = pairs * tiles_max;
+        const int64_t target = slots * 4;
+        c = (total + target - 1) / (target > 0 ? target : 1);
+    }
     c = (c + ATTN_WARPS - 1) / ATTN_WARPS * ATTN_WARPS;
     if (c < ATTN_WARPS) c = ATTN_WARPS;
     if (c > KQ8_MAX_CHUNK) c = KQ8_MAX_CHUNK;
@@ -59,12 +69,16 @@ void chunking(int64_t B, int64_t nkv, int64_t tiles_max, int sms, int& ct, int& 
     if (nch < 1) nch = 1;
 }
 
+// Resident attention CTAs per SM (registers and shared memory of the kernel).
+int attn_ctas_per_sm(int G) { return G <= 4 ? 3 : 2; }
+
 // The block-sparse lists are short (at most G * k blocks): sized for a single
-// wave of three CTAs per SM instead, as few chunks per list as fill it, so
+// wave of resident CTAs instead, as few chunks per list as fill it, so
 // that no CTA is left with a prologue and a merge for a couple of tiles.
-void chunking_one_wave(int64_t B, int64_t nkv, int64_t tiles_max, int sms, int& ct, int& nch) {
+void chunking_one_wave(int64_t B, int64_t nkv, int64_t tiles_max, int sms, int per_sm, int& ct,
+                       int& nch) {
     const int64_t pairs = B * nkv > 0 ? B * nkv : 1;
-    int64_t per = ((int64_t)sms * 3) / pairs;  // chunks per list that still fit one wave
+    int64_t per = ((int64_t)sms * per_sm) / pairs;  // chunks per list that still fit one wave
     if (per < 1) per = 1;
     int64_t c = (tiles_max + per - 1) / per;
     c = (c + ATTN_WARPS - 1) / ATTN_WARPS * ATTN_WARPS;
@@ -86,7 +100,8 @@ struct Plan {
 Plan plan_exact(int B, int nq, int nkv, int max_seq_len) {
     Plan p;
     const int64_t tiles = ((int64_t)max_seq_len + TILE - 1) / TILE;
-    chunking(B, nkv, tiles, device_sms(), p.chunk_tiles, p.num_chunks);
+    chunking(B, nkv, tiles, device_sms(), attn_ctas_per_sm(nkv > 0 ? nq / nkv : 1), p.chunk_tiles,
+             p.num_chunks);
     size_t o = HEADER_BYTES;
     p.off_ms = o;
     o = align_up(o + (size_t)B * nq * p.num_chunks * sizeof(float2), WS_ALIGN);
@@ -105,7 +120,7 @@ Plan plan_exact_range(int B, int nq, int nkv, int max_seq_len, int max_range) {
     // a range not starting on a tile boundary touches one tile more
     const int64_t tiles = ((int64_t)max_range + TILE - 1) / TILE + 1;
     int ct, nch;
-    chunking(B, nkv, tiles, device_sms(), ct, nch);
+    chunking(B, nkv, tiles, device_sms(), attn_ctas_per_sm(nkv > 0 ? nq / nkv : 1), ct, nch);
     if (nch > p.num_chunks) {
         ct = (int)((tiles + p.num_chunks - 1) / p.num_chunks);
         ct = (ct + ATTN_WARPS - 1) / ATTN_WARPS * ATTN_WARPS;
@@ -127,7 +142,8 @@ Plan plan_sparse(int B, int nq, int nkv, int max_seq_len, int block, int topk) {
     if (cap < 2 * m && cap < tiles) cap = tiles < 2 * m ? tiles : 2 * m;
     if (cap < 1) cap = 1;
     p.list_cap = (int)cap;
-    chunking_one_wave(B, nkv, p.list_cap, device_sms(), p.chunk_tiles, p.num_chunks);
+    chunking_one_wave(B, nkv, p.list_cap, device_sms(), attn_ctas_per_sm(G), p.chunk_tiles,
+                      p.num_chunks);
     size_t o = HEADER_BYTES;
     p.off_scores = o;
     o = align_up(o + (size_t)B * nq * p.max_nblk * sizeof(float), WS_ALIGN);
