@@ -18,7 +18,14 @@
  *     host-side outputs that are documented as such.  The library allocates
  *     nothing and keeps no state between calls.
  *   - Calls enqueue work on `stream` (a cudaStream_t; NULL = the legacy default
- *     stream) and return without waiting for it.
+ *     stream) and return without waiting for it.  Stream order holds as for
+ *     ordinary launches.  The decode kernels and the appends are programmatic
+ *     launches (cudaLaunchAttributeProgrammaticStreamSerialization): one of
+ *     them may be scheduled while this library's kernel just before it on
+ *     the stream finishes, and it waits for that kernel's completion before it
+ *     reads or writes anything the earlier kernel touches.  A kernel of any
+ *     other code in between still completes first.  In stream capture these
+ *     launches become programmatic graph edges.
  *   - Return value: KQ8_OK (0) or a negative KQ8_ERR_* code.  On an error
  *     nothing was enqueued.  kq8_strerror() names a code.
  *   - Device-resident metadata (sequence lengths, page tables, write slots) is
