@@ -4,17 +4,32 @@
 
 namespace kq8 {
 
+// The probe is a programmatic launch: its CTAs may be scheduled, and stage
+// their page ids and Q, while the kernel before it (the append of the new
+// tokens, or the previous call's attention) finishes; they wait for it before
+// touching the cache or the workspace.
 template <int G>
 static int launch_probe_g(const SparseParams& p, int B, int nkv, cudaStream_t s) {
-    dim3 grid((p.max_nblk + p.probe_bpc - 1) / p.probe_bpc, nkv, B);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.max_nblk + p.probe_bpc - 1) / p.probe_bpc, nkv, B);
+    cfg.blockDim = dim3(PROBE_WARPS * 32);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (p.probe_tma) {
         auto kern = kq8_probe_kernel<G, true>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)PROBE_RING_BYTES) != cudaSuccess)
             return KQ8_ERR_CUDA;
-        kern<<<grid, PROBE_WARPS * 32, PROBE_RING_BYTES, s>>>(p);
+        cfg.dynamicSmemBytes = PROBE_RING_BYTES;
+        if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return KQ8_ERR_CUDA;
     } else {
-        kq8_probe_kernel<G, false><<<grid, PROBE_WARPS * 32, 0, s>>>(p);
+        cfg.dynamicSmemBytes = 0;
+        if (cudaLaunchKernelEx(&cfg, kq8_probe_kernel<G, false>, p) != cudaSuccess)
+            return KQ8_ERR_CUDA;
     }
     return cudaGetLastError() == cudaSuccess ? KQ8_OK : KQ8_ERR_CUDA;
 }

@@ -571,8 +571,13 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32, 2)
     // probe CTA has started; it waits for this grid's completion before it
     // reads the tile lists
     griddep_launch_dependents();
+    // A programmatic launch: until griddep_wait() returns, kernels of the call
+    // before this one may still be running, so only CTA-local work (page ids,
+    // Q, shared state) comes before it; nothing global is written or read from
+    // the workspace or the cache.
     int n = sparse_seq_len(P, b);
     if (n < 0 || n <= 2 * P.block) {  // gate: the exact path needs no probe
+        griddep_wait();
         if (P.tickets && blockIdx.x == 0) {
             if (n < 0 && threadIdx.x == 0 && h == 0 && P.status)
                 atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
@@ -587,6 +592,7 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32, 2)
         // every block is kept whatever its score: the selection is blocks 0 ..
         // nblk - 1 in order for every head, the union every tile (no scores are
         // needed; with tickets nothing after this kernel reads them)
+        griddep_wait();
         if (blockIdx.x == 0) {
             if (P.sel_blocks)
                 for (int g = 0; g < G; g++) {
@@ -613,11 +619,6 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32, 2)
     }
     for (int i = threadIdx.x; i < (j1 - j0) * G; i += PROBE_WARPS * 32)
         best[i / G][i % G] = -INFINITY;
-    // the top-k kernel ORs its heads' choices into these blocks' masks (a
-    // probe-only call passes none)
-    if (P.masks)
-        for (int i = threadIdx.x; i < j1 - j0; i += PROBE_WARPS * 32)
-            P.masks[(size_t)(b * nkv + h) * P.max_nblk + j0 + i] = 0u;
     for (int g = warp; g < G; g += PROBE_WARPS) {
         const float4 x =
             reinterpret_cast<const float4*>(P.q + ((size_t)b * P.nq + (size_t)h * G + g) * HD)[lane];
@@ -635,6 +636,15 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32, 2)
         fence_barrier_init();
     }
     __syncthreads();
+    // the kernel before this one has completed: its KV, scores, lists and masks
+    // are final
+    griddep_wait();
+    // the selection ORs its heads' choices into these blocks' masks (rows of
+    // more than 2048 blocks, or the separate top-k kernel; a probe-only call
+    // passes none)
+    if (P.masks)
+        for (int i = threadIdx.x; i < j1 - j0; i += PROBE_WARPS * 32)
+            P.masks[(size_t)(b * nkv + h) * P.max_nblk + j0 + i] = 0u;
 
     const int gb = lane >> 3, pr = lane & 7;
     const int stride = P.block / P.probe;
