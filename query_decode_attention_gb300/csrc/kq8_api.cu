@@ -44,7 +44,8 @@ int device_sms() {
 // chunks of `chunk_tiles` tiles (a multiple of the CTA's 4 warps), for
 // `per_sm` resident attention CTAs per SM.  If every list fits one wave of CTAs
 // with chunks of at most KQ8_MAX_CHUNK tiles, the chunks are sized for exactly
-// one wave (no tail of a few long CTAs that cannot keep HBM busy).  Otherwise
+// one wave (no tail of a few long CTAs that cannot keep HBM busy), with at most
+// 16 chunks per list.  Otherwise
 // they are sized for about four waves, between 4 and KQ8_MAX_CHUNK tiles (128 to
 // 4096 tokens): each CTA has a prologue and a merge tail in which it streams
 // nothing, so large problems take long chunks.
@@ -52,7 +53,10 @@ void chunking(int64_t B, int64_t nkv, int64_t tiles_max, int sms, int per_sm, in
     static_assert(KQ8_MAX_CHUNK % ATTN_WARPS == 0 && KQ8_MAX_CHUNK <= MAX_CHUNK_TILES, "chunk");
     const int64_t pairs = B * nkv > 0 ? B * nkv : 1;
     const int64_t slots = (int64_t)sms * per_sm;
-    const int64_t per = slots / pairs;  // chunks per list that one wave holds
+    // chunks per list that one wave holds; at most 16: past that (batch 1 or 2)
+    // the merge of the chunks' partials costs more than the added streams give
+    int64_t per = slots / pairs;
+    if (per > 16) per = 16;
     int64_t c;
     if (per >= 1 && (tiles_max + per - 1) / per <= KQ8_MAX_CHUNK) {
         c = (tiles_max + per - 1) / per;
