@@ -94,7 +94,10 @@ __device__ __forceinline__ int block_excl_scan(int v, int* tmp, int& total) {
 constexpr int SEL_HG = 2;
 constexpr int TOPK_KPT = 8;  // consecutive block scores per thread (in-register form)
 
+constexpr int SEL_SMALL = 256;  // rows of up to this many blocks: one warp per head
+
 struct SelectSmem {
+    uint32_t keptw[8][SEL_SMALL / 32];  // short rows: bit l of word [r][i] = row r keeps block 32 i + l
     int hist[2][SEL_HG][256];  // double-buffered: a pass clears the next one's
     int scan_tmp[SEL_HG + 1][TOPK_THREADS / 32];
     uint32_t prefix[SEL_HG];
@@ -493,10 +496,135 @@ __device__ __forceinline__ void select_rows_smem(const SparseParams& P, int b, i
     if (tid == 0) P.list_len[b * nkv + h] = list_tot;
 }
 
+// Short rows (at most SEL_SMALL blocks): one warp per row, no CTA barrier until
+// the union.  Lane l holds the keys of blocks l + 32 i (i < KPL), so a ballot
+// over slice i lists blocks 32 i .. 32 i + 31 in order.  The k-th largest key t
+// comes from a bitwise binary search (the largest t with at least k keys >= t,
+// counted with ballots); keys above t are kept, and of the keys equal to t the
+// first ones by block index until k are kept.  Kept ids are written in
+// ascending order from prefix counts of the slices' ballots.
+template <int G, bool SHARED, int KPL>
+__device__ __forceinline__ void select_rows_warp(const SparseParams& P, int b, int h, int n,
+                                                 int nblk, SelectSmem& S) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nkv = P.cache.num_kv_heads;
+    constexpr int rows = SHARED ? 1 : G;
+    const int k = min(P.topk, nblk);
+    if (warp < rows) {
+        const float* sc0 = P.scores + ((size_t)b * P.nq + (size_t)h * G) * P.max_nblk;
+        uint32_t key[KPL];  // 0 marks "no block" (real keys are >= 1)
+#pragma unroll
+        for (int i = 0; i < KPL; i++) {
+            const int j = lane + 32 * i;
+            float v = -INFINITY;
+            if (j < nblk) {
+                if (SHARED) {
+                    v = __ldcg(sc0 + j);
+#pragma unroll
+                    for (int g = 1; g < G; g++) {
+                        const float x = __ldcg(sc0 + (size_t)g * P.max_nblk + j);
+                        v = x > v ? x : v;
+                    }
+                } else {
+                    v = __ldcg(sc0 + (size_t)warp * P.max_nblk + j);
+                }
+            }
+            key[i] = j < nblk ? order_key(v) : 0u;
+        }
+        // the k-th largest key (k <= the number of real keys)
+        uint32_t t = 0u;
+        for (int bit = 31; bit >= 0; bit--) {
+            const uint32_t cand = t | (1u << bit);
+            int cnt = 0;
+#pragma unroll
+            for (int i = 0; i < KPL; i++) cnt += __popc(__ballot_sync(0xffffffffu, key[i] >= cand));
+            if (cnt >= k) t = cand;
+        }
+        int above = 0;
+#pragma unroll
+        for (int i = 0; i < KPL; i++) above += __popc(__ballot_sync(0xffffffffu, key[i] > t));
+        int need = k - above;  // keys equal to t still to keep, lowest blocks first
+        int32_t* sel = P.sel_blocks
+                           ? P.sel_blocks + ((size_t)b * P.nq + (size_t)h * G + warp) * P.topk
+                           : nullptr;
+        constexpr int sel_rows = SHARED ? G : 1;
+        const uint32_t lt = (1u << lane) - 1u;
+        int base = 0;
+#pragma unroll
+        for (int i = 0; i < KPL; i++) {
+            uint32_t eq = __ballot_sync(0xffffffffu, key[i] == t && key[i] != 0u);
+            if (need <= 0) {
+                eq = 0u;
+            } else if (__popc(eq) > need) {  // a tie across the k-th place: lowest blocks
+                uint32_t take = 0u, e = eq;
+                for (int c = 0; c < need; c++) {
+                    take |= e & (0u - e);  // lowest set bit
+                    e &= e - 1u;
+                }
+                eq = take;
+            }
+            need -= __popc(eq);
+            const uint32_t kept = __ballot_sync(0xffffffffu, key[i] > t) | eq;
+            if (sel && ((kept >> lane) & 1u)) {
+                const int pos = base + __popc(kept & lt);
+#pragma unroll
+                for (int r = 0; r < sel_rows; r++) sel[(size_t)r * P.topk + pos] = lane + 32 * i;
+            }
+            base += __popc(kept);
+            if (lane == 0) S.keptw[warp][i] = kept;
+        }
+        if (sel)  // fewer blocks than topk: the rest of the row is -1
+            for (int i = k + lane; i < P.topk; i += 32)
+#pragma unroll
+                for (int r = 0; r < sel_rows; r++) sel[(size_t)r * P.topk + i] = -1;
+    }
+    __syncthreads();
+    // the union tile list (warp 0): ascending blocks, entry = tile | head mask << 24
+    if (warp == 0) {
+        const int ntiles = (n + TILE - 1) / TILE;
+        const int m = P.block / TILE;  // tiles per block
+        int32_t* list = P.tile_list + (size_t)(b * nkv + h) * P.list_cap;
+        int written = 0;
+#pragma unroll
+        for (int i = 0; i < KPL; i++) {
+            const int j = lane + 32 * i;
+            uint32_t mk = 0u;
+#pragma unroll
+            for (int r = 0; r < rows; r++) mk |= ((S.keptw[r][i] >> lane) & 1u) << r;
+            if (SHARED) mk = mk ? ((1u << G) - 1u) : 0u;
+            const int c = mk ? min(m, ntiles - j * m) : 0;
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            int pos = written + incl - c;
+            for (int s2 = 0; s2 < c; s2++) list[pos++] = (j * m + s2) | (int32_t)(mk << 24);
+            written += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) P.list_len[b * nkv + h] = written;
+    }
+}
+
 template <int G>
 __device__ __forceinline__ void select_all(const SparseParams& P, int b, int h, int n,
                                            SelectSmem& S) {
     const int nblk = (n + P.block - 1) / P.block;
+    if (nblk <= SEL_SMALL / 2) {
+        if (P.shared_sel)
+            select_rows_warp<G, true, SEL_SMALL / 64>(P, b, h, n, nblk, S);
+        else
+            select_rows_warp<G, false, SEL_SMALL / 64>(P, b, h, n, nblk, S);
+        return;
+    }
+    if (nblk <= SEL_SMALL) {
+        if (P.shared_sel)
+            select_rows_warp<G, true, SEL_SMALL / 32>(P, b, h, n, nblk, S);
+        else
+            select_rows_warp<G, false, SEL_SMALL / 32>(P, b, h, n, nblk, S);
+        return;
+    }
     if (nblk <= TOPK_THREADS * TOPK_KPT) {
         if (P.shared_sel)
             select_rows_smem<G, true>(P, b, h, n, nblk, S);
