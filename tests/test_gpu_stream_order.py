@@ -1,0 +1,105 @@
+"""Stream order through the library's programmatic launches: each decode,
+append and probe kernel may be scheduled while the kernel before it on the
+stream finishes, and waits for it before touching anything that kernel reads or
+writes.  These cases put other work between and around the calls on one stream
+and check that every call sees exactly what stream order promises, against the
+oracle."""
+import numpy as np
+import pytest
+
+from kq8_testlib import assert_out_close, host_inputs, oracle_decode
+from query_decode_attention_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from query_decode_attention_gb300 import kq8, paged  # noqa: E402
+
+DEV = "cuda:0"
+
+
+def _case(lens, seed):
+    wl = W.custom(len(lens), 16, 8, lens, seed=seed)
+    q, Ks, Vs = host_inputs(wl)
+    return wl, q, Ks, Vs
+
+
+def test_append_then_rewritten_q_then_decode():
+    # the last token of every sequence is appended, then a PyTorch kernel
+    # rewrites q in place, then the decode: it must see both
+    wl, q, Ks, Vs = _case([600, 1000, 33, 2], seed=90)
+    cache, pt = paged.new_cache(wl, device=DEV)
+    first = np.concatenate([W.slots_for(wl, pt, b, 0, n - 1) for b, n in enumerate(wl.seq_lens)])
+    last = np.concatenate([W.slots_for(wl, pt, b, n - 1, n) for b, n in enumerate(wl.seq_lens)])
+    k_first = np.concatenate([K[:-1].reshape(-1, wl.nkv, 128) for K in Ks])
+    v_first = np.concatenate([V[:-1].reshape(-1, wl.nkv, 128) for V in Vs])
+    k_last = np.concatenate([K[-1:].reshape(-1, wl.nkv, 128) for K in Ks])
+    v_last = np.concatenate([V[-1:].reshape(-1, wl.nkv, 128) for V in Vs])
+    kq8.kq8_append_kv(cache, torch.tensor(k_first, device=DEV), torch.tensor(v_first, device=DEV),
+                      torch.tensor(first, dtype=torch.int32, device=DEV))
+    torch.cuda.synchronize()
+    kl, vl = torch.tensor(k_last, device=DEV), torch.tensor(v_last, device=DEV)
+    sl = torch.tensor(last, dtype=torch.int32, device=DEV)
+    qd = torch.tensor(q, device=DEV)
+    page_table = torch.tensor(pt, dtype=torch.int32, device=DEV)
+    seq_lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=DEV)
+    out = torch.empty((wl.B, wl.nq, 128), device=DEV)
+    ws = kq8.new_workspace(kq8.kq8_decode_workspace_bytes(wl.B, wl.nq, wl.nkv, wl.max_seq_len), DEV)
+    kq8.kq8_append_kv(cache, kl, vl, sl)
+    qd.mul_(-1.5)
+    kq8.kq8_decode_attn(out, qd, cache, page_table, seq_lens, wl.max_seq_len, wl.scale, ws)
+    assert kq8.kq8_read_status(ws) == 0
+    q2 = (q.astype(np.float32) * np.float32(-1.5)).astype(np.float32)
+    assert_out_close(out.cpu().numpy(), oracle_decode(wl, q2, Ks, Vs), "append, q rewritten, decode")
+
+
+def test_back_to_back_decodes_sharing_output_and_workspace():
+    wl, q, Ks, Vs = _case([4000, 1500, 700], seed=91)
+    case = paged.fill_from_host(wl, Ks, Vs, DEV, q_host=q)
+    q1 = case.q
+    q2 = torch.tensor(np.random.default_rng(5).standard_normal(q.shape).astype(np.float32),
+                      device=DEV)
+    out = torch.empty((wl.B, wl.nq, 128), device=DEV)
+    out_b = torch.empty_like(out)
+    ws = kq8.new_workspace(kq8.kq8_decode_workspace_bytes(wl.B, wl.nq, wl.nkv, wl.max_seq_len), DEV)
+    args = (case.cache, case.page_table, case.seq_lens, wl.max_seq_len, wl.scale, ws)
+    kq8.kq8_decode_attn(out, q1, *args)
+    snap = out.clone()                  # another kernel between the two calls
+    kq8.kq8_decode_attn(out, q2, *args)  # same output and workspace
+    kq8.kq8_decode_attn(out_b, q1, *args)  # and directly after it, no kernel between
+    torch.cuda.synchronize()
+    assert kq8.kq8_read_status(ws) == 0
+    ref1 = oracle_decode(wl, q, Ks, Vs)
+    ref2 = oracle_decode(wl, q2.cpu().numpy(), Ks, Vs)
+    assert_out_close(snap.cpu().numpy(), ref1, "first decode")
+    assert_out_close(out.cpu().numpy(), ref2, "second decode, same buffers")
+    assert np.array_equal(out_b.cpu().numpy(), snap.cpu().numpy()), "third decode = first"
+
+
+def test_sparse_exact_sparse_on_one_stream():
+    wl = W.sparse_planted(4059, B=3)
+    q, Ks, Vs = host_inputs(wl)
+    case = paged.fill_from_host(wl, Ks, Vs, DEV, q_host=q)
+    out_s, out_e, out_s2 = (torch.empty((wl.B, wl.nq, 128), device=DEV) for _ in range(3))
+    sel, sel2 = (torch.full((wl.B, wl.nq, wl.topk), -7, dtype=torch.int32, device=DEV)
+                 for _ in range(2))
+    wss = kq8.new_workspace(kq8.kq8_sparse_decode_workspace_bytes(
+        wl.B, wl.nq, wl.nkv, wl.max_seq_len, wl.block, wl.topk), DEV)
+    wse = kq8.new_workspace(kq8.kq8_decode_workspace_bytes(wl.B, wl.nq, wl.nkv, wl.max_seq_len),
+                            DEV)
+    sargs = (case.q, case.cache, case.page_table, case.seq_lens, wl.max_seq_len, wl.scale,
+             wl.block, wl.topk, wl.probe, wss)
+    kq8.kq8_sparse_decode_attn(out_s, *sargs, sel_blocks=sel)
+    kq8.kq8_decode_attn(out_e, case.q, case.cache, case.page_table, case.seq_lens,
+                        wl.max_seq_len, wl.scale, wse)
+    kq8.kq8_sparse_decode_attn(out_s2, *sargs, sel_blocks=sel2)
+    torch.cuda.synchronize()
+    assert kq8.kq8_read_status(wss) == 0 and kq8.kq8_read_status(wse) == 0
+    ref_s, rsel = oracle_decode(wl, q, Ks, Vs, sparse=True)
+    assert np.array_equal(sel.cpu().numpy(), rsel) and np.array_equal(sel2.cpu().numpy(), rsel)
+    assert_out_close(out_s.cpu().numpy(), ref_s, "sparse, first")
+    assert np.array_equal(out_s2.cpu().numpy(), out_s.cpu().numpy()), "sparse, again"
+    assert_out_close(out_e.cpu().numpy(), oracle_decode(wl, q, Ks, Vs), "exact between")
