@@ -161,16 +161,21 @@ __global__ void __launch_bounds__(PF_THREADS, 1) kq8_prefill_kernel(const Prefil
     constexpr int TQ = PF_ROWS / G;  // new tokens per query tile
     extern __shared__ __align__(1024) uint8_t sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.y, b = blockIdx.z;
+    // CTAs start in linear order (x fastest): the linear index is read with the
+    // (KV head, sequence) fastest and the query tile slowest, longest first, so
+    // that every head's and sequence's longest tiles start in the first wave
+    const unsigned lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    const unsigned hbn = gridDim.y * gridDim.z;
+    const int h = (int)((lin % hbn) % gridDim.y), b = (int)((lin % hbn) / gridDim.y);
     const int nkv = P.cache.num_kv_heads, kv_bs = P.cache.kv_bs;
-    const int qt = gridDim.x - 1 - blockIdx.x;  // the longest query tiles start first
+    const int qt = (int)gridDim.x - 1 - (int)(lin / hbn);
 
     const int n = P.seq_lens[b];
     const int q0 = P.q_off[b];
     const int nb = P.q_off[b + 1] - q0;
     if (n < 0 || n > P.max_seq_len || nb < 0 || nb > n || nb > P.max_q_len || q0 < 0 ||
         (int64_t)q0 + nb > P.total_q) {
-        if (tid == 0 && blockIdx.x == 0 && h == 0) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
+        if (tid == 0 && qt == (int)gridDim.x - 1 && h == 0) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
         return;
     }
     const int i0 = qt * 2 * TQ;  // first new token of tile A; tile B follows
