@@ -5,10 +5,13 @@
 // the chunk's tiles w, w+4, ...  All G query heads of KV head h are handled by
 // the same warp, so each K/V byte is read from HBM once for the whole group.
 //
-// Per warp, a ring of ATTN_STAGES shared-memory stages is filled by bulk-async
-// copies (one lane issues them; completion on an mbarrier per stage) while the
-// warp computes on the previous stage.  The page ids of the warp's tiles are
-// fetched once, one per lane, so issuing a copy never waits on memory.  Per
+// Per warp, a ring of ATTN_STAGES shared-memory stages is filled by bulk and
+// tensor copies (one lane issues them; completion on an mbarrier per stage)
+// while the warp computes on the previous stage.  The page ids of the warp's
+// tiles are fetched once, one per lane, so issuing a copy never waits on
+// memory.  The kernel is a programmatic launch: its prologue (Q quantisation,
+// page ids, barriers) may overlap the kernel before it on the stream, and the
+// first copy waits for that kernel's completion (griddepcontrol.wait).  Per
 // tile:
 //   score phase (lane = token): int32 block dots of the token's K row with
 //     the G int8 query rows (dp4a), the fp32 score in the method's order on

@@ -281,9 +281,8 @@ __device__ __forceinline__ void block_excl_scan_v(const int (&v)[NV], int (&excl
 // t*KPT .. t*KPT+KPT-1 of SEL_HG rows at a time (the G heads' rows, or one row
 // of the heads' maxima for a shared selection).  Per row a radix select finds
 // the k-th largest key 8 bits a pass from the top: every thread adds its keys
-// to the row's digit histogram (updates aggregated per warp with
-// __match_any_sync, one shared atomic per distinct digit), then warp r alone
-// scans row r's 256 counts and picks the digit -- two CTA barriers a pass; it
+// to the row's digit histogram with shared atomics, then warp r alone scans
+// row r's 256 counts and picks the digit -- two CTA barriers a pass; it
 // stops once every key of the chosen bucket is kept.  Keys above the
 // threshold are kept, plus the first kk equal to it by block index (a scan
 // ranks the ties, only when some are left out); one scan over per-thread
