@@ -21,10 +21,12 @@
  *     stream) and return without waiting for it.  Stream order holds as for
  *     ordinary launches.  The decode kernels and the appends are programmatic
  *     launches (cudaLaunchAttributeProgrammaticStreamSerialization): one of
- *     them may be scheduled while this library's kernel just before it on
- *     the stream finishes, and it waits for that kernel's completion before it
- *     reads or writes anything the earlier kernel touches.  A kernel of any
- *     other code in between still completes first.  In stream capture these
+ *     them may be scheduled while the kernel just before it on the stream
+ *     finishes (this library's, or any code's that signals its dependents
+ *     early), but before that kernel has completed it only sets up its own
+ *     shared memory: it reads and writes global memory -- the query, lengths,
+ *     page tables, cache, workspace and outputs -- only after the earlier
+ *     kernel's completion (griddepcontrol.wait).  In stream capture these
  *     launches become programmatic graph edges.
  *   - Return value: KQ8_OK (0) or a negative KQ8_ERR_* code.  On an error
  *     nothing was enqueued.  kq8_strerror() names a code.

@@ -15,10 +15,10 @@ static int launch_attn_g(const AttnParams& p, int B, int nkv, cudaStream_t s) {
         return KQ8_ERR_CUDA;
     dim3 grid(p.num_chunks, nkv, B);
     {
-        // programmatic launch: the CTAs may start while the kernel before them
-        // (the append of the new tokens, or the selection) finishes; they wait
-        // for it before reading what it writes (the KV, or the tile lists).  A
-        // kernel that does not signal its dependents still completes first.
+        // programmatic launch: the CTAs may start, and set up their barriers,
+        // while the kernel before them (the append of the new tokens, or the
+        // selection) finishes; they wait for its completion before they read or
+        // write global memory.
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
         cfg.blockDim = dim3(ATTN_THREADS);

@@ -183,9 +183,11 @@ struct SeqRange {
     bool bad;
 };
 template <bool SPARSE>
-__device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h) {
+__device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h, int raw_len) {
     SeqRange r;
-    r.n = valid_seq_len(P, b);
+    // a sparse list's length is loaded with the sequence length, not after it
+    const int list_len = SPARSE ? P.list_len[b * P.cache.num_kv_heads + h] : 0;
+    r.n = (raw_len < 0 || raw_len > P.max_seq_len) ? -1 : raw_len;
     r.bad = r.n < 0;
     if (r.bad) r.n = 0;
     r.begin = 0;
@@ -200,7 +202,7 @@ __device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h)
     if (r.n == r.begin)
         r.entries = 0;
     else if (SPARSE)
-        r.entries = P.list_len[b * P.cache.num_kv_heads + h];
+        r.entries = list_len;
     else
         r.entries = (r.n + TILE - 1) / TILE - r.first_tile;
     if (r.entries > P.num_chunks * P.chunk_tiles) {  // longer than the plan's grid covers
@@ -208,6 +210,10 @@ __device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h)
         r.entries = 0;
     }
     return r;
+}
+template <bool SPARSE>
+__device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h) {
+    return seq_range<SPARSE>(P, b, h, P.seq_lens[b]);
 }
 
 // Folds a result (m, s, a) into a running state (mo, so, ao), maxima in score
@@ -240,74 +246,109 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     const int subs = kv_bs / TILE;
     // a programmatic launch after this one (the next append, update or layer)
     // may be scheduled now: each of those waits for this grid's completion
-    // before it touches what this kernel reads or writes
+    // before it reads or writes global memory
     griddep_launch_dependents();
     // fetch the V tensor map's descriptor while the prologue runs
-    if (!Q4 && threadIdx.x == 0)
+    if (threadIdx.x == 0)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.vmap))
                      : "memory");
-
-    // ---- prologue: quantise the G query heads once (article 9-2 §2 seg. 1)
-    auto quantise_q = [&]() {
-    for (int g = warp; g < G; g += ATTN_WARPS) {
-        const float4 x =
-            reinterpret_cast<const float4*>(P.q + ((size_t)b * P.nq + (size_t)h * G + g) * HD)[lane];
-        float qs;
-        const uint32_t codes = quantize_q_lane(x, qs);
-        reinterpret_cast<uint32_t*>(S.qi[g])[lane] = codes;
-        if ((lane & 7) == 0) S.qsc[g][lane >> 3] = qs;
-        if (Q4) {  // q4: dot = sum q * (u - 8) = dp4a(u, q) - 8 * sum q per block
-            int qs4 = __dp4a((int)codes, 0x01010101, 0);
-            qs4 += __shfl_xor_sync(0xffffffffu, qs4, 1);
-            qs4 += __shfl_xor_sync(0xffffffffu, qs4, 2);
-            qs4 += __shfl_xor_sync(0xffffffffu, qs4, 4);
-            if ((lane & 7) == 0) S.qsum[g][lane >> 3] = -8 * qs4;  // the dots' start value
-        }
-    }
-    };
-    if (SPARSE) {
-        // the tile lists come from the kernel before this one: with a
-        // programmatic launch this CTA is already resident while that kernel
-        // finishes, quantises Q, and only then waits for its results
-        quantise_q();
-        griddep_wait();
-    }
-    const SeqRange rng = seq_range<SPARSE>(P, b, h);
-    if (rng.bad && threadIdx.x == 0 && chunk == 0 && h == 0) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
-    const int n = rng.n, begin = rng.begin;
-    const int entries = rng.entries;
-    const int nch = max(1, (entries + P.chunk_tiles - 1) / P.chunk_tiles);
-    if (chunk >= nch) return;
-    const int e0 = chunk * P.chunk_tiles;
-    const int e1 = min(e0 + P.chunk_tiles, entries);
-    const int mine = (e1 - e0 > warp) ? (e1 - e0 - warp + ATTN_WARPS - 1) / ATTN_WARPS : 0;
-    if (!SPARSE) quantise_q();
-    // ---- this warp's tiles, one per lane: tile index, head mask, page (-1 if bad)
-    int my_tile = 0;
-    uint32_t my_mask = 0;
-    int32_t my_page = -1;
-    if (lane < mine) {
-        const int e = e0 + warp + ATTN_WARPS * lane;
-        if (SPARSE) {
-            const int32_t v = P.tile_list[(size_t)(b * nkv + h) * P.list_cap + e];
-            my_tile = v & 0xFFFFFF;
-            my_mask = (uint32_t)v >> 24;
-        } else {
-            my_tile = rng.first_tile + e;
-            my_mask = 0xFFu;
-        }
-        const int32_t pg =
-            P.page_table[(size_t)(P.row_seq ? P.row_seq[b] : b) * P.max_pages + my_tile / subs];
-        if (pg >= 0 && pg < P.cache.num_pages) {
-            my_page = pg;
-        } else {
-            atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
-        }
-    }
+    // Until griddep_wait() returns, the kernel before this one on the stream
+    // (this library's or any other code's, when it signals its dependents
+    // early) may still be writing anything this kernel reads -- Q, the
+    // lengths, the page table, the KV, the tile lists.  So before it this CTA
+    // sets up its barriers and, on the plain exact walk, reads its inputs only
+    // as a guess: after the wait the same inputs are read again, and the walk
+    // goes on from the guess only if every value is the same (else it drops
+    // what it began and starts over from the values read after the wait).
     if (lane == 0)
         for (int s = 0; s < NS; s++) mbar_init(&S.bar[warp][s], 1);
     fence_barrier_init();
     __syncthreads();
+
+    // The plain exact walk's list entry e is tile e, so its page ids need no
+    // list: they are part of the guess; a sparse walk's entries are loaded with
+    // the length after the wait (its page ids follow them).  Not at G = 4:
+    // there the walk sits at the 168 registers of three CTAs per SM, and with
+    // these loads (guessed or only early) the serving step measured 0.3 %
+    // slower than with the length first and the rest after it.
+    constexpr bool EARLY = G != 4;
+    constexpr int QR = (G + ATTN_WARPS - 1) / ATTN_WARPS;  // query rows per warp
+    const bool guess = EARLY && !SPARSE && P.seq_begin == nullptr && P.row_seq == nullptr;
+    const int e_spec = chunk * P.chunk_tiles + warp + ATTN_WARPS * lane;
+    const bool in_chunk = warp + ATTN_WARPS * lane < P.chunk_tiles;
+    const bool pg_idx_ok = in_chunk && e_spec / subs < P.max_pages;
+    auto load_inputs = [&](float4 (&qv)[QR], int32_t& len, int32_t& pg) {
+#pragma unroll
+        for (int k = 0; k < QR; k++) {
+            const int g = warp + k * ATTN_WARPS;
+            if (g < G)
+                qv[k] = reinterpret_cast<const float4*>(
+                    P.q + ((size_t)b * P.nq + (size_t)h * G + g) * HD)[lane];
+        }
+        len = P.seq_lens[b];
+        pg = -1;
+        if (guess && pg_idx_ok) pg = P.page_table[(size_t)b * P.max_pages + e_spec / subs];
+    };
+    float4 qx[QR];  // the query rows the walk quantises
+    int32_t tl_spec = 0;
+
+    // ---- prologue: quantise the G query heads once (article 9-2 §2 seg. 1)
+    auto quantise_q = [&]() {
+#pragma unroll
+        for (int k = 0; k < QR; k++) {
+            const int g = warp + k * ATTN_WARPS;
+            if (g >= G) continue;
+            float qs;
+            const uint32_t codes = quantize_q_lane(qx[k], qs);
+            reinterpret_cast<uint32_t*>(S.qi[g])[lane] = codes;
+            if ((lane & 7) == 0) S.qsc[g][lane >> 3] = qs;
+            if (Q4) {  // q4: dot = sum q * (u - 8) = dp4a(u, q) - 8 * sum q per block
+                int qs4 = __dp4a((int)codes, 0x01010101, 0);
+                qs4 += __shfl_xor_sync(0xffffffffu, qs4, 1);
+                qs4 += __shfl_xor_sync(0xffffffffu, qs4, 2);
+                qs4 += __shfl_xor_sync(0xffffffffu, qs4, 4);
+                if ((lane & 7) == 0) S.qsum[g][lane >> 3] = -8 * qs4;  // the dots' start value
+            }
+        }
+    };
+    // ---- the walk's plan from a length (and, on the plain exact walk, a page
+    // id): this chunk's entries and this warp's tiles, one per lane
+    SeqRange rng;
+    int nch = 1, mine = 0, my_tile = 0;
+    uint32_t my_mask = 0;
+    int32_t my_page = -1;
+    bool bad_page = false;
+    auto plan = [&](int32_t len, int32_t pg_pre) {
+        rng = seq_range<SPARSE>(P, b, h, len);
+        nch = max(1, (rng.entries + P.chunk_tiles - 1) / P.chunk_tiles);
+        const int e0 = chunk * P.chunk_tiles;
+        const int e1 = min(e0 + P.chunk_tiles, rng.entries);
+        mine = (chunk < nch && e1 - e0 > warp) ? (e1 - e0 - warp + ATTN_WARPS - 1) / ATTN_WARPS : 0;
+        my_tile = 0;
+        my_mask = 0;
+        my_page = -1;
+        bad_page = false;
+        if (lane < mine) {
+            const int e = e0 + warp + ATTN_WARPS * lane;  // = e_spec
+            if (SPARSE) {
+                const int32_t v =
+                    EARLY ? tl_spec : P.tile_list[(size_t)(b * nkv + h) * P.list_cap + e];
+                my_tile = v & 0xFFFFFF;
+                my_mask = (uint32_t)v >> 24;
+            } else {
+                my_tile = rng.first_tile + e;
+                my_mask = 0xFFu;
+            }
+            const int32_t pg =
+                guess ? pg_pre
+                      : P.page_table[(size_t)(P.row_seq ? P.row_seq[b] : b) * P.max_pages +
+                                     my_tile / subs];
+            if (pg >= 0 && pg < P.cache.num_pages)
+                my_page = pg;
+            else
+                bad_page = true;
+        }
+    };
 
     // all lanes call this (it shuffles); lane 0 issues the stage's copies
     auto issue = [&](int i) {
@@ -341,11 +382,72 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             }
         }
     };
-    // the KV this call reads may have been appended by the kernel just before
-    // (a programmatic launch lets this CTA's prologue overlap it): wait for it
-    // before the first copy
-    if (!SPARSE) griddep_wait();
+    // the guess: inputs, plan and Q's codes before the wait (no global writes)
+    int32_t len_g = 0, pg_g = -1;
+    if (guess) {
+        load_inputs(qx, len_g, pg_g);
+        plan(len_g, pg_g);
+        quantise_q();
+    }
+    griddep_wait();
+    float4 qv[QR];  // after the wait: the check of the guess, or the inputs
+    int32_t len_v = 0, pg_v = -1;
+    if (guess) {
+        load_inputs(qv, len_v, pg_v);
+    } else {
+        load_inputs(qx, len_v, pg_v);
+        if (EARLY && SPARSE && in_chunk && e_spec < P.list_cap)
+            tl_spec = P.tile_list[(size_t)(b * nkv + h) * P.list_cap + e_spec];
+        plan(len_v, pg_v);
+    }
     for (int i = 0; i < NS && i < mine; i++) issue(i);
+    // Q's codes while the first copies are in flight; every warp reads all heads'
+    if (!guess) quantise_q();
+    bool failed = false;
+    if (guess) {
+        bool same = len_g == len_v && pg_g == pg_v;
+#pragma unroll
+        for (int k = 0; k < QR; k++)
+            if (warp + k * ATTN_WARPS < G)
+                same = same && __float_as_uint(qx[k].x) == __float_as_uint(qv[k].x) &&
+                       __float_as_uint(qx[k].y) == __float_as_uint(qv[k].y) &&
+                       __float_as_uint(qx[k].z) == __float_as_uint(qv[k].z) &&
+                       __float_as_uint(qx[k].w) == __float_as_uint(qv[k].w);
+        if (!__syncthreads_and(same)) {
+            // rare: an input changed between the guess and the wait.  Let the
+            // copies issued from the guess land, re-arm the barriers and start
+            // over from the values read after the wait.
+            bool landed = true;
+            for (int i = 0; i < NS && i < mine; i++)
+                landed = __all_sync(0xffffffffu, mbar_wait_bounded(&S.bar[warp][i], 0)) && landed;
+            if (landed) {
+                if (lane == 0)
+                    for (int s = 0; s < NS; s++) {
+                        mbar_inval(&S.bar[warp][s]);
+                        mbar_init(&S.bar[warp][s], 1);
+                    }
+                fence_barrier_init();
+                __syncwarp();
+            }
+            __syncthreads();  // every warp is done with the guess's Q codes
+#pragma unroll
+            for (int k = 0; k < QR; k++) qx[k] = qv[k];
+            plan(len_v, pg_v);
+            if (landed) {
+                for (int i = 0; i < NS && i < mine; i++) issue(i);
+            } else {
+                failed = true;  // a copy never landed: this warp walks nothing
+                mine = 0;
+            }
+            quantise_q();
+        }
+    }
+    // the inputs are settled: report bad values
+    if (rng.bad && threadIdx.x == 0 && chunk == 0 && h == 0) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
+    if (bad_page) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
+    if (chunk >= nch) return;
+    const int n = rng.n, begin = rng.begin;
+    __syncthreads();
 
     float M2[G], Sl[G];
     // The value phase runs on the tensor cores: 16 m16n8 accumulator tiles D[.][.]
@@ -376,7 +478,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     // stored K max -> step (1/127); the softmax scale is applied after it
     const float kstep = Q4 ? inv7() : inv127();
 
-    bool failed = false;
     int i = 0;
     for (; i < mine; i++) {
         const int tile = __shfl_sync(0xffffffffu, my_tile, i);

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(256)
     // before this one has completed
     griddep_wait();
     // the decode attention launched after this kernel may start its prologue
-    // now; it waits for this grid's completion before reading the cache
+    // now; it waits for this grid's completion before reading global memory
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31, j = lane % LPR, grp = lane / LPR;
     const int64_t item0 =

@@ -4,10 +4,10 @@
 
 namespace kq8 {
 
-// The probe is a programmatic launch: its CTAs may be scheduled, and stage
-// their page ids and Q, while the kernel before it (the append of the new
-// tokens, or the previous call's attention) finishes; they wait for it before
-// touching the cache or the workspace.
+// The probe is a programmatic launch: its CTAs may be scheduled, and set up
+// their barriers, while the kernel before it (the append of the new tokens, or
+// the previous call's attention) finishes; they wait for its completion before
+// they read or write global memory.
 template <int G>
 static int launch_probe_g(const SparseParams& p, int B, int nkv, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};

@@ -696,15 +696,46 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32, 2)
     const int nkv = P.cache.num_kv_heads, kv_bs = P.cache.kv_bs;
     // the attention kernel after this one may become resident as soon as every
     // probe CTA has started; it waits for this grid's completion before it
-    // reads the tile lists
+    // reads global memory
     griddep_launch_dependents();
-    // A programmatic launch: until griddep_wait() returns, kernels of the call
-    // before this one may still be running, so only CTA-local work (page ids,
-    // Q, shared state) comes before it; nothing global is written or read from
-    // the workspace or the cache.
+    // A programmatic launch: until griddep_wait() returns, the kernel before
+    // this one on the stream (this library's or any other code's, when it
+    // signals its dependents early) may still be writing anything this kernel
+    // reads -- Q, the lengths, the page table, the KV -- so before it only this
+    // CTA's own barriers are set up.
+    if (TMA) {
+        if (lane == 0)
+            for (int i = 0; i < PROBE_STAGES; i++) mbar_init(&pbar[warp][i], 1);
+        if (threadIdx.x == 0)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.kmap))
+                         : "memory");
+        fence_barrier_init();
+    }
+    griddep_wait();
+    // Loads that do not depend on the length go out with it: the Q rows and
+    // (unless rows map to sequences through row_seq) the page ids this CTA's
+    // blocks can span: pages pg0 .. pg0 + ceil(probe_bpc * block / kv_bs)
+    static_assert(G <= PROBE_WARPS, "one Q row per warp");
+    static_assert(PROBE_MAX_PAGES % (PROBE_WARPS * 32) == 0, "page ids per thread");
+    constexpr int PPT = PROBE_MAX_PAGES / (PROBE_WARPS * 32);
+    const int j0 = blockIdx.x * P.probe_bpc;
+    const int pg0 = (j0 * P.block) / kv_bs;
+    const bool pg_early = P.row_seq == nullptr;
+    const int span = (P.probe_bpc * P.block + kv_bs - 1) / kv_bs;
+    int32_t pspec[PPT];
+#pragma unroll
+    for (int k = 0; k < PPT; k++) {
+        const int i = threadIdx.x + k * PROBE_WARPS * 32;
+        pspec[k] = -1;
+        if (pg_early && i <= span && pg0 + i < P.max_pages)
+            pspec[k] = P.page_table[(size_t)b * P.max_pages + pg0 + i];
+    }
+    float4 qx = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (warp < G)
+        qx = reinterpret_cast<const float4*>(
+            P.q + ((size_t)b * P.nq + (size_t)h * G + warp) * HD)[lane];
     int n = sparse_seq_len(P, b);
     if (n < 0 || n <= 2 * P.block) {  // gate: the exact path needs no probe
-        griddep_wait();
         if (P.tickets && blockIdx.x == 0) {
             if (n < 0 && threadIdx.x == 0 && h == 0 && P.status)
                 atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
@@ -719,7 +750,6 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32, 2)
         // every block is kept whatever its score: the selection is blocks 0 ..
         // nblk - 1 in order for every head, the union every tile (no scores are
         // needed; with tickets nothing after this kernel reads them)
-        griddep_wait();
         if (blockIdx.x == 0) {
             if (P.sel_blocks)
                 for (int g = 0; g < G; g++) {
@@ -731,41 +761,30 @@ __global__ void __launch_bounds__(PROBE_WARPS * 32, 2)
         }
         return;
     }
-    const int j0 = blockIdx.x * P.probe_bpc;
     if (j0 >= nblk) return;
     const int j1 = min(j0 + P.probe_bpc, nblk);
-    const int pg0 = (j0 * P.block) / kv_bs;
     const int pg1 = (min(j1 * P.block, n) - 1) / kv_bs;
 
-    const size_t pt_row = (size_t)(P.row_seq ? P.row_seq[b] : b) * P.max_pages;
-    for (int i = threadIdx.x; i <= pg1 - pg0; i += PROBE_WARPS * 32) {
-        const int32_t pg = P.page_table[pt_row + pg0 + i];
-        const bool ok = pg >= 0 && pg < P.cache.num_pages;
-        if (!ok && P.status) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
-        pages[i] = ok ? pg : -1;
+    const size_t pt_row = (size_t)(pg_early ? b : P.row_seq[b]) * P.max_pages;
+#pragma unroll
+    for (int k = 0; k < PPT; k++) {
+        const int i = threadIdx.x + k * PROBE_WARPS * 32;
+        if (i <= pg1 - pg0) {
+            const int32_t pg = pg_early ? pspec[k] : P.page_table[pt_row + pg0 + i];
+            const bool ok = pg >= 0 && pg < P.cache.num_pages;
+            if (!ok && P.status) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
+            pages[i] = ok ? pg : -1;
+        }
     }
     for (int i = threadIdx.x; i < (j1 - j0) * G; i += PROBE_WARPS * 32)
         best[i / G][i % G] = -INFINITY;
-    for (int g = warp; g < G; g += PROBE_WARPS) {
-        const float4 x =
-            reinterpret_cast<const float4*>(P.q + ((size_t)b * P.nq + (size_t)h * G + g) * HD)[lane];
+    if (warp < G) {
         float qs;
-        const uint32_t codes = quantize_q_lane(x, qs);
-        reinterpret_cast<uint32_t*>(qi[g])[lane] = codes;
-        if ((lane & 7) == 0) qsc[g][lane >> 3] = qs;
-    }
-    if (TMA) {
-        if (lane == 0)
-            for (int i = 0; i < PROBE_STAGES; i++) mbar_init(&pbar[warp][i], 1);
-        if (threadIdx.x == 0)
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&P.kmap))
-                         : "memory");
-        fence_barrier_init();
+        const uint32_t codes = quantize_q_lane(qx, qs);
+        reinterpret_cast<uint32_t*>(qi[warp])[lane] = codes;
+        if ((lane & 7) == 0) qsc[warp][lane >> 3] = qs;
     }
     __syncthreads();
-    // the kernel before this one has completed: its KV, scores, lists and masks
-    // are final
-    griddep_wait();
     // the selection ORs its heads' choices into these blocks' masks (rows of
     // more than 2048 blocks, or the separate top-k kernel; a probe-only call
     // passes none)

@@ -103,3 +103,53 @@ def test_sparse_exact_sparse_on_one_stream():
     assert_out_close(out_s.cpu().numpy(), ref_s, "sparse, first")
     assert np.array_equal(out_s2.cpu().numpy(), out_s.cpu().numpy()), "sparse, again"
     assert_out_close(out_e.cpu().numpy(), oracle_decode(wl, q, Ks, Vs), "exact between")
+
+
+def _exact(out, q, case, wl, ws):
+    kq8.kq8_decode_attn(out, q, case.cache, case.page_table, case.seq_lens, wl.max_seq_len,
+                        wl.scale, ws)
+
+
+def _sparse(out, q, case, wl, ws):
+    kq8.kq8_sparse_decode_attn(out, q, case.cache, case.page_table, case.seq_lens,
+                               wl.max_seq_len, wl.scale, wl.block, wl.topk, wl.probe, ws)
+
+
+@pytest.mark.parametrize("nq", [16, 32])
+@pytest.mark.parametrize("first,second", [("exact", "exact"), ("exact", "sparse"),
+                                          ("sparse", "exact"), ("sparse", "sparse")])
+def test_query_is_the_previous_calls_output(first, second, nq):
+    # The second call's query is the first call's output, with no other kernel
+    # between them: the second call's CTAs may be resident while the first
+    # call's last CTAs still write that output, and must not use it before the
+    # first call has completed.  The first call is many waves long (its rows
+    # are written up to its very end) and its output starts as NaN, so an early
+    # read shows.  At 16 query heads (2 per KV head) the exact walk reads its
+    # inputs before the wait as a guess and checks them after it: the guess is
+    # then stale, and the walk has to start over from the values read after the
+    # wait.  Reference: the same second call after a synchronisation.
+    lens = list(W._rng(93).integers(4096, 16384, 32))
+    wl = W.custom(32, nq, 8, lens, seed=93)
+    case = paged.fill_cache(wl, 0, DEV)
+    run = {"exact": _exact, "sparse": _sparse}
+    nbytes = max(kq8.kq8_decode_workspace_bytes(wl.B, wl.nq, wl.nkv, wl.max_seq_len),
+                 kq8.kq8_sparse_decode_workspace_bytes(wl.B, wl.nq, wl.nkv, wl.max_seq_len,
+                                                       wl.block, wl.topk))
+    ws1, ws2 = kq8.new_workspace(nbytes, DEV), kq8.new_workspace(nbytes, DEV)
+    a = torch.empty((wl.B, wl.nq, 128), device=DEV)
+    c = torch.empty_like(a)
+    ref = torch.empty_like(a)
+    for rep in range(3):
+        a.fill_(float("nan"))
+        c.fill_(0.0)
+        run[first](a, case.q, case, wl, ws1)
+        run[second](c, a, case, wl, ws2)
+        torch.cuda.synchronize()
+        run[second](ref, a, case, wl, ws2)
+        torch.cuda.synchronize()
+        assert kq8.kq8_read_status(ws1) == 0 and kq8.kq8_read_status(ws2) == 0
+        assert not torch.isnan(a).any(), "first call left rows unwritten"
+        got, want = c.cpu().numpy(), ref.cpu().numpy()
+        assert np.array_equal(got, want), (
+            f"rep {rep}: {int((got != want).any(axis=2).sum())} of {wl.B * wl.nq} rows "
+            "computed from a query read before the previous call completed")
