@@ -183,7 +183,8 @@ struct SeqRange {
     bool bad;
 };
 template <bool SPARSE>
-__device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h, int raw_len) {
+__device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h, int raw_len,
+                                              int raw_begin) {
     SeqRange r;
     // a sparse list's length is loaded with the sequence length, not after it
     const int list_len = SPARSE ? P.list_len[b * P.cache.num_kv_heads + h] : 0;
@@ -192,7 +193,7 @@ __device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h,
     if (r.bad) r.n = 0;
     r.begin = 0;
     if (!SPARSE && P.seq_begin) {
-        r.begin = P.seq_begin[b];
+        r.begin = raw_begin;
         if (r.begin < 0 || r.begin > r.n) {
             r.bad = true;
             r.begin = r.n;
@@ -213,7 +214,7 @@ __device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h,
 }
 template <bool SPARSE>
 __device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h) {
-    return seq_range<SPARSE>(P, b, h, P.seq_lens[b]);
+    return seq_range<SPARSE>(P, b, h, P.seq_lens[b], (!SPARSE && P.seq_begin) ? P.seq_begin[b] : 0);
 }
 
 // Folds a result (m, s, a) into a running state (mo, so, ao), maxima in score
@@ -265,29 +266,38 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     fence_barrier_init();
     __syncthreads();
 
-    // The plain exact walk's list entry e is tile e, so its page ids need no
-    // list: they are part of the guess; a sparse walk's entries are loaded with
-    // the length after the wait (its page ids follow them).  Not at G = 4:
+    // The exact walk's list entry e is tile first + e (first: the tile of the
+    // streamed start, else 0), so its page ids need no list: they are part of
+    // the guess, loaded at the guessed start; a sparse walk's entries are
+    // loaded with the length after the wait (its page ids follow them).  A row
+    // map (row_seq) keeps its loads after the wait.  Not at G = 4:
     // there the walk sits at the 168 registers of three CTAs per SM, and with
     // these loads (guessed or only early) the serving step measured 0.3 %
     // slower than with the length first and the rest after it.
     constexpr bool EARLY = G != 4;
     constexpr int QR = (G + ATTN_WARPS - 1) / ATTN_WARPS;  // query rows per warp
-    const bool guess = EARLY && !SPARSE && P.seq_begin == nullptr && P.row_seq == nullptr;
+    const bool guess = EARLY && !SPARSE && P.row_seq == nullptr;
     const int e_spec = chunk * P.chunk_tiles + warp + ATTN_WARPS * lane;
     const bool in_chunk = warp + ATTN_WARPS * lane < P.chunk_tiles;
-    const bool pg_idx_ok = in_chunk && e_spec / subs < P.max_pages;
-    auto load_inputs = [&](float4 (&qv)[QR], int32_t& len, int32_t& pg) {
+    // L2-only loads (ld.global.cg): a guess must not leave a line in this SM's
+    // L1 that the check after the wait could hit
+    auto load_inputs = [&](float4 (&qv)[QR], int32_t& len, int32_t& beg) {
 #pragma unroll
         for (int k = 0; k < QR; k++) {
             const int g = warp + k * ATTN_WARPS;
             if (g < G)
-                qv[k] = reinterpret_cast<const float4*>(
-                    P.q + ((size_t)b * P.nq + (size_t)h * G + g) * HD)[lane];
+                qv[k] = __ldcg(reinterpret_cast<const float4*>(
+                                   P.q + ((size_t)b * P.nq + (size_t)h * G + g) * HD) +
+                               lane);
         }
-        len = P.seq_lens[b];
-        pg = -1;
-        if (guess && pg_idx_ok) pg = P.page_table[(size_t)b * P.max_pages + e_spec / subs];
+        len = __ldcg(P.seq_lens + b);
+        beg = (!SPARSE && P.seq_begin) ? __ldcg(P.seq_begin + b) : 0;
+    };
+    // the page id of this lane's entry for a walk that starts at token beg
+    auto page_at = [&](int32_t beg) -> int32_t {
+        const int t = max(beg, 0) / TILE + e_spec;
+        if (!in_chunk || t / subs >= P.max_pages) return -1;
+        return __ldcg(P.page_table + (size_t)b * P.max_pages + t / subs);
     };
     float4 qx[QR];  // the query rows the walk quantises
     int32_t tl_spec = 0;
@@ -318,8 +328,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     uint32_t my_mask = 0;
     int32_t my_page = -1;
     bool bad_page = false;
-    auto plan = [&](int32_t len, int32_t pg_pre) {
-        rng = seq_range<SPARSE>(P, b, h, len);
+    auto plan = [&](int32_t len, int32_t beg, int32_t pg_pre, bool use_pre) {
+        rng = seq_range<SPARSE>(P, b, h, len, beg);
         nch = max(1, (rng.entries + P.chunk_tiles - 1) / P.chunk_tiles);
         const int e0 = chunk * P.chunk_tiles;
         const int e1 = min(e0 + P.chunk_tiles, rng.entries);
@@ -340,8 +350,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                 my_mask = 0xFFu;
             }
             const int32_t pg =
-                guess ? pg_pre
-                      : P.page_table[(size_t)(P.row_seq ? P.row_seq[b] : b) * P.max_pages +
+                use_pre ? pg_pre
+                        : P.page_table[(size_t)(P.row_seq ? P.row_seq[b] : b) * P.max_pages +
                                      my_tile / subs];
             if (pg >= 0 && pg < P.cache.num_pages)
                 my_page = pg;
@@ -383,29 +393,33 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
         }
     };
     // the guess: inputs, plan and Q's codes before the wait (no global writes)
-    int32_t len_g = 0, pg_g = -1;
+    int32_t len_g = 0, beg_g = 0, pg_g = -1;
     if (guess) {
-        load_inputs(qx, len_g, pg_g);
-        plan(len_g, pg_g);
+        load_inputs(qx, len_g, beg_g);
+        pg_g = page_at(beg_g);
+        plan(len_g, beg_g, pg_g, true);
         quantise_q();
     }
     griddep_wait();
     float4 qv[QR];  // after the wait: the check of the guess, or the inputs
-    int32_t len_v = 0, pg_v = -1;
+    int32_t len_v = 0, beg_v = 0, pg_v = -1;
     if (guess) {
-        load_inputs(qv, len_v, pg_v);
+        // the page id at the guessed start: if the start is confirmed, it is the
+        // page id the walk needs
+        load_inputs(qv, len_v, beg_v);
+        pg_v = page_at(beg_g);
     } else {
-        load_inputs(qx, len_v, pg_v);
+        load_inputs(qx, len_v, beg_v);
         if (EARLY && SPARSE && in_chunk && e_spec < P.list_cap)
             tl_spec = P.tile_list[(size_t)(b * nkv + h) * P.list_cap + e_spec];
-        plan(len_v, pg_v);
+        plan(len_v, beg_v, -1, false);
     }
     for (int i = 0; i < NS && i < mine; i++) issue(i);
     // Q's codes while the first copies are in flight; every warp reads all heads'
     if (!guess) quantise_q();
     bool failed = false;
     if (guess) {
-        bool same = len_g == len_v && pg_g == pg_v;
+        bool same = len_g == len_v && beg_g == beg_v && pg_g == pg_v;
 #pragma unroll
         for (int k = 0; k < QR; k++)
             if (warp + k * ATTN_WARPS < G)
@@ -432,7 +446,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
             __syncthreads();  // every warp is done with the guess's Q codes
 #pragma unroll
             for (int k = 0; k < QR; k++) qx[k] = qv[k];
-            plan(len_v, pg_v);
+            plan(len_v, beg_v, -1, false);  // page ids read afresh
             if (landed) {
                 for (int i = 0; i < NS && i < mine; i++) issue(i);
             } else {

@@ -1,9 +1,11 @@
 """Stream order through the library's programmatic launches: each decode,
 append and probe kernel may be scheduled while the kernel before it on the
-stream finishes, and waits for it before touching anything that kernel reads or
-writes.  These cases put other work between and around the calls on one stream
-and check that every call sees exactly what stream order promises, against the
-oracle."""
+stream finishes, and waits for that kernel's completion before it uses global
+memory (the plain exact walk reads its inputs earlier only as a guess, which it
+checks after the wait).  These cases put other work between and around the
+calls on one stream and check that every call sees exactly what stream order
+promises, against the oracle or against the same call after a
+synchronisation."""
 import numpy as np
 import pytest
 
