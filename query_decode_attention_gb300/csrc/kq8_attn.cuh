@@ -257,10 +257,11 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     // (this library's or any other code's, when it signals its dependents
     // early) may still be writing anything this kernel reads -- Q, the
     // lengths, the page table, the KV, the tile lists.  So before it this CTA
-    // sets up its barriers and, on the plain exact walk, reads its inputs only
-    // as a guess: after the wait the same inputs are read again, and the walk
-    // goes on from the guess only if every value is the same (else it drops
-    // what it began and starts over from the values read after the wait).
+    // sets up its barriers and, on the exact walk without a row map, reads its
+    // inputs only as a guess: after the wait the same inputs are read again,
+    // and the walk goes on from the guess only if every value is the same
+    // (else it drops what it began and starts over from the values read after
+    // the wait).
     if (lane == 0)
         for (int s = 0; s < NS; s++) mbar_init(&S.bar[warp][s], 1);
     fence_barrier_init();
@@ -399,13 +400,15 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
         pg_g = page_at(beg_g);
         plan(len_g, beg_g, pg_g, true);
         quantise_q();
+        __syncthreads();  // the guessed Q codes, for every warp
     }
     griddep_wait();
     float4 qv[QR];  // after the wait: the check of the guess, or the inputs
     int32_t len_v = 0, beg_v = 0, pg_v = -1;
     if (guess) {
         // the page id at the guessed start: if the start is confirmed, it is the
-        // page id the walk needs
+        // page id the walk needs.  The check itself waits until the walk is done,
+        // so that these loads are off its path.
         load_inputs(qv, len_v, beg_v);
         pg_v = page_at(beg_g);
     } else {
@@ -415,10 +418,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
         plan(len_v, beg_v, -1, false);
     }
     for (int i = 0; i < NS && i < mine; i++) issue(i);
-    // Q's codes while the first copies are in flight; every warp reads all heads'
-    if (!guess) quantise_q();
+    if (!guess) {
+        // Q's codes while the first copies are in flight; every warp reads all heads'
+        quantise_q();
+        __syncthreads();
+    }
     bool failed = false;
-    if (guess) {
+    // the check of the guess: the same inputs read after the wait
+    auto guess_holds = [&]() {
         bool same = len_g == len_v && beg_g == beg_v && pg_g == pg_v;
 #pragma unroll
         for (int k = 0; k < QR; k++)
@@ -427,10 +434,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                        __float_as_uint(qx[k].y) == __float_as_uint(qv[k].y) &&
                        __float_as_uint(qx[k].z) == __float_as_uint(qv[k].z) &&
                        __float_as_uint(qx[k].w) == __float_as_uint(qv[k].w);
-        if (!__syncthreads_and(same)) {
-            // rare: an input changed between the guess and the wait.  Let the
-            // copies issued from the guess land, re-arm the barriers and start
-            // over from the values read after the wait.
+        return __syncthreads_and(same) != 0;
+    };
+    if (guess) {
+        if (!guess_holds()) {
+            // let the copies issued from the guess land, re-arm the barriers and
+            // start over from the values read after the wait
             bool landed = true;
             for (int i = 0; i < NS && i < mine; i++)
                 landed = __all_sync(0xffffffffu, mbar_wait_bounded(&S.bar[warp][i], 0)) && landed;
@@ -443,7 +452,6 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                 fence_barrier_init();
                 __syncwarp();
             }
-            __syncthreads();  // every warp is done with the guess's Q codes
 #pragma unroll
             for (int k = 0; k < QR; k++) qx[k] = qv[k];
             plan(len_v, beg_v, -1, false);  // page ids read afresh
@@ -454,14 +462,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
                 mine = 0;
             }
             quantise_q();
+            __syncthreads();  // the new Q codes, for every warp
         }
     }
-    // the inputs are settled: report bad values
-    if (rng.bad && threadIdx.x == 0 && chunk == 0 && h == 0) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
-    if (bad_page) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
-    if (chunk >= nch) return;
-    const int n = rng.n, begin = rng.begin;
-    __syncthreads();
+    const int gq = lane >> 2, c4 = lane & 3;  // mma fragment coordinates
+    // stored K max -> step (1/127); the softmax scale is applied after it
+    const float kstep = Q4 ? inv7() : inv127();
 
     float M2[G], Sl[G];
     // The value phase runs on the tensor cores: 16 m16n8 accumulator tiles D[.][.]
@@ -472,293 +478,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     // {0, 1, 4, 5}[k]; lane (g, c) holds head g's elements 32q + 8c .. + 7.
     float D[HD / 16][2][4];
     // the weights go to the tensor cores as fp16 scaled by 2^-ev (see below)
-    int ev = -149;
-#pragma unroll
-    for (int g = 0; g < G; g++) {
-        M2[g] = M_INIT;
-        Sl[g] = 0.0f;
-    }
-#pragma unroll
-    for (int cg = 0; cg < HD / 16; cg++)
-#pragma unroll
-        for (int j = 0; j < 4; j++) D[cg][0][j] = D[cg][1][j] = 0.0f;
-    const int gq = lane >> 2, c4 = lane & 3;  // mma fragment coordinates
-    float2 qsc2[GP][NB];  // block scales of head pairs (2gp, 2gp+1)
-#pragma unroll
-    for (int gp = 0; gp < GP; gp++)
-#pragma unroll
-        for (int bb = 0; bb < NB; bb++)
-            qsc2[gp][bb] = make_float2(S.qsc[2 * gp][bb], S.qsc[min(2 * gp + 1, G - 1)][bb]);
-    // stored K max -> step (1/127); the softmax scale is applied after it
-    const float kstep = Q4 ? inv7() : inv127();
-
-    int i = 0;
-    for (; i < mine; i++) {
-        const int tile = __shfl_sync(0xffffffffu, my_tile, i);
-        const uint32_t mask = __shfl_sync(0xffffffffu, my_mask, i);
-        const int32_t pg = __shfl_sync(0xffffffffu, my_page, i);
-        // every lane waits (each needs the barrier's acquire of the copied
-        // bytes); the warp gives up only together, so no lane is left behind
-        // in a shuffle
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&S.bar[warp][i % NS], (i / NS) & 1))) {
-            failed = true;
-            break;
-        }
-        if (pg >= 0) {
-            const int8_t* kst = reinterpret_cast<const int8_t*>(S.k[warp][i % NS]);
-            const int8_t* vst = reinterpret_cast<const int8_t*>(S.v[warp][i % NS]);
-            const float* kss = S.sc[warp][i % NS][0];
-            const float* vss = S.sc[warp][i % NS][1];
-
-            // ---- score phase: lane q reads K position q, i.e. token row
-            // t = krow(q) of the tile, and scores it for all G heads
-            const int q = lane;
-            const int t = krow(q);
-            const bool live = tile * TILE + t < n && tile * TILE + t >= begin;
-            int dot[G][NB];
-            const int hs = Q4 ? 0 : (q >> 2) & 1;  // half order: conflict-free loads
-#pragma unroll
-            for (int bb = 0; bb < NB; bb++) {
-                uint4 kA, kB;
-                if (Q4) {  // 16 B = 32 nibbles -> offset-binary bytes in element order
-                    const uint4 kp = *reinterpret_cast<const uint4*>(kst + bb * 512 + q * 16);
-                    kA = make_uint4(kp.x & 0x0F0F0F0Fu, (kp.x >> 4) & 0x0F0F0F0Fu,
-                                    kp.y & 0x0F0F0F0Fu, (kp.y >> 4) & 0x0F0F0F0Fu);
-                    kB = make_uint4(kp.z & 0x0F0F0F0Fu, (kp.z >> 4) & 0x0F0F0F0Fu,
-                                    kp.w & 0x0F0F0F0Fu, (kp.w >> 4) & 0x0F0F0F0Fu);
-                } else {
-                    kA = *reinterpret_cast<const uint4*>(kst + bb * 1024 + q * 32 + hs * 16);
-                    kB = *reinterpret_cast<const uint4*>(kst + bb * 1024 + q * 32 +
-                                                         (hs ^ 1) * 16);
-                }
-#pragma unroll
-                for (int g = 0; g < G; g++) {
-                    const uint4 qA =
-                        *reinterpret_cast<const uint4*>(S.qi[g] + bb * 32 + hs * 16);
-                    const uint4 qB =
-                        *reinterpret_cast<const uint4*>(S.qi[g] + bb * 32 + (hs ^ 1) * 16);
-                    int d;
-                    if (Q4) {
-                        d = dp4a_us(kA.x, qA.x, S.qsum[g][bb]);
-                        d = dp4a_us(kA.y, qA.y, d);
-                        d = dp4a_us(kA.z, qA.z, d);
-                        d = dp4a_us(kA.w, qA.w, d);
-                        d = dp4a_us(kB.x, qB.x, d);
-                        d = dp4a_us(kB.y, qB.y, d);
-                        d = dp4a_us(kB.z, qB.z, d);
-                        d = dp4a_us(kB.w, qB.w, d);
-                    } else {
-                        d = __dp4a((int)kA.x, (int)qA.x, 0);
-                        d = __dp4a((int)kA.y, (int)qA.y, d);
-                        d = __dp4a((int)kA.z, (int)qA.z, d);
-                        d = __dp4a((int)kA.w, (int)qA.w, d);
-                        d = __dp4a((int)kB.x, (int)qB.x, d);
-                        d = __dp4a((int)kB.y, (int)qB.y, d);
-                        d = __dp4a((int)kB.z, (int)qB.z, d);
-                        d = __dp4a((int)kB.w, (int)qB.w, d);
-                    }
-                    dot[g][bb] = d;
-                }
-            }
-            // s = (s * ks) * scale with ks = kscale / 127, each product rounded
-            // as the method writes it, so every score equals the oracle's
-            const float ks = __fmul_rn(kss[t], kstep);
-            const float vstep = __fmul_rn(vss[t], Q4 ? inv7() : inv127());
-            float sv[2 * GP];
-#pragma unroll
-            for (int gp = 0; gp < GP; gp++) {
-                const int g1 = min(2 * gp + 1, G - 1);
-                // s = sum_b dot_b * qsc_b in block order (the first add, 0 + x, is exact);
-                // the int32 dots are < 2^22 in magnitude, so the conversions are exact
-                float2 s = __fmul2_rn(make_float2(__int2float_rn(dot[2 * gp][0]),
-                                                  __int2float_rn(dot[g1][0])),
-                                      qsc2[gp][0]);
-#pragma unroll
-                for (int bb = 1; bb < NB; bb++)
-                    s = __fadd2_rn(s, __fmul2_rn(make_float2(__int2float_rn(dot[2 * gp][bb]),
-                                                             __int2float_rn(dot[g1][bb])),
-                                                 qsc2[gp][bb]));
-                s = __fmul2_rn(__fmul2_rn(s, make_float2(ks, ks)), make_float2(P.scale, P.scale));
-                sv[2 * gp] = s.x;
-                sv[2 * gp + 1] = s.y;
-            }
-#pragma unroll
-            for (int g = 0; g < G; g++) {
-                const bool on = live && ((mask >> g) & 1u);
-                sv[g] = on ? sv[g] : -INFINITY;
-            }
-            // (s - M) * log2(e): the difference first, then base 2 (masked: -inf)
-            float dd[2 * GP];
-            bool grow = false;
-#pragma unroll
-            for (int gp = 0; gp < GP; gp++) {
-                const int g1 = min(2 * gp + 1, G - 1);
-                const float2 x = __fmul2_rn(
-                    __fadd2_rn(make_float2(sv[2 * gp], sv[g1]), make_float2(-M2[2 * gp], -M2[g1])),
-                    make_float2(LOG2E, LOG2E));
-                dd[2 * gp] = x.x;
-                dd[2 * gp + 1] = x.y;
-                grow |= x.x > RESCALE_SLACK || x.y > RESCALE_SLACK;
-            }
-            if (__any_sync(0xffffffffu, grow)) {
-                // rare: some head's maximum grew by a wide margin -> rescale its state
-                float cl = 1.0f;  // the factor of this lane's accumulator head gq
-#pragma unroll
-                for (int g = 0; g < G; g++) {
-                    const float mn = fmaxf(M2[g], warp_max(sv[g]));
-                    if (mn > M2[g]) {
-                        const float c = exp_diff(M2[g], mn);
-                        Sl[g] *= c;
-                        cl = (g == gq) ? c : cl;
-                        M2[g] = mn;
-                        dd[g] = (sv[g] - mn) * LOG2E;
-                    }
-                }
-#pragma unroll
-                for (int cg = 0; cg < HD / 16; cg++)
-#pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        D[cg][0][j] *= cl;
-                        D[cg][1][j] *= cl;
-                    }
-            }
-            float w[2 * GP];
-#pragma unroll
-            for (int g = 0; g < G; g++) {
-                w[g] = ex2(dd[g]);  // masked: ex2(-inf) = 0
-                Sl[g] += w[g];
-            }
-            if constexpr ((G & 1) != 0) w[G] = 0.0f;
-            {
-                // weights for the tensor cores: P' = w * vstep * 2^-ev as fp16 hi + lo
-                // (22 significant bits).  ev keeps the tile's largest live V step
-                // times 2^-ev below 2^7, so with w <= 2^8 (the lazy rescale bound)
-                // P' < 2^15, inside the fp16 range; a tile that needs a larger ev
-                // first scales the accumulators by the exact power of two 2^(old - new)
-                const uint32_t vb = __reduce_max_sync(
-                    0xffffffffu, (live && mask != 0u) ? __float_as_uint(vstep) : 0u);
-                const int ve = (int)(vb >> 23) - 127;
-                if (vb != 0u && ve > ev + 6) {  // warp-uniform, rare
-                    const int en = ve - 6;
-                    const float f = (ev - en >= -126) ? pow2i(ev - en) : 0.0f;
-#pragma unroll
-                    for (int cg = 0; cg < HD / 16; cg++)
-#pragma unroll
-                        for (int j = 0; j < 4; j++) {
-                            D[cg][0][j] *= f;
-                            D[cg][1][j] *= f;
-                        }
-                    ev = en;
-                }
-                const int k1 = min(max(-ev, -126), 127);
-                const float vsc = __fmul_rn(__fmul_rn(vstep, pow2i(k1)),
-                                            pow2i(min(max(-ev - k1, -126), 127)));
-                // token t's slot: sigma(t) = 8c + 4ks + 2h + j for t = 16ks + 8h + 2c + j,
-                // so the 8 tokens an mma lane (., c) needs are contiguous
-                const int slot = ((t >> 1) & 3) * 8 + (t >> 4) * 4 + ((t >> 3) & 1) * 2 + (t & 1);
-#pragma unroll
-                for (int gp = 0; gp < GP; gp++) {
-                    float2 pp = __fmul2_rn(make_float2(w[2 * gp], w[2 * gp + 1]),
-                                           make_float2(vsc, vsc));
-                    // masked tokens have w = 0; their (possibly stale) scale must not leak in
-                    pp.x = (w[2 * gp] != 0.0f) ? pp.x : 0.0f;
-                    pp.y = (w[2 * gp + 1] != 0.0f) ? pp.y : 0.0f;
-                    const uint32_t hi = f2_to_h2(pp.x, pp.y);
-                    const float2 hf = h2_to_f2(hi);
-                    const float2 r = __fadd2_rn(pp, make_float2(-hf.x, -hf.y));  // exact
-                    const uint32_t lo = f2_to_h2(r.x, r.y);
-                    S.pw[warp][2 * gp][slot] = __byte_perm(hi, lo, 0x5410);
-                    if (2 * gp + 1 < G) S.pw[warp][2 * gp + 1][slot] = __byte_perm(hi, lo, 0x7632);
-                }
-            }
-            __syncwarp();
-
-            {
-                // ---- value phase on the tensor cores: D += P' (rows: heads hi | lo,
-                // k: 32 tokens) x V (k: tokens, n: elements), two m16n8k16 k-steps per
-                // 8-element n-tile.  A (this lane's head gq; zero rows for gq >= G):
-                // tokens 2c, 2c+1, 2c+8, 2c+9 | +16, from slots 8c .. 8c+7.
-                uint32_t a0[4] = {0u, 0u, 0u, 0u}, a1[4] = {0u, 0u, 0u, 0u};
-                if (gq < G) {
-                    const uint4 x0 = *reinterpret_cast<const uint4*>(&S.pw[warp][gq][8 * c4]);
-                    const uint4 x1 = *reinterpret_cast<const uint4*>(&S.pw[warp][gq][8 * c4 + 4]);
-                    a0[0] = __byte_perm(x0.x, x0.y, 0x5410);  // hi of tokens 2c, 2c+1
-                    a0[1] = __byte_perm(x0.x, x0.y, 0x7632);  // lo
-                    a0[2] = __byte_perm(x0.z, x0.w, 0x5410);  // hi of 2c+8, 2c+9
-                    a0[3] = __byte_perm(x0.z, x0.w, 0x7632);
-                    a1[0] = __byte_perm(x1.x, x1.y, 0x5410);  // k-step 1: tokens + 16
-                    a1[1] = __byte_perm(x1.x, x1.y, 0x7632);
-                    a1[2] = __byte_perm(x1.z, x1.w, 0x5410);
-                    a1[3] = __byte_perm(x1.z, x1.w, 0x7632);
-                }
-                if (Q4) {
-                    // B (q4): per 16-byte chunk cq of a 64-byte row (32 elements), one
-                    // transposed ldmatrix of the four 8-token blocks as 16-bit words
-                    // (64-byte swizzle: chunk cq of row t at cq ^ ((t / 2) % 4)).
-                    // Register i holds for tokens 8i + 2c and + 1 the bytes 2(g%2),
-                    // 2(g%2) + 1 of word 4cq + g/2: elements e0 = 32cq + 8(g/2) + 2(g%2),
-                    // e0 + 1 (low nibbles) and e0 + 4, e0 + 5 (high nibbles).  A low
-                    // nibble u = code + 8 masked into the mantissa of 1024 gives 1024 + u,
-                    // minus 1032; a high one gives 1024 + 16u, times 1/16 minus 72 (one
-                    // fma): both exact.
-                    const uint32_t vrow = smem_u32(vst) + (uint32_t)lane * (HD / 2);
-#pragma unroll
-                    for (int cq = 0; cq < HD / 32; cq++) {
-                        uint32_t r[4];
-                        ldsm_x4_trans(vrow + ((uint32_t)(cq ^ ((lane >> 1) & 3)) << 4), r[0],
-                                      r[1], r[2], r[3]);
-                        uint32_t b[4][4];  // [n-tile: +0, +1, +4, +5][register]
-#pragma unroll
-                        for (int j = 0; j < 4; j++) {
-                            const uint32_t r8 = r[j] >> 8;  // bytes 1, 3 -> 0, 2
-                            b[0][j] = hsub2(and_or(r[j], 0x000F000Fu, 0x64006400u), 0x64086408u);
-                            b[1][j] = hsub2(and_or(r8, 0x000F000Fu, 0x64006400u), 0x64086408u);
-                            b[2][j] = hfma2(and_or(r[j], 0x00F000F0u, 0x64006400u), 0x2C002C00u,
-                                            0xD480D480u);
-                            b[3][j] = hfma2(and_or(r8, 0x00F000F0u, 0x64006400u), 0x2C002C00u,
-                                            0xD480D480u);
-                        }
-#pragma unroll
-                        for (int k = 0; k < 4; k++) {
-                            mma_f16_16816(D[2 * cq + (k >> 1)][k & 1], a0, b[k][0], b[k][1]);
-                            mma_f16_16816(D[2 * cq + (k >> 1)][k & 1], a1, b[k][2], b[k][3]);
-                        }
-                    }
-                } else {
-                    // B: per 16-byte chunk cg, one transposed ldmatrix of the four 8-token
-                    // blocks as 16-bit element pairs: register i holds, for tokens 8i + 2c
-                    // and + 1, elements 16cg + 2g and + 1.  Lane L gives token row L's
-                    // chunk, at its 128-byte-swizzled place.
-                    const uint32_t vrow = smem_u32(vst) + (uint32_t)lane * HD;
-#pragma unroll
-                    for (int cg = 0; cg < HD / 16; cg++) {
-                        uint32_t r[4];
-                        ldsm_x4_trans(vrow + ((uint32_t)(cg ^ (lane & 7)) << 4), r[0], r[1], r[2], r[3]);
-                        // int8 pair -> fp16 pair exactly: offset binary u = c + 128 into the
-                        // mantissa of 1024 (0x64uu), minus 1152
-                        uint32_t be[4], bo[4];
-#pragma unroll
-                        for (int j = 0; j < 4; j++) {
-                            const uint32_t u = r[j] ^ 0x80808080u;
-                            be[j] = hsub2(__byte_perm(u, 0x64646464u, 0x4240), 0x64806480u);
-                            bo[j] = hsub2(__byte_perm(u, 0x64646464u, 0x4341), 0x64806480u);
-                        }
-                        mma_f16_16816(D[cg][0], a0, be[0], be[1]);
-                        mma_f16_16816(D[cg][0], a1, be[2], be[3]);
-                        mma_f16_16816(D[cg][1], a0, bo[0], bo[1]);
-                        mma_f16_16816(D[cg][1], a1, bo[2], bo[3]);
-                    }
-                }
-            }
-        }
-        __syncwarp();
-        if (i + NS < mine) issue(i + NS);
-    }
-    if (failed) {
-        if (lane == 0) atomicOr(P.status, KQ8_STATUS_TIMEOUT);
-        // let the copies this warp still has in flight land before leaving
-        for (int j = i; j < mine && j < i + NS; j++)
-            __all_sync(0xffffffffu, mbar_wait_bounded(&S.bar[warp][j % NS], (j / NS) & 1));
+    int ev;
+    {  // the walk
+        ev = -149;
 #pragma unroll
         for (int g = 0; g < G; g++) {
             M2[g] = M_INIT;
@@ -768,7 +490,298 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
         for (int cg = 0; cg < HD / 16; cg++)
 #pragma unroll
             for (int j = 0; j < 4; j++) D[cg][0][j] = D[cg][1][j] = 0.0f;
+        float2 qsc2[GP][NB];  // block scales of head pairs (2gp, 2gp+1)
+#pragma unroll
+        for (int gp = 0; gp < GP; gp++)
+#pragma unroll
+            for (int bb = 0; bb < NB; bb++)
+                qsc2[gp][bb] = make_float2(S.qsc[2 * gp][bb], S.qsc[min(2 * gp + 1, G - 1)][bb]);
+
+        int i = 0;
+        for (; i < mine; i++) {
+            const int tile = __shfl_sync(0xffffffffu, my_tile, i);
+            const uint32_t mask = __shfl_sync(0xffffffffu, my_mask, i);
+            const int32_t pg = __shfl_sync(0xffffffffu, my_page, i);
+            // every lane waits (each needs the barrier's acquire of the copied
+            // bytes); the warp gives up only together, so no lane is left behind
+            // in a shuffle
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait_bounded(&S.bar[warp][i % NS], (i / NS) & 1))) {
+                failed = true;
+                break;
+            }
+            if (pg >= 0) {
+                const int st = i % NS;
+                const int8_t* kst = reinterpret_cast<const int8_t*>(S.k[warp][st]);
+                const int8_t* vst = reinterpret_cast<const int8_t*>(S.v[warp][st]);
+                const float* kss = S.sc[warp][st][0];
+                const float* vss = S.sc[warp][st][1];
+
+                // ---- score phase: lane q reads K position q, i.e. token row
+                // t = krow(q) of the tile, and scores it for all G heads
+                const int q = lane;
+                const int t = krow(q);
+                const bool live = tile * TILE + t < rng.n && tile * TILE + t >= rng.begin;
+                int dot[G][NB];
+                const int hs = Q4 ? 0 : (q >> 2) & 1;  // half order: conflict-free loads
+#pragma unroll
+                for (int bb = 0; bb < NB; bb++) {
+                    uint4 kA, kB;
+                    if (Q4) {  // 16 B = 32 nibbles -> offset-binary bytes in element order
+                        const uint4 kp = *reinterpret_cast<const uint4*>(kst + bb * 512 + q * 16);
+                        kA = make_uint4(kp.x & 0x0F0F0F0Fu, (kp.x >> 4) & 0x0F0F0F0Fu,
+                                        kp.y & 0x0F0F0F0Fu, (kp.y >> 4) & 0x0F0F0F0Fu);
+                        kB = make_uint4(kp.z & 0x0F0F0F0Fu, (kp.z >> 4) & 0x0F0F0F0Fu,
+                                        kp.w & 0x0F0F0F0Fu, (kp.w >> 4) & 0x0F0F0F0Fu);
+                    } else {
+                        kA = *reinterpret_cast<const uint4*>(kst + bb * 1024 + q * 32 + hs * 16);
+                        kB = *reinterpret_cast<const uint4*>(kst + bb * 1024 + q * 32 +
+                                                             (hs ^ 1) * 16);
+                    }
+#pragma unroll
+                    for (int g = 0; g < G; g++) {
+                        const uint4 qA =
+                            *reinterpret_cast<const uint4*>(S.qi[g] + bb * 32 + hs * 16);
+                        const uint4 qB =
+                            *reinterpret_cast<const uint4*>(S.qi[g] + bb * 32 + (hs ^ 1) * 16);
+                        int d;
+                        if (Q4) {
+                            d = dp4a_us(kA.x, qA.x, S.qsum[g][bb]);
+                            d = dp4a_us(kA.y, qA.y, d);
+                            d = dp4a_us(kA.z, qA.z, d);
+                            d = dp4a_us(kA.w, qA.w, d);
+                            d = dp4a_us(kB.x, qB.x, d);
+                            d = dp4a_us(kB.y, qB.y, d);
+                            d = dp4a_us(kB.z, qB.z, d);
+                            d = dp4a_us(kB.w, qB.w, d);
+                        } else {
+                            d = __dp4a((int)kA.x, (int)qA.x, 0);
+                            d = __dp4a((int)kA.y, (int)qA.y, d);
+                            d = __dp4a((int)kA.z, (int)qA.z, d);
+                            d = __dp4a((int)kA.w, (int)qA.w, d);
+                            d = __dp4a((int)kB.x, (int)qB.x, d);
+                            d = __dp4a((int)kB.y, (int)qB.y, d);
+                            d = __dp4a((int)kB.z, (int)qB.z, d);
+                            d = __dp4a((int)kB.w, (int)qB.w, d);
+                        }
+                        dot[g][bb] = d;
+                    }
+                }
+                // s = (s * ks) * scale with ks = kscale / 127, each product rounded
+                // as the method writes it, so every score equals the oracle's
+                const float ks = __fmul_rn(kss[t], kstep);
+                const float vstep = __fmul_rn(vss[t], Q4 ? inv7() : inv127());
+                float sv[2 * GP];
+#pragma unroll
+                for (int gp = 0; gp < GP; gp++) {
+                    const int g1 = min(2 * gp + 1, G - 1);
+                    // s = sum_b dot_b * qsc_b in block order (the first add, 0 + x, is exact);
+                    // the int32 dots are < 2^22 in magnitude, so the conversions are exact
+                    float2 s = __fmul2_rn(make_float2(__int2float_rn(dot[2 * gp][0]),
+                                                      __int2float_rn(dot[g1][0])),
+                                          qsc2[gp][0]);
+#pragma unroll
+                    for (int bb = 1; bb < NB; bb++)
+                        s = __fadd2_rn(s, __fmul2_rn(make_float2(__int2float_rn(dot[2 * gp][bb]),
+                                                                 __int2float_rn(dot[g1][bb])),
+                                                     qsc2[gp][bb]));
+                    s = __fmul2_rn(__fmul2_rn(s, make_float2(ks, ks)), make_float2(P.scale, P.scale));
+                    sv[2 * gp] = s.x;
+                    sv[2 * gp + 1] = s.y;
+                }
+#pragma unroll
+                for (int g = 0; g < G; g++) {
+                    const bool on = live && ((mask >> g) & 1u);
+                    sv[g] = on ? sv[g] : -INFINITY;
+                }
+                // (s - M) * log2(e): the difference first, then base 2 (masked: -inf)
+                float dd[2 * GP];
+                bool grow = false;
+#pragma unroll
+                for (int gp = 0; gp < GP; gp++) {
+                    const int g1 = min(2 * gp + 1, G - 1);
+                    const float2 x = __fmul2_rn(
+                        __fadd2_rn(make_float2(sv[2 * gp], sv[g1]), make_float2(-M2[2 * gp], -M2[g1])),
+                        make_float2(LOG2E, LOG2E));
+                    dd[2 * gp] = x.x;
+                    dd[2 * gp + 1] = x.y;
+                    grow |= x.x > RESCALE_SLACK || x.y > RESCALE_SLACK;
+                }
+                if (__any_sync(0xffffffffu, grow)) {
+                    // rare: some head's maximum grew by a wide margin -> rescale its state
+                    float cl = 1.0f;  // the factor of this lane's accumulator head gq
+#pragma unroll
+                    for (int g = 0; g < G; g++) {
+                        const float mn = fmaxf(M2[g], warp_max(sv[g]));
+                        if (mn > M2[g]) {
+                            const float c = exp_diff(M2[g], mn);
+                            Sl[g] *= c;
+                            cl = (g == gq) ? c : cl;
+                            M2[g] = mn;
+                            dd[g] = (sv[g] - mn) * LOG2E;
+                        }
+                    }
+#pragma unroll
+                    for (int cg = 0; cg < HD / 16; cg++)
+#pragma unroll
+                        for (int j = 0; j < 4; j++) {
+                            D[cg][0][j] *= cl;
+                            D[cg][1][j] *= cl;
+                        }
+                }
+                float w[2 * GP];
+#pragma unroll
+                for (int g = 0; g < G; g++) {
+                    w[g] = ex2(dd[g]);  // masked: ex2(-inf) = 0
+                    Sl[g] += w[g];
+                }
+                if constexpr ((G & 1) != 0) w[G] = 0.0f;
+                {
+                    // weights for the tensor cores: P' = w * vstep * 2^-ev as fp16 hi + lo
+                    // (22 significant bits).  ev keeps the tile's largest live V step
+                    // times 2^-ev below 2^7, so with w <= 2^8 (the lazy rescale bound)
+                    // P' < 2^15, inside the fp16 range; a tile that needs a larger ev
+                    // first scales the accumulators by the exact power of two 2^(old - new)
+                    const uint32_t vb = __reduce_max_sync(
+                        0xffffffffu, (live && mask != 0u) ? __float_as_uint(vstep) : 0u);
+                    const int ve = (int)(vb >> 23) - 127;
+                    if (vb != 0u && ve > ev + 6) {  // warp-uniform, rare
+                        const int en = ve - 6;
+                        const float f = (ev - en >= -126) ? pow2i(ev - en) : 0.0f;
+#pragma unroll
+                        for (int cg = 0; cg < HD / 16; cg++)
+#pragma unroll
+                            for (int j = 0; j < 4; j++) {
+                                D[cg][0][j] *= f;
+                                D[cg][1][j] *= f;
+                            }
+                        ev = en;
+                    }
+                    const int k1 = min(max(-ev, -126), 127);
+                    const float vsc = __fmul_rn(__fmul_rn(vstep, pow2i(k1)),
+                                                pow2i(min(max(-ev - k1, -126), 127)));
+                    // token t's slot: sigma(t) = 8c + 4ks + 2h + j for t = 16ks + 8h + 2c + j,
+                    // so the 8 tokens an mma lane (., c) needs are contiguous
+                    const int slot = ((t >> 1) & 3) * 8 + (t >> 4) * 4 + ((t >> 3) & 1) * 2 + (t & 1);
+#pragma unroll
+                    for (int gp = 0; gp < GP; gp++) {
+                        float2 pp = __fmul2_rn(make_float2(w[2 * gp], w[2 * gp + 1]),
+                                               make_float2(vsc, vsc));
+                        // masked tokens have w = 0; their (possibly stale) scale must not leak in
+                        pp.x = (w[2 * gp] != 0.0f) ? pp.x : 0.0f;
+                        pp.y = (w[2 * gp + 1] != 0.0f) ? pp.y : 0.0f;
+                        const uint32_t hi = f2_to_h2(pp.x, pp.y);
+                        const float2 hf = h2_to_f2(hi);
+                        const float2 r = __fadd2_rn(pp, make_float2(-hf.x, -hf.y));  // exact
+                        const uint32_t lo = f2_to_h2(r.x, r.y);
+                        S.pw[warp][2 * gp][slot] = __byte_perm(hi, lo, 0x5410);
+                        if (2 * gp + 1 < G) S.pw[warp][2 * gp + 1][slot] = __byte_perm(hi, lo, 0x7632);
+                    }
+                }
+                __syncwarp();
+
+                {
+                    // ---- value phase on the tensor cores: D += P' (rows: heads hi | lo,
+                    // k: 32 tokens) x V (k: tokens, n: elements), two m16n8k16 k-steps per
+                    // 8-element n-tile.  A (this lane's head gq; zero rows for gq >= G):
+                    // tokens 2c, 2c+1, 2c+8, 2c+9 | +16, from slots 8c .. 8c+7.
+                    uint32_t a0[4] = {0u, 0u, 0u, 0u}, a1[4] = {0u, 0u, 0u, 0u};
+                    if (gq < G) {
+                        const uint4 x0 = *reinterpret_cast<const uint4*>(&S.pw[warp][gq][8 * c4]);
+                        const uint4 x1 = *reinterpret_cast<const uint4*>(&S.pw[warp][gq][8 * c4 + 4]);
+                        a0[0] = __byte_perm(x0.x, x0.y, 0x5410);  // hi of tokens 2c, 2c+1
+                        a0[1] = __byte_perm(x0.x, x0.y, 0x7632);  // lo
+                        a0[2] = __byte_perm(x0.z, x0.w, 0x5410);  // hi of 2c+8, 2c+9
+                        a0[3] = __byte_perm(x0.z, x0.w, 0x7632);
+                        a1[0] = __byte_perm(x1.x, x1.y, 0x5410);  // k-step 1: tokens + 16
+                        a1[1] = __byte_perm(x1.x, x1.y, 0x7632);
+                        a1[2] = __byte_perm(x1.z, x1.w, 0x5410);
+                        a1[3] = __byte_perm(x1.z, x1.w, 0x7632);
+                    }
+                    if (Q4) {
+                        // B (q4): per 16-byte chunk cq of a 64-byte row (32 elements), one
+                        // transposed ldmatrix of the four 8-token blocks as 16-bit words
+                        // (64-byte swizzle: chunk cq of row t at cq ^ ((t / 2) % 4)).
+                        // Register i holds for tokens 8i + 2c and + 1 the bytes 2(g%2),
+                        // 2(g%2) + 1 of word 4cq + g/2: elements e0 = 32cq + 8(g/2) + 2(g%2),
+                        // e0 + 1 (low nibbles) and e0 + 4, e0 + 5 (high nibbles).  A low
+                        // nibble u = code + 8 masked into the mantissa of 1024 gives 1024 + u,
+                        // minus 1032; a high one gives 1024 + 16u, times 1/16 minus 72 (one
+                        // fma): both exact.
+                        const uint32_t vrow = smem_u32(vst) + (uint32_t)lane * (HD / 2);
+#pragma unroll
+                        for (int cq = 0; cq < HD / 32; cq++) {
+                            uint32_t r[4];
+                            ldsm_x4_trans(vrow + ((uint32_t)(cq ^ ((lane >> 1) & 3)) << 4), r[0],
+                                          r[1], r[2], r[3]);
+                            uint32_t b[4][4];  // [n-tile: +0, +1, +4, +5][register]
+#pragma unroll
+                            for (int j = 0; j < 4; j++) {
+                                const uint32_t r8 = r[j] >> 8;  // bytes 1, 3 -> 0, 2
+                                b[0][j] = hsub2(and_or(r[j], 0x000F000Fu, 0x64006400u), 0x64086408u);
+                                b[1][j] = hsub2(and_or(r8, 0x000F000Fu, 0x64006400u), 0x64086408u);
+                                b[2][j] = hfma2(and_or(r[j], 0x00F000F0u, 0x64006400u), 0x2C002C00u,
+                                                0xD480D480u);
+                                b[3][j] = hfma2(and_or(r8, 0x00F000F0u, 0x64006400u), 0x2C002C00u,
+                                                0xD480D480u);
+                            }
+#pragma unroll
+                            for (int k = 0; k < 4; k++) {
+                                mma_f16_16816(D[2 * cq + (k >> 1)][k & 1], a0, b[k][0], b[k][1]);
+                                mma_f16_16816(D[2 * cq + (k >> 1)][k & 1], a1, b[k][2], b[k][3]);
+                            }
+                        }
+                    } else {
+                        // B: per 16-byte chunk cg, one transposed ldmatrix of the four 8-token
+                        // blocks as 16-bit element pairs: register i holds, for tokens 8i + 2c
+                        // and + 1, elements 16cg + 2g and + 1.  Lane L gives token row L's
+                        // chunk, at its 128-byte-swizzled place.
+                        const uint32_t vrow = smem_u32(vst) + (uint32_t)lane * HD;
+#pragma unroll
+                        for (int cg = 0; cg < HD / 16; cg++) {
+                            uint32_t r[4];
+                            ldsm_x4_trans(vrow + ((uint32_t)(cg ^ (lane & 7)) << 4), r[0], r[1], r[2], r[3]);
+                            // int8 pair -> fp16 pair exactly: offset binary u = c + 128 into the
+                            // mantissa of 1024 (0x64uu), minus 1152
+                            uint32_t be[4], bo[4];
+#pragma unroll
+                            for (int j = 0; j < 4; j++) {
+                                const uint32_t u = r[j] ^ 0x80808080u;
+                                be[j] = hsub2(__byte_perm(u, 0x64646464u, 0x4240), 0x64806480u);
+                                bo[j] = hsub2(__byte_perm(u, 0x64646464u, 0x4341), 0x64806480u);
+                            }
+                            mma_f16_16816(D[cg][0], a0, be[0], be[1]);
+                            mma_f16_16816(D[cg][0], a1, be[2], be[3]);
+                            mma_f16_16816(D[cg][1], a0, bo[0], bo[1]);
+                            mma_f16_16816(D[cg][1], a1, bo[2], bo[3]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (i + NS < mine) issue(i + NS);
+        }
+        if (failed) {
+            if (lane == 0) atomicOr(P.status, KQ8_STATUS_TIMEOUT);
+            // let the copies this warp still has in flight land before leaving
+            for (int j = i; j < mine && j < i + NS; j++)
+                __all_sync(0xffffffffu,
+                           mbar_wait_bounded(&S.bar[warp][j % NS], (j / NS) & 1));
+#pragma unroll
+            for (int g = 0; g < G; g++) {
+                M2[g] = M_INIT;
+                Sl[g] = 0.0f;
+            }
+#pragma unroll
+            for (int cg = 0; cg < HD / 16; cg++)
+#pragma unroll
+                for (int j = 0; j < 4; j++) D[cg][0][j] = D[cg][1][j] = 0.0f;
+        }
     }
+    // the inputs are settled: report bad values
+    if (rng.bad && threadIdx.x == 0 && chunk == 0 && h == 0) atomicOr(P.status, KQ8_STATUS_BAD_SEQLEN);
+    if (bad_page) atomicOr(P.status, KQ8_STATUS_BAD_PAGE);
+    if (chunk >= nch) return;
 
 #pragma unroll
     for (int g = 0; g < G; g++) Sl[g] = warp_sum(Sl[g]);
