@@ -1,7 +1,8 @@
 // kq8_attn.cuh -- the split-KV one-pass attention kernel and the chunk merge.
 //
 // Work decomposition: CTA = (KV chunk, KV head h, sequence b), 4 warps.  A
-// chunk is a run of `chunk_tiles` 32-token sub-tiles; warp w of the CTA takes
+// chunk is a run of `chunk_tiles` 32-token sub-tiles (a sparse list deals its
+// entries out to the chunks in turn, see list_chunks); warp w of the CTA takes
 // the chunk's tiles w, w+4, ...  All G query heads of KV head h are handled by
 // the same warp, so each K/V byte is read from HBM once for the whole group.
 //
@@ -212,6 +213,27 @@ __device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h,
     }
     return r;
 }
+// The chunks of a list and their entries.  An exact walk's chunk c holds the
+// run of chunk_tiles entries from c * chunk_tiles.  A sparse list's length is
+// known only once the selection has run, so its entries are dealt out in turn:
+// chunk c holds entries c, c + num_chunks, c + 2 num_chunks, ..., and every CTA
+// the grid has for the list walks an even share of it.
+template <bool SPARSE>
+__device__ __forceinline__ int list_chunks(const AttnParams& P, int entries) {
+    return SPARSE ? max(1, min(P.num_chunks, entries))
+                  : max(1, (entries + P.chunk_tiles - 1) / P.chunk_tiles);
+}
+// list entry of the k-th entry of chunk c
+template <bool SPARSE>
+__device__ __forceinline__ int list_entry(const AttnParams& P, int c, int k) {
+    return SPARSE ? c + P.num_chunks * k : c * P.chunk_tiles + k;
+}
+// entries of chunk c
+template <bool SPARSE>
+__device__ __forceinline__ int chunk_entries(const AttnParams& P, int c, int entries) {
+    return SPARSE ? (entries > c ? (entries - c + P.num_chunks - 1) / P.num_chunks : 0)
+                  : max(0, min(P.chunk_tiles, entries - c * P.chunk_tiles));
+}
 template <bool SPARSE>
 __device__ __forceinline__ SeqRange seq_range(const AttnParams& P, int b, int h) {
     return seq_range<SPARSE>(P, b, h, P.seq_lens[b], (!SPARSE && P.seq_begin) ? P.seq_begin[b] : 0);
@@ -278,7 +300,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     constexpr bool EARLY = G != 4;
     constexpr int QR = (G + ATTN_WARPS - 1) / ATTN_WARPS;  // query rows per warp
     const bool guess = EARLY && !SPARSE && P.row_seq == nullptr;
-    const int e_spec = chunk * P.chunk_tiles + warp + ATTN_WARPS * lane;
+    const int e_spec = list_entry<SPARSE>(P, chunk, warp + ATTN_WARPS * lane);
     const bool in_chunk = warp + ATTN_WARPS * lane < P.chunk_tiles;
     // L2-only loads (ld.global.cg): a guess must not leave a line in this SM's
     // L1 that the check after the wait could hit
@@ -331,16 +353,15 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     bool bad_page = false;
     auto plan = [&](int32_t len, int32_t beg, int32_t pg_pre, bool use_pre) {
         rng = seq_range<SPARSE>(P, b, h, len, beg);
-        nch = max(1, (rng.entries + P.chunk_tiles - 1) / P.chunk_tiles);
-        const int e0 = chunk * P.chunk_tiles;
-        const int e1 = min(e0 + P.chunk_tiles, rng.entries);
-        mine = (chunk < nch && e1 - e0 > warp) ? (e1 - e0 - warp + ATTN_WARPS - 1) / ATTN_WARPS : 0;
+        nch = list_chunks<SPARSE>(P, rng.entries);
+        const int ce = chunk < nch ? chunk_entries<SPARSE>(P, chunk, rng.entries) : 0;
+        mine = ce > warp ? (ce - warp + ATTN_WARPS - 1) / ATTN_WARPS : 0;
         my_tile = 0;
         my_mask = 0;
         my_page = -1;
         bad_page = false;
         if (lane < mine) {
-            const int e = e0 + warp + ATTN_WARPS * lane;  // = e_spec
+            const int e = e_spec;
             if (SPARSE) {
                 const int32_t v =
                     EARLY ? tl_spec : P.tile_list[(size_t)(b * nkv + h) * P.list_cap + e];
@@ -921,7 +942,7 @@ __global__ void __launch_bounds__(HD) kq8_merge_kernel(const AttnParams P) {
     const int G = P.nq / P.cache.num_kv_heads;
     const int h = hq / G;
     const int entries = seq_range<SPARSE>(P, b, h).entries;
-    const int nch = (entries + P.chunk_tiles - 1) / P.chunk_tiles;
+    const int nch = entries > 0 ? list_chunks<SPARSE>(P, entries) : 0;
     if (nch <= 1) return;
     const size_t base = (size_t)row * P.num_chunks;
     float mx = M_INIT;
