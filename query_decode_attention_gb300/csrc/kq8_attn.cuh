@@ -428,8 +428,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, AttnShape<G>::MIN_CTAS)
     int32_t len_v = 0, beg_v = 0, pg_v = -1;
     if (guess) {
         // the page id at the guessed start: if the start is confirmed, it is the
-        // page id the walk needs.  The check itself waits until the walk is done,
-        // so that these loads are off its path.
+        // page id the walk needs.  The check compares these with the guess once
+        // the first copies are out.
         load_inputs(qv, len_v, beg_v);
         pg_v = page_at(beg_g);
     } else {
