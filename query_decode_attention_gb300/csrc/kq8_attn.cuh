@@ -171,12 +171,6 @@ __device__ __forceinline__ float2 i2f_pair(int d0, int d1) {
                       make_float2(-12582912.0f, -12582912.0f));
 }
 
-__device__ __forceinline__ int valid_seq_len(const AttnParams& P, int b) {
-    int n = P.seq_lens[b];
-    if (n < 0 || n > P.max_seq_len) return -1;
-    return n;
-}
-
 // The tokens of sequence b one call attends: [begin, n), as list entries
 // (tiles) starting at tile first_tile; bad lengths/starts give an empty range.
 struct SeqRange {
