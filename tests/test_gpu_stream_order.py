@@ -155,3 +155,36 @@ def test_query_is_the_previous_calls_output(first, second, nq):
         assert np.array_equal(got, want), (
             f"rep {rep}: {int((got != want).any(axis=2).sum())} of {wl.B * wl.nq} rows "
             "computed from a query read before the previous call completed")
+
+
+def test_streamed_start_written_by_the_previous_call():
+    # A streamed update whose start index is an int32 the call just before it
+    # writes (the first block a sparse call selects, read as a token index), with
+    # nothing between: the update may read its start early, as a guess, while the
+    # sparse call's selection is still to come, and must then start over from the
+    # value read after the wait.  Reference: the same update after a
+    # synchronisation.
+    wl = W.custom(1, 16, 8, [4059], seed=94)
+    case = paged.fill_cache(wl, 0, DEV)
+    ws_s = kq8.new_workspace(kq8.kq8_sparse_decode_workspace_bytes(
+        wl.B, wl.nq, wl.nkv, wl.max_seq_len, wl.block, wl.topk), DEV)
+    ws_u = kq8.new_workspace(kq8.kq8_decode_workspace_bytes(wl.B, wl.nq, wl.nkv, wl.max_seq_len),
+                             DEV)
+    out_s = torch.empty((wl.B, wl.nq, 128), device=DEV)
+    sel = torch.empty((wl.B, wl.nq, wl.topk), dtype=torch.int32, device=DEV)
+    start = sel.view(-1)[:1]  # [B] = [1]: head 0's first selected block
+    for rep in range(3):
+        sel.fill_(-7)
+        s1, s2 = kq8.AttnState(wl.B, wl.nq, DEV), kq8.AttnState(wl.B, wl.nq, DEV)  # reset
+        kq8.kq8_sparse_decode_attn(out_s, case.q, case.cache, case.page_table, case.seq_lens,
+                                   wl.max_seq_len, wl.scale, wl.block, wl.topk, wl.probe, ws_s,
+                                   sel_blocks=sel)
+        kq8.kq8_decode_attn_update(s1, case.q, case.cache, case.page_table, start, case.seq_lens,
+                                   wl.max_seq_len, wl.scale, ws_u)
+        torch.cuda.synchronize()
+        kq8.kq8_decode_attn_update(s2, case.q, case.cache, case.page_table, start, case.seq_lens,
+                                   wl.max_seq_len, wl.scale, ws_u)
+        torch.cuda.synchronize()
+        assert kq8.kq8_read_status(ws_s) == 0 and kq8.kq8_read_status(ws_u) == 0
+        assert int(start.item()) >= 0
+        assert torch.equal(s1.acc, s2.acc) and torch.equal(s1.ms, s2.ms), f"rep {rep}"
