@@ -119,8 +119,10 @@ size_t kq8_decode_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int32_t ma
 /*
  * The split kq8_decode_attn uses for these sizes on the current device:
  * *chunk_tiles 32-token tiles per CTA (a multiple of 4) and *num_chunks chunks
- * for a sequence of max_seq_len tokens.  num_chunks > 1 means a merge kernel
- * runs after the attention kernel.  Host pointers.
+ * for a sequence of max_seq_len tokens.  A sequence split over several chunks
+ * has its partial results merged by the last of its CTAs to finish, or, when
+ * B * nkv exceeds the 16384 ticket counters, by a merge kernel launched after
+ * the attention kernel.  Host pointers.
  */
 int kq8_decode_plan(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len, int32_t* chunk_tiles,
                     int32_t* num_chunks);
@@ -200,7 +202,8 @@ size_t kq8_sparse_decode_workspace_bytes(int32_t B, int32_t nq, int32_t nkv, int
 
 /*
  * The split kq8_sparse_decode_attn uses for its bounded attention (as
- * kq8_decode_plan).  num_chunks > 1 means a merge kernel runs after it.
+ * kq8_decode_plan, for lists of up to G * topk blocks): a list's entries are
+ * dealt out to its num_chunks chunks in turn, at most chunk_tiles each.
  */
 int kq8_sparse_decode_plan(int32_t B, int32_t nq, int32_t nkv, int32_t max_seq_len, int32_t block,
                            int32_t topk, int32_t* chunk_tiles, int32_t* num_chunks);
