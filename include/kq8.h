@@ -23,10 +23,11 @@
  *     launches (cudaLaunchAttributeProgrammaticStreamSerialization): one of
  *     them may be scheduled while the kernel just before it on the stream
  *     finishes (this library's, or any code's that signals its dependents
- *     early), but before that kernel has completed it only sets up its own
- *     shared memory: it reads and writes global memory -- the query, lengths,
- *     page tables, cache, workspace and outputs -- only after the earlier
- *     kernel's completion (griddepcontrol.wait).  In stream capture these
+ *     early).  Until that kernel has completed (griddepcontrol.wait) it writes
+ *     no global memory and reads no cache, workspace or output; the exact
+ *     decode may read its query, lengths and page ids early, but only as a
+ *     guess that it uses once the same values, read again after the wait,
+ *     agree (else it starts over from those).  In stream capture these
  *     launches become programmatic graph edges.
  *   - Return value: KQ8_OK (0) or a negative KQ8_ERR_* code.  On an error
  *     nothing was enqueued.  kq8_strerror() names a code.
