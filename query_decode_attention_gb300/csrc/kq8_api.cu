@@ -29,11 +29,13 @@ constexpr size_t HEADER_BYTES = STATUS_BYTES + MAX_COUNTERS * sizeof(uint32_t);
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
+// SMs of the current device; without one (plans asked for on a host without a
+// GPU) a GB300's 152.
 int device_sms() {
     int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        return 148;
+        return 152;
     return sms;
 }
 
