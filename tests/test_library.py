@@ -167,3 +167,51 @@ def test_q4_argument_validation_without_device(lib):
     assert dec(*args, 100, 1, 16, ctypes.c_float(0.1), 512, 1 << 20, None) == lib.KQ8_ERR_INVALID_ARG
     assert dec(*args, 64, 1, 16, ctypes.c_float(0.1), None, 1 << 20, None) == lib.KQ8_ERR_WORKSPACE
     assert dec(*args, 64, 0, 16, ctypes.c_float(0.1), 512, 1 << 20, None) == lib.KQ8_OK
+
+
+def _prototypes():
+    """name -> list of parameter type strings, from include/kq8.h."""
+    text = open(os.path.join(ROOT, "include", "kq8.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(kq8_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text):
+        params = [p.strip() for p in m.group(2).replace("\n", " ").split(",")]
+        if params == ["void"] or params == [""]:
+            params = []
+        out[m.group(1)] = params
+    return out
+
+
+def _ctype_class(c_param):
+    """The ctypes class a C parameter must be marshalled as."""
+    if "*" in c_param or c_param.startswith("kq8_stream_t"):
+        return "pointer"
+    for ctype, cls in (("int32_t", "int32"), ("uint32_t", "uint32"), ("size_t", "size"),
+                       ("float", "float"), ("int ", "int32")):
+        if c_param.startswith(ctype) or c_param.startswith("const " + ctype):
+            return cls
+    raise AssertionError(f"unrecognised parameter type: {c_param}")
+
+
+def _ctypes_class(t):
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or hasattr(t, "_type_") and isinstance(
+            getattr(t, "_type_"), type):
+        return "pointer"
+    return {ctypes.c_int32: "int32", ctypes.c_uint32: "uint32", ctypes.c_size_t: "size",
+            ctypes.c_float: "float"}[t]
+
+
+def test_binding_argtypes_match_the_header(lib):
+    # ctypes marshals by the declared argtypes without checking them against
+    # the C prototype: a drift between binding and header passes silently
+    protos = _prototypes()
+    checked = 0
+    for name, params in protos.items():
+        fn = getattr(lib._lib, name)
+        if fn.argtypes is None:
+            continue
+        got = [_ctypes_class(t) for t in fn.argtypes]
+        want = [_ctype_class(p) for p in params]
+        assert got == want, f"{name}: binding {got} vs header {want}"
+        checked += 1
+    assert checked >= 20, checked
